@@ -1,0 +1,327 @@
+"""Pins for the fp64 oracle (CPU only).
+
+Each check ties the oracle to something other than itself: pure-loop brute
+force, a library routine (torch's SDPA math path in float64, scipy's Hadamard),
+hand-worked values, closed forms and invariants of the definition.  The last
+group plants plausible mistakes in a copy of the oracle and shows that at least
+one pin rejects each of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import sdpa as oracle_attention_mod
+from fa_inputs import make_qkv, sample_rows, WORKLOADS, sweep_workload
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand(shape, seed, dtype=torch.float64):
+    g = torch.Generator().manual_seed(seed)
+    return [torch.randn(shape, generator=g, dtype=torch.float64).to(dtype) for _ in range(3)]
+
+
+# ----------------------------------------------------------------------------- definition pins
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_brute_force_loops_agree(causal):
+    q, k, v = _rand((2, 2, 13, 8), 11)
+    o, lse = oracle.attention(q, k, v, 0.37, causal)
+    ob, lb = oracle.brute_force_attention(q, k, v, 0.37, causal)
+    assert np.abs(o - ob).max() < 1e-12
+    assert np.abs(lse - lb).max() < 1e-12
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_torch_sdpa_float64(causal):
+    q, k, v = _rand((2, 3, 100, 64), 12)
+    scale = 1.0 / 8.0
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=causal, scale=scale)
+    s = scale * q @ k.transpose(-1, -2)
+    if causal:
+        s = s.masked_fill(torch.ones(100, 100, dtype=torch.bool).triu(1), float("-inf"))
+    ref_lse = torch.logsumexp(s, dim=-1)
+    o, lse = oracle.attention(q, k, v, scale, causal)
+    assert np.abs(o - ref.numpy()).max() < 1e-12
+    assert np.abs(lse - ref_lse.numpy()).max() < 1e-12
+
+
+def _golden_value(x):
+    if isinstance(x, str):
+        return {"ln2": math.log(2.0), "ln3": math.log(3.0), "ln4": math.log(4.0)}[x]
+    return float(x)
+
+
+def _golden_array(a):
+    return np.array([[_golden_value(x) for x in row] for row in a])
+
+
+@pytest.mark.parametrize("mode", ["non_causal", "causal"])
+def test_hand_worked_golden(mode):
+    with open(os.path.join(GOLDEN, "hand_worked_2x2.json")) as f:
+        g = json.load(f)
+    q = _golden_array(g["q"])[None, None]
+    k = _golden_array(g["k"])[None, None]
+    v = _golden_array(g["v"])[None, None]
+    o, lse = oracle.attention(q, k, v, g["scale"], mode == "causal")
+    assert np.abs(o[0, 0] - _golden_array(g[mode]["o"])).max() < 1e-14
+    want_lse = np.array([_golden_value(x) for x in g[mode]["lse"]])
+    assert np.abs(lse[0, 0] - want_lse).max() < 1e-14
+
+
+def test_constant_v_gives_constant_output():
+    q, k, _ = _rand((1, 2, 64, 16), 13)
+    c = torch.linspace(-2, 3, 16, dtype=torch.float64)
+    v = c.expand(1, 2, 64, 16).clone()
+    for causal in (False, True):
+        o, _ = oracle.attention(q, k, v, 0.25, causal)
+        assert np.abs(o - c.numpy()).max() < 1e-13
+
+
+def test_causal_row0_is_v0_and_lse_is_the_score():
+    q, k, v = _rand((2, 2, 40, 32), 14)
+    o, lse = oracle.attention(q, k, v, 0.3, True)
+    assert np.array_equal(o[:, :, 0], v[:, :, 0].numpy())
+    s00 = 0.3 * (q[:, :, 0] * k[:, :, 0]).sum(-1)
+    assert np.abs(lse[:, :, 0] - s00.numpy()).max() < 1e-13
+
+
+def test_single_key():
+    q, k, v = _rand((1, 1, 1, 8), 15)
+    o, lse = oracle.attention(q, k, v, 0.5, False)
+    assert np.allclose(o[0, 0, 0], v[0, 0, 0].numpy(), rtol=0, atol=1e-15)
+    assert abs(lse[0, 0, 0] - 0.5 * float((q * k).sum())) < 1e-14
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_probability_rows_sum_to_one(causal):
+    q, k, v = _rand((1, 2, 50, 16), 16)
+    p = oracle.attention_probs(q, k, v, 0.25, causal)
+    assert np.abs(p.sum(-1) - 1.0).max() < 1e-12
+    if causal:
+        assert np.all(p[..., np.triu_indices(50, 1)[0], np.triu_indices(50, 1)[1]] == 0.0)
+
+
+def test_key_permutation_equivariance():
+    q, k, v = _rand((1, 2, 70, 16), 17)
+    perm = torch.randperm(70, generator=torch.Generator().manual_seed(5))
+    o1, l1 = oracle.attention(q, k, v, 0.25, False)
+    o2, l2 = oracle.attention(q, k[:, :, perm], v[:, :, perm], 0.25, False)
+    assert np.abs(o1 - o2).max() < 1e-12
+    assert np.abs(l1 - l2).max() < 1e-12
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_score_shift_moves_lse_not_output(causal):
+    q, k, v = _rand((1, 2, 48, 16), 18)
+    u = torch.randn(16, generator=torch.Generator().manual_seed(7), dtype=torch.float64)
+    scale = 0.25
+    o1, l1 = oracle.attention(q, k, v, scale, causal)
+    o2, l2 = oracle.attention(q, k + u, v, scale, causal)
+    shift = scale * (q @ u).numpy()               # per-row score offset scale * q_i . u
+    assert np.abs(o1 - o2).max() < 1e-12
+    assert np.abs((l2 - l1) - shift).max() < 1e-12
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_output_reconstructs_from_lse(causal):
+    q, k, v = _rand((1, 2, 33, 8), 19)
+    scale = 0.4
+    o, lse = oracle.attention(q, k, v, scale, causal)
+    s = scale * (q @ k.transpose(-1, -2)).numpy()
+    if causal:
+        s = np.where(np.tril(np.ones((33, 33), bool)), s, -np.inf)
+    rec = np.exp(s - lse[..., None]) @ v.numpy()
+    assert np.abs(rec - o).max() < 1e-12
+
+
+def test_sampled_rows_match_full():
+    q, k, v = _rand((2, 2, 300, 16), 20)
+    rows = sample_rows(300, 17)
+    for causal in (False, True):
+        of, lf = oracle.attention(q, k, v, 0.25, causal)
+        os_, ls = oracle.attention(q, k, v, 0.25, causal, rows=rows)
+        assert np.array_equal(of[:, :, rows], os_) or np.abs(of[:, :, rows] - os_).max() < 1e-13
+        assert np.abs(lf[:, :, rows] - ls).max() < 1e-13
+
+
+def test_row_chunking_changes_nothing(monkeypatch):
+    q, k, v = _rand((1, 1, 257, 16), 21)
+    o1, l1 = oracle.attention(q, k, v, 0.25, True)
+    monkeypatch.setattr(oracle_attention_mod, "_MAX_BLOCK_ELEMS", 257 * 7)
+    o2, l2 = oracle.attention(q, k, v, 0.25, True)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+# ----------------------------------------------------------------------------- online softmax
+
+@pytest.mark.parametrize("block", [1, 3, 16, 64, 200])
+@pytest.mark.parametrize("causal", [False, True])
+def test_online_softmax_equals_direct(block, causal):
+    q, k, v = _rand((1, 2, 150, 16), 22)
+    q = 3.0 * q                                  # widen the score range so the max moves often
+    o, lse = oracle.attention(q, k, v, 0.5, causal)
+    oo, lo = oracle.online_softmax_attention(q, k, v, 0.5, causal, block)
+    assert np.abs(o - oo).max() < 1e-12
+    assert np.abs(lse - lo).max() < 1e-12
+
+
+# ----------------------------------------------------------------------------- Hadamard / FP8
+
+@pytest.mark.parametrize("d", [1, 2, 8, 64, 128])
+def test_sylvester_matches_scipy_and_is_orthogonal(d):
+    scipy_linalg = pytest.importorskip("scipy.linalg")
+    h = oracle.sylvester_hadamard(d)
+    assert np.array_equal(h, scipy_linalg.hadamard(d).astype(np.float64))
+    assert np.array_equal(h @ h.T, d * np.eye(d))
+
+
+def test_rotation_preserves_scores():
+    q, k, _ = _rand((2, 2, 32, 128), 23)
+    s = (q @ k.transpose(-1, -2)).numpy()
+    qr, kr = oracle.hadamard_rotate(q), oracle.hadamard_rotate(k)
+    assert np.abs(qr @ np.swapaxes(kr, -1, -2) - s).max() < 1e-11
+    assert not np.allclose(qr, q.numpy())
+
+
+def test_e4m3_grid_from_definition():
+    codes = np.arange(256, dtype=np.uint8)
+    vals = oracle.e4m3_decode(codes)
+    nan = np.isnan(vals)
+    assert set(codes[nan].tolist()) == {0x7F, 0xFF}
+    assert np.nanmax(vals) == 448.0 and np.nanmin(vals) == -448.0
+    assert vals[1] == 2.0 ** -9 and vals[8] == 2.0 ** -6          # smallest subnormal, smallest normal
+    assert vals[0x38] == 1.0 and vals[0x40] == 2.0 and vals[0x3C] == 1.5
+    finite = ~nan
+    assert np.array_equal(oracle.e4m3_encode(vals[finite]), codes[finite])
+    assert np.array_equal(oracle.round_to_e4m3(vals[finite]), vals[finite])
+
+
+def test_e4m3_rounding_ties_to_even_and_saturates():
+    pos = np.unique(oracle.e4m3_decode(np.arange(0x00, 0x7F, dtype=np.uint8)))
+    mids = 0.5 * (pos[:-1] + pos[1:])
+    r = oracle.round_to_e4m3(mids)
+    codes_lo = oracle.e4m3_encode(pos[:-1])
+    want = np.where(codes_lo % 2 == 0, pos[:-1], pos[1:])
+    assert np.array_equal(r, want)
+    assert oracle.round_to_e4m3(np.array([1e6, -500.0, 460.0]))[0] == 448.0
+    assert oracle.round_to_e4m3(np.array([-500.0]))[0] == -448.0
+
+
+def test_e4m3_rounding_matches_torch_cast():
+    g = torch.Generator().manual_seed(24)
+    x = torch.cat([torch.randn(200000, generator=g) * 10 ** e for e in (-4, -3, -2, -1, 0, 1, 2)])
+    x = x[x.abs() < 464.0]                       # torch's cast gives NaN above the saturation point
+    want = x.to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(oracle.round_to_e4m3(x.to(torch.float64)), want)
+
+
+@pytest.mark.parametrize("hadamard", [False, True])
+def test_block_quantisation_properties(hadamard):
+    q, _, _ = make_qkv((2, 3, 200, 128), torch.bfloat16, 3, outliers=True)
+    codes, scales = oracle.quantize_fp8_blocks(q, 64, hadamard)
+    y = oracle.hadamard_rotate(q) if hadamard else q.double().numpy()
+    assert scales.shape == (2, 3, 4)
+    for i in range(4):
+        blk = y[:, :, i * 64:(i + 1) * 64]
+        amax = np.abs(blk).max(axis=(2, 3))
+        assert np.allclose(scales[:, :, i], amax / 448.0, rtol=1e-15, atol=0)
+        assert np.all(np.abs(oracle.e4m3_decode(codes[:, :, i * 64:(i + 1) * 64])).max(axis=(2, 3)) == 448.0)
+    deq = oracle.dequantize_fp8_blocks(codes, scales)
+    rep = np.repeat(scales, 64, axis=2)[:, :, :200, None]
+    scaled = np.abs(y) / rep
+    _, e2 = np.frexp(scaled)
+    quantum = np.where(scaled >= 2.0 ** -6, np.exp2(e2 - 1 - 3.0), 2.0 ** -9)
+    assert np.all(np.abs(deq - y) <= 0.5 * quantum * rep * (1 + 1e-12))
+
+
+def test_zero_block_gets_unit_scale():
+    x = torch.zeros(1, 1, 64, 64)
+    codes, scales = oracle.quantize_fp8_blocks(x, 64, False)
+    assert scales[0, 0, 0] == 1.0 and not codes.any()
+
+
+def test_hadamard_lowers_predicted_fp8_error_on_outliers():
+    q, k, v = make_qkv((1, 2, 512, 128), torch.bfloat16, 3, outliers=True)
+    scale = 1 / math.sqrt(128)
+    ref, _ = oracle.attention(q, k, v, scale, False)
+    off = oracle.rel_rms(oracle.emulate_fp8_attention(q, k, v, scale, False, False)[0], ref)
+    on = oracle.rel_rms(oracle.emulate_fp8_attention(q, k, v, scale, False, True)[0], ref)
+    assert on < off
+
+
+# ----------------------------------------------------------------------------- inputs
+
+def test_inputs_are_seeded_and_cast():
+    a = make_qkv((1, 2, 8, 16), torch.bfloat16, 5)
+    b = make_qkv((1, 2, 8, 16), torch.bfloat16, 5)
+    assert all(torch.equal(x, y) for x, y in zip(a, b))
+    assert a[0].dtype == torch.bfloat16
+    q, k, v = make_qkv((2, 2, 256, 128), torch.bfloat16, 3, outliers=True)
+    n_big = int((q.float().abs() > 6).sum())
+    assert 0 < n_big <= round(1e-3 * q.numel())
+    assert WORKLOADS["bf16"].flops(True) == WORKLOADS["bf16"].flops(False) / 2
+    assert sweep_workload(8192, 128).B == 2
+    rows = sample_rows(32768)
+    assert len(rows) == 64 and rows[0] == 0 and rows[-1] == 32767
+
+
+# ----------------------------------------------------------------------------- planted mistakes
+
+def _mutant(kind):
+    """A copy of the oracle's per-head routine with one plausible mistake."""
+    def rows_of_head(qh, kh, vh, scale, causal, rows):
+        n_keys = kh.shape[0]
+        if kind == "no_scale":
+            s = qh[rows] @ kh.T
+        elif kind == "transposed":
+            s = scale * (kh @ qh.T)[rows]
+        else:
+            s = scale * (qh[rows] @ kh.T)
+        if causal:
+            if kind == "mask_direction":
+                visible = np.arange(n_keys)[None, :] >= rows[:, None]
+            elif kind == "mask_diagonal":
+                visible = np.arange(n_keys)[None, :] < np.maximum(rows[:, None], 1)
+            else:
+                visible = np.arange(n_keys)[None, :] <= rows[:, None]
+            s = np.where(visible, s, -np.inf)
+        m = s.max(axis=1)
+        p = np.exp(s - m[:, None])
+        l = p.sum(axis=1)
+        o = p @ vh if kind == "no_normalise" else (p @ vh) / l[:, None]
+        if kind == "lse_no_max":
+            lse = np.log(l)
+        elif kind == "lse_log2":
+            lse = m + np.log2(l)
+        else:
+            lse = m + np.log(l)
+        return o, lse
+    return rows_of_head
+
+
+def _pins_pass():
+    """Run a subset of the pins above against whatever ``_rows_of_head`` is installed."""
+    try:
+        for causal in (False, True):
+            test_brute_force_loops_agree(causal)
+            test_output_reconstructs_from_lse(causal)
+            test_hand_worked_golden("causal" if causal else "non_causal")
+        test_causal_row0_is_v0_and_lse_is_the_score()
+        test_constant_v_gives_constant_output()
+    except AssertionError:
+        return False
+    return True
+
+
+@pytest.mark.parametrize("kind", ["no_scale", "transposed", "mask_direction", "mask_diagonal",
+                                  "no_normalise", "lse_no_max", "lse_log2"])
+def test_pins_reject_planted_mistakes(kind, monkeypatch):
+    assert _pins_pass()
+    monkeypatch.setattr(oracle_attention_mod, "_rows_of_head", _mutant(kind))
+    assert not _pins_pass(), f"no pin caught the planted mistake {kind!r}"
