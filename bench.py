@@ -1,0 +1,383 @@
+"""Attention forward benchmark: one JSON line on rank 0.
+
+A step is one pass of the forward over one batch of synthetic inputs already
+resident in HBM.  Default workload: bf16 Q/K/V [16, 16, 2048, 128], scale
+1/sqrt(128), one non-causal and one causal forward per step (both masks of that
+workload), TFLOP/s = algorithmic FLOPs (4*B*H*N^2*d, halved for causal) / time.
+
+Other workloads (for profiling; the default is the headline):
+  --workload sweep:N:d   B*N = 16384, H = 16, both masks
+  --workload long        [1, 32, 32768, 128], causal
+  --workload fp8         [4, 16, 4096, 128] E4M3 forward (Hadamard on), quantisation excluded
+  --workload tiny        [1, 1, 128, 64] fp16, both masks
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs the same per-GPU
+workload on its own shard of heads (weak scaling, no collective on the data
+path; a barrier and a MAX all-reduce of the timings only).
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead, on a
+bounded sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from fa_inputs import WORKLOADS, make_inputs, make_qkv, sweep_workload  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s and % of GB300 dense BF16/FP8 tensor peak"
+SPEC_PEAK_TFLOPS = {"bf16": 2250.0, "fp16": 2250.0, "e4m3": 4500.0}
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+SMI_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def _dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _workload(name: str):
+    if name.startswith("sweep:"):
+        _, n, d = name.split(":")
+        return sweep_workload(int(n), int(d))
+    return WORKLOADS[name]
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms during the timed region."""
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={SMI_QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        time.sleep(0.3)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        loaded = [s for s, p in zip(sm, pw) if p is not None and p > 200.0] or sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(pw) if pw else None}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def _oracle_sample(w, budget_s: float, max_units=None):
+    """Times the fp64 oracle over (mask, head) pairs of workload ``w`` until
+    ``budget_s`` seconds have passed; returns (flops, seconds, description)."""
+    import numpy as np  # noqa: F401
+    import oracle
+    q, k, v = make_qkv((1, min(w.H, 4), w.N, w.d), w.dtype, w.seed, w.outliers)
+    flops = 0.0
+    done = 0
+    t0 = time.perf_counter()
+    pairs = [(c, h) for h in range(q.shape[1]) for c in w.causal_modes]
+    i = 0
+    while True:
+        causal, h = pairs[i % len(pairs)]
+        sl = (slice(0, 1), slice(h, h + 1))
+        oracle.attention(q[sl], k[sl], v[sl], w.scale, causal)
+        flops += (4.0 * w.N * w.N * w.d) / (2.0 if causal else 1.0)
+        done += 1
+        i += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_units is not None and done >= max_units):
+            break
+    desc = (f"{done} full (b,h) heads of [{w.B},{w.H},{w.N},{w.d}] "
+            f"({'/'.join('causal' if c else 'non-causal' for c in w.causal_modes)} alternating), fp64 numpy")
+    return flops, time.perf_counter() - t0, desc
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    world, rank, _ = _dist_env()
+    if rank != 0:
+        return 0
+    w = _workload(args.workload)
+    for _ in range(args.warmup):
+        _oracle_sample(w, 0.0, max_units=1)
+    flops = 0.0
+    secs = 0.0
+    desc = ""
+    for _ in range(args.steps):
+        f, s, desc = _oracle_sample(w, args.ref_step_seconds)
+        flops += f
+        secs += s
+    value = flops / secs / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                       "masks": ["causal" if c else "non-causal" for c in w.causal_modes]},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
+                             "sample": f"per step: {desc}"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import transformer_attention_flashattention_gb300 as fa
+    world, rank, local = _dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the GPU arm has no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    fa.load_library()
+    w = _workload(args.workload)
+    fp8 = args.workload == "fp8"
+    # Each rank draws its own shard (same shape, seed offset by rank): weak scaling.
+    q, k, v = make_qkv(w.shape, w.dtype, w.seed + 7919 * rank, w.outliers)
+    masks = list(w.causal_modes)
+    stream = torch.cuda.current_stream(dev)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    if fp8:
+        q8, qs = fa.quantize_fp8(qd, hadamard=True)
+        k8, ks = fa.quantize_fp8(kd, hadamard=True)
+        v8, vs = fa.quantize_fp8(vd, hadamard=False, transpose_out=True)
+    o = torch.empty(w.shape, device=dev, dtype=torch.bfloat16 if fp8 else w.dtype)
+    lse = torch.empty(w.shape[:3], device=dev, dtype=torch.float32)
+
+    def one(causal):
+        if fp8:
+            fa.attention_fp8(q8, k8, v8, qs, ks, vs, causal=causal, hadamard=True, out=o, lse=lse)
+        else:
+            fa.attention(qd, kd, vd, causal=causal, out=o, lse=lse)
+
+    step_flops = sum(w.flops(c) for c in masks)
+    for _ in range(args.warmup):
+        for c in masks:
+            one(c)
+    torch.cuda.synchronize()
+
+    # Timed region: events around every launch on the launching stream.
+    n_ev = args.steps * len(masks)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local) as clk:
+        t_start.record(stream)
+        i = 0
+        for _ in range(args.steps):
+            for c in masks:
+                ev[i][0].record(stream)
+                one(c)
+                ev[i][1].record(stream)
+                i += 1
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    st, bits = fa.last_device_status()
+    if st != fa.FA_OK:
+        raise SystemExit(f"bench.py: device status word set ({bits:#x}) during the timed region")
+    per_mask_ms = {c: [launch_ms[j] for j in range(len(launch_ms)) if masks[j % len(masks)] == c] for c in masks}
+
+    if pg:
+        t = torch.tensor([total_ms, sum(launch_ms)], device=dev, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms, kern_ms = float(t[0]), float(t[1])
+    else:
+        kern_ms = sum(launch_ms)
+    value = world * step_flops * args.steps / (total_ms * 1e-3) / 1e12
+
+    # End-to-end through the public API with pinned host buffers (this rank's shard).
+    e2e = None
+    if not fp8:
+        qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+        e_steps = max(1, min(args.steps, 5))
+        for _ in range(2):
+            for c in masks:
+                fa.attention_host(qh, kh, vh, causal=c)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(e_steps):
+            for c in masks:
+                fa.attention_host(qh, kh, vh, causal=c)
+        e_s = time.perf_counter() - t0
+        if pg:
+            t = torch.tensor([e_s], device=dev, dtype=torch.float64)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            e_s = float(t[0])
+        h2d = len(masks) * 3 * q.numel() * q.element_size()
+        d2h = len(masks) * (q.numel() * q.element_size() + 4 * q.numel() // w.d)
+        e2e = {"value": world * step_flops * e_steps / e_s / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "note": "fa.attention_host per mask: pinned Q/K/V H2D, fa_fwd, O and LSE D2H, synchronised"}
+
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return 0
+
+    peaks, peak_src = _peaks()
+    dtype_name = "e4m3" if fp8 else ("bf16" if w.dtype == torch.bfloat16 else "fp16")
+    if fp8:
+        peak = 2.0 * peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        peak_note = f"2 x {peak_src} bf16 peak (nominal e4m3:bf16 ratio)"
+    else:
+        peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        peak_note = f"{peak_src} bf16 burst peak"
+    kern_tflops = step_flops * args.steps / (kern_ms * 1e-3) / 1e12
+    traffic = _committed_traffic(w.name, fp8)
+    variants = {("causal" if c else "non_causal"): {
+        "tflops": w.flops(c) / (statistics.median(per_mask_ms[c]) * 1e-3) / 1e12,
+        "median_ms": statistics.median(per_mask_ms[c]),
+        "pct_of_spec_peak": 100.0 * w.flops(c) / (statistics.median(per_mask_ms[c]) * 1e-3) / 1e12
+        / SPEC_PEAK_TFLOPS[dtype_name]} for c in masks}
+
+    cpu = None
+    if world == 1 or rank == 0:
+        if not args.skip_cpu_baseline:
+            f, s, desc = _oracle_sample(w, args.cpu_seconds)
+            cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
+                   "sample": desc + f", {s:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype_name, "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "masks": ["causal" if c else "non-causal" for c in masks],
+                   "scale": "1/sqrt(d)", "global_batch_heads": world * w.B * w.H,
+                   "l2": "inputs larger than L2 (no flush): Q/K/V = %d MB per rank" %
+                         (3 * q.numel() * q.element_size() // 2**20),
+                   "parallelism": f"dp{world} (independent head shards, no data-path collective)"},
+        "pct_of_spec_peak": 100.0 * value / world / SPEC_PEAK_TFLOPS[dtype_name],
+        "roofline": {"bound": "tensor", "achieved": kern_tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": kern_tflops / peak, "traffic": traffic, "peak_source": peak_note,
+                     "kernel": "fa_fwd_fp8_kernel" if fp8 else "fa_fwd_kernel"},
+        "variants": variants,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": n_ev,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+def _committed_traffic(workload: str, fp8: bool):
+    """DRAM bytes per launch from the committed ncu summary, if one matches."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d.get(("fp8:" if fp8 else "") + workload)
+    except (OSError, ValueError):
+        return None
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="bf16")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=6.0)
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("bench.py: at least 3 warm-up steps")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

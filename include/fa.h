@@ -1,0 +1,120 @@
+/*
+ * fa.h — C ABI of the GB300 (sm_103a) attention forward library, libfa.so.
+ *
+ * The operation is exact scaled-dot-product attention,
+ *     O = softmax(scale * Q K^T [+ causal mask]) V,
+ * the problem statement of the concept card "FlashAttention 2 + 3 —
+ * speicherbewusste Attention-Kernels" (section "Kernpunkte": the same output as
+ * softmax(QK^T/sqrt(d)) V, with the N x N matrix never written to HBM) and of the
+ * "Flash Attention" glossary (section "/01 Was ist Flash Attention?"), computed
+ * tile by tile with an online softmax (concept card, "Begriffe auf dieser Seite",
+ * Online-Softmax).  Each call also writes the per-row log-sum-exp.  The FP8 entry
+ * points follow the FlashAttention-3 news piece ("Drei technische Hebel", item 3:
+ * block-wise 8-bit quantisation with a Hadamard transform) and the concept card's
+ * absmax scaling ("Kernpunkte", FP8 item).
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are contiguous, row-major [B, H, N, d] with d innermost; LSE is
+ *     [B, H, N] float32; block scales are [B, H, ceil(N/64)] float32.
+ *   - Data pointers are DEVICE pointers owned by the caller, 16-byte aligned
+ *     (LSE and scales 4-byte aligned).  The library keeps no pointer after the
+ *     call returns and allocates no per-call memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Calls are asynchronous on that stream; nothing synchronises
+ *     except fa_last_device_status.
+ *   - The current CUDA device must be an sm_103 GPU.
+ *   - Errors are returned as fa_status codes, never thrown.  Argument errors are
+ *     detected on the host before any device work is enqueued.
+ *   - Causal masking is top-left aligned: query row i sees keys 0..i.
+ *   - Supported: B, H, N >= 1; d in {64, 128}; B*H*N*d < 2^40.
+ */
+#ifndef FA_GB300_H_
+#define FA_GB300_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { FA_F16 = 0, FA_BF16 = 1 } fa_dtype;
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_NULL = -1,            /* a required pointer is NULL */
+  FA_ERR_ALIGN = -2,           /* a pointer is not aligned as stated above */
+  FA_ERR_SHAPE = -3,           /* B, H or N out of range, or sizes overflow */
+  FA_ERR_UNSUPPORTED = -4,     /* head dim, dtype or flag value not supported */
+  FA_ERR_LAUNCH = -5,          /* the kernel launch was rejected by the runtime */
+  FA_ERR_DEVICE_TIMEOUT = -6,  /* a kernel gave up on a pipeline wait (see fa_last_device_status) */
+  FA_ERR_ARCH = -7,            /* the current device is not an sm_103 GPU */
+  FA_ERR_CUDA = -8             /* another CUDA runtime or driver call failed */
+} fa_status;
+
+/*
+ * Attention forward in f16 or bf16.
+ *   q, k, v : [B, H, N, d] of `dtype` (FA_F16 or FA_BF16)
+ *   o       : [B, H, N, d] of `dtype`, written
+ *   lse     : [B, H, N] float32, written: natural log of sum_j exp(scale * q_i.k_j)
+ *             over the visible keys; may be NULL (not written)
+ *   scale   : multiplies Q K^T (1/sqrt(d) gives the textbook definition); finite and > 0
+ *   causal  : 0 or 1
+ * Accumulation is fp32; the softmax weights are rounded to `dtype` before the
+ * weighted sum over V, and O is rounded to `dtype` once at the end.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+           int d, float scale, int causal, int dtype, void* stream);
+
+/*
+ * FP8 prologue: optional Hadamard rotation along d, block absmax, E4M3 quantisation.
+ *   x        : [B, H, N, d] bfloat16 input
+ *   x8       : E4M3 output, [B, H, N, d]; with transpose_out = 1 it is [B, H, d, N]
+ *              instead (the layout fa_fwd_fp8 wants for V), which needs N % 16 == 0
+ *   scale    : [B, H, ceil(N/64)] float32, written: s = absmax/448 of the (rotated)
+ *              64-row block, 1 for an all-zero block; x8 = e4m3_rn_satfinite(x/s)
+ *   hadamard : 1 applies x -> x H_d / sqrt(d) (Sylvester order) before the absmax;
+ *              0 does not.  Use 1 for Q and K only, never for V.
+ */
+int fa_quantize_fp8(const void* x, void* x8, float* scale, int B, int H, int N, int d, int hadamard,
+                    int transpose_out, void* stream);
+
+/*
+ * Attention forward from E4M3 inputs produced by fa_quantize_fp8.
+ *   q8, k8   : [B, H, N, d] E4M3 (rotated by the same Hadamard matrix, or both not)
+ *   v8t      : [B, H, d, N] E4M3 (V quantised with transpose_out = 1, not rotated)
+ *   q_scale, k_scale, v_scale : [B, H, ceil(N/64)] float32 block scales
+ *   o        : [B, H, N, d] bfloat16, written;  lse as for fa_fwd (may be NULL)
+ *   hadamard : records whether Q and K were rotated (0 or 1); (QH)(KH)^T = QK^T,
+ *              so it changes no arithmetic here and is only validated
+ * Supported: d == 128, N % 16 == 0, non-causal or causal.
+ */
+int fa_fwd_fp8(const void* q8, const void* k8, const void* v8t, void* o, float* lse, int B, int H,
+               int N, int d, float scale, int causal, const float* q_scale, const float* k_scale,
+               const float* v_scale, int hadamard, void* stream);
+
+/* Static English text for a status code (never NULL). */
+const char* fa_strerror(int status);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word, which kernels set when a bounded pipeline wait gives up.  Returns FA_OK
+ * or FA_ERR_DEVICE_TIMEOUT; *bits (if not NULL) receives the raw word
+ * (1 load warp, 2 MMA warp, 4 softmax warps, 8 drain of in-flight copies).
+ */
+int fa_last_device_status(void* stream, unsigned int* bits);
+
+/*
+ * Test hook for the failure path: the next fa_fwd call's producer leaves out
+ * K/V load number `load_index` of every CTA (so the consumers' bounded waits
+ * run out), and every wait of that call gives up after `timeout_ms` ms.  The
+ * call still returns FA_OK; fa_last_device_status then reports the timeout.
+ * load_index < 0 clears the hook.  Not for production use.
+ */
+int fa_debug_inject_stall(int load_index, int timeout_ms);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H_ */

@@ -1,0 +1,74 @@
+"""The C-ABI library builds, loads and exports every entry point include/fa.h
+declares; host-side argument checks return their documented codes without
+touching a GPU (CPU only: no compute call is made)."""
+import ctypes
+import math
+import os
+import re
+import shutil
+
+import pytest
+
+import transformer_attention_flashattention_gb300 as fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:int|const char\s*\*)\s*(fa_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available")
+    from transformer_attention_flashattention_gb300 import _build
+    _build.build()
+    return fa.load_library()
+
+
+def test_header_declares_the_boundary():
+    assert _declared() == sorted(["fa_fwd", "fa_quantize_fp8", "fa_fwd_fp8", "fa_strerror",
+                                  "fa_last_device_status", "fa_debug_inject_stall", "fa_version"])
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert sorted(fa.exported_symbols()) == _declared()
+
+
+def test_strerror_and_version(lib):
+    for code in range(-8, 1):
+        assert lib.fa_strerror(code)
+    assert lib.fa_strerror(-99) == b"unknown status"
+    assert lib.fa_version() >= 100
+
+
+A = 0x10000          # a 16-byte aligned fake address; never dereferenced by these calls
+
+
+@pytest.mark.parametrize("args,want", [
+    ((0, A, A, A, 0, 1, 1, 128, 64, 0.125, 0, 1), fa.FA_ERR_NULL),
+    ((A, A, A, 0, 0, 1, 1, 128, 64, 0.125, 0, 1), fa.FA_ERR_NULL),
+    ((A, A, A, A, 0, 1, 1, 128, 96, 0.125, 0, 1), fa.FA_ERR_UNSUPPORTED),
+    ((A, A, A, A, 0, 1, 1, 128, 64, 0.125, 0, 7), fa.FA_ERR_UNSUPPORTED),
+    ((A, A, A, A, 0, 1, 1, 128, 64, 0.125, 2, 1), fa.FA_ERR_UNSUPPORTED),
+    ((A, A, A, A, 0, 1, 1, 128, 64, float("nan"), 0, 1), fa.FA_ERR_UNSUPPORTED),
+    ((A, A, A, A, 0, 1, 1, 128, 64, 0.0, 0, 1), fa.FA_ERR_UNSUPPORTED),
+    ((A, A, A, A, 0, 1, 1, 128, 64, -0.125, 0, 1), fa.FA_ERR_UNSUPPORTED),
+    ((A, A, A, A, 0, 0, 1, 128, 64, 0.125, 0, 1), fa.FA_ERR_SHAPE),
+    ((A, A, A, A, 0, 1, 1, 0, 64, 0.125, 0, 1), fa.FA_ERR_SHAPE),
+    ((A, A, A, A, 0, 1, -3, 128, 64, 0.125, 0, 1), fa.FA_ERR_SHAPE),
+    ((A, A, A, A, 0, 65536, 65536, 65536, 64, 0.125, 0, 1), fa.FA_ERR_SHAPE),
+    ((A + 8, A, A, A, 0, 1, 1, 128, 64, 0.125, 0, 1), fa.FA_ERR_ALIGN),
+    ((A, A, A, A + 2, 0, 1, 1, 128, 64, 0.125, 0, 1), fa.FA_ERR_ALIGN),
+    ((A, A, A, A, A + 2, 1, 1, 128, 64, 0.125, 0, 1), fa.FA_ERR_ALIGN),
+])
+def test_fwd_rejects_bad_arguments_on_the_host(lib, args, want):
+    q, k, v, o, lse, B, H, N, d, scale, causal, dtype = args
+    assert lib.fa_fwd(q or None, k or None, v or None, o or None, lse or None, B, H, N, d, scale,
+                      causal, dtype, None) == want

@@ -1,0 +1,195 @@
+"""GPU parity of the f16/bf16 forward against the fp64 oracle, through the C ABI.
+
+Tolerances (stated once, used everywhere): max |O_gpu - O_ref| <= 1e-2 and
+max |LSE_gpu - LSE_ref| <= 1e-3 over the compared elements.  Small shapes are
+compared element by element on every row; the full-size workloads are run in
+the launch configuration the benchmark times and compared on sampled rows of
+every head (plus every row of a few heads), which the oracle computes one by one.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fa_inputs import SWEEP_NS, WORKLOADS, make_inputs, make_qkv, sample_rows, sweep_workload
+
+pytestmark = pytest.mark.gpu
+
+O_TOL = 1e-2
+LSE_TOL = 1e-3
+
+
+def _run(fa, q, k, v, causal, scale=None):
+    o, lse = fa.attention(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    return o.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def _assert_close(o, lse, ro, rl, what):
+    assert np.isfinite(o).all(), f"{what}: non-finite O"
+    assert np.isfinite(lse).all(), f"{what}: non-finite LSE"
+    eo = float(np.abs(o - ro).max())
+    el = float(np.abs(lse - rl).max())
+    assert eo <= O_TOL and el <= LSE_TOL, f"{what}: max|dO|={eo:.3e} max|dLSE|={el:.3e}"
+    return eo, el
+
+
+def _compare_full(fa, q, k, v, causal, scale=None, what=""):
+    d = q.shape[-1]
+    s = scale if scale is not None else 1.0 / math.sqrt(d)
+    o, lse = _run(fa, q, k, v, causal, scale)
+    ro, rl = oracle.attention(q, k, v, s, causal)
+    return _assert_close(o, lse, ro, rl, what)
+
+
+def _compare_sampled(fa, q, k, v, causal, full_heads=2, what=""):
+    B, H, N, d = q.shape
+    s = 1.0 / math.sqrt(d)
+    o, lse = _run(fa, q, k, v, causal)
+    rows = sample_rows(N)
+    ro, rl = oracle.attention(q, k, v, s, causal, rows=rows)
+    _assert_close(o[:, :, rows], lse[:, :, rows], ro, rl, what + " sampled rows")
+    # every row of the first and the last head
+    for (b, h) in [(0, 0), (B - 1, H - 1)][:full_heads]:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ro, rl = oracle.attention(q[sl], k[sl], v[sl], s, causal)
+        _assert_close(o[sl], lse[sl], ro, rl, what + f" head ({b},{h})")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_tiny_workload(gpu_lib, causal):
+    q, k, v = make_inputs(WORKLOADS["tiny"])
+    _compare_full(gpu_lib, q, k, v, causal, what="tiny")
+
+
+RAGGED = [
+    # B, H, N, d, dtype
+    (1, 1, 1, 64, torch.bfloat16),
+    (1, 2, 2, 128, torch.float16),
+    (2, 1, 17, 64, torch.bfloat16),
+    (1, 3, 127, 128, torch.bfloat16),
+    (1, 1, 128, 128, torch.bfloat16),
+    (1, 2, 129, 64, torch.float16),
+    (2, 2, 200, 128, torch.bfloat16),
+    (1, 1, 255, 64, torch.bfloat16),
+    (1, 2, 256, 128, torch.float16),
+    (1, 1, 257, 128, torch.bfloat16),
+    (1, 2, 384, 64, torch.bfloat16),
+    (2, 1, 511, 128, torch.bfloat16),
+    (1, 1, 640, 64, torch.float16),
+    (1, 2, 1000, 128, torch.bfloat16),
+    (1, 1, 1536, 64, torch.bfloat16),
+    (3, 5, 333, 128, torch.bfloat16),
+]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,N,d,dtype", RAGGED)
+def test_ragged_shapes(gpu_lib, B, H, N, d, dtype, causal):
+    q, k, v = make_qkv((B, H, N, d), dtype, 100 + N)
+    _compare_full(gpu_lib, q, k, v, causal, what=f"{B}x{H}x{N}x{d} {dtype}")
+
+
+def test_explicit_scale(gpu_lib):
+    q, k, v = make_qkv((1, 2, 300, 64), torch.bfloat16, 7)
+    _compare_full(gpu_lib, q, k, v, False, scale=0.3, what="scale 0.3")
+    _compare_full(gpu_lib, q, k, v, True, scale=0.05, what="scale 0.05")
+
+
+def test_growing_maximum_exercises_rescaling(gpu_lib):
+    """Scores that grow from one K/V tile to the next force the running maximum
+    (and with it O and the row sum) to be corrected many times."""
+    B, H, N, d = 1, 2, 1024, 64
+    q, k, v = make_qkv((B, H, N, d), torch.float32, 8)
+    ramp = torch.linspace(0.2, 3.0, N).view(1, 1, N, 1)
+    q = (q.abs() + 0.5).to(torch.bfloat16)
+    k = (k.abs() * ramp).to(torch.bfloat16)
+    v = (0.25 * v).to(torch.bfloat16)
+    for causal in (False, True):
+        _compare_full(gpu_lib, q, k, v, causal, what="growing max")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_workload(gpu_lib, causal):
+    q, k, v = make_inputs(WORKLOADS["bf16"])
+    _compare_sampled(gpu_lib, q, k, v, causal, what="bf16 16x16x2048x128")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", SWEEP_NS)
+def test_sweep_workloads(gpu_lib, N, d):
+    w = sweep_workload(N, d)
+    q, k, v = make_inputs(w)
+    for causal in (False, True):
+        _compare_sampled(gpu_lib, q, k, v, causal, full_heads=1 if N >= 8192 else 2, what=w.name)
+
+
+def test_long_context_workload(gpu_lib):
+    w = WORKLOADS["long"]
+    q, k, v = make_inputs(w)
+    _compare_sampled(gpu_lib, q, k, v, True, full_heads=0, what="long 1x32x32768x128")
+
+
+def test_repeat_runs_are_bitwise_identical(gpu_lib):
+    q, k, v = (t.cuda() for t in make_qkv((4, 8, 1024, 128), torch.bfloat16, 9))
+    for causal in (False, True):
+        o1, l1 = gpu_lib.attention(q, k, v, causal=causal)
+        o2, l2 = gpu_lib.attention(q, k, v, causal=causal)
+        torch.cuda.synchronize()
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_guard_regions_and_poisoned_outputs(gpu_lib):
+    """Outputs are pre-filled with NaN inside guard bands of a sentinel: every
+    output element must be written and nothing outside the outputs touched."""
+    B, H, N, d = 2, 3, 333, 128
+    q, k, v = (t.cuda() for t in make_qkv((B, H, N, d), torch.bfloat16, 10))
+    pad = 4096
+    n_o = B * H * N * d
+    o_buf = torch.full((pad + n_o + pad,), 12345.0, device="cuda", dtype=torch.bfloat16)
+    o_buf[pad:pad + n_o] = float("nan")
+    l_buf = torch.full((pad + B * H * N + pad,), -777.0, device="cuda", dtype=torch.float32)
+    l_buf[pad:pad + B * H * N] = float("nan")
+    out = o_buf[pad:pad + n_o].view(B, H, N, d)
+    lse = l_buf[pad:pad + B * H * N].view(B, H, N)
+    for causal in (False, True):
+        gpu_lib.attention(q, k, v, causal=causal, out=out, lse=lse)
+        torch.cuda.synchronize()
+        assert not torch.isnan(out).any() and not torch.isnan(lse).any()
+        assert bool((o_buf[:pad] == 12345.0).all()) and bool((o_buf[pad + n_o:] == 12345.0).all())
+        assert bool((l_buf[:pad] == -777.0).all()) and bool((l_buf[pad + B * H * N:] == -777.0).all())
+        ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), 1 / math.sqrt(d), causal)
+        _assert_close(out.float().cpu().numpy(), lse.cpu().numpy(), ro, rl, "guarded")
+        out.fill_(float("nan"))
+        lse.fill_(float("nan"))
+
+
+def test_lse_optional_and_side_stream(gpu_lib):
+    q, k, v = make_qkv((1, 4, 700, 64), torch.float16, 11)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+        o, lse = gpu_lib.attention(qd, kd, vd, causal=True, return_lse=False, stream=s)
+    s.synchronize()
+    assert lse is None
+    ro, _ = oracle.attention(q, k, v, 1 / 8.0, True)
+    assert float(np.abs(o.float().cpu().numpy() - ro).max()) <= O_TOL
+
+
+def test_host_buffers_end_to_end(gpu_lib):
+    q, k, v = (t.pin_memory() for t in make_qkv((2, 2, 512, 128), torch.bfloat16, 12))
+    o, lse = gpu_lib.attention_host(q, k, v, causal=False)
+    assert o.device.type == "cpu" and lse.device.type == "cpu"
+    ro, rl = oracle.attention(q, k, v, 1 / math.sqrt(128), False)
+    _assert_close(o.float().numpy(), lse.numpy(), ro, rl, "host buffers")
+
+
+def test_device_rejections(gpu_lib):
+    q = torch.zeros((1, 1, 64, 96), device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(gpu_lib.FAError) as e:
+        gpu_lib.attention(q, q, q)
+    assert e.value.status == gpu_lib.FA_ERR_UNSUPPORTED
+    st, bits = gpu_lib.last_device_status()
+    assert st == gpu_lib.FA_OK and bits == 0

@@ -1,0 +1,235 @@
+"""GB300 (sm_103a) attention forward: a thin ctypes binding over libfa.so.
+
+Every step of the computation runs in the library's CUDA kernels; this module
+only checks arguments, allocates outputs with torch (device memory and streams
+are all torch is used for) and passes raw pointers through the C ABI declared
+in ``include/fa.h``.  There is no fallback: if the library is missing or the
+device is not an sm_103 GPU, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+import torch
+
+__all__ = [
+    "FAError",
+    "load_library",
+    "library_path",
+    "exported_symbols",
+    "attention",
+    "attention_host",
+    "quantize_fp8",
+    "attention_fp8",
+    "last_device_status",
+    "inject_stall",
+    "FA_OK",
+    "FA_ERR_NULL",
+    "FA_ERR_ALIGN",
+    "FA_ERR_SHAPE",
+    "FA_ERR_UNSUPPORTED",
+    "FA_ERR_LAUNCH",
+    "FA_ERR_DEVICE_TIMEOUT",
+    "FA_ERR_ARCH",
+    "FA_ERR_CUDA",
+]
+
+FA_OK = 0
+FA_ERR_NULL = -1
+FA_ERR_ALIGN = -2
+FA_ERR_SHAPE = -3
+FA_ERR_UNSUPPORTED = -4
+FA_ERR_LAUNCH = -5
+FA_ERR_DEVICE_TIMEOUT = -6
+FA_ERR_ARCH = -7
+FA_ERR_CUDA = -8
+
+_PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+_LIB: Optional[ctypes.CDLL] = None
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_f = ctypes.c_float
+_SIGNATURES = {
+    "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _vp]),
+    "fa_quantize_fp8": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]),
+    "fa_fwd_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _i, _vp]),
+    "fa_strerror": (ctypes.c_char_p, [_i]),
+    "fa_last_device_status": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),
+    "fa_debug_inject_stall": (_i, [_i, _i]),
+    "fa_version": (_i, []),
+}
+
+
+class FAError(RuntimeError):
+    """A non-zero status returned by the C ABI."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _LIB.fa_strerror(status).decode() if _LIB is not None else str(status)
+        super().__init__(f"{where}: {msg} (status {status})")
+
+
+def library_path() -> str:
+    return os.environ.get("FA_LIBRARY", os.path.join(_PKG_DIR, "libfa.so"))
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libfa.so (built by ``__graft_entry__.build()``) and declare its signatures."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = path or library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libfa.so not found at {path}: build it with "
+                           "`python -m transformer_attention_flashattention_gb300._build`")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+def exported_symbols():
+    return list(_SIGNATURES)
+
+
+def _check(status: int, where: str) -> None:
+    if status != FA_OK:
+        raise FAError(status, where)
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream], device: torch.device) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+_DTYPES = {torch.float16: 0, torch.bfloat16: 1}
+
+
+def _check_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor):
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError(f"q, k, v must share one [B, H, N, d] shape; got {tuple(q.shape)}, "
+                         f"{tuple(k.shape)}, {tuple(v.shape)}")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if t.device != q.device or t.dtype != q.dtype:
+            raise ValueError("q, k, v must share device and dtype")
+
+
+def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+              scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+              lse: Optional[torch.Tensor] = None, return_lse: bool = True,
+              stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """O = softmax(scale * Q K^T [+ causal mask]) V and the natural-log LSE.
+
+    q, k, v: contiguous CUDA tensors [B, H, N, d], float16 or bfloat16, d in {64, 128}.
+    Returns (O [B, H, N, d] of q's dtype, LSE [B, H, N] float32 or None).
+    """
+    lib = load_library()
+    _check_qkv(q, k, v)
+    if q.dtype not in _DTYPES:
+        raise ValueError(f"dtype must be float16 or bfloat16, got {q.dtype}")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    st = lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, float(scale),
+                    int(bool(causal)), _DTYPES[q.dtype], _stream_handle(stream, q.device))
+    _check(st, "fa_fwd")
+    return out, lse
+
+
+def attention_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+                   scale: Optional[float] = None, device: Optional[torch.device] = None,
+                   stream: Optional[torch.cuda.Stream] = None):
+    """End-to-end call on HOST tensors (pinned for best speed): copy Q, K, V to the
+    GPU, run ``fa_fwd``, copy O and LSE back.  Returns host tensors."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.stream(s):
+        qd = q.to(dev, non_blocking=True)
+        kd = k.to(dev, non_blocking=True)
+        vd = v.to(dev, non_blocking=True)
+        o, lse = attention(qd, kd, vd, causal=causal, scale=scale, stream=s)
+        pin = q.is_pinned()
+        oh = torch.empty(o.shape, dtype=o.dtype, pin_memory=pin)
+        lh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=pin)
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+    s.synchronize()
+    return oh, lh
+
+
+def quantize_fp8(x: torch.Tensor, hadamard: bool = False, transpose_out: bool = False,
+                 stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Block absmax E4M3 quantisation of bf16 ``x [B,H,N,d]`` (optionally Hadamard-rotated).
+
+    Returns (codes as uint8 [B,H,N,d] or [B,H,d,N] when transposed, scales fp32 [B,H,ceil(N/64)]).
+    """
+    lib = load_library()
+    if x.dim() != 4 or not x.is_cuda or not x.is_contiguous() or x.dtype != torch.bfloat16:
+        raise ValueError("x must be a contiguous CUDA bfloat16 tensor [B, H, N, d]")
+    B, H, N, d = x.shape
+    shape = (B, H, d, N) if transpose_out else (B, H, N, d)
+    x8 = torch.empty(shape, device=x.device, dtype=torch.uint8)
+    sc = torch.empty((B, H, (N + 63) // 64), device=x.device, dtype=torch.float32)
+    st = lib.fa_quantize_fp8(_ptr(x), _ptr(x8), _ptr(sc), B, H, N, d, int(bool(hadamard)),
+                             int(bool(transpose_out)), _stream_handle(stream, x.device))
+    _check(st, "fa_quantize_fp8")
+    return x8, sc
+
+
+def attention_fp8(q8: torch.Tensor, k8: torch.Tensor, v8t: torch.Tensor, q_scale: torch.Tensor,
+                  k_scale: torch.Tensor, v_scale: torch.Tensor, causal: bool = False,
+                  scale: Optional[float] = None, hadamard: bool = False,
+                  out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                  return_lse: bool = True, stream: Optional[torch.cuda.Stream] = None):
+    """Attention forward from E4M3 codes (see ``quantize_fp8``); bf16 output."""
+    lib = load_library()
+    B, H, N, d = q8.shape
+    if k8.shape != q8.shape or v8t.shape != (B, H, d, N):
+        raise ValueError("k8 must be [B,H,N,d] and v8t [B,H,d,N]")
+    for t in (q8, k8, v8t, q_scale, k_scale, v_scale):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("all inputs must be contiguous CUDA tensors")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H, N, d), device=q8.device, dtype=torch.bfloat16)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), device=q8.device, dtype=torch.float32)
+    st = lib.fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8t), _ptr(out), _ptr(lse), B, H, N, d, float(scale),
+                        int(bool(causal)), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
+                        int(bool(hadamard)), _stream_handle(stream, q8.device))
+    _check(st, "fa_fwd_fp8")
+    return out, lse
+
+
+def last_device_status(stream: Optional[torch.cuda.Stream] = None) -> Tuple[int, int]:
+    """Synchronise and read/clear the device status word: (status, raw bits)."""
+    lib = load_library()
+    bits = ctypes.c_uint(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    st = lib.fa_last_device_status(_stream_handle(stream, dev), ctypes.byref(bits))
+    return st, bits.value
+
+
+def inject_stall(load_index: int, timeout_ms: int = 100) -> None:
+    """Test hook: the next ``attention`` call leaves out one K/V load (see include/fa.h)."""
+    _check(load_library().fa_debug_inject_stall(int(load_index), int(timeout_ms)), "fa_debug_inject_stall")

@@ -1,0 +1,209 @@
+// C ABI of libfa.so: argument validation, TMA descriptor encoding, launch, status.
+// The operations and their contracts are documented in include/fa.h.
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/fa.h"
+#include "fa_launch.h"
+#include "fa_params.h"
+
+namespace fa {
+
+// Per-device word that kernels set when a bounded wait gives up.
+__device__ unsigned int g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kUnitRows = 256;   // query rows per forward work unit (two 128-row tiles)
+
+struct DeviceInfo {
+  bool probed = false;
+  bool is_sm103 = false;
+  int sm_count = 0;
+  unsigned int* status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+int g_dbg_skip_load = -1;
+int g_dbg_timeout_ms = 0;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Current device's cached properties (probed once); nullptr if a CUDA call failed.
+const DeviceInfo* current_device(int* status) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *status = FA_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& di = g_dev[dev];
+  if (!di.probed) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      *status = FA_ERR_CUDA;
+      return nullptr;
+    }
+    di.is_sm103 = (major == 10 && minor == 3);
+    di.sm_count = sms;
+    if (di.is_sm103) {
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) {
+        *status = FA_ERR_CUDA;
+        return nullptr;
+      }
+      di.status = static_cast<unsigned int*>(ptr);
+    }
+    if (g_encode == nullptr) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        *status = FA_ERR_CUDA;
+        return nullptr;
+      }
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    di.probed = true;
+  }
+  if (!di.is_sm103) {
+    *status = FA_ERR_ARCH;
+    return nullptr;
+  }
+  *status = FA_OK;
+  return &di;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// 3-D tiled map over a contiguous [outer, rows, inner] tensor, box {box_inner, box_rows, 1},
+// 128-byte swizzle, out-of-bounds elements read as zero.
+bool encode_3d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const void* base,
+               uint64_t inner, uint64_t rows, uint64_t outer, uint32_t box_inner, uint32_t box_rows) {
+  const cuuint64_t dims[3] = {inner, rows, outer};
+  const cuuint64_t strides[2] = {inner * elem_bytes, inner * rows * elem_bytes};
+  const cuuint32_t box[3] = {box_inner, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+unsigned long long timeout_ns_for_call() {
+  if (g_dbg_timeout_ms > 0) return static_cast<unsigned long long>(g_dbg_timeout_ms) * 1000000ull;
+  const char* env = std::getenv("FA_TIMEOUT_MS");
+  long ms = env ? std::strtol(env, nullptr, 10) : 0;
+  if (ms <= 0) ms = 2000;
+  return static_cast<unsigned long long>(ms) * 1000000ull;
+}
+
+int check_shape(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long double total = static_cast<long double>(B) * H * N * d;
+  if (total >= static_cast<long double>(1ull << 40)) return FA_ERR_SHAPE;
+  if (static_cast<long long>(B) * H >= (1ll << 31)) return FA_ERR_SHAPE;
+  return FA_OK;
+}
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                      int N, int d, float scale, int causal, int dtype, void* stream) {
+  if (!q || !k || !v || !o) return FA_ERR_NULL;
+  if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+  if (causal != 0 && causal != 1) return FA_ERR_UNSUPPORTED;
+  int st = check_shape(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      (lse && !aligned(lse, 4)))
+    return FA_ERR_ALIGN;
+
+  const DeviceInfo* di = current_device(&st);
+  if (!di) return st;
+
+  FwdParams p;
+  const CUtensorMapDataType dt = dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const uint64_t BH = static_cast<uint64_t>(B) * H;
+  if (!encode_3d(&p.tm_q, dt, 2, q, d, N, BH, 64, 128) || !encode_3d(&p.tm_k, dt, 2, k, d, N, BH, 64, 128) ||
+      !encode_3d(&p.tm_v, dt, 2, v, d, N, BH, 64, 128))
+    return FA_ERR_CUDA;
+  p.o = o;
+  p.lse = lse;
+  p.status = di->status;
+  p.scale_log2 = scale * 1.44269504088896340736f;
+  p.N = N;
+  p.BH = static_cast<int>(BH);
+  p.n_qblk = (N + kUnitRows - 1) / kUnitRows;
+  const long long units = static_cast<long long>(p.n_qblk) * p.BH;
+  if (units >= (1ll << 31)) return FA_ERR_SHAPE;
+  p.num_units = static_cast<int>(units);
+  p.causal = causal;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    p.timeout_ns = timeout_ns_for_call();
+    p.dbg_skip_load = g_dbg_skip_load;
+    g_dbg_skip_load = -1;
+    g_dbg_timeout_ms = 0;
+  }
+  const int grid = static_cast<int>(units < di->sm_count ? units : di->sm_count);
+  const cudaError_t e = launch_fwd(d, dtype == FA_BF16, p, grid, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+extern "C" int fa_last_device_status(void* stream, unsigned int* bits) {
+  int st = FA_OK;
+  const DeviceInfo* di = current_device(&st);
+  if (!di) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_status_word, sizeof(word)) != cudaSuccess) return FA_ERR_CUDA;
+  const unsigned int zero = 0;
+  if (word != 0 && cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (bits) *bits = word;
+  return word == 0 ? FA_OK : FA_ERR_DEVICE_TIMEOUT;
+}
+
+extern "C" int fa_debug_inject_stall(int load_index, int timeout_ms) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_dbg_skip_load = load_index < 0 ? -1 : load_index;
+  g_dbg_timeout_ms = load_index < 0 ? 0 : (timeout_ms > 0 ? timeout_ms : 100);
+  return FA_OK;
+}
+
+extern "C" const char* fa_strerror(int status) {
+  switch (status) {
+    case FA_OK: return "success";
+    case FA_ERR_NULL: return "a required pointer is NULL";
+    case FA_ERR_ALIGN: return "a pointer is not aligned (16 bytes for tensors, 4 for LSE and scales)";
+    case FA_ERR_SHAPE: return "B, H or N out of range, or the sizes overflow";
+    case FA_ERR_UNSUPPORTED: return "unsupported head dim, dtype or flag value";
+    case FA_ERR_LAUNCH: return "kernel launch failed";
+    case FA_ERR_DEVICE_TIMEOUT: return "a kernel gave up on a pipeline wait (device status word set)";
+    case FA_ERR_ARCH: return "the current CUDA device is not an sm_103 GPU";
+    case FA_ERR_CUDA: return "a CUDA runtime or driver call failed";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int fa_version(void) { return 100; }

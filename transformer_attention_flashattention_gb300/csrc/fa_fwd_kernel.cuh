@@ -1,0 +1,427 @@
+// Attention forward, f16/bf16, head dim 64 or 128, for sm_103a.
+//
+// Computes O = softmax(scale * Q K^T [+ causal mask]) V and the per-row natural-log
+// LSE, tile by tile with an online softmax, so the N x N score matrix never leaves
+// the SM (the tiling and the streaming softmax with a running maximum and a
+// correction factor at each tile boundary are the method of "FlashAttention 2 + 3 —
+// speicherbewusste Attention-Kernels", sections "Kernpunkte" and "Begriffe auf
+// dieser Seite"; the asynchronous copy of the next block during compute and the
+// producer/consumer warp roles are the levers of the FlashAttention-3 news piece,
+// section "Drei technische Hebel", re-designed here for tcgen05/TMEM).
+//
+// One persistent CTA per SM walks work units (b*h, q-block of 256 rows = two
+// 128-row Q tiles).  Warp roles (384 threads, three warpgroups):
+//   warps 0-3   softmax warpgroup for Q tile 0 (thread i owns row i, TMEM lane i)
+//   warps 4-7   softmax warpgroup for Q tile 1
+//   warp  8     TMA producer: Q tiles, then K_j, V_j into a shared-memory ring
+//   warp  9     MMA issuer: S_t = Q_t K_j^T and O_t += P_t V_j on tcgen05, TMEM alloc
+//   warps 10-11 idle
+// The softmax warpgroups hold a whole 128-score row in registers, so registers move
+// to them (setmaxnreg): 2 x 128 threads x 224 + 128 x 56 = 384 x 168 at launch.
+// TMEM (512 columns): S_0 | S_1 | O_0 | O_1; P_t (16-bit, packed in pairs) overwrites
+// the first 64 columns of S_t and feeds the P.V MMA straight from TMEM.
+#pragma once
+
+#include "fa_params.h"
+#include "ptx.cuh"
+
+namespace fa {
+
+constexpr int kBlockM = 128;          // query rows per Q tile
+constexpr int kBlockN = 128;          // key rows per K/V tile
+constexpr int kQTiles = 2;            // Q tiles per work unit
+constexpr int kUnitRows = kBlockM * kQTiles;
+constexpr int kThreads = 384;
+constexpr uint32_t kSoftmaxRegs = 224;
+constexpr uint32_t kControlRegs = 56;
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+// The running max is only moved when it grows by more than 2^8 (log2 units): the
+// un-normalised weights then stay below 256, and the output and the sum are
+// rescaled far less often.  Exact in real arithmetic; the final division uses the
+// same stale maximum for numerator and denominator.
+constexpr float kRescaleThreshold = 8.0f;
+constexpr float kLn2 = 0.693147180559945309f;
+
+// Bits of the device status word.
+constexpr unsigned kStatusLoadTimeout = 1u;
+constexpr unsigned kStatusMmaTimeout = 2u;
+constexpr unsigned kStatusSoftmaxTimeout = 4u;
+constexpr unsigned kStatusDrainTimeout = 8u;
+
+template <int D>
+struct FwdSmem {
+  static_assert(D == 64 || D == 128, "head dim 64 or 128");
+  static constexpr int kAtoms = D / 64;                 // 128-byte swizzle atoms along d
+  static constexpr int kAtomBytes = kBlockM * 128;      // one atom of a 128-row tile
+  static constexpr int kTileBytes = kBlockM * D * 2;
+  static constexpr int kStages = D == 128 ? 5 : 8;
+  static constexpr int kQOff = 0;
+  static constexpr int kKVOff = kQOff + kQTiles * kTileBytes;
+  static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+  // barrier indices
+  static constexpr int kQFull = 0, kQEmpty = 2, kKVFull = 4, kKVEmpty = 4 + kStages;
+  static constexpr int kSFull = 4 + 2 * kStages, kPFull = kSFull + 2, kOFull = kPFull + 2;
+  static constexpr int kMmaDone = kOFull + 2;
+  static constexpr int kNumBars = kMmaDone + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM base slot, abort flag
+  static constexpr int kBytes = kMiscOff + 16;
+  static constexpr int kAlloc = kBytes + 1024;             // room to align the base to 1 KB
+  static constexpr uint32_t kTmemS = 0;                    // + t * 128
+  static constexpr uint32_t kTmemO = 256;                  // + t * D
+};
+
+__device__ __forceinline__ void decode_unit(const FwdParams& p, int u, int& bh, int& qb) {
+  if (p.causal) {
+    // longest rows first: the last q-blocks of every head, then the next-to-last, ...
+    qb = p.n_qblk - 1 - u / p.BH;
+    bh = u % p.BH;
+  } else {
+    // consecutive units share a head, so concurrently running CTAs reuse K/V in L2
+    bh = u / p.n_qblk;
+    qb = u % p.n_qblk;
+  }
+}
+
+// Number of K/V tiles Q tile t of q-block qb attends to (0 if the tile is past N).
+__device__ __forceinline__ int tile_nkv(const FwdParams& p, int qb, int t) {
+  const int r0 = qb * kUnitRows + t * kBlockM;
+  if (r0 >= p.N) return 0;
+  const int nkv = (p.N + kBlockN - 1) / kBlockN;
+  return p.causal ? min(nkv, r0 / kBlockN + 1) : nkv;
+}
+
+// ---------------------------------------------------------------------------- producer
+
+template <int D>
+__device__ __forceinline__ void fwd_producer(const FwdParams& p, uint32_t sbase,
+                                             const ptx::WaitCtl& ctl) {
+  using L = FwdSmem<D>;
+  auto bar = [&](int i) { return sbase + L::kBarOff + 8u * i; };
+  uint32_t load_idx = 0;
+  uint32_t q_fills[kQTiles] = {0, 0};
+  uint32_t last_fill[L::kStages];
+#pragma unroll
+  for (int s = 0; s < L::kStages; ++s) last_fill[s] = 0xFFFFFFFFu;
+
+  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    int bh, qb;
+    decode_unit(p, u, bh, qb);
+    const int n0 = tile_nkv(p, qb, 0), n1 = tile_nkv(p, qb, 1);
+    const int n = max(n0, n1);
+#pragma unroll
+    for (int t = 0; t < kQTiles; ++t) {
+      if ((t == 0 ? n0 : n1) == 0) continue;
+      if (!ptx::mbar_wait(bar(L::kQEmpty + t), (q_fills[t] & 1u) ^ 1u, ctl, kStatusLoadTimeout))
+        goto drain;
+      ptx::mbar_arrive_expect_tx(bar(L::kQFull + t), L::kTileBytes);
+#pragma unroll
+      for (int a = 0; a < L::kAtoms; ++a)
+        ptx::tma_load_3d(sbase + L::kQOff + t * L::kTileBytes + a * L::kAtomBytes, &p.tm_q,
+                         bar(L::kQFull + t), a * 64, qb * kUnitRows + t * kBlockM, bh);
+      ++q_fills[t];
+    }
+    for (int j = 0; j < n; ++j) {
+#pragma unroll
+      for (int kv = 0; kv < 2; ++kv) {
+        const uint32_t slot = load_idx % L::kStages;
+        const uint32_t fill = load_idx / L::kStages;
+        if (!ptx::mbar_wait(bar(L::kKVEmpty + slot), (fill & 1u) ^ 1u, ctl, kStatusLoadTimeout))
+          goto drain;
+        if (static_cast<int>(load_idx) != p.dbg_skip_load) {
+          ptx::mbar_arrive_expect_tx(bar(L::kKVFull + slot), L::kTileBytes);
+#pragma unroll
+          for (int a = 0; a < L::kAtoms; ++a)
+            ptx::tma_load_3d(sbase + L::kKVOff + slot * L::kTileBytes + a * L::kAtomBytes,
+                             kv == 0 ? &p.tm_k : &p.tm_v, bar(L::kKVFull + slot), a * 64,
+                             j * kBlockN, bh);
+          last_fill[slot] = fill;
+        }
+        ++load_idx;
+      }
+    }
+  }
+drain:
+  // Copies still in flight must land before the CTA may exit: wait for the latest
+  // issued fill of every slot (immediate on the normal path).
+  for (int s = 0; s < L::kStages; ++s)
+    if (last_fill[s] != 0xFFFFFFFFu &&
+        !ptx::mbar_wait_drain(bar(L::kKVFull + s), last_fill[s] & 1u, ctl.timeout_ns))
+      atomicOr(ctl.status, kStatusDrainTimeout);
+  for (int t = 0; t < kQTiles; ++t)
+    if (q_fills[t] > 0 &&
+        !ptx::mbar_wait_drain(bar(L::kQFull + t), (q_fills[t] - 1u) & 1u, ctl.timeout_ns))
+      atomicOr(ctl.status, kStatusDrainTimeout);
+}
+
+// ---------------------------------------------------------------------------- MMA issuer
+
+template <int D, bool BF16>
+__device__ __forceinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_t tmem,
+                                        const ptx::WaitCtl& ctl) {
+  using L = FwdSmem<D>;
+  auto bar = [&](int i) { return sbase + L::kBarOff + 8u * i; };
+  constexpr uint32_t kType = BF16 ? 1u : 0u;
+  constexpr uint32_t idesc_qk = ptx::idesc_make(kBlockM, kBlockN, kType, false, false);
+  constexpr uint32_t idesc_pv = ptx::idesc_make(kBlockM, D, kType, false, true);
+  uint32_t load_idx = 0;
+  uint32_t q_uses[kQTiles] = {0, 0};
+  uint32_t p_uses[kQTiles] = {0, 0};
+
+  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    int bh, qb;
+    decode_unit(p, u, bh, qb);
+    const int nt[kQTiles] = {tile_nkv(p, qb, 0), tile_nkv(p, qb, 1)};
+    const int n = max(nt[0], nt[1]);
+    for (int j = 0; j <= n; ++j) {
+      uint32_t kslot = 0, vslot = 0;
+      if (j < n) {
+        const uint32_t li = load_idx + 2u * j;
+        kslot = li % L::kStages;
+        if (!ptx::mbar_wait(bar(L::kKVFull + kslot), (li / L::kStages) & 1u, ctl, kStatusMmaTimeout))
+          goto done;
+      }
+      if (j >= 1) {
+        const uint32_t li = load_idx + 2u * (j - 1) + 1u;
+        vslot = li % L::kStages;
+        if (!ptx::mbar_wait(bar(L::kKVFull + vslot), (li / L::kStages) & 1u, ctl, kStatusMmaTimeout))
+          goto done;
+      }
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int t = 0; t < kQTiles; ++t) {
+        if (j >= 1 && j - 1 < nt[t]) {
+          // O_t += P_t V_{j-1}
+          if (!ptx::mbar_wait(bar(L::kPFull + t), p_uses[t] & 1u, ctl, kStatusMmaTimeout)) goto done;
+          ++p_uses[t];
+          ptx::tc_fence_after();
+          const uint32_t vbase = sbase + L::kKVOff + vslot * L::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < kBlockN / 16; ++kk) {
+            // B = V tile, MN-major (d contiguous): 16 key rows per step, atoms along d 16 KB apart
+            const uint64_t bdesc = ptx::sdesc_sw128(vbase + kk * 16 * 128, L::kAtomBytes, 1024);
+            ptx::mma_f16_ts(tmem + L::kTmemO + t * D, tmem + L::kTmemS + t * kBlockN + kk * 8, bdesc,
+                            idesc_pv, (j - 1 > 0 || kk > 0) ? 1u : 0u);
+          }
+          if (j - 1 == nt[t] - 1) ptx::mma_commit(bar(L::kOFull + t));
+        }
+        if (j < nt[t]) {
+          // S_t = Q_t K_j^T
+          if (j == 0) {
+            if (!ptx::mbar_wait(bar(L::kQFull + t), q_uses[t] & 1u, ctl, kStatusMmaTimeout)) goto done;
+            ++q_uses[t];
+            ptx::tc_fence_after();
+          }
+          const uint32_t qbase = sbase + L::kQOff + t * L::kTileBytes;
+          const uint32_t kbase = sbase + L::kKVOff + kslot * L::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            // K-major operands: 16 elements (32 bytes) per step inside a 128-byte swizzle atom
+            const uint32_t off = (kk / 4) * L::kAtomBytes + (kk % 4) * 32;
+            ptx::mma_f16_ss(tmem + L::kTmemS + t * kBlockN, ptx::sdesc_sw128(qbase + off, 16, 1024),
+                            ptx::sdesc_sw128(kbase + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(bar(L::kSFull + t));
+          if (j == nt[t] - 1) ptx::mma_commit(bar(L::kQEmpty + t));
+        }
+      }
+      if (j >= 1) ptx::mma_commit(bar(L::kKVEmpty + vslot));
+      if (j < n) ptx::mma_commit(bar(L::kKVEmpty + kslot));
+    }
+    load_idx += 2u * n;
+  }
+done:
+  // Every MMA issued so far must finish before TMEM is released.
+  ptx::mma_commit(bar(L::kMmaDone));
+  if (!ptx::mbar_wait_drain(bar(L::kMmaDone), 0, ctl.timeout_ns)) atomicOr(ctl.status, kStatusDrainTimeout);
+}
+
+// ---------------------------------------------------------------------------- softmax
+
+template <int D, bool BF16>
+__device__ __forceinline__ void fwd_softmax(const FwdParams& p, int t, uint32_t sbase, uint32_t tmem,
+                                            const ptx::WaitCtl& ctl) {
+  using L = FwdSmem<D>;
+  auto bar = [&](int i) { return sbase + L::kBarOff + 8u * i; };
+  const int r = threadIdx.x - t * kBlockM;                          // row within the tile
+  const uint32_t lane_base = static_cast<uint32_t>((threadIdx.x / 32) & 3) * 32u;
+  const uint32_t tS = tmem + (lane_base << 16) + L::kTmemS + t * kBlockN;
+  const uint32_t tO = tmem + (lane_base << 16) + L::kTmemO + t * D;
+  const float sl2 = p.scale_log2;
+  uint32_t s_uses = 0, o_uses = 0;
+  const int lane = threadIdx.x & 31;
+
+  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    int bh, qb;
+    decode_unit(p, u, bh, qb);
+    const int ntile = tile_nkv(p, qb, t);
+    if (ntile == 0) continue;
+    const int r0 = qb * kUnitRows + t * kBlockM;
+    const int row = r0 + r;
+    float m = -INFINITY, l = 0.f;
+
+    for (int j = 0; j < ntile; ++j) {
+      const bool got = ptx::mbar_wait(bar(L::kSFull + t), s_uses & 1u, ctl, kStatusSoftmaxTimeout);
+      if (!__all_sync(0xFFFFFFFFu, got)) return;
+      ++s_uses;
+      ptx::tc_fence_after();
+
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + 32 * c, sr[c]);
+      ptx::tmem_wait_ld();
+
+      const int col0 = j * kBlockN;
+      if (col0 + kBlockN > p.N || (p.causal && col0 + kBlockN - 1 > r0)) {
+#pragma unroll
+        for (int c = 0; c < kBlockN; ++c) {
+          const int col = col0 + c;
+          if (col >= p.N || (p.causal && col > row)) sr[c / 32][c % 32] = __float_as_uint(-INFINITY);
+        }
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kBlockN; ++c) mx = fmaxf(mx, __uint_as_float(sr[c / 32][c % 32]));
+      const float m_new = fmaxf(m, mx * sl2);
+
+      float m_use, alpha = 1.f;
+      bool rescale_o = false;
+      if (j == 0) {
+        m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      } else {
+        const bool need = m_new > m + kRescaleThreshold;
+        m_use = need ? m_new : m;
+        alpha = need ? ptx::ex2(m - m_new) : 1.f;
+        rescale_o = __any_sync(0xFFFFFFFFu, need);
+      }
+
+      // P = 2^(s * scale * log2 e - m), packed in pairs; row sum in fp32
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+      for (int c = 0; c < kBlockN / 2; ++c) {
+        const float p0 = ptx::ex2(fmaf(__uint_as_float(sr[(2 * c) / 32][(2 * c) % 32]), sl2, -m_use));
+        const float p1 = ptx::ex2(fmaf(__uint_as_float(sr[(2 * c + 1) / 32][(2 * c + 1) % 32]), sl2, -m_use));
+        sum0 += p0;
+        sum1 += p1;
+        sr[c / 32][c % 32] = ptx::pack2<BF16>(p0, p1);   // packed P overwrites consumed scores
+      }
+      l = l * alpha + (sum0 + sum1);
+
+      if (rescale_o) {
+        // The previous O_t += P V has completed: the S_t commit that woke us tracks it.
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t orr[32];
+          ptx::tmem_ld32(tO + 32 * c, orr);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+          ptx::tmem_st32(tO + 32 * c, orr);
+        }
+      }
+      ptx::tmem_st32(tS + 0, sr[0]);
+      ptx::tmem_st32(tS + 32, sr[1]);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(L::kPFull + t));
+      m = m_use;
+    }
+
+    // epilogue: O = O_acc / l, LSE = ln 2 * (m + log2 l)
+    const bool got = ptx::mbar_wait(bar(L::kOFull + t), o_uses & 1u, ctl, kStatusSoftmaxTimeout);
+    if (!__all_sync(0xFFFFFFFFu, got)) return;
+    ++o_uses;
+    ptx::tc_fence_after();
+    const float inv_l = l > 0.f ? 1.f / l : 0.f;
+    const bool live = row < p.N;
+    uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
+                                           (static_cast<size_t>(bh) * p.N + (live ? row : 0)) * D);
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t orr[32];
+      ptx::tmem_ld32(tO + 32 * c, orr);
+      ptx::tmem_wait_ld();
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        pk[i] = ptx::pack2<BF16>(__uint_as_float(orr[2 * i]) * inv_l, __uint_as_float(orr[2 * i + 1]) * inv_l);
+      if (live) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) orow[c * 4 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      }
+    }
+    if (live && p.lse != nullptr)
+      p.lse[static_cast<size_t>(bh) * p.N + row] = l > 0.f ? (m + ptx::lg2(l)) * kLn2 : -INFINITY;
+    ptx::tc_fence_before();
+  }
+}
+
+// ---------------------------------------------------------------------------- kernel
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using L = FwdSmem<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = ptx::smem_u32(smem);
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+
+  if (threadIdx.x == 0) {
+    auto bar = [&](int i) { return sbase + L::kBarOff + 8u * i; };
+    for (int t = 0; t < kQTiles; ++t) {
+      ptx::mbar_init(bar(L::kQFull + t), 1);
+      ptx::mbar_init(bar(L::kQEmpty + t), 1);
+      ptx::mbar_init(bar(L::kSFull + t), 1);
+      ptx::mbar_init(bar(L::kPFull + t), 4);   // one arrival per softmax warp
+      ptx::mbar_init(bar(L::kOFull + t), 1);
+    }
+    for (int s = 0; s < L::kStages; ++s) {
+      ptx::mbar_init(bar(L::kKVFull + s), 1);
+      ptx::mbar_init(bar(L::kKVEmpty + s), 1);
+    }
+    ptx::mbar_init(bar(L::kMmaDone), 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    ptx::prefetch_tensormap(&p.tm_q);
+    ptx::prefetch_tensormap(&p.tm_k);
+    ptx::prefetch_tensormap(&p.tm_v);
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const ptx::WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+
+  if (warp >= 8) {
+    ptx::setmaxnreg_dec<kControlRegs>();
+    if (warp == kLoadWarp) {
+      if (lane == 0) fwd_producer<D>(p, sbase, ctl);
+    } else if (warp == kMmaWarp) {
+      if (lane == 0) fwd_mma<D, BF16>(p, sbase, tmem, ctl);
+    }
+  } else {
+    ptx::setmaxnreg_inc<kSoftmaxRegs>();
+    fwd_softmax<D, BF16>(p, warp / 4, sbase, tmem, ctl);
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace fa
