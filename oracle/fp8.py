@@ -60,10 +60,13 @@ def sylvester_hadamard(d: int) -> np.ndarray:
 
 
 def hadamard_rotate(x) -> np.ndarray:
-    """x @ H_d / sqrt(d) along the last axis, in fp64."""
+    """x @ H_d / sqrt(d) along the last axis, in fp64.
+
+    The +-1 matrix is applied first (sums of the inputs, exact in fp64 for
+    bf16 data) and the result divided by sqrt(d) once."""
     x = _f64(x)
     d = x.shape[-1]
-    return x @ (sylvester_hadamard(d) / np.sqrt(d))
+    return (x @ sylvester_hadamard(d)) / np.sqrt(d)
 
 
 def round_to_e4m3(x) -> np.ndarray:

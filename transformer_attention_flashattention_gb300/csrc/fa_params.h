@@ -9,10 +9,10 @@
 namespace fa {
 
 struct FwdParams {
-  CUtensorMap tm_q;   // 3-D {d, N, B*H}, box {64, 128, 1}, 128-byte swizzle
+  CUtensorMap tm_q;   // 3-D {d, N, B*H}, box {128 bytes of d, 128 rows, 1}, 128-byte swizzle
   CUtensorMap tm_k;
-  CUtensorMap tm_v;
-  void* o;            // [B, H, N, d], same 16-bit type as Q
+  CUtensorMap tm_v;   // as Q for 16-bit inputs; E4M3: V^T, 3-D {N, d, B*H}, box {128, 128, 1}
+  void* o;            // [B, H, N, d]: the input type for 16-bit inputs, bf16 for E4M3
   float* lse;         // [B, H, N] or nullptr
   unsigned int* status;
   unsigned long long timeout_ns;
@@ -23,6 +23,24 @@ struct FwdParams {
   int num_units;      // BH * n_qblk
   int causal;
   int dbg_skip_load;  // K/V load index the producer leaves out (fault-path test), -1 = none
+  // E4M3 path only: per-(b*h, 64-row block) dequantisation scales, [B*H, n_sblk]
+  const float* q_scale;
+  const float* k_scale;
+  const float* v_scale;
+  int n_sblk;         // ceil(N / 64)
+};
+
+// FP8 prologue: block absmax E4M3 quantisation with an optional Hadamard rotation.
+struct QuantParams {
+  const void* x;      // bf16 [B*H, N, d]
+  uint8_t* x8;        // e4m3 [B*H, N, d], or [B*H, d, N] when transpose_out
+  float* scale;       // [B*H, n_sblk]
+  int N;
+  int d;
+  int BH;
+  int n_sblk;
+  int hadamard;
+  int transpose_out;
 };
 
 }  // namespace fa
