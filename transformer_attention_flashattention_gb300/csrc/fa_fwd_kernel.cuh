@@ -18,7 +18,9 @@
 //   warp  9     MMA issuer: S_t = Q_t K_j^T and O_t += P_t V_j on tcgen05, TMEM alloc
 //   warps 10-11 idle
 // The softmax warpgroups hold a whole 128-score row in registers, so registers move
-// to them (setmaxnreg): 2 x 128 threads x 224 + 128 x 56 = 384 x 168 at launch.
+// to them (setmaxnreg): 2 x 128 threads x 216 + 128 x 72 = 384 x 168 at launch.  The
+// producer and MMA roles are separate (non-inlined) functions so that nothing the
+// softmax code keeps live has to fit the control warps' 72 registers.
 // TMEM (512 columns): S_0 | S_1 | O_0 | O_1.  P_t overwrites the first columns of
 // S_t (two 16-bit or four E4M3 values per column) and feeds the P.V MMA from TMEM.
 //
@@ -40,8 +42,8 @@ constexpr int kBlockN = 128;          // key rows per K/V tile
 constexpr int kQTiles = 2;            // Q tiles per work unit
 constexpr int kUnitRows = kBlockM * kQTiles;
 constexpr int kThreads = 384;
-constexpr uint32_t kSoftmaxRegs = 224;
-constexpr uint32_t kControlRegs = 56;
+constexpr uint32_t kSoftmaxRegs = 216;
+constexpr uint32_t kControlRegs = 72;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
@@ -115,7 +117,7 @@ __device__ __forceinline__ int tile_nkv(const FwdParams& p, int qb, int t) {
 // ---------------------------------------------------------------------------- producer
 
 template <int D, Elem E>
-__device__ __forceinline__ void fwd_producer(const FwdParams& p, uint32_t sbase,
+__device__ __noinline__ void fwd_producer(const FwdParams& p, uint32_t sbase,
                                              const ptx::WaitCtl& ctl) {
   using L = FwdCfg<D, E>;
   auto bar = [&](int i) { return sbase + L::kBarOff + 8u * i; };
@@ -183,7 +185,7 @@ drain:
 // ---------------------------------------------------------------------------- MMA issuer
 
 template <int D, Elem E>
-__device__ __forceinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_t tmem,
+__device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_t tmem,
                                         const ptx::WaitCtl& ctl) {
   using L = FwdCfg<D, E>;
   auto bar = [&](int i) { return sbase + L::kBarOff + 8u * i; };
@@ -324,6 +326,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, int t, uint32_t 
       ptx::tc_fence_after();
 
       uint32_t sr[4][32];
+#define S_(c) __uint_as_float(sr[(c) / 32][(c) % 32])
 #pragma unroll
       for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + 32 * c, sr[c]);
 
@@ -340,19 +343,28 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, int t, uint32_t 
 
       const int col0 = j * kBlockN;
       if (col0 + kBlockN > p.N || (p.causal && col0 + kBlockN - 1 > r0)) {
+        // columns c >= visible of this tile are masked (past N, or past the diagonal)
+        const int visible = (p.causal ? min(p.N, row + 1) : p.N) - col0;
 #pragma unroll
-        for (int c = 0; c < kBlockN; ++c) {
-          const int col = col0 + c;
-          if (col >= p.N || (p.causal && col > row)) sr[c / 32][c % 32] = __float_as_uint(-INFINITY);
+        for (int c = 0; c < kBlockN; ++c)
+          if (c >= visible) sr[c / 32][c % 32] = __float_as_uint(-INFINITY);
+      }
+      // row maxima of the two 64-column halves: 3-input max trees, 4 chains per half
+      float mh[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float acc[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          const int b = 64 * h + 16 * a;
+          float x = ptx::max3(S_(b), S_(b + 1), S_(b + 2));
+#pragma unroll
+          for (int i = 3; i < 15; i += 2) x = ptx::max3(x, S_(b + i), S_(b + i + 1));
+          acc[a] = fmaxf(x, S_(b + 15));
         }
+        mh[h] = ptx::max3(acc[0], acc[1], fmaxf(acc[2], acc[3]));
       }
-      float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < kBlockN / 2; ++c) {
-        mx0 = fmaxf(mx0, __uint_as_float(sr[c / 32][c % 32]));
-        mx1 = fmaxf(mx1, __uint_as_float(sr[(c + 64) / 32][(c + 64) % 32]));
-      }
-      const float m_new = fmaxf(m, fmaxf(mx0 * f0, mx1 * f1));
+      const float m_new = fmaxf(m, fmaxf(mh[0] * f0, mh[1] * f1));
 
       float m_use, alpha = 1.f;
       bool rescale_o = false;
@@ -364,34 +376,41 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, int t, uint32_t 
         alpha = need ? ptx::ex2(m - m_new) : 1.f;
         rescale_o = __any_sync(0xFFFFFFFFu, need);
       }
-      const float nb0 = b0 - m_use, nb1 = b1 - m_use;
 
-      // P = 2^(s * f - m) (times V's relative block scale for E4M3), packed for the MMA
-      float sum0 = 0.f, sum1 = 0.f;
-      if constexpr (L::kFp8) {
+      // P = 2^(s * f - m) (times V's relative block scale for E4M3), packed for the MMA;
+      // s * f - m in packed pairs, row sums in 4 packed accumulators per half
+      float2 hs[2];
 #pragma unroll
-        for (int c = 0; c < kBlockN / 4; ++c) {
-          const bool hi = c >= kBlockN / 8;
-          const float f = hi ? f1 : f0, nb = hi ? nb1 : nb0;
-          float pv[4];
+      for (int h = 0; h < 2; ++h) {
+        const float2 fh = make_float2(h ? f1 : f0, h ? f1 : f0);
+        const float nbh = (h ? b1 : b0) - m_use;
+        const float2 nb = make_float2(nbh, nbh);
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            pv[e] = ptx::ex2(fmaf(__uint_as_float(sr[(4 * c + e) / 32][(4 * c + e) % 32]), f, nb));
-          if (hi) sum1 += (pv[0] + pv[1]) + (pv[2] + pv[3]);
-          else sum0 += (pv[0] + pv[1]) + (pv[2] + pv[3]);
-          sr[c / 32][c % 32] = ptx::pack4_e4m3(pv[0], pv[1], pv[2], pv[3]);
+        for (int q = 0; q < 16; ++q) {           // four columns per step
+          const int c = 64 * h + 4 * q;
+          const float2 x01 = ptx::fma2(make_float2(S_(c), S_(c + 1)), fh, nb);
+          const float2 x23 = ptx::fma2(make_float2(S_(c + 2), S_(c + 3)), fh, nb);
+          const float2 p01 = make_float2(ptx::ex2(x01.x), ptx::ex2(x01.y));
+          const float2 p23 = make_float2(ptx::ex2(x23.x), ptx::ex2(x23.y));
+          acc[q & 3] = ptx::add2(acc[q & 3], ptx::add2(p01, p23));
+          // packed P overwrites scores already consumed (slot index <= c)
+          if constexpr (L::kFp8) {
+            sr[(c / 4) / 32][(c / 4) % 32] = ptx::pack4_e4m3(p01.x, p01.y, p23.x, p23.y);
+          } else {
+            sr[(c / 2) / 32][(c / 2) % 32] = ptx::pack2<L::kBf16Out>(p01.x, p01.y);
+            sr[(c / 2 + 1) / 32][(c / 2 + 1) % 32] = ptx::pack2<L::kBf16Out>(p23.x, p23.y);
+          }
         }
+        const float2 t = ptx::add2(ptx::add2(acc[0], acc[1]), ptx::add2(acc[2], acc[3]));
+        hs[h] = t;
+      }
+      const float sum0 = hs[0].x + hs[0].y, sum1 = hs[1].x + hs[1].y;
+      if constexpr (L::kFp8) {
         // row sum of P itself: divide V's relative scale back out of each half
         l = l * alpha + (sum0 * ptx::ex2(-b0) + sum1 * ptx::ex2(-b1));
       } else {
-#pragma unroll
-        for (int c = 0; c < kBlockN / 2; ++c) {
-          const float p0 = ptx::ex2(fmaf(__uint_as_float(sr[(2 * c) / 32][(2 * c) % 32]), sl2, -m_use));
-          const float p1 = ptx::ex2(fmaf(__uint_as_float(sr[(2 * c + 1) / 32][(2 * c + 1) % 32]), sl2, -m_use));
-          sum0 += p0;
-          sum1 += p1;
-          sr[c / 32][c % 32] = ptx::pack2<L::kBf16Out>(p0, p1);   // packed P overwrites consumed scores
-        }
         l = l * alpha + (sum0 + sum1);
       }
 
@@ -403,10 +422,16 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, int t, uint32_t 
           ptx::tmem_ld32(tO + 32 * c, orr);
           ptx::tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+          for (int i = 0; i < 32; i += 2) {
+            const float2 v = ptx::mul2(make_float2(__uint_as_float(orr[i]), __uint_as_float(orr[i + 1])),
+                                       make_float2(alpha, alpha));
+            orr[i] = __float_as_uint(v.x);
+            orr[i + 1] = __float_as_uint(v.y);
+          }
           ptx::tmem_st32(tO + 32 * c, orr);
         }
       }
+#undef S_
       ptx::tmem_st32(tS + 0, sr[0]);
       if constexpr (!L::kFp8) ptx::tmem_st32(tS + 32, sr[1]);
       ptx::tmem_wait_st();
@@ -432,9 +457,11 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, int t, uint32_t 
       ptx::tmem_wait_ld();
       uint32_t pk[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        pk[i] = ptx::pack2<L::kBf16Out>(__uint_as_float(orr[2 * i]) * inv_l,
-                                         __uint_as_float(orr[2 * i + 1]) * inv_l);
+      for (int i = 0; i < 16; ++i) {
+        const float2 v = ptx::mul2(make_float2(__uint_as_float(orr[2 * i]), __uint_as_float(orr[2 * i + 1])),
+                                   make_float2(inv_l, inv_l));
+        pk[i] = ptx::pack2<L::kBf16Out>(v.x, v.y);
+      }
       if (live) {
 #pragma unroll
         for (int i = 0; i < 4; ++i)
