@@ -114,6 +114,13 @@ __device__ __forceinline__ int tile_nkv(const FwdParams& p, int qb, int t) {
   return p.causal ? min(nkv, r0 / kBlockN + 1) : nkv;
 }
 
+// Order of the K/V loads of a unit with n key tiles: K_0, K_1, V_0, K_2, V_1, ...,
+// K_{n-1}, V_{n-2}, V_{n-1}.  K runs one tile ahead of V, matching the MMA order
+// (S_t(j) needs K_j one step before O_t += P_t V_j), so the ring holds about two
+// steps of lead for both operands.
+__device__ __forceinline__ uint32_t k_pos(int j) { return j == 0 ? 0u : 2u * j - 1u; }
+__device__ __forceinline__ uint32_t v_pos(int j, int n) { return j + 1 < n ? 2u * j + 2u : 2u * n - 1u; }
+
 // ---------------------------------------------------------------------------- producer
 
 template <int D, Elem E>
@@ -144,9 +151,12 @@ __device__ __noinline__ void fwd_producer(const FwdParams& p, uint32_t sbase,
                          bar(L::kQFull + t), a * L::kAtomElems, qb * kUnitRows + t * kBlockM, bh);
       ++q_fills[t];
     }
-    for (int j = 0; j < n; ++j) {
-#pragma unroll
-      for (int kv = 0; kv < 2; ++kv) {
+    for (int pos = 0; pos < 2 * n; ++pos) {
+      // position -> (K or V, tile j), the inverse of k_pos / v_pos
+      const bool is_k = pos == 0 || ((pos & 1) && (pos + 1) / 2 < n);
+      const int kv = is_k ? 0 : 1;
+      const int j = is_k ? (pos + 1) / 2 : (pos == 2 * n - 1 ? n - 1 : pos / 2 - 1);
+      {
         const uint32_t slot = load_idx % L::kStages;
         const uint32_t fill = load_idx / L::kStages;
         if (!ptx::mbar_wait(bar(L::kKVEmpty + slot), (fill & 1u) ^ 1u, ctl, kStatusLoadTimeout))
@@ -203,19 +213,13 @@ __device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_
     const int n = max(nt[0], nt[1]);
     for (int j = 0; j <= n; ++j) {
       uint32_t kslot = 0, vslot = 0;
-      if (j < n) {
-        const uint32_t li = load_idx + 2u * j;
-        kslot = li % L::kStages;
-        if (!ptx::mbar_wait(bar(L::kKVFull + kslot), (li / L::kStages) & 1u, ctl, kStatusMmaTimeout))
-          goto done;
-      }
+      bool k_ready = false;
       if (j >= 1) {
-        const uint32_t li = load_idx + 2u * (j - 1) + 1u;
+        const uint32_t li = load_idx + v_pos(j - 1, n);
         vslot = li % L::kStages;
         if (!ptx::mbar_wait(bar(L::kKVFull + vslot), (li / L::kStages) & 1u, ctl, kStatusMmaTimeout))
           goto done;
       }
-      ptx::tc_fence_after();
 #pragma unroll
       for (int t = 0; t < kQTiles; ++t) {
         if (j >= 1 && j - 1 < nt[t]) {
@@ -242,11 +246,18 @@ __device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_
         }
         if (j < nt[t]) {
           // S_t = Q_t K_j^T
+          if (!k_ready) {
+            const uint32_t li = load_idx + k_pos(j);
+            kslot = li % L::kStages;
+            if (!ptx::mbar_wait(bar(L::kKVFull + kslot), (li / L::kStages) & 1u, ctl, kStatusMmaTimeout))
+              goto done;
+            k_ready = true;
+          }
           if (j == 0) {
             if (!ptx::mbar_wait(bar(L::kQFull + t), q_uses[t] & 1u, ctl, kStatusMmaTimeout)) goto done;
             ++q_uses[t];
-            ptx::tc_fence_after();
           }
+          ptx::tc_fence_after();
           const uint32_t qbase = sbase + L::kQOff + t * L::kTileBytes;
           const uint32_t kbase = sbase + L::kKVOff + kslot * L::kTileBytes;
 #pragma unroll
@@ -265,7 +276,7 @@ __device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_
         }
       }
       if (j >= 1) ptx::mma_commit(bar(L::kKVEmpty + vslot));
-      if (j < n) ptx::mma_commit(bar(L::kKVEmpty + kslot));
+      if (k_ready) ptx::mma_commit(bar(L::kKVEmpty + kslot));
     }
     load_idx += 2u * n;
   }
