@@ -15,9 +15,8 @@
 //   warps 0-3   softmax warpgroup for Q tile 0 (thread i owns row i, TMEM lane i)
 //   warps 4-7   softmax warpgroup for Q tile 1
 //   warp  8     TMA producer: Q tiles, then K_j, V_j into a shared-memory ring
-//   warps 9, 10 MMA issuers, one per Q tile: S_t = Q_t K_j^T, O_t += P_t V_j on tcgen05
-//               (warp 9 also allocates TMEM)
-//   warp  11    idle
+//   warp  9     MMA issuer: S_t = Q_t K_j^T and O_t += P_t V_j on tcgen05, TMEM alloc
+//   warps 10-11 idle
 // The softmax warpgroups hold a whole 128-score row in registers, so registers move
 // to them (setmaxnreg): 2 x 128 threads x 216 + 128 x 72 = 384 x 168 at launch.  The
 // producer and MMA roles are separate (non-inlined) functions so that nothing the
@@ -86,7 +85,7 @@ struct FwdCfg {
   static constexpr int kQFull = 0, kQEmpty = 2, kKVFull = 4, kKVEmpty = 4 + kStages;
   static constexpr int kSFull = 4 + 2 * kStages, kPFull = kSFull + 2, kOFull = kPFull + 2;
   static constexpr int kMmaDone = kOFull + 2;
-  static constexpr int kNumBars = kMmaDone + 2;
+  static constexpr int kNumBars = kMmaDone + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM base slot, abort flag
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes + 1024;             // room to align the base to 1 KB
@@ -193,109 +192,122 @@ drain:
       atomicOr(ctl.status, kStatusDrainTimeout);
 }
 
-// ---------------------------------------------------------------------------- MMA issuers
+// ---------------------------------------------------------------------------- MMA issuer
 
-// One thread per Q tile issues that tile's MMAs: S_t = Q_t K_j^T and O_t += P_t V_j.
-// tcgen05.mma issue blocks while the tensor pipe's short queue is full, so every
-// instruction or barrier wait between two issues is idle tensor time; with two
-// issuers, one tile's MMAs keep the pipe busy while the other tile's thread waits
-// for its P or its K/V stage.  Each thread's MMAs run in issue order, which is
-// what lets S_t(j+1) overwrite the TMEM holding P_t(j) after O_t += P_t(j) V_j.
-// A K/V stage is free once both threads released it (a commit after their MMAs
-// read it, or a plain arrive if the tile does not use that stage).
+// PV and S MMAs of Q tile t for key step j (called by the single MMA thread).
 template <int D, Elem E>
-__device__ __noinline__ void fwd_mma(const FwdParams& p, int t, uint32_t sbase, uint32_t tmem,
+__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tS, uint32_t vbase, bool accumulate) {
+  using L = FwdCfg<D, E>;
+  constexpr uint32_t idesc_pv = ptx::idesc_make(kBlockM, D, L::kAbType, false, !L::kFp8);
+  constexpr uint32_t desc_hi = ptx::sdesc_hi(1024);
+  if constexpr (L::kFp8) {
+    // V^T rows (d) of 128 key bytes: 32 keys (32 bytes) per step inside the atom
+    const uint32_t v_lo = ptx::sdesc_lo(vbase, 16);
+    if (accumulate) ptx::mma_f8_ts_c<1>(tO, tS, v_lo, desc_hi, idesc_pv);
+    else ptx::mma_f8_ts_c<0>(tO, tS, v_lo, desc_hi, idesc_pv);
+#pragma unroll
+    for (int kk = 1; kk < L::kPvSteps; ++kk)
+      ptx::mma_f8_ts_c<1>(tO, tS + kk * 8, v_lo + ((kk * 32) >> 4), desc_hi, idesc_pv);
+  } else {
+    // V is [N, d] (MN-major B): 16 key rows (2 KB) per step; 64-wide d atoms 16 KB apart
+    const uint32_t v_lo = ptx::sdesc_lo(vbase, L::kAtomBytes);
+    if (accumulate) ptx::mma_f16_ts_c<1>(tO, tS, v_lo, desc_hi, idesc_pv);
+    else ptx::mma_f16_ts_c<0>(tO, tS, v_lo, desc_hi, idesc_pv);
+#pragma unroll
+    for (int kk = 1; kk < L::kPvSteps; ++kk)
+      ptx::mma_f16_ts_c<1>(tO, tS + kk * 8, v_lo + ((kk * 16 * 128) >> 4), desc_hi, idesc_pv);
+  }
+}
+
+template <int D, Elem E>
+__device__ __forceinline__ void issue_s(uint32_t tS, uint32_t q_lo, uint32_t k_lo) {
+  using L = FwdCfg<D, E>;
+  constexpr uint32_t idesc_qk = ptx::idesc_make(kBlockM, kBlockN, L::kAbType, false, false);
+  constexpr uint32_t desc_hi = ptx::sdesc_hi(1024);
+  // K-major operands: 32 bytes of d per step inside a 128-byte swizzle atom
+#pragma unroll
+  for (int kk = 0; kk < D / L::kMmaK; ++kk) {
+    const uint32_t off = ((kk * 32 / 128) * L::kAtomBytes + (kk * 32) % 128) >> 4;
+    if constexpr (L::kFp8) {
+      if (kk == 0) ptx::mma_f8_ss_c<0>(tS, q_lo, desc_hi, k_lo, desc_hi, idesc_qk);
+      else ptx::mma_f8_ss_c<1>(tS, q_lo + off, desc_hi, k_lo + off, desc_hi, idesc_qk);
+    } else {
+      if (kk == 0) ptx::mma_f16_ss_c<0>(tS, q_lo, desc_hi, k_lo, desc_hi, idesc_qk);
+      else ptx::mma_f16_ss_c<1>(tS, q_lo + off, desc_hi, k_lo + off, desc_hi, idesc_qk);
+    }
+  }
+}
+
+// One thread issues every MMA, in the order
+//   O_0 += P_0 V_{j-1};  S_0 = Q_0 K_j^T;  O_1 += P_1 V_{j-1};  S_1 = Q_1 K_j^T
+// so the tensor pipe runs one tile's pair while the other tile's softmax works.
+// tcgen05.mma issue blocks on a very short queue, so the thread does as little as
+// possible between issues: descriptors are a precomputed base plus a constant, and
+// accumulate flags are compile-time constants.  MMAs run in issue order, which is
+// what lets S_t(j+1) overwrite the TMEM holding P_t(j) after O_t += P_t(j) V_j.
+template <int D, Elem E>
+__device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_t tmem,
                                      const ptx::WaitCtl& ctl) {
   using L = FwdCfg<D, E>;
   auto bar = [&](int i) { return sbase + L::kBarOff + 8u * i; };
-  constexpr uint32_t idesc_qk = ptx::idesc_make(kBlockM, kBlockN, L::kAbType, false, false);
-  // 16-bit V is [N, d] in shared memory (d contiguous): MN-major B.  E4M3 V^T is K-major.
-  constexpr uint32_t idesc_pv = ptx::idesc_make(kBlockM, D, L::kAbType, false, !L::kFp8);
-  constexpr uint32_t desc_hi = ptx::sdesc_hi(1024);      // 8-row groups 1 KB apart, 128-byte swizzle
-  const uint32_t q_lo = ptx::sdesc_lo(sbase + L::kQOff + t * L::kTileBytes, 16);
-  const uint32_t tS = tmem + L::kTmemS + t * kBlockN;
-  const uint32_t tO = tmem + L::kTmemO + t * D;
-  uint32_t load_idx = 0, q_uses = 0, p_uses = 0;
+  const uint32_t q_lo0 = ptx::sdesc_lo(sbase + L::kQOff, 16);
+  const uint32_t q_lo1 = ptx::sdesc_lo(sbase + L::kQOff + L::kTileBytes, 16);
+  uint32_t load_idx = 0;
+  uint32_t q_uses[kQTiles] = {0, 0};
+  uint32_t p_uses[kQTiles] = {0, 0};
 
   for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
     int bh, qb;
     decode_unit(p, u, bh, qb);
-    const int nt = tile_nkv(p, qb, t);
-    const int n = max(tile_nkv(p, qb, 0), tile_nkv(p, qb, 1));
+    const int nt[kQTiles] = {tile_nkv(p, qb, 0), tile_nkv(p, qb, 1)};
+    const int n = max(nt[0], nt[1]);
     for (int j = 0; j <= n; ++j) {
+      uint32_t kslot = 0, vslot = 0;
+      bool k_ready = false;
       if (j >= 1) {
-        // O_t += P_t V_{j-1}
         const uint32_t li = load_idx + v_pos(j - 1, n);
-        const uint32_t vslot = li % L::kStages;
+        vslot = li % L::kStages;
         if (!ptx::mbar_wait(bar(L::kKVFull + vslot), (li / L::kStages) & 1u, ctl, kStatusMmaTimeout))
           goto done;
-        if (j - 1 < nt) {
-          if (!ptx::mbar_wait(bar(L::kPFull + t), p_uses & 1u, ctl, kStatusMmaTimeout)) goto done;
-          ++p_uses;
-          ptx::tc_fence_after();
-          const uint32_t vbase = sbase + L::kKVOff + vslot * L::kTileBytes;
-          if constexpr (L::kFp8) {
-            // V^T rows (d) of 128 key bytes: 32 keys (32 bytes) per step inside the atom
-            const uint32_t v_lo = ptx::sdesc_lo(vbase, 16);
-            if (j - 1 > 0) ptx::mma_f8_ts_c<1>(tO, tS, v_lo, desc_hi, idesc_pv);
-            else ptx::mma_f8_ts_c<0>(tO, tS, v_lo, desc_hi, idesc_pv);
-#pragma unroll
-            for (int kk = 1; kk < L::kPvSteps; ++kk)
-              ptx::mma_f8_ts_c<1>(tO, tS + kk * 8, v_lo + ((kk * 32) >> 4), desc_hi, idesc_pv);
-          } else {
-            // 16 key rows (2 KB) per step; the 64-wide d atoms lie 16 KB apart (LBO)
-            const uint32_t v_lo = ptx::sdesc_lo(vbase, L::kAtomBytes);
-            if (j - 1 > 0) ptx::mma_f16_ts_c<1>(tO, tS, v_lo, desc_hi, idesc_pv);
-            else ptx::mma_f16_ts_c<0>(tO, tS, v_lo, desc_hi, idesc_pv);
-#pragma unroll
-            for (int kk = 1; kk < L::kPvSteps; ++kk)
-              ptx::mma_f16_ts_c<1>(tO, tS + kk * 8, v_lo + ((kk * 16 * 128) >> 4), desc_hi, idesc_pv);
-          }
-          if (j - 1 == nt - 1) ptx::mma_commit(bar(L::kOFull + t));
-          ptx::mma_commit(bar(L::kKVEmpty + vslot));
-        } else {
-          ptx::mbar_arrive(bar(L::kKVEmpty + vslot));   // stage not used by this tile
-        }
       }
-      if (j < n) {
-        // S_t = Q_t K_j^T
-        const uint32_t li = load_idx + k_pos(j);
-        const uint32_t kslot = li % L::kStages;
-        if (!ptx::mbar_wait(bar(L::kKVFull + kslot), (li / L::kStages) & 1u, ctl, kStatusMmaTimeout))
-          goto done;
-        if (j < nt) {
+#pragma unroll
+      for (int t = 0; t < kQTiles; ++t) {
+        const uint32_t tS = tmem + L::kTmemS + t * kBlockN;
+        if (j >= 1 && j - 1 < nt[t]) {
+          // O_t += P_t V_{j-1}
+          if (!ptx::mbar_wait(bar(L::kPFull + t), p_uses[t] & 1u, ctl, kStatusMmaTimeout)) goto done;
+          ++p_uses[t];
+          ptx::tc_fence_after();
+          issue_pv<D, E>(tmem + L::kTmemO + t * D, tS, sbase + L::kKVOff + vslot * L::kTileBytes, j - 1 > 0);
+          if (j - 1 == nt[t] - 1) ptx::mma_commit(bar(L::kOFull + t));
+        }
+        if (j < nt[t]) {
+          // S_t = Q_t K_j^T
+          if (!k_ready) {
+            const uint32_t li = load_idx + k_pos(j);
+            kslot = li % L::kStages;
+            if (!ptx::mbar_wait(bar(L::kKVFull + kslot), (li / L::kStages) & 1u, ctl, kStatusMmaTimeout))
+              goto done;
+            k_ready = true;
+          }
           if (j == 0) {
-            if (!ptx::mbar_wait(bar(L::kQFull + t), q_uses & 1u, ctl, kStatusMmaTimeout)) goto done;
-            ++q_uses;
+            if (!ptx::mbar_wait(bar(L::kQFull + t), q_uses[t] & 1u, ctl, kStatusMmaTimeout)) goto done;
+            ++q_uses[t];
           }
-          ptx::tc_fence_after();
-          const uint32_t k_lo = ptx::sdesc_lo(sbase + L::kKVOff + kslot * L::kTileBytes, 16);
-          // K-major operands: 32 bytes of d per step inside a 128-byte swizzle atom
-#pragma unroll
-          for (int kk = 0; kk < D / L::kMmaK; ++kk) {
-            const uint32_t off = ((kk * 32 / 128) * L::kAtomBytes + (kk * 32) % 128) >> 4;
-            if constexpr (L::kFp8) {
-              if (kk == 0) ptx::mma_f8_ss_c<0>(tS, q_lo, desc_hi, k_lo, desc_hi, idesc_qk);
-              else ptx::mma_f8_ss_c<1>(tS, q_lo + off, desc_hi, k_lo + off, desc_hi, idesc_qk);
-            } else {
-              if (kk == 0) ptx::mma_f16_ss_c<0>(tS, q_lo, desc_hi, k_lo, desc_hi, idesc_qk);
-              else ptx::mma_f16_ss_c<1>(tS, q_lo + off, desc_hi, k_lo + off, desc_hi, idesc_qk);
-            }
-          }
+          issue_s<D, E>(tS, t == 0 ? q_lo0 : q_lo1, ptx::sdesc_lo(sbase + L::kKVOff + kslot * L::kTileBytes, 16));
           ptx::mma_commit(bar(L::kSFull + t));
-          if (j == nt - 1) ptx::mma_commit(bar(L::kQEmpty + t));
-          ptx::mma_commit(bar(L::kKVEmpty + kslot));
-        } else {
-          ptx::mbar_arrive(bar(L::kKVEmpty + kslot));   // stage not used by this tile
+          if (j == nt[t] - 1) ptx::mma_commit(bar(L::kQEmpty + t));
         }
       }
+      if (j >= 1) ptx::mma_commit(bar(L::kKVEmpty + vslot));
+      if (k_ready) ptx::mma_commit(bar(L::kKVEmpty + kslot));
     }
     load_idx += 2u * n;
   }
 done:
-  // Every MMA this thread issued must finish before TMEM is released.
-  ptx::mma_commit(bar(L::kMmaDone + t));
-  if (!ptx::mbar_wait_drain(bar(L::kMmaDone + t), 0, ctl.timeout_ns)) atomicOr(ctl.status, kStatusDrainTimeout);
+  // Every MMA issued so far must finish before TMEM is released.
+  ptx::mma_commit(bar(L::kMmaDone));
+  if (!ptx::mbar_wait_drain(bar(L::kMmaDone), 0, ctl.timeout_ns)) atomicOr(ctl.status, kStatusDrainTimeout);
 }
 
 // ---------------------------------------------------------------------------- softmax
@@ -521,10 +533,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     }
     for (int s = 0; s < L::kStages; ++s) {
       ptx::mbar_init(bar(L::kKVFull + s), 1);
-      ptx::mbar_init(bar(L::kKVEmpty + s), 2);   // released by both tiles' MMA threads
+      ptx::mbar_init(bar(L::kKVEmpty + s), 1);
     }
     ptx::mbar_init(bar(L::kMmaDone), 1);
-    ptx::mbar_init(bar(L::kMmaDone + 1), 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -547,8 +558,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     ptx::setmaxnreg_dec<kControlRegs>();
     if (warp == kLoadWarp) {
       if (lane == 0) fwd_producer<D, E>(p, sbase, ctl);
-    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
-      if (lane == 0) fwd_mma<D, E>(p, warp - kMmaWarp, sbase, tmem, ctl);
+    } else if (warp == kMmaWarp) {
+      if (lane == 0) fwd_mma<D, E>(p, sbase, tmem, ctl);
     }
   } else {
     ptx::setmaxnreg_inc<kSoftmaxRegs>();
