@@ -62,6 +62,17 @@ def _peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def shard_seed(w, rank: int) -> int:
+    """Seed of rank ``rank``'s shard: every rank runs the same per-GPU workload on
+    its own heads (weak scaling), drawn from its own seed."""
+    return w.seed + 7919 * rank
+
+
+def aggregate_tflops(step_flops: float, steps: int, world: int, max_total_ms: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return world * step_flops * steps / (max_total_ms * 1e-3) / 1e12
+
+
 def _workload(name: str):
     if name.startswith("sweep:"):
         _, n, d = name.split(":")
@@ -213,7 +224,7 @@ def run_gpu(args):
     w = _workload(args.workload)
     fp8 = args.workload == "fp8"
     # Each rank draws its own shard (same shape, seed offset by rank): weak scaling.
-    q, k, v = make_qkv(w.shape, w.dtype, w.seed + 7919 * rank, w.outliers)
+    q, k, v = make_qkv(w.shape, w.dtype, shard_seed(w, rank), w.outliers)
     masks = list(w.causal_modes)
     stream = torch.cuda.current_stream(dev)
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
@@ -270,7 +281,7 @@ def run_gpu(args):
         total_ms, kern_ms = float(t[0]), float(t[1])
     else:
         kern_ms = sum(launch_ms)
-    value = world * step_flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = aggregate_tflops(step_flops, args.steps, world, total_ms)
 
     # End-to-end through the public API with pinned host buffers (this rank's shard).
     e2e = None
