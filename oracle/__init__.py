@@ -6,6 +6,7 @@ never does, and this package imports nothing from it.
 """
 from .sdpa import (  # noqa: F401
     attention,
+    attention_decode,
     attention_probs,
     brute_force_attention,
     online_softmax_attention,

@@ -35,6 +35,7 @@ import numpy as np
 
 __all__ = [
     "attention",
+    "attention_decode",
     "attention_probs",
     "brute_force_attention",
     "online_softmax_attention",
@@ -187,3 +188,35 @@ def rel_rms(x, ref) -> float:
     """||x - ref||_F / ||ref||_F over all elements."""
     x, ref = _f64(x), _f64(ref)
     return float(np.linalg.norm((x - ref).ravel()) / np.linalg.norm(ref.ravel()))
+
+
+def attention_decode(q, k, v, scale: float, causal: bool):
+    """Attention of N_q query rows against N_k >= N_q keys (a KV-cache step), fp64.
+
+    q: ``[B, H, N_q, d]``; k, v: ``[B, H, N_k, d]``.  The queries are the last N_q
+    positions of the sequence, so with ``causal`` query row i sees keys
+    0 .. N_k - N_q + i (bottom-right alignment); without it every row sees all
+    keys.  Same definition as ``attention`` otherwise; returns
+    ``(O [B,H,N_q,d], LSE [B,H,N_q])``.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    if q.ndim != 4 or k.shape != v.shape or k.shape[:2] != q.shape[:2] or k.shape[3] != q.shape[3]:
+        raise ValueError(f"bad decode shapes {q.shape} {k.shape} {v.shape}")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if Nq > Nk:
+        raise ValueError("N_q must not exceed N_k")
+    o = np.empty((B, H, Nq, d))
+    lse = np.empty((B, H, Nq))
+    for b in range(B):
+        for h in range(H):
+            s = scale * (q[b, h] @ k[b, h].T)                       # [N_q, N_k]
+            if causal:
+                last = (Nk - Nq) + np.arange(Nq)                    # last visible key per row
+                s = np.where(np.arange(Nk)[None, :] <= last[:, None], s, -np.inf)
+            m = s.max(axis=1)
+            p = np.exp(s - m[:, None])
+            l = p.sum(axis=1)
+            o[b, h] = (p @ v[b, h]) / l[:, None]
+            lse[b, h] = m + np.log(l)
+    return o, lse

@@ -325,3 +325,35 @@ def test_pins_reject_planted_mistakes(kind, monkeypatch):
     assert _pins_pass()
     monkeypatch.setattr(oracle_attention_mod, "_rows_of_head", _mutant(kind))
     assert not _pins_pass(), f"no pin caught the planted mistake {kind!r}"
+
+
+# ----------------------------------------------------------------------------- decode (N_q < N_k)
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_decode_rows_equal_the_last_rows_of_full_attention(causal):
+    q, k, v = _rand((2, 2, 57, 16), 25)
+    full_o, full_l = oracle.attention(q, k, v, 0.25, causal)
+    for nq in (1, 4, 57):
+        o, l = oracle.attention_decode(q[:, :, -nq:], k, v, 0.25, causal)
+        assert np.abs(o - full_o[:, :, -nq:]).max() < 1e-12
+        assert np.abs(l - full_l[:, :, -nq:]).max() < 1e-12
+
+
+def test_decode_single_query_by_loops():
+    q, k, v = _rand((1, 1, 1, 8), 26)
+    _, k2, v2 = _rand((1, 1, 37, 8), 27)
+    o, l = oracle.attention_decode(q, k2, v2, 0.5, True)
+    scores = [0.5 * float((q[0, 0, 0] * k2[0, 0, j]).sum()) for j in range(37)]
+    mx = max(scores)
+    w = [math.exp(s - mx) for s in scores]
+    want = [sum(w[j] * float(v2[0, 0, j, c]) for j in range(37)) / sum(w) for c in range(8)]
+    assert np.abs(o[0, 0, 0] - np.array(want)).max() < 1e-13
+    assert abs(l[0, 0, 0] - (mx + math.log(sum(w)))) < 1e-13
+
+
+def test_decode_causal_first_row_sees_the_prefix():
+    q, k, v = _rand((1, 1, 3, 8), 28)
+    _, k2, v2 = _rand((1, 1, 10, 8), 29)
+    o, _ = oracle.attention_decode(q, k2, v2, 0.5, True)
+    ref, _ = oracle.attention_decode(q[:, :, :1], k2[:, :, :8], v2[:, :, :8], 0.5, False)
+    assert np.abs(o[0, 0, 0] - ref[0, 0, 0]).max() < 1e-13
