@@ -10,6 +10,8 @@ Other workloads (for profiling; the default is the headline):
   --workload long        [1, 32, 32768, 128], causal
   --workload fp8         [4, 16, 4096, 128] E4M3 forward (Hadamard on), quantisation excluded
   --workload tiny        [1, 1, 128, 64] fp16, both masks
+  --workload decode      one query row per head against a [8, 32, 32768, 128] bf16 key cache
+                         (split-KV on the CUDA cores; HBM roofline)
 
 Multi-GPU (torchrun, one rank per GPU): every rank runs the same per-GPU
 workload on its own shard of heads (weak scaling, no collective on the data
@@ -73,7 +75,13 @@ def aggregate_tflops(step_flops: float, steps: int, world: int, max_total_ms: fl
     return world * step_flops * steps / (max_total_ms * 1e-3) / 1e12
 
 
+DECODE = dict(B=8, H=32, Nq=1, Nk=32768, d=128)
+
+
 def _workload(name: str):
+    if name == "decode":
+        from fa_inputs import Workload
+        return Workload("decode", DECODE["B"], DECODE["H"], DECODE["Nk"], DECODE["d"], torch.bfloat16, 5, (False,))
     if name.startswith("sweep:"):
         _, n, d = name.split(":")
         return sweep_workload(int(n), int(d))
@@ -223,8 +231,13 @@ def run_gpu(args):
     fa.load_library()
     w = _workload(args.workload)
     fp8 = args.workload == "fp8"
+    dec = args.workload == "decode"
     # Each rank draws its own shard (same shape, seed offset by rank): weak scaling.
-    q, k, v = make_qkv(w.shape, w.dtype, shard_seed(w, rank), w.outliers)
+    if dec:
+        q, _, _ = make_qkv((w.B, w.H, DECODE["Nq"], w.d), w.dtype, shard_seed(w, rank))
+        _, k, v = make_qkv(w.shape, w.dtype, shard_seed(w, rank) + 1)
+    else:
+        q, k, v = make_qkv(w.shape, w.dtype, shard_seed(w, rank), w.outliers)
     masks = list(w.causal_modes)
     stream = torch.cuda.current_stream(dev)
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
@@ -232,16 +245,26 @@ def run_gpu(args):
         q8, qs = fa.quantize_fp8(qd, hadamard=True)
         k8, ks = fa.quantize_fp8(kd, hadamard=True)
         v8, vs = fa.quantize_fp8(vd, hadamard=False, transpose_out=True)
-    o = torch.empty(w.shape, device=dev, dtype=torch.bfloat16 if fp8 else w.dtype)
-    lse = torch.empty(w.shape[:3], device=dev, dtype=torch.float32)
+    o = torch.empty(q.shape, device=dev, dtype=torch.bfloat16 if fp8 else w.dtype)
+    lse = torch.empty(q.shape[:3], device=dev, dtype=torch.float32)
+    ws = None
+    if dec:
+        import ctypes
+        need = ctypes.c_ulonglong(0)
+        fa.load_library().fa_decode_workspace_size(w.B, w.H, DECODE["Nq"], w.N, w.d, 0, ctypes.byref(need))
+        ws = torch.empty(max(need.value, 256), device=dev, dtype=torch.uint8)
 
     def one(causal):
-        if fp8:
+        if dec:
+            fa.decode(qd, kd, vd, causal=causal, out=o, lse=lse, workspace=ws)
+        elif fp8:
             fa.attention_fp8(q8, k8, v8, qs, ks, vs, causal=causal, hadamard=True, out=o, lse=lse)
         else:
             fa.attention(qd, kd, vd, causal=causal, out=o, lse=lse)
 
     step_flops = sum(w.flops(c) for c in masks)
+    if dec:
+        step_flops = 4.0 * w.B * w.H * DECODE["Nq"] * w.N * w.d * len(masks)
     for _ in range(args.warmup):
         for c in masks:
             one(c)
@@ -285,7 +308,7 @@ def run_gpu(args):
 
     # End-to-end through the public API with pinned host buffers (this rank's shard).
     e2e = None
-    if not fp8:
+    if not fp8 and not dec:
         qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
         e_steps = max(1, min(args.steps, 5))
         for _ in range(2):
@@ -321,7 +344,20 @@ def run_gpu(args):
         peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
         peak_note = f"{peak_src} bf16 burst peak"
     kern_tflops = step_flops * args.steps / (kern_ms * 1e-3) / 1e12
+    if dec:
+        # HBM-bound: algorithmic bytes = K + V read once, Q read, O written, LSE written
+        dec_bytes = (2 * k.numel() + q.numel() + o.numel()) * k.element_size() + 4 * lse.numel()
+        dec_gbs = dec_bytes * args.steps * len(masks) / (kern_ms * 1e-3) / 1e9
     traffic = _committed_traffic(w.name, fp8)
+    if dec:
+        roof = {"bound": "hbm", "achieved": dec_gbs, "peak": peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]),
+                "unit": "GB/s", "frac": dec_gbs / peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]),
+                "traffic": None, "peak_source": f"{peak_src} HBM copy bandwidth",
+                "kernel": "fa_decode_split_kernel + fa_decode_merge_kernel", "bytes_per_step": dec_bytes}
+    else:
+        roof = {"bound": "tensor", "achieved": kern_tflops, "peak": peak, "unit": "TFLOP/s",
+                "frac": kern_tflops / peak, "traffic": traffic, "peak_source": peak_note,
+                "kernel": "fa_fwd_fp8_kernel" if fp8 else "fa_fwd_kernel"}
     variants = {("causal" if c else "non_causal"): {
         "tflops": w.flops(c) / (statistics.median(per_mask_ms[c]) * 1e-3) / 1e12,
         "median_ms": statistics.median(per_mask_ms[c]),
@@ -346,13 +382,11 @@ def run_gpu(args):
                          (3 * q.numel() * q.element_size() // 2**20),
                    "parallelism": f"dp{world} (independent head shards, no data-path collective)"},
         "pct_of_spec_peak": 100.0 * value / world / SPEC_PEAK_TFLOPS[dtype_name],
-        "roofline": {"bound": "tensor", "achieved": kern_tflops, "peak": peak, "unit": "TFLOP/s",
-                     "frac": kern_tflops / peak, "traffic": traffic, "peak_source": peak_note,
-                     "kernel": "fa_fwd_fp8_kernel" if fp8 else "fa_fwd_kernel"},
+        "roofline": roof,
         "variants": variants,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": n_ev,
+        "gpu_launches": n_ev * (2 if dec else 1),
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)

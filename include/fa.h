@@ -46,7 +46,8 @@ typedef enum {
   FA_ERR_LAUNCH = -5,          /* the kernel launch was rejected by the runtime */
   FA_ERR_DEVICE_TIMEOUT = -6,  /* a kernel gave up on a pipeline wait (see fa_last_device_status) */
   FA_ERR_ARCH = -7,            /* the current device is not an sm_103 GPU */
-  FA_ERR_CUDA = -8             /* another CUDA runtime or driver call failed */
+  FA_ERR_CUDA = -8,            /* another CUDA runtime or driver call failed */
+  FA_ERR_WORKSPACE = -9        /* workspace missing or smaller than fa_decode_workspace_size */
 } fa_status;
 
 /*
@@ -89,6 +90,31 @@ int fa_quantize_fp8(const void* x, void* x8, float* scale, int B, int H, int N, 
 int fa_fwd_fp8(const void* q8, const void* k8, const void* v8t, void* o, float* lse, int B, int H,
                int N, int d, float scale, int causal, const float* q_scale, const float* k_scale,
                const float* v_scale, int hadamard, void* stream);
+
+/*
+ * Attention of a few query rows against a long key cache (one decode step): the
+ * same definition as fa_fwd, for the last N_q positions of a sequence of N_k keys
+ * (the concept card's problem statement, "Kernpunkte", applied to the KV cache of
+ * "Begriffe auf dieser Seite").  With causal = 1, query row i sees keys
+ * 0 .. N_k - N_q + i (bottom-right alignment); with 0, all keys.
+ *   q          : [B, H, N_q, d] of `dtype`, 1 <= N_q <= 16, N_q <= N_k
+ *   k, v       : [B, H, N_k, d] of `dtype`
+ *   o, lse     : [B, H, N_q, d] of `dtype` and [B, H, N_q] float32 (lse may be NULL)
+ *   num_splits : key chunks per head processed in parallel and merged by log-sum-exp;
+ *                0 picks a count from the SM count and N_k
+ *   workspace  : device scratch of at least fa_decode_workspace_size() bytes, 256-byte
+ *                aligned, owned by the caller; may be NULL when that size is 0.  Its
+ *                contents on entry do not matter; calls sharing one workspace must not
+ *                overlap on the GPU.
+ * Computed on the CUDA cores (the work is a stream over K and V, HBM-bound).
+ */
+int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+              int Nk, int d, float scale, int causal, int dtype, int num_splits, void* workspace,
+              unsigned long long workspace_bytes, void* stream);
+
+/* Scratch bytes fa_decode needs for these sizes on the current device (0 if none). */
+int fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits,
+                             unsigned long long* bytes);
 
 /* Static English text for a status code (never NULL). */
 const char* fa_strerror(int status);

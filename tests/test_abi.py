@@ -32,7 +32,8 @@ def lib():
 
 def test_header_declares_the_boundary():
     assert _declared() == sorted(["fa_fwd", "fa_quantize_fp8", "fa_fwd_fp8", "fa_strerror",
-                                  "fa_last_device_status", "fa_debug_inject_stall", "fa_version"])
+                                  "fa_last_device_status", "fa_debug_inject_stall", "fa_version",
+                                  "fa_decode", "fa_decode_workspace_size"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -42,7 +43,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_strerror_and_version(lib):
-    for code in range(-8, 1):
+    for code in range(-9, 1):
         assert lib.fa_strerror(code)
     assert lib.fa_strerror(-99) == b"unknown status"
     assert lib.fa_version() >= 100
@@ -72,3 +73,17 @@ def test_fwd_rejects_bad_arguments_on_the_host(lib, args, want):
     q, k, v, o, lse, B, H, N, d, scale, causal, dtype = args
     assert lib.fa_fwd(q or None, k or None, v or None, o or None, lse or None, B, H, N, d, scale,
                       causal, dtype, None) == want
+
+
+@pytest.mark.parametrize("args,want", [
+    ((0, A, A, A, 0, 1, 1, 1, 128, 64, 0.125, 0, 1, 0, 0, 0), fa.FA_ERR_NULL),
+    ((A, A, A, A, 0, 1, 1, 17, 128, 64, 0.125, 0, 1, 0, 0, 0), fa.FA_ERR_SHAPE),    # N_q > 16
+    ((A, A, A, A, 0, 1, 1, 4, 3, 64, 0.125, 0, 1, 0, 0, 0), fa.FA_ERR_SHAPE),       # N_q > N_k
+    ((A, A, A, A, 0, 1, 1, 1, 128, 80, 0.125, 0, 1, 0, 0, 0), fa.FA_ERR_UNSUPPORTED),
+    ((A, A, A, A, 0, 1, 1, 1, 128, 64, 0.125, 3, 1, 0, 0, 0), fa.FA_ERR_UNSUPPORTED),
+    ((A, A, A, A, 0, 1, 1, 1, 128, 64, 0.125, 0, 1, 0, A + 16, 1024), fa.FA_ERR_ALIGN),
+])
+def test_decode_rejects_bad_arguments_on_the_host(lib, args, want):
+    q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype, splits, ws, wsb = args
+    assert lib.fa_decode(q or None, k or None, v or None, o or None, lse or None, B, H, Nq, Nk, d, scale,
+                         causal, dtype, splits, ws or None, wsb, None) == want

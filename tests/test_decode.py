@@ -1,0 +1,85 @@
+"""GPU parity of the split-KV decode path (few query rows, long key cache).
+
+Compared with the fp64 oracle's decode definition (bottom-right causal), with
+the forward pass's tolerances: |O_gpu - O_ref| <= 1e-2 + half an ulp of the
+output type at |O_ref|, |LSE_gpu - LSE_ref| <= 1e-3.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fa_inputs import make_qkv
+
+pytestmark = pytest.mark.gpu
+
+
+def _half_ulp(x, mant_bits):
+    a = np.maximum(np.abs(x), 2.0 ** -14)
+    _, e2 = np.frexp(a)
+    return np.exp2(e2 - 1 - mant_bits - 1)
+
+
+def _inputs(B, H, Nq, Nk, d, dtype, seed):
+    q, _, _ = make_qkv((B, H, Nq, d), dtype, seed)
+    _, k, v = make_qkv((B, H, Nk, d), dtype, seed + 1)
+    return q, k, v
+
+
+def _check(fa, q, k, v, causal, num_splits=0, workspace=None):
+    d = q.shape[-1]
+    o, lse = fa.decode(q.cuda(), k.cuda(), v.cuda(), causal=causal, num_splits=num_splits, workspace=workspace)
+    torch.cuda.synchronize()
+    st, bits = fa.last_device_status()
+    assert st == fa.FA_OK, f"status {bits:#x}"
+    ro, rl = oracle.attention_decode(q, k, v, 1 / math.sqrt(d), causal)
+    on, ln = o.float().cpu().numpy(), lse.cpu().numpy()
+    mant = 10 if q.dtype == torch.float16 else 7
+    assert np.isfinite(on).all() and np.isfinite(ln).all()
+    excess = float((np.abs(on - ro) - 1e-2 - _half_ulp(ro, mant)).max())
+    el = float(np.abs(ln - rl).max())
+    assert excess <= 0 and el <= 1e-3, f"max|dO|={np.abs(on - ro).max():.3e} excess={excess:.3e} max|dLSE|={el:.3e}"
+
+
+CASES = [
+    # B, H, Nq, Nk, d, dtype
+    (1, 1, 1, 1, 128, torch.bfloat16),
+    (2, 3, 1, 63, 64, torch.float16),
+    (1, 2, 1, 64, 128, torch.bfloat16),
+    (1, 2, 3, 65, 128, torch.bfloat16),
+    (2, 2, 16, 1000, 64, torch.bfloat16),
+    (1, 4, 5, 4096, 128, torch.float16),
+    (4, 8, 1, 8192, 128, torch.bfloat16),
+    (1, 2, 16, 16, 128, torch.bfloat16),
+]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,Nq,Nk,d,dtype", CASES)
+def test_decode_matches_oracle(gpu_lib, B, H, Nq, Nk, d, dtype, causal):
+    q, k, v = _inputs(B, H, Nq, Nk, d, dtype, 300 + Nk)
+    _check(gpu_lib, q, k, v, causal)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 7, 64])
+def test_decode_split_counts(gpu_lib, splits):
+    q, k, v = _inputs(1, 2, 4, 3000, 128, torch.bfloat16, 41)
+    for causal in (False, True):
+        _check(gpu_lib, q, k, v, causal, num_splits=splits)
+
+
+def test_decode_long_cache_with_reused_workspace(gpu_lib):
+    q, k, v = _inputs(1, 4, 2, 32768, 128, torch.bfloat16, 42)
+    ws = torch.empty(64 << 20, device="cuda", dtype=torch.uint8)
+    for _ in range(2):
+        _check(gpu_lib, q, k, v, True, workspace=ws)
+
+
+def test_decode_workspace_too_small(gpu_lib):
+    q, k, v = (t.cuda() for t in _inputs(1, 2, 1, 5000, 128, torch.bfloat16, 43))
+    ws = torch.empty(256, device="cuda", dtype=torch.uint8)
+    with pytest.raises(gpu_lib.FAError) as e:
+        gpu_lib.decode(q, k, v, num_splits=8, workspace=ws)
+    assert e.value.status == gpu_lib.FA_ERR_WORKSPACE

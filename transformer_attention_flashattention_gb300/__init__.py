@@ -24,6 +24,7 @@ __all__ = [
     "attention_host",
     "quantize_fp8",
     "attention_fp8",
+    "decode",
     "last_device_status",
     "inject_stall",
     "FA_OK",
@@ -35,6 +36,7 @@ __all__ = [
     "FA_ERR_DEVICE_TIMEOUT",
     "FA_ERR_ARCH",
     "FA_ERR_CUDA",
+    "FA_ERR_WORKSPACE",
 ]
 
 FA_OK = 0
@@ -46,6 +48,7 @@ FA_ERR_LAUNCH = -5
 FA_ERR_DEVICE_TIMEOUT = -6
 FA_ERR_ARCH = -7
 FA_ERR_CUDA = -8
+FA_ERR_WORKSPACE = -9
 
 _PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 _LIB: Optional[ctypes.CDLL] = None
@@ -57,6 +60,8 @@ _SIGNATURES = {
     "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _vp]),
     "fa_quantize_fp8": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]),
     "fa_fwd_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _i, _vp]),
+    "fa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _vp, ctypes.c_ulonglong, _vp]),
+    "fa_decode_workspace_size": (_i, [_i, _i, _i, _i, _i, _i, ctypes.POINTER(ctypes.c_ulonglong)]),
     "fa_strerror": (ctypes.c_char_p, [_i]),
     "fa_last_device_status": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),
     "fa_debug_inject_stall": (_i, [_i, _i]),
@@ -218,6 +223,45 @@ def attention_fp8(q8: torch.Tensor, k8: torch.Tensor, v8t: torch.Tensor, q_scale
                         int(bool(causal)), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
                         int(bool(hadamard)), _stream_handle(stream, q8.device))
     _check(st, "fa_fwd_fp8")
+    return out, lse
+
+
+def decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+           scale: Optional[float] = None, num_splits: int = 0, out: Optional[torch.Tensor] = None,
+           lse: Optional[torch.Tensor] = None, return_lse: bool = True,
+           workspace: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None):
+    """Attention of q [B,H,N_q,d] (N_q <= 16) against a key cache k, v [B,H,N_k,d].
+
+    Split-KV on the CUDA cores with a log-sum-exp merge; a scratch workspace is
+    allocated with torch unless one is given.  Returns (O, LSE).
+    """
+    lib = load_library()
+    B, H, Nq, d = q.shape
+    if k.dim() != 4 or k.shape != v.shape or k.shape[:2] != (B, H) or k.shape[3] != d:
+        raise ValueError(f"k, v must be [B, H, N_k, d] matching q; got {tuple(k.shape)}, {tuple(v.shape)}")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype:
+            raise ValueError(f"{name} must be a contiguous CUDA tensor of q's dtype")
+    if q.dtype not in _DTYPES:
+        raise ValueError(f"dtype must be float16 or bfloat16, got {q.dtype}")
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = ctypes.c_ulonglong(0)
+    with torch.cuda.device(q.device):
+        _check(lib.fa_decode_workspace_size(B, H, Nq, Nk, d, int(num_splits), ctypes.byref(need)),
+               "fa_decode_workspace_size")
+    if workspace is None and need.value > 0:
+        workspace = torch.empty(need.value, device=q.device, dtype=torch.uint8)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, Nq), device=q.device, dtype=torch.float32)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.fa_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nk, d, float(scale),
+                       int(bool(causal)), _DTYPES[q.dtype], int(num_splits), _ptr(workspace), ws_bytes,
+                       _stream_handle(stream, q.device))
+    _check(st, "fa_decode")
     return out, lse
 
 

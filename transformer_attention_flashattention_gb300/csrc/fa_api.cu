@@ -244,6 +244,99 @@ extern "C" int fa_fwd_fp8(const void* q8, const void* k8, const void* v8t, void*
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
+namespace fa {
+namespace {
+
+constexpr int kDecodeMaxQ = 16;
+
+// Key chunks per head: enough CTAs for about two per SM, at least 256 keys each.
+void decode_split(int BH, int Nk, int requested, int sm_count, int* splits, int* chunk) {
+  int s = requested;
+  if (s <= 0) {
+    s = (2 * sm_count + BH - 1) / BH;
+    const int by_len = (Nk + 255) / 256;
+    if (s > by_len) s = by_len;
+  }
+  if (s < 1) s = 1;
+  int c = (Nk + s - 1) / s;
+  c = (c + 63) / 64 * 64;
+  *chunk = c;
+  *splits = (Nk + c - 1) / c;
+}
+
+unsigned long long decode_workspace(int BH, int Nq, int d, int splits) {
+  if (splits <= 1) return 0;
+  const unsigned long long o = static_cast<unsigned long long>(BH) * splits * Nq * d * 4;
+  const unsigned long long l = static_cast<unsigned long long>(BH) * splits * Nq * 4;
+  return (o + 255) / 256 * 256 + l;
+}
+
+int check_decode(int B, int H, int Nq, int Nk, int d) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (Nq > kDecodeMaxQ || Nq > Nk) return FA_ERR_SHAPE;
+  if (static_cast<long double>(B) * H * Nk * d >= static_cast<long double>(1ull << 40)) return FA_ERR_SHAPE;
+  if (static_cast<long long>(B) * H * 4096 >= (1ll << 31)) return FA_ERR_SHAPE;
+  return FA_OK;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" int fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits,
+                                        unsigned long long* bytes) {
+  if (!bytes) return FA_ERR_NULL;
+  int st = check_decode(B, H, Nq, Nk, d);
+  if (st != FA_OK) return st;
+  const DeviceInfo* di = current_device(&st);
+  if (!di) return st;
+  int splits, chunk;
+  decode_split(B * H, Nk, num_splits, di->sm_count, &splits, &chunk);
+  *bytes = decode_workspace(B * H, Nq, d, splits);
+  return FA_OK;
+}
+
+extern "C" int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                         int Nq, int Nk, int d, float scale, int causal, int dtype, int num_splits,
+                         void* workspace, unsigned long long workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o) return FA_ERR_NULL;
+  if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+  if (causal != 0 && causal != 1) return FA_ERR_UNSUPPORTED;
+  int st = check_decode(B, H, Nq, Nk, d);
+  if (st != FA_OK) return st;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || (lse && !aligned(lse, 4)) ||
+      (workspace && !aligned(workspace, 256)))
+    return FA_ERR_ALIGN;
+  const DeviceInfo* di = current_device(&st);
+  if (!di) return st;
+  DecodeParams p;
+  decode_split(B * H, Nk, num_splits, di->sm_count, &p.splits, &p.chunk);
+  const unsigned long long need = decode_workspace(B * H, Nq, d, p.splits);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return FA_ERR_WORKSPACE;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.lse = lse;
+  p.part_o = need ? static_cast<float*>(workspace) : nullptr;
+  p.part_lse = need ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                               (static_cast<unsigned long long>(B) * H * p.splits * Nq * d * 4 + 255) / 256 * 256)
+                    : nullptr;
+  p.status = di->status;
+  p.scale_log2 = scale * 1.44269504088896340736f;
+  p.BH = B * H;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.causal = causal;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    p.timeout_ns = timeout_ns_for_call();
+  }
+  const cudaError_t e = launch_decode(d, dtype == FA_BF16, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
 extern "C" int fa_last_device_status(void* stream, unsigned int* bits) {
   int st = FA_OK;
   const DeviceInfo* di = current_device(&st);
@@ -276,6 +369,7 @@ extern "C" const char* fa_strerror(int status) {
     case FA_ERR_DEVICE_TIMEOUT: return "a kernel gave up on a pipeline wait (device status word set)";
     case FA_ERR_ARCH: return "the current CUDA device is not an sm_103 GPU";
     case FA_ERR_CUDA: return "a CUDA runtime or driver call failed";
+    case FA_ERR_WORKSPACE: return "the workspace is missing or smaller than fa_decode_workspace_size reports";
     default: return "unknown status";
   }
 }

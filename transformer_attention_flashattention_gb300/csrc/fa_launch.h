@@ -8,10 +8,12 @@ namespace fa {
 
 struct FwdParams;
 struct QuantParams;
+struct DecodeParams;
 
 // Launch one forward kernel instantiation on `stream`; returns the launch status.
 cudaError_t launch_fwd(int d, bool bf16, const FwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_fwd_fp8(const FwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_quant_fp8(const QuantParams& p, cudaStream_t stream);
+cudaError_t launch_decode(int d, bool bf16, const DecodeParams& p, cudaStream_t stream);
 
 }  // namespace fa

@@ -43,4 +43,24 @@ struct QuantParams {
   int transpose_out;
 };
 
+// Split-KV attention of N_q query rows against N_k cached keys.
+struct DecodeParams {
+  const void* q;      // [B*H, Nq, d]
+  const void* k;      // [B*H, Nk, d]
+  const void* v;
+  void* o;            // [B*H, Nq, d]
+  float* lse;         // [B*H, Nq] or nullptr
+  float* part_o;      // scratch [B*H, splits, Nq, d] (splits > 1)
+  float* part_lse;    // scratch [B*H, splits, Nq]
+  unsigned int* status;
+  unsigned long long timeout_ns;
+  float scale_log2;
+  int BH;
+  int Nq;
+  int Nk;
+  int splits;
+  int chunk;          // keys per split, a multiple of 64
+  int causal;
+};
+
 }  // namespace fa
