@@ -358,10 +358,12 @@ def run_gpu(args):
         roof = {"bound": "tensor", "achieved": kern_tflops, "peak": peak, "unit": "TFLOP/s",
                 "frac": kern_tflops / peak, "traffic": traffic, "peak_source": peak_note,
                 "kernel": "fa_fwd_fp8_kernel" if fp8 else "fa_fwd_kernel"}
+    def mask_flops(c):
+        return step_flops / len(masks) if dec else w.flops(c)
     variants = {("causal" if c else "non_causal"): {
-        "tflops": w.flops(c) / (statistics.median(per_mask_ms[c]) * 1e-3) / 1e12,
+        "tflops": mask_flops(c) / (statistics.median(per_mask_ms[c]) * 1e-3) / 1e12,
         "median_ms": statistics.median(per_mask_ms[c]),
-        "pct_of_spec_peak": 100.0 * w.flops(c) / (statistics.median(per_mask_ms[c]) * 1e-3) / 1e12
+        "pct_of_spec_peak": 100.0 * mask_flops(c) / (statistics.median(per_mask_ms[c]) * 1e-3) / 1e12
         / SPEC_PEAK_TFLOPS[dtype_name]} for c in masks}
 
     cpu = None
@@ -379,7 +381,7 @@ def run_gpu(args):
                    "masks": ["causal" if c else "non-causal" for c in masks],
                    "scale": "1/sqrt(d)", "global_batch_heads": world * w.B * w.H,
                    "l2": "inputs larger than L2 (no flush): Q/K/V = %d MB per rank" %
-                         (3 * q.numel() * q.element_size() // 2**20),
+                         ((q.numel() + k.numel() + v.numel()) * q.element_size() // 2**20),
                    "parallelism": f"dp{world} (independent head shards, no data-path collective)"},
         "pct_of_spec_peak": 100.0 * value / world / SPEC_PEAK_TFLOPS[dtype_name],
         "roofline": roof,

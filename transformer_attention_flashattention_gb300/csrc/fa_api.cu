@@ -311,6 +311,11 @@ extern "C" int fa_decode(const void* q, const void* k, const void* v, void* o, f
   const DeviceInfo* di = current_device(&st);
   if (!di) return st;
   DecodeParams p;
+  const CUtensorMapDataType dt = dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if (!encode_3d(&p.tm_k, dt, 2, k, d, Nk, static_cast<uint64_t>(B) * H, 64, 64) ||
+      !encode_3d(&p.tm_v, dt, 2, v, d, Nk, static_cast<uint64_t>(B) * H, 64, 64))
+    return FA_ERR_CUDA;
   decode_split(B * H, Nk, num_splits, di->sm_count, &p.splits, &p.chunk);
   const unsigned long long need = decode_workspace(B * H, Nq, d, p.splits);
   if (need > 0 && (!workspace || workspace_bytes < need)) return FA_ERR_WORKSPACE;

@@ -8,12 +8,13 @@
 // With N_q <= 16 the work is a stream over K and V (2 * N_k * d * 2 bytes per head):
 // HBM-bound, so it runs on the CUDA cores, not the tensor cores.  The key range is
 // cut into `splits` chunks; one CTA per (b*h, chunk):
-//   warp 8        producer: per 64-key tile, one cp.async.bulk per K and per V row into
-//                 shared memory rows padded to 2d+16 bytes (conflict-free 16-byte reads),
-//                 a 3-stage ring with mbarrier full/empty handoff
-//   warps 0-7     scores (one key per thread, its K row in registers), online softmax
-//                 per query row (running max and correction, as in the forward pass),
-//                 then O += P V (two d-columns per thread)
+//   lane 0 of warp 0 also issues the loads: per 64-key tile, TMA loads of K and V
+//                 (128-byte swizzle, which keeps the per-row reads bank-conflict free) into
+//                 a 6-stage ring; a stage is refilled once all 8 warps released it
+//   warps 0-7     each warp owns 8 keys of every tile: scores (lanes split d, then a
+//                 9-shuffle reduce-scatter), its own online softmax per query row (running
+//                 max and correction, as in the forward pass) and its own O slice; the 8
+//                 warps are merged by log-sum-exp once at the end (no barrier per tile)
 // Each chunk writes its normalised partial O and LSE to scratch; a second kernel merges
 // the chunks: LSE = log sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s.  With one
 // chunk the first kernel writes O and LSE directly.
@@ -31,17 +32,19 @@ namespace fa {
 namespace {
 
 constexpr int kDecTile = 64;                 // keys per stage
-constexpr int kDecStages = 3;
+constexpr int kDecStages = 6;
 constexpr int kDecCompute = 256;             // compute threads (8 warps)
-constexpr int kDecThreads = kDecCompute + 32;
+constexpr int kDecThreads = kDecCompute;
 constexpr int kDecMaxQ = 16;
 constexpr float kDecLn2 = 0.693147180559945309f;
 constexpr unsigned kDecStatusTimeout = 16u;
 
 template <int D>
 struct DecCfg {
-  static constexpr int kRow = 2 * D + 16;                  // padded row bytes
-  static constexpr int kStageBytes = 2 * kDecTile * kRow;  // K and V of one tile
+  static constexpr int kBoxes = D / 64;                    // 128-byte swizzle atoms per row
+  static constexpr int kBoxBytes = kDecTile * 128;         // one atom column of a tile
+  static constexpr int kTileBytes = kBoxes * kBoxBytes;    // K (or V) tile
+  static constexpr int kStageBytes = 2 * kTileBytes;       // K and V of one tile
   static constexpr int kKOff = 0;
   static constexpr int kQOff = kDecStages * kStageBytes;   // q * scale * log2(e), fp32 [kDecMaxQ][D]
   static constexpr int kSOff = kQOff + kDecMaxQ * D * 4;   // scores / weights [kDecMaxQ][kDecTile]
@@ -54,11 +57,10 @@ __device__ __forceinline__ void compute_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kDecCompute) : "memory");
 }
 
-__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
+// Byte offset of 16-byte chunk c (0 .. D/8-1) of tile row r under the 128-byte swizzle.
+template <int D>
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  return (c / 8) * DecCfg<D>::kBoxBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
 template <bool BF16>
@@ -73,7 +75,8 @@ __device__ __forceinline__ float2 unpack2(uint32_t w) {
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const __grid_constant__ DecodeParams p) {
   using C = DecCfg<D>;
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = ptx::smem_u32(smem);
   auto full = [&](int s) { return sbase + C::kBarOff + 8u * s; };
   auto empty = [&](int s) { return sbase + C::kBarOff + 8u * (kDecStages + s); };
@@ -117,166 +120,231 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const __gr
   __syncthreads();
   const ptx::WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
 
-  if (warp == kDecCompute / 32) {
-    // ---------------------------------------------------------------- producer
-    if (lane == 0) {
-      const uint8_t* kg = static_cast<const uint8_t*>(p.k) + static_cast<size_t>(bh) * p.Nk * D * 2;
-      const uint8_t* vg = static_cast<const uint8_t*>(p.v) + static_cast<size_t>(bh) * p.Nk * D * 2;
-      int issued[kDecStages] = {-1, -1, -1};
-      for (int i = 0; i < ntiles; ++i) {
-        const int s = i % kDecStages;
-        const uint32_t fill = i / kDecStages;
-        if (!ptx::mbar_wait(empty(s), (fill & 1u) ^ 1u, ctl, kDecStatusTimeout)) break;
-        const int r0 = k0 + i * kDecTile;
-        const int rows = min(kDecTile, k1 - r0);
-        ptx::mbar_arrive_expect_tx(full(s), static_cast<uint32_t>(rows) * D * 4);
-        const uint32_t kd = sbase + C::kKOff + s * C::kStageBytes;
-        const uint32_t vd = kd + kDecTile * C::kRow;
-        for (int r = 0; r < rows; ++r) {
-          bulk_copy(kd + r * C::kRow, kg + static_cast<size_t>(r0 + r) * D * 2, D * 2, full(s));
-          bulk_copy(vd + r * C::kRow, vg + static_cast<size_t>(r0 + r) * D * 2, D * 2, full(s));
-        }
-        issued[s] = static_cast<int>(fill);
-      }
-      // copies in flight land before the CTA exits
-      for (int s = 0; s < kDecStages; ++s)
-        if (issued[s] >= 0 && !ptx::mbar_wait_drain(full(s), static_cast<uint32_t>(issued[s]) & 1u, p.timeout_ns))
-          atomicOr(p.status, kDecStatusTimeout);
+  // ------------------------------------------------------------------ loads
+  // issued by lane 0 of warp 0: the first stages up front, then stage s is refilled
+  // with tile i + kDecStages once every warp released tile i
+  const bool loader = tid == 0;
+  int last_issued = -1;
+  auto issue = [&](int i) {
+    const int st = i % kDecStages;
+    const int r0 = k0 + i * kDecTile;
+    // full boxes are transferred (rows past N_k read as zero), so expect all bytes
+    ptx::mbar_arrive_expect_tx(full(st), C::kStageBytes);
+    const uint32_t kd = sbase + C::kKOff + st * C::kStageBytes;
+    const uint32_t vd = kd + C::kTileBytes;
+#pragma unroll
+    for (int b = 0; b < C::kBoxes; ++b) {
+      ptx::tma_load_3d(kd + b * C::kBoxBytes, &p.tm_k, full(st), b * 64, r0, bh);
+      ptx::tma_load_3d(vd + b * C::kBoxBytes, &p.tm_v, full(st), b * 64, r0, bh);
     }
-    return;
+    last_issued = i;
+  };
+  if (loader) {
+    ptx::prefetch_tensormap(&p.tm_k);
+    ptx::prefetch_tensormap(&p.tm_v);
+    for (int i = 0; i < min(ntiles, kDecStages); ++i) issue(i);
   }
 
   // ------------------------------------------------------------------ compute warps
-  const int kk = tid & (kDecTile - 1);        // key of this thread in the score phase
-  const int qg = tid / kDecTile;              // query group 0..3 (rows qg, qg+4, ...)
-  constexpr int kCols2 = D / 2;               // column pairs
-  constexpr int kQSets = kDecCompute / kCols2;   // 4 (d=128) or 8 (d=64) query sets in P.V
-  const int cp = tid % kCols2;                // column pair of this thread in P.V
-  const int qset = tid / kCols2;
-  float2 acc[kDecMaxQ / kQSets];
+  // Warp w owns keys 8w .. 8w+7 of every tile and keeps its own running max, sum and
+  // O slice per query row (lane l owns d-elements E*l .. E*l+E-1); the 8 warps' partial
+  // results are merged once at the end.  No CTA-wide barrier per tile.
+  constexpr int E = D / 32;
+  constexpr int kKeysPerWarp = kDecTile / (kDecCompute / 32);   // 8
+  const int last_key_shift = p.Nk - p.Nq;                       // causal: row i sees keys <= shift + i
+  float acc[kDecMaxQ][E];
+  float m_w[kDecMaxQ], l_w[kDecMaxQ];
 #pragma unroll
-  for (int i = 0; i < kDecMaxQ / kQSets; ++i) acc[i] = make_float2(0.f, 0.f);
-  const int last_key_shift = p.Nk - p.Nq;     // causal: row i sees keys <= shift + i
+  for (int qi = 0; qi < kDecMaxQ; ++qi) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[qi][e] = 0.f;
+    m_w[qi] = -INFINITY;
+    l_w[qi] = 0.f;
+  }
+  // key of this lane after the reduce-scatter: lane bits 4, 3, 2 -> key bits 2, 1, 0
+  const int my_key = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
 
+  bool ok = true;
   for (int i = 0; i < ntiles; ++i) {
     const int s = i % kDecStages;
-    const bool got = ptx::mbar_wait(full(s), (i / kDecStages) & 1u, ctl, kDecStatusTimeout);
-    compute_sync();
-    if (!got || *abort_flag) break;               // every compute warp leaves together
+    if (!ptx::mbar_wait(full(s), (i / kDecStages) & 1u, ctl, kDecStatusTimeout)) { ok = false; break; }
     const uint8_t* ks = smem + C::kKOff + s * C::kStageBytes;
-    const uint8_t* vs = ks + kDecTile * C::kRow;
-    const int key = k0 + i * kDecTile + kk;
-    const int valid = min(kDecTile, k1 - (k0 + i * kDecTile));   // rows loaded in this tile
-
-    // scores: this thread's K row against its query rows
-    {
-      uint4 krow[D / 8];
+    const uint8_t* vs = ks + C::kTileBytes;
+    const int kbase = warp * kKeysPerWarp;               // first key of this warp in the tile
+    const int key0 = k0 + i * kDecTile + kbase;
+    // this lane's d-slice of the warp's 8 K rows (E bf16/f16 values = E*2 bytes)
+    float kv[kKeysPerWarp][E];
+    uint32_t roff[kKeysPerWarp];
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) krow[c] = *reinterpret_cast<const uint4*>(ks + kk * C::kRow + 16 * c);
-      for (int qi = qg; qi < p.Nq; qi += kDecCompute / kDecTile) {
-        const float* qr = qs + qi * D;
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-          const float4 qa = *reinterpret_cast<const float4*>(qr + 8 * c);
-          const float4 qb = *reinterpret_cast<const float4*>(qr + 8 * c + 4);
-          const float2 x0 = unpack2<BF16>(krow[c].x), x1 = unpack2<BF16>(krow[c].y);
-          const float2 x2 = unpack2<BF16>(krow[c].z), x3 = unpack2<BF16>(krow[c].w);
-          a0 = fmaf(qa.x, x0.x, a0); a1 = fmaf(qa.y, x0.y, a1);
-          a0 = fmaf(qa.z, x1.x, a0); a1 = fmaf(qa.w, x1.y, a1);
-          a0 = fmaf(qb.x, x2.x, a0); a1 = fmaf(qb.y, x2.y, a1);
-          a0 = fmaf(qb.z, x3.x, a0); a1 = fmaf(qb.w, x3.y, a1);
-        }
-        const bool visible = key < k1 && (!p.causal || key <= last_key_shift + qi);
-        sc[qi * kDecTile + kk] = visible ? a0 + a1 : -INFINITY;
+    for (int r = 0; r < kKeysPerWarp; ++r) {
+      roff[r] = swz<D>(kbase + r, (E * lane) / 8) + ((E * lane) % 8) * 2;
+      if constexpr (E == 4) {
+        const uint2 kw = *reinterpret_cast<const uint2*>(ks + roff[r]);
+        const float2 k01 = unpack2<BF16>(kw.x), k23 = unpack2<BF16>(kw.y);
+        kv[r][0] = k01.x; kv[r][1] = k01.y; kv[r][2] = k23.x; kv[r][3] = k23.y;
+      } else {
+        const float2 k01 = unpack2<BF16>(*reinterpret_cast<const uint32_t*>(ks + roff[r]));
+        kv[r][0] = k01.x; kv[r][1] = k01.y;
       }
     }
-    compute_sync();
 
-    // online softmax: warp w owns rows w and w + 8
-    for (int qi = warp; qi < p.Nq; qi += kDecCompute / 32) {
-      float* row = sc + qi * kDecTile;
-      const float s0 = row[lane], s1 = row[lane + 32];
-      float mx = fmaxf(s0, s1);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-      const float m_old = m_run[qi];
-      const float m_new = fmaxf(m_old, mx);
+    for (int qi = 0; qi < kDecMaxQ; ++qi) {
+      if (qi >= p.Nq) break;
+      // partial dot products over this lane's slice, then a reduce-scatter across lanes
+      float qv[E];
+      if constexpr (E == 4) {
+        const float4 q4 = *reinterpret_cast<const float4*>(qs + qi * D + E * lane);
+        qv[0] = q4.x; qv[1] = q4.y; qv[2] = q4.z; qv[3] = q4.w;
+      } else {
+        const float2 q2 = *reinterpret_cast<const float2*>(qs + qi * D + E * lane);
+        qv[0] = q2.x; qv[1] = q2.y;
+      }
+      float t8[kKeysPerWarp];
+#pragma unroll
+      for (int r = 0; r < kKeysPerWarp; ++r) {
+        float a = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) a = fmaf(qv[e], kv[r][e], a);
+        t8[r] = a;
+      }
+      float t4[4], t2[2];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const bool hi = lane & 16;
+        const float send = hi ? t8[r] : t8[r + 4];
+        const float keep = hi ? t8[r + 4] : t8[r];
+        t4[r] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+      }
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const bool hi = lane & 8;
+        const float send = hi ? t4[r] : t4[r + 2];
+        const float keep = hi ? t4[r + 2] : t4[r];
+        t2[r] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
+      }
+      float sc1;
+      {
+        const bool hi = lane & 4;
+        const float send = hi ? t2[0] : t2[1];
+        const float keep = hi ? t2[1] : t2[0];
+        sc1 = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 4);
+      }
+      sc1 += __shfl_xor_sync(0xFFFFFFFFu, sc1, 2);
+      sc1 += __shfl_xor_sync(0xFFFFFFFFu, sc1, 1);
+      const int key = key0 + my_key;
+      const bool visible = key < k1 && (!p.causal || key <= last_key_shift + qi);
+      if (!visible) sc1 = -INFINITY;
+      // online softmax over the warp's 8 keys
+      float mx = sc1;
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
+      const float m_new = fmaxf(m_w[qi], mx);
       const float m_use = m_new == -INFINITY ? 0.f : m_new;
-      const float p0 = ptx::ex2(s0 - m_use), p1 = ptx::ex2(s1 - m_use);
-      float sum = p0 + p1;
+      const float pk = ptx::ex2(sc1 - m_use);
+      float sum = pk;
+      sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
+      sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 8);
+      sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 16);
+      const float corr = m_w[qi] == -INFINITY ? 0.f : ptx::ex2(m_w[qi] - m_use);
+      l_w[qi] = l_w[qi] * corr + sum;
+      m_w[qi] = m_new;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-      row[lane] = p0;
-      row[lane + 32] = p1;
-      __syncwarp();
-      if (lane == 0) {
-        const float a = m_old == -INFINITY ? 0.f : ptx::ex2(m_old - m_use);
-        alpha[qi] = a;
-        l_run[qi] = l_run[qi] * a + sum;
-        m_run[qi] = m_new;
-      }
-    }
-    compute_sync();
-
-    // O += P V: two columns per thread, rows qset, qset + kQSets, ...
+      for (int e = 0; e < E; ++e) acc[qi][e] *= corr;
 #pragma unroll
-    for (int a = 0; a < kDecMaxQ / kQSets; ++a) {
-      const int qi = qset + a * kQSets;
-      if (qi < p.Nq) {
-        const float* pr = sc + qi * kDecTile;
-        float2 o2 = acc[a];
-        const float al = alpha[qi];
-        o2.x *= al;
-        o2.y *= al;
-        for (int k = 0; k < valid; ++k) {             // rows past `valid` were never loaded
-          const float w = pr[k];
-          const float2 v2 = unpack2<BF16>(*reinterpret_cast<const uint32_t*>(vs + k * C::kRow + 4 * cp));
-          o2.x = fmaf(w, v2.x, o2.x);
-          o2.y = fmaf(w, v2.y, o2.y);
+      for (int r = 0; r < kKeysPerWarp; ++r) {
+        // weight of key r lives in the lanes whose bits 4,3,2 spell r
+        const float w = __shfl_sync(0xFFFFFFFFu, pk, ((r >> 2) & 1) * 16 + ((r >> 1) & 1) * 8 + (r & 1) * 4);
+        float vv[E];
+        if constexpr (E == 4) {
+          const uint2 vw = *reinterpret_cast<const uint2*>(vs + roff[r]);
+          const float2 v01 = unpack2<BF16>(vw.x), v23 = unpack2<BF16>(vw.y);
+          vv[0] = v01.x; vv[1] = v01.y; vv[2] = v23.x; vv[3] = v23.y;
+        } else {
+          const float2 v01 = unpack2<BF16>(*reinterpret_cast<const uint32_t*>(vs + roff[r]));
+          vv[0] = v01.x; vv[1] = v01.y;
         }
-        acc[a] = o2;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[qi][e] = fmaf(w, vv[e], acc[qi][e]);
       }
     }
-    // this stage may be refilled once every compute warp is past it
+    // this warp's rows are read: the stage may be refilled once all 8 warps are here
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(empty(s));
-    compute_sync();
-  }
-  if (*abort_flag) return;
-
-  // normalise; write the final output (one chunk) or this chunk's partial
-  const bool single = p.splits == 1;
-#pragma unroll
-  for (int a = 0; a < kDecMaxQ / kQSets; ++a) {
-    const int qi = qset + a * kQSets;
-    if (qi < p.Nq) {
-      const float l = l_run[qi];
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const float ox = acc[a].x * inv, oy = acc[a].y * inv;
-      if (single) {
-        uint32_t w;
-        if constexpr (BF16) {
-          const __nv_bfloat162 h = __floats2bfloat162_rn(ox, oy);
-          w = *reinterpret_cast<const uint32_t*>(&h);
-        } else {
-          const __half2 h = __floats2half2_rn(ox, oy);
-          w = *reinterpret_cast<const uint32_t*>(&h);
-        }
-        reinterpret_cast<uint32_t*>(p.o)[(qbase + static_cast<size_t>(qi) * D) / 2 + cp] = w;
-      } else {
-        const size_t pb = ((static_cast<size_t>(bh) * p.splits + split) * p.Nq + qi) * D;
-        reinterpret_cast<float2*>(p.part_o)[pb / 2 + cp] = make_float2(ox, oy);
-      }
+    if (loader && i + kDecStages < ntiles) {
+      if (!ptx::mbar_wait(empty(s), (i / kDecStages) & 1u, ctl, kDecStatusTimeout)) { ok = false; break; }
+      issue(i + kDecStages);
     }
   }
-  if (tid < p.Nq) {
-    const float l = l_run[tid];
-    const float lse = l > 0.f ? (m_run[tid] + ptx::lg2(l)) * kDecLn2 : -INFINITY;
+  // copies in flight land before the CTA exits (immediate on the normal path)
+  if (loader) {
+    // tiles are issued in order, so the last fill of stage st is the largest tile
+    // index <= last_issued that maps to st
+    for (int st = 0; st < kDecStages && st <= last_issued; ++st) {
+      const int i = last_issued - (last_issued - st) % kDecStages;
+      if (!ptx::mbar_wait_drain(full(st), static_cast<uint32_t>(i / kDecStages) & 1u, p.timeout_ns))
+        atomicOr(p.status, kDecStatusTimeout);
+    }
+  }
+  // leave together if any warp gave up
+  compute_sync();
+  if (!ok || *abort_flag) return;
+
+  // merge the 8 warps: M = max m_w, L = sum l_w 2^(m_w - M), O = sum acc_w 2^(m_w - M) / L
+  float* red_o = reinterpret_cast<float*>(smem + C::kKOff);     // the ring is idle now
+  float* red_m = sc;                                            // [8 warps][kDecMaxQ]
+  float* red_l = sc + (kDecCompute / 32) * kDecMaxQ;
+#pragma unroll
+  for (int qi = 0; qi < kDecMaxQ; ++qi) {
+    if (qi >= p.Nq) break;
+#pragma unroll
+    for (int e = 0; e < E; ++e) red_o[(warp * kDecMaxQ + qi) * D + E * lane + e] = acc[qi][e];
+    if (lane == 0) {
+      red_m[warp * kDecMaxQ + qi] = m_w[qi];
+      red_l[warp * kDecMaxQ + qi] = l_w[qi];
+    }
+  }
+  compute_sync();
+  const bool single = p.splits == 1;
+  for (int idx = tid; idx < p.Nq * (D / 2); idx += kDecCompute) {
+    const int qi = idx / (D / 2), cpair = idx % (D / 2);
+    float M = -INFINITY;
+    for (int w = 0; w < kDecCompute / 32; ++w) M = fmaxf(M, red_m[w * kDecMaxQ + qi]);
+    float L = 0.f, ox = 0.f, oy = 0.f;
+    if (M != -INFINITY) {
+      for (int w = 0; w < kDecCompute / 32; ++w) {
+        const float mw = red_m[w * kDecMaxQ + qi];
+        const float f = mw == -INFINITY ? 0.f : ptx::ex2(mw - M);
+        L = fmaf(red_l[w * kDecMaxQ + qi], f, L);
+        ox = fmaf(red_o[(w * kDecMaxQ + qi) * D + 2 * cpair], f, ox);
+        oy = fmaf(red_o[(w * kDecMaxQ + qi) * D + 2 * cpair + 1], f, oy);
+      }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    ox *= inv;
+    oy *= inv;
     if (single) {
-      if (p.lse) p.lse[static_cast<size_t>(bh) * p.Nq + tid] = lse;
+      uint32_t wv;
+      if constexpr (BF16) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(ox, oy);
+        wv = *reinterpret_cast<const uint32_t*>(&h);
+      } else {
+        const __half2 h = __floats2half2_rn(ox, oy);
+        wv = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      reinterpret_cast<uint32_t*>(p.o)[(qbase + static_cast<size_t>(qi) * D) / 2 + cpair] = wv;
     } else {
-      p.part_lse[(static_cast<size_t>(bh) * p.splits + split) * p.Nq + tid] = lse;
+      const size_t pb = ((static_cast<size_t>(bh) * p.splits + split) * p.Nq + qi) * D;
+      reinterpret_cast<float2*>(p.part_o)[pb / 2 + cpair] = make_float2(ox, oy);
+    }
+    if (cpair == 0) {
+      const float lse = L > 0.f ? (M + ptx::lg2(L)) * kDecLn2 : -INFINITY;
+      if (single) {
+        if (p.lse) p.lse[static_cast<size_t>(bh) * p.Nq + qi] = lse;
+      } else {
+        p.part_lse[(static_cast<size_t>(bh) * p.splits + split) * p.Nq + qi] = lse;
+      }
     }
   }
 }
@@ -328,9 +396,10 @@ __global__ void __launch_bounds__(256) fa_decode_merge_kernel(const __grid_const
 template <int D, bool BF16>
 cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
   auto split = fa_decode_split_kernel<D, BF16>;
-  cudaError_t e = cudaFuncSetAttribute(split, cudaFuncAttributeMaxDynamicSharedMemorySize, DecCfg<D>::kBytes);
+  constexpr int kSmem = DecCfg<D>::kBytes + 1024;          // room to align the base to 1 KB
+  cudaError_t e = cudaFuncSetAttribute(split, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  split<<<p.BH * p.splits, kDecThreads, DecCfg<D>::kBytes, stream>>>(p);
+  split<<<p.BH * p.splits, kDecThreads, kSmem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess || p.splits == 1) return e;
   fa_decode_merge_kernel<D, BF16><<<(p.BH * p.Nq + 7) / 8, 256, 0, stream>>>(p);

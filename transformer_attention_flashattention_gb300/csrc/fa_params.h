@@ -45,6 +45,8 @@ struct QuantParams {
 
 // Split-KV attention of N_q query rows against N_k cached keys.
 struct DecodeParams {
+  CUtensorMap tm_k;   // 3-D {d, Nk, B*H}, box {64, 64, 1}, 128-byte swizzle
+  CUtensorMap tm_v;
   const void* q;      // [B*H, Nq, d]
   const void* k;      // [B*H, Nk, d]
   const void* v;
