@@ -116,6 +116,43 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, 
 int fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits,
                              unsigned long long* bytes);
 
+/* Size of the static scratch area behind fa_decode_noalloc, per device (8 MiB). */
+#define FA_DECODE_NOALLOC_SCRATCH_BYTES (8ull << 20)
+
+/*
+ * fa_decode without a workspace argument, for callers that cannot allocate
+ * device memory: a plugin that the host program hands only its input and output
+ * buffers, or a serving loop that must not allocate once it has started.  The
+ * attention pages define no such call; it computes exactly what fa_decode
+ * computes, with the same arguments (minus workspace), the same kernels and the
+ * same results.
+ *
+ * The split scratch is a fixed FA_DECODE_NOALLOC_SCRATCH_BYTES array of device
+ * memory inside this library (one per device, reserved when the library's device
+ * code is loaded there).  The call allocates nothing: no cudaMalloc, no pool, no
+ * allocating library routine.
+ *   - Limit: with num_splits = 0 the scratch fa_decode needs is at most 5,003,136
+ *     bytes (under 4.8 MiB) for every supported shape on a GB300 (152 SMs), so
+ *     only an explicit large num_splits can exceed the area.  When fa_decode_workspace_size reports more
+ *     than FA_DECODE_NOALLOC_SCRATCH_BYTES for these sizes, the call returns
+ *     FA_ERR_WORKSPACE and launches nothing; use a smaller num_splits, or
+ *     fa_decode with a workspace of your own.
+ *   - Set-up: the first call on each device looks up the array's address with
+ *     cudaGetSymbolAddress (which may load this library's device code on that
+ *     device) and returns FA_ERR_CUDA if that fails.  Make that first call
+ *     outside any stream capture.
+ *   - Zeroing: none needed.  Each call writes every scratch slot it reads, before
+ *     reading it.
+ *   - Races: all calls on one device share the one array.  Calls that can run on
+ *     the GPU at the same time (on two streams, or from two host threads without
+ *     ordering) corrupt each other's results; keep them on one stream or order
+ *     them with events.
+ * Other errors are those of fa_decode.
+ */
+int fa_decode_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                      int Nq, int Nk, int d, float scale, int causal, int dtype, int num_splits,
+                      void* stream);
+
 /* Static English text for a status code (never NULL). */
 const char* fa_strerror(int status);
 

@@ -33,7 +33,7 @@ def lib():
 def test_header_declares_the_boundary():
     assert _declared() == sorted(["fa_fwd", "fa_quantize_fp8", "fa_fwd_fp8", "fa_strerror",
                                   "fa_last_device_status", "fa_debug_inject_stall", "fa_version",
-                                  "fa_decode", "fa_decode_workspace_size"])
+                                  "fa_decode", "fa_decode_workspace_size", "fa_decode_noalloc"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -87,3 +87,13 @@ def test_decode_rejects_bad_arguments_on_the_host(lib, args, want):
     q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype, splits, ws, wsb = args
     assert lib.fa_decode(q or None, k or None, v or None, o or None, lse or None, B, H, Nq, Nk, d, scale,
                          causal, dtype, splits, ws or None, wsb, None) == want
+
+
+@pytest.mark.parametrize("Nq,Nk,d,want", [
+    (17, 128, 64, fa.FA_ERR_SHAPE),      # N_q > 16
+    (4, 3, 64, fa.FA_ERR_SHAPE),         # N_q > N_k
+    (0, 128, 64, fa.FA_ERR_SHAPE),
+    (1, 128, 80, fa.FA_ERR_UNSUPPORTED),
+])
+def test_decode_noalloc_rejects_bad_shapes_on_the_host(lib, Nq, Nk, d, want):
+    assert lib.fa_decode_noalloc(A, A, A, A, None, 1, 1, Nq, Nk, d, 0.125, 0, 1, 0, None) == want

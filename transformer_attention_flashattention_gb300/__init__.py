@@ -25,6 +25,8 @@ __all__ = [
     "quantize_fp8",
     "attention_fp8",
     "decode",
+    "decode_noalloc",
+    "DECODE_NOALLOC_SCRATCH_BYTES",
     "last_device_status",
     "inject_stall",
     "FA_OK",
@@ -50,6 +52,9 @@ FA_ERR_ARCH = -7
 FA_ERR_CUDA = -8
 FA_ERR_WORKSPACE = -9
 
+# Size of the static scratch area behind decode_noalloc (FA_DECODE_NOALLOC_SCRATCH_BYTES).
+DECODE_NOALLOC_SCRATCH_BYTES = 8 << 20
+
 _PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 _LIB: Optional[ctypes.CDLL] = None
 
@@ -62,6 +67,7 @@ _SIGNATURES = {
     "fa_fwd_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _i, _vp]),
     "fa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _vp, ctypes.c_ulonglong, _vp]),
     "fa_decode_workspace_size": (_i, [_i, _i, _i, _i, _i, _i, ctypes.POINTER(ctypes.c_ulonglong)]),
+    "fa_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _vp]),
     "fa_strerror": (ctypes.c_char_p, [_i]),
     "fa_last_device_status": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),
     "fa_debug_inject_stall": (_i, [_i, _i]),
@@ -262,6 +268,44 @@ def decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = Fal
                        int(bool(causal)), _DTYPES[q.dtype], int(num_splits), _ptr(workspace), ws_bytes,
                        _stream_handle(stream, q.device))
     _check(st, "fa_decode")
+    return out, lse
+
+
+def decode_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+                   scale: Optional[float] = None, num_splits: int = 0, out: Optional[torch.Tensor] = None,
+                   lse: Optional[torch.Tensor] = None, return_lse: bool = True,
+                   stream: Optional[torch.cuda.Stream] = None):
+    """``decode`` through ``fa_decode_noalloc``: the split scratch is the library's
+    static per-device area, so the C call allocates nothing (pass ``out`` and
+    ``lse`` to keep this wrapper from allocating them).  Calls that can overlap on
+    the GPU share that area and race; the first call on a device does a one-time
+    address look-up and belongs outside stream capture.  Raises FAError
+    (FA_ERR_WORKSPACE) when these sizes need more than DECODE_NOALLOC_SCRATCH_BYTES.
+    """
+    lib = load_library()
+    B, H, Nq, d = q.shape
+    if k.dim() != 4 or k.shape != v.shape or k.shape[:2] != (B, H) or k.shape[3] != d:
+        raise ValueError(f"k, v must be [B, H, N_k, d] matching q; got {tuple(k.shape)}, {tuple(v.shape)}")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype:
+            raise ValueError(f"{name} must be a contiguous CUDA tensor of q's dtype")
+    if q.dtype not in _DTYPES:
+        raise ValueError(f"dtype must be float16 or bfloat16, got {q.dtype}")
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, Nq), device=q.device, dtype=torch.float32)
+    with torch.cuda.device(q.device):
+        st = lib.fa_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nk, d,
+                                   float(scale), int(bool(causal)), _DTYPES[q.dtype], int(num_splits),
+                                   _stream_handle(stream, q.device))
+    if st == FA_ERR_WORKSPACE:
+        raise FAError(st, f"fa_decode_noalloc (these sizes need more than the "
+                          f"{DECODE_NOALLOC_SCRATCH_BYTES}-byte static scratch: lower num_splits or use decode)")
+    _check(st, "fa_decode_noalloc")
     return out, lse
 
 
