@@ -195,63 +195,70 @@ drain:
 // ---------------------------------------------------------------------------- MMA issuer
 
 // PV and S MMAs of Q tile t for key step j (called by the single MMA thread).
+// Descriptor low words of ring slot s are the slot-0 word plus s * (tile bytes >> 4):
+// shared addresses stay below 2^18, so the sum never carries into the LBO field.
 template <int D, Elem E>
-__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tS, uint32_t vbase, bool accumulate) {
+__host__ __device__ constexpr uint32_t v_lbo() {
+  // 16-bit V is [N, d] (MN-major B, 64-wide d atoms one atom apart); E4M3 V^T is K-major
+  return FwdCfg<D, E>::kFp8 ? 16u : static_cast<uint32_t>(FwdCfg<D, E>::kAtomBytes);
+}
+
+// The MMAs of one PV or S block, unrolled at compile time so that every operand
+// offset is an immediate (see the _o wrappers).
+template <int D, Elem E, bool ACC, int KK = 0>
+__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tS, uint32_t v_lo) {
   using L = FwdCfg<D, E>;
-  constexpr uint32_t idesc_pv = ptx::idesc_make(kBlockM, D, L::kAbType, false, !L::kFp8);
-  constexpr uint32_t desc_hi = ptx::sdesc_hi(1024);
-  if constexpr (L::kFp8) {
-    // V^T rows (d) of 128 key bytes: 32 keys (32 bytes) per step inside the atom
-    const uint32_t v_lo = ptx::sdesc_lo(vbase, 16);
-    if (accumulate) ptx::mma_f8_ts_c<1>(tO, tS, v_lo, desc_hi, idesc_pv);
-    else ptx::mma_f8_ts_c<0>(tO, tS, v_lo, desc_hi, idesc_pv);
-#pragma unroll
-    for (int kk = 1; kk < L::kPvSteps; ++kk)
-      ptx::mma_f8_ts_c<1>(tO, tS + kk * 8, v_lo + ((kk * 32) >> 4), desc_hi, idesc_pv);
-  } else {
-    // V is [N, d] (MN-major B): 16 key rows (2 KB) per step; 64-wide d atoms 16 KB apart
-    const uint32_t v_lo = ptx::sdesc_lo(vbase, L::kAtomBytes);
-    if (accumulate) ptx::mma_f16_ts_c<1>(tO, tS, v_lo, desc_hi, idesc_pv);
-    else ptx::mma_f16_ts_c<0>(tO, tS, v_lo, desc_hi, idesc_pv);
-#pragma unroll
-    for (int kk = 1; kk < L::kPvSteps; ++kk)
-      ptx::mma_f16_ts_c<1>(tO, tS + kk * 8, v_lo + ((kk * 16 * 128) >> 4), desc_hi, idesc_pv);
+  if constexpr (KK < L::kPvSteps) {
+    constexpr uint32_t idesc_pv = ptx::idesc_make(kBlockM, D, L::kAbType, false, !L::kFp8);
+    constexpr uint32_t desc_hi = ptx::sdesc_hi(1024);
+    constexpr int kAcc = (ACC || KK > 0) ? 1 : 0;
+    // P: 8 TMEM columns per step (16 packed 16-bit or 32 packed E4M3 keys).  B: 16-bit
+    // V is [N, d], 16 key rows (2 KB) per step; E4M3 V^T rows hold 32 keys per step.
+    constexpr uint32_t kOb = L::kFp8 ? (KK * 32) >> 4 : (KK * 16 * 128) >> 4;
+    if constexpr (L::kFp8) ptx::mma_f8_ts_o<kAcc, KK * 8, kOb>(tO, tS, v_lo, desc_hi, idesc_pv);
+    else ptx::mma_f16_ts_o<kAcc, KK * 8, kOb>(tO, tS, v_lo, desc_hi, idesc_pv);
+    issue_pv<D, E, ACC, KK + 1>(tO, tS, v_lo);
   }
 }
 
-template <int D, Elem E>
+template <int D, Elem E, int KK = 0>
 __device__ __forceinline__ void issue_s(uint32_t tS, uint32_t q_lo, uint32_t k_lo) {
   using L = FwdCfg<D, E>;
-  constexpr uint32_t idesc_qk = ptx::idesc_make(kBlockM, kBlockN, L::kAbType, false, false);
-  constexpr uint32_t desc_hi = ptx::sdesc_hi(1024);
-  // K-major operands: 32 bytes of d per step inside a 128-byte swizzle atom
-#pragma unroll
-  for (int kk = 0; kk < D / L::kMmaK; ++kk) {
-    const uint32_t off = ((kk * 32 / 128) * L::kAtomBytes + (kk * 32) % 128) >> 4;
-    if constexpr (L::kFp8) {
-      if (kk == 0) ptx::mma_f8_ss_c<0>(tS, q_lo, desc_hi, k_lo, desc_hi, idesc_qk);
-      else ptx::mma_f8_ss_c<1>(tS, q_lo + off, desc_hi, k_lo + off, desc_hi, idesc_qk);
-    } else {
-      if (kk == 0) ptx::mma_f16_ss_c<0>(tS, q_lo, desc_hi, k_lo, desc_hi, idesc_qk);
-      else ptx::mma_f16_ss_c<1>(tS, q_lo + off, desc_hi, k_lo + off, desc_hi, idesc_qk);
-    }
+  if constexpr (KK < D / L::kMmaK) {
+    constexpr uint32_t idesc_qk = ptx::idesc_make(kBlockM, kBlockN, L::kAbType, false, false);
+    constexpr uint32_t desc_hi = ptx::sdesc_hi(1024);
+    // K-major operands: 32 bytes of d per step inside a 128-byte swizzle atom
+    constexpr uint32_t kOff = ((KK * 32 / 128) * L::kAtomBytes + (KK * 32) % 128) >> 4;
+    if constexpr (L::kFp8) ptx::mma_f8_ss_o<KK ? 1 : 0, kOff, kOff>(tS, q_lo, k_lo, desc_hi, idesc_qk);
+    else ptx::mma_f16_ss_o<KK ? 1 : 0, kOff, kOff>(tS, q_lo, k_lo, desc_hi, idesc_qk);
+    issue_s<D, E, KK + 1>(tS, q_lo, k_lo);
   }
 }
 
 // One thread issues every MMA, in the order
 //   O_0 += P_0 V_{j-1};  S_0 = Q_0 K_j^T;  O_1 += P_1 V_{j-1};  S_1 = Q_1 K_j^T
 // so the tensor pipe runs one tile's pair while the other tile's softmax works.
-// tcgen05.mma issue blocks on a very short queue, so the thread does as little as
-// possible between issues: descriptors are a precomputed base plus a constant, and
-// accumulate flags are compile-time constants.  MMAs run in issue order, which is
-// what lets S_t(j+1) overwrite the TMEM holding P_t(j) after O_t += P_t(j) V_j.
+// tcgen05.mma issue blocks on a very short queue: an MMA takes about as long to
+// issue as the tensor pipe takes to run the one before it, so every instruction
+// between MMA groups leaves the pipe idle.  The steps where both tiles do the same
+// thing (all but the first two and the last ones of a unit) therefore run in a
+// separate loop without per-tile conditions, with ring slots and barrier parities
+// advanced incrementally and descriptors formed by one add.  MMAs run in issue
+// order, which is what lets S_t(j+1) overwrite the TMEM holding P_t(j) after
+// O_t += P_t(j) V_j.
 template <int D, Elem E>
 __device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_t tmem,
                                      const ptx::WaitCtl& ctl) {
   using L = FwdCfg<D, E>;
-  auto bar = [&](int i) { return sbase + L::kBarOff + 8u * i; };
+  const uint32_t bar0 = sbase + L::kBarOff;
+  auto bar = [bar0](int i) { return bar0 + 8u * i; };
+  constexpr uint32_t kSlotDesc = L::kTileBytes >> 4;
   const uint32_t q_lo0 = ptx::sdesc_lo(sbase + L::kQOff, 16);
   const uint32_t q_lo1 = ptx::sdesc_lo(sbase + L::kQOff + L::kTileBytes, 16);
+  const uint32_t k_lo0 = ptx::sdesc_lo(sbase + L::kKVOff, 16);
+  const uint32_t v_lo0 = ptx::sdesc_lo(sbase + L::kKVOff, v_lbo<D, E>());
+  const uint32_t tS0 = tmem + L::kTmemS, tS1 = tS0 + kBlockN;
+  const uint32_t tO0 = tmem + L::kTmemO, tO1 = tO0 + D;
   uint32_t load_idx = 0;
   uint32_t q_uses[kQTiles] = {0, 0};
   uint32_t p_uses[kQTiles] = {0, 0};
@@ -261,7 +268,42 @@ __device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_
     decode_unit(p, u, bh, qb);
     const int nt[kQTiles] = {tile_nkv(p, qb, 0), tile_nkv(p, qb, 1)};
     const int n = max(nt[0], nt[1]);
+    // steps 2 .. steady_end - 1: both tiles run PV(j-1) and S(j), none of them is a
+    // tile's last PV or last S, and V_{j-1} sits right after K_j in the ring
+    const int steady_end = min(nt[0], nt[1]) - 1;
     for (int j = 0; j <= n; ++j) {
+      if (j == 2 && steady_end > 2) {
+        uint32_t c = load_idx + 2u * j - 1u;                 // ring position of K_j
+        uint32_t ks = c % L::kStages, kph = (c / L::kStages) & 1u;
+        uint32_t pp0 = p_uses[0] & 1u, pp1 = p_uses[1] & 1u;
+        for (; j < steady_end; ++j) {
+          uint32_t vs = ks + 1, vph = kph;
+          if (vs == L::kStages) { vs = 0; vph ^= 1u; }
+          const uint32_t v_lo = v_lo0 + vs * kSlotDesc, k_lo = k_lo0 + ks * kSlotDesc;
+          if (!ptx::mbar_wait(bar(L::kKVFull) + 8u * vs, vph, ctl, kStatusMmaTimeout)) goto done;
+          if (!ptx::mbar_wait(bar(L::kPFull), pp0, ctl, kStatusMmaTimeout)) goto done;
+          ptx::tc_fence_after();
+          issue_pv<D, E, true>(tO0, tS0, v_lo);
+          if (!ptx::mbar_wait(bar(L::kKVFull) + 8u * ks, kph, ctl, kStatusMmaTimeout)) goto done;
+          issue_s<D, E>(tS0, q_lo0, k_lo);
+          ptx::mma_commit(bar(L::kSFull));
+          if (!ptx::mbar_wait(bar(L::kPFull + 1), pp1, ctl, kStatusMmaTimeout)) goto done;
+          ptx::tc_fence_after();
+          issue_pv<D, E, true>(tO1, tS1, v_lo);
+          issue_s<D, E>(tS1, q_lo1, k_lo);
+          ptx::mma_commit(bar(L::kSFull + 1));
+          ptx::mma_commit(bar(L::kKVEmpty) + 8u * vs);
+          ptx::mma_commit(bar(L::kKVEmpty) + 8u * ks);
+          pp0 ^= 1u;
+          pp1 ^= 1u;
+          ks = vs + 1;
+          kph = vph;
+          if (ks == L::kStages) { ks = 0; kph ^= 1u; }
+        }
+        p_uses[0] += steady_end - 2;
+        p_uses[1] += steady_end - 2;
+        if (j > n) break;
+      }
       uint32_t kslot = 0, vslot = 0;
       bool k_ready = false;
       if (j >= 1) {
@@ -272,13 +314,15 @@ __device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_
       }
 #pragma unroll
       for (int t = 0; t < kQTiles; ++t) {
-        const uint32_t tS = tmem + L::kTmemS + t * kBlockN;
+        const uint32_t tS = t ? tS1 : tS0;
         if (j >= 1 && j - 1 < nt[t]) {
           // O_t += P_t V_{j-1}
           if (!ptx::mbar_wait(bar(L::kPFull + t), p_uses[t] & 1u, ctl, kStatusMmaTimeout)) goto done;
           ++p_uses[t];
           ptx::tc_fence_after();
-          issue_pv<D, E>(tmem + L::kTmemO + t * D, tS, sbase + L::kKVOff + vslot * L::kTileBytes, j - 1 > 0);
+          const uint32_t v_lo = v_lo0 + vslot * kSlotDesc;
+          if (j - 1 > 0) issue_pv<D, E, true>(t ? tO1 : tO0, tS, v_lo);
+          else issue_pv<D, E, false>(t ? tO1 : tO0, tS, v_lo);
           if (j - 1 == nt[t] - 1) ptx::mma_commit(bar(L::kOFull + t));
         }
         if (j < nt[t]) {
@@ -294,7 +338,7 @@ __device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_
             if (!ptx::mbar_wait(bar(L::kQFull + t), q_uses[t] & 1u, ctl, kStatusMmaTimeout)) goto done;
             ++q_uses[t];
           }
-          issue_s<D, E>(tS, t == 0 ? q_lo0 : q_lo1, ptx::sdesc_lo(sbase + L::kKVOff + kslot * L::kTileBytes, 16));
+          issue_s<D, E>(tS, t == 0 ? q_lo0 : q_lo1, k_lo0 + kslot * kSlotDesc);
           ptx::mma_commit(bar(L::kSFull + t));
           if (j == nt[t] - 1) ptx::mma_commit(bar(L::kQEmpty + t));
         }

@@ -215,6 +215,59 @@ __device__ __forceinline__ void mma_f8_ts_c(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// Same MMAs with compile-time offsets added inside the asm block: OA / OB to the
+// low descriptor words (16-byte units), OT to the TMEM address of A.  Keeping the
+// adds inside the asm stops the compiler from hoisting one register per offset out
+// of the issuing loop; the A and B descriptors share their high word.
+template <int ACC, uint32_t OA, uint32_t OB>
+__device__ __forceinline__ void mma_f16_ss_o(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                             uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b32 la, lb;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "add.u32 la, %1, %6;\n\tadd.u32 lb, %2, %7;\n\t"
+      "mov.b64 da, {la, %3};\n\tmov.b64 db, {lb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "n"(ACC), "n"(OA), "n"(OB)
+      : "memory");
+}
+template <int ACC, uint32_t OT, uint32_t OB>
+__device__ __forceinline__ void mma_f16_ts_o(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                                             uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b32 ta, lb;\n\t.reg .b64 db;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "add.u32 ta, %1, %6;\n\tadd.u32 lb, %2, %7;\n\t"
+      "mov.b64 db, {lb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "n"(ACC), "n"(OT), "n"(OB)
+      : "memory");
+}
+template <int ACC, uint32_t OA, uint32_t OB>
+__device__ __forceinline__ void mma_f8_ss_o(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                            uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b32 la, lb;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "add.u32 la, %1, %6;\n\tadd.u32 lb, %2, %7;\n\t"
+      "mov.b64 da, {la, %3};\n\tmov.b64 db, {lb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "n"(ACC), "n"(OA), "n"(OB)
+      : "memory");
+}
+template <int ACC, uint32_t OT, uint32_t OB>
+__device__ __forceinline__ void mma_f8_ts_o(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                                            uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b32 ta, lb;\n\t.reg .b64 db;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "add.u32 ta, %1, %6;\n\tadd.u32 lb, %2, %7;\n\t"
+      "mov.b64 db, {lb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [ta], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "n"(ACC), "n"(OT), "n"(OB)
+      : "memory");
+}
+
 // Arrives once on `bar` when every tcgen05 operation issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
