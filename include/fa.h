@@ -166,8 +166,9 @@ int fa_last_device_status(void* stream, unsigned int* bits);
 
 /*
  * Test hook for the failure path: the next fa_fwd call's producer leaves out
- * K/V load number `load_index` of every CTA (so the consumers' bounded waits
- * run out), and every wait of that call gives up after `timeout_ms` ms.  The
+ * the K/V loads of the pipeline step that holds K/V load number `load_index`
+ * of every CTA (so the consumers' bounded waits run out), and every wait of
+ * that call gives up after `timeout_ms` ms.  The
  * call still returns FA_OK; fa_last_device_status then reports the timeout.
  * load_index < 0 clears the hook.  Not for production use.
  */

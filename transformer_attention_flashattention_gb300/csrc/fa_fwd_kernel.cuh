@@ -81,9 +81,15 @@ struct FwdCfg {
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kQOff + kQTiles * kTileBytes;
   static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
-  // barrier indices
-  static constexpr int kQFull = 0, kQEmpty = 2, kKVFull = 4, kKVEmpty = 4 + kStages;
-  static constexpr int kSFull = 4 + 2 * kStages, kPFull = kSFull + 2, kOFull = kPFull + 2;
+  // barrier indices.  K/V handoff is per MMA step, not per ring slot: the loads a
+  // step consumes complete on one "ready" barrier and one commit per step frees
+  // its slots ("done").  A ring of kSteps > kStages step barriers never aliases a
+  // phase: every step carries at least one load, so a slot's previous occupant
+  // belongs to a step at most kStages back.
+  static constexpr int kSteps = 16;
+  static_assert(kSteps > kStages, "step ring must outlast the load ring");
+  static constexpr int kQFull = 0, kQEmpty = 2, kReady = 4, kDone = 4 + kSteps;
+  static constexpr int kSFull = 4 + 2 * kSteps, kPFull = kSFull + 2, kOFull = kPFull + 2;
   static constexpr int kMmaDone = kOFull + 2;
   static constexpr int kNumBars = kMmaDone + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM base slot, abort flag
@@ -123,16 +129,21 @@ __device__ __forceinline__ uint32_t v_pos(int j, int n) { return j + 1 < n ? 2u 
 
 // ---------------------------------------------------------------------------- producer
 
+// MMA step j of a unit consumes K_j (j < n) and V_{j-1} (j >= 1); the producer issues
+// them in that order into consecutive ring slots, completing on the step's ready
+// barrier, once the steps that consumed those slots' previous tiles are done.
 template <int D, Elem E>
 __device__ __noinline__ void fwd_producer(const FwdParams& p, uint32_t sbase,
                                              const ptx::WaitCtl& ctl) {
   using L = FwdCfg<D, E>;
   auto bar = [&](int i) { return sbase + L::kBarOff + 8u * i; };
-  uint32_t load_idx = 0;
+  uint32_t load_idx = 0;                 // ring position of the next K/V tile
+  uint32_t step = 0;                     // MMA steps prepared so far
   uint32_t q_fills[kQTiles] = {0, 0};
-  uint32_t last_fill[L::kStages];
+  uint32_t slot_step[L::kStages];        // 1 + the step consuming each slot's tile (0: empty)
 #pragma unroll
-  for (int s = 0; s < L::kStages; ++s) last_fill[s] = 0xFFFFFFFFu;
+  for (int s = 0; s < L::kStages; ++s) slot_step[s] = 0;
+  uint32_t armed = 0;                    // bit g % kSteps: step g's loads were issued
 
   for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
     int bh, qb;
@@ -151,40 +162,56 @@ __device__ __noinline__ void fwd_producer(const FwdParams& p, uint32_t sbase,
                          bar(L::kQFull + t), a * L::kAtomElems, qb * kUnitRows + t * kBlockM, bh);
       ++q_fills[t];
     }
-    for (int pos = 0; pos < 2 * n; ++pos) {
-      // position -> (K or V, tile j), the inverse of k_pos / v_pos
-      const bool is_k = pos == 0 || ((pos & 1) && (pos + 1) / 2 < n);
-      const int kv = is_k ? 0 : 1;
-      const int j = is_k ? (pos + 1) / 2 : (pos == 2 * n - 1 ? n - 1 : pos / 2 - 1);
-      {
-        const uint32_t slot = load_idx % L::kStages;
-        const uint32_t fill = load_idx / L::kStages;
-        if (!ptx::mbar_wait(bar(L::kKVEmpty + slot), (fill & 1u) ^ 1u, ctl, kStatusLoadTimeout))
+    for (int j = 0; j <= n; ++j, ++step) {
+      const uint32_t cnt = (j < n ? 1u : 0u) + (j >= 1 ? 1u : 0u);
+      const uint32_t bit = 1u << (step % L::kSteps);
+      const uint32_t rb = bar(L::kReady + step % L::kSteps);
+      armed &= ~bit;
+      // test hook: the step holding load number dbg_skip_load gets none of its loads
+      const bool skip = p.dbg_skip_load >= 0 && static_cast<uint32_t>(p.dbg_skip_load) >= load_idx &&
+                        static_cast<uint32_t>(p.dbg_skip_load) < load_idx + cnt;
+      // each tile goes out as soon as its own slot is free; the step's last tile
+      // arrives on the ready barrier, earlier ones only add their bytes
+      for (uint32_t i = 0; i < cnt; ++i) {
+        const uint32_t slot = (load_idx + i) % L::kStages;
+        const uint32_t prev = slot_step[slot];
+        if (prev != 0 && !ptx::mbar_wait(bar(L::kDone + (prev - 1) % L::kSteps),
+                                         ((prev - 1) / L::kSteps) & 1u, ctl, kStatusLoadTimeout)) {
+          if (i > 0 && !skip) {
+            // a copy of this step is in flight: arrive so its phase completes when it lands
+            ptx::mbar_arrive(rb);
+            armed |= bit;
+          }
           goto drain;
-        if (static_cast<int>(load_idx) != p.dbg_skip_load) {
+        }
+        if (!skip) {
+          if (i + 1 < cnt) ptx::mbar_expect_tx(rb, L::kTileBytes);
+          else ptx::mbar_arrive_expect_tx(rb, L::kTileBytes);
+          const bool is_k = i == 0 && j < n;
+          const int jj = is_k ? j : j - 1;
           const uint32_t dst = sbase + L::kKVOff + slot * L::kTileBytes;
-          ptx::mbar_arrive_expect_tx(bar(L::kKVFull + slot), L::kTileBytes);
-          if (L::kFp8 && kv == 1) {
+          if (L::kFp8 && !is_k) {
             // V^T tile: 128 rows of d, 128 keys (bytes) each
-            ptx::tma_load_3d(dst, &p.tm_v, bar(L::kKVFull + slot), j * kBlockN, 0, bh);
+            ptx::tma_load_3d(dst, &p.tm_v, rb, jj * kBlockN, 0, bh);
           } else {
 #pragma unroll
             for (int a = 0; a < L::kAtoms; ++a)
-              ptx::tma_load_3d(dst + a * L::kAtomBytes, kv == 0 ? &p.tm_k : &p.tm_v,
-                               bar(L::kKVFull + slot), a * L::kAtomElems, j * kBlockN, bh);
+              ptx::tma_load_3d(dst + a * L::kAtomBytes, is_k ? &p.tm_k : &p.tm_v, rb, a * L::kAtomElems,
+                               jj * kBlockN, bh);
           }
-          last_fill[slot] = fill;
         }
-        ++load_idx;
+        slot_step[slot] = step + 1;
       }
+      if (!skip) armed |= bit;
+      load_idx += cnt;
     }
   }
 drain:
-  // Copies still in flight must land before the CTA may exit: wait for the latest
-  // issued fill of every slot (immediate on the normal path).
-  for (int s = 0; s < L::kStages; ++s)
-    if (last_fill[s] != 0xFFFFFFFFu &&
-        !ptx::mbar_wait_drain(bar(L::kKVFull + s), last_fill[s] & 1u, ctl.timeout_ns))
+  // Copies still in flight must land before the CTA may exit: wait for the ready
+  // phase of every step issued among the last kSteps (immediate on the normal path).
+  for (uint32_t g = step > static_cast<uint32_t>(L::kSteps) ? step - L::kSteps : 0; g < step; ++g)
+    if (((armed >> (g % L::kSteps)) & 1u) &&
+        !ptx::mbar_wait_drain(bar(L::kReady + g % L::kSteps), (g / L::kSteps) & 1u, ctl.timeout_ns))
       atomicOr(ctl.status, kStatusDrainTimeout);
   for (int t = 0; t < kQTiles; ++t)
     if (q_fills[t] > 0 &&
@@ -259,7 +286,9 @@ __device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_
   const uint32_t v_lo0 = ptx::sdesc_lo(sbase + L::kKVOff, v_lbo<D, E>());
   const uint32_t tS0 = tmem + L::kTmemS, tS1 = tS0 + kBlockN;
   const uint32_t tO0 = tmem + L::kTmemO, tO1 = tO0 + D;
+  const uint32_t ready0 = bar(L::kReady), done0 = bar(L::kDone);
   uint32_t load_idx = 0;
+  uint32_t step = 0;                     // MMA steps issued so far (the producer counts alike)
   uint32_t q_uses[kQTiles] = {0, 0};
   uint32_t p_uses[kQTiles] = {0, 0};
 
@@ -271,20 +300,18 @@ __device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_
     // steps 2 .. steady_end - 1: both tiles run PV(j-1) and S(j), none of them is a
     // tile's last PV or last S, and V_{j-1} sits right after K_j in the ring
     const int steady_end = min(nt[0], nt[1]) - 1;
-    for (int j = 0; j <= n; ++j) {
+    for (int j = 0; j <= n; ++j, ++step) {
       if (j == 2 && steady_end > 2) {
-        uint32_t c = load_idx + 2u * j - 1u;                 // ring position of K_j
-        uint32_t ks = c % L::kStages, kph = (c / L::kStages) & 1u;
+        uint32_t ks = (load_idx + 2u * j - 1u) % L::kStages;     // ring slot of K_j
         uint32_t pp0 = p_uses[0] & 1u, pp1 = p_uses[1] & 1u;
-        for (; j < steady_end; ++j) {
-          uint32_t vs = ks + 1, vph = kph;
-          if (vs == L::kStages) { vs = 0; vph ^= 1u; }
+        for (; j < steady_end; ++j, ++step) {
+          const uint32_t vs = ks + 1 == L::kStages ? 0u : ks + 1;  // V_{j-1} follows K_j
           const uint32_t v_lo = v_lo0 + vs * kSlotDesc, k_lo = k_lo0 + ks * kSlotDesc;
-          if (!ptx::mbar_wait(bar(L::kKVFull) + 8u * vs, vph, ctl, kStatusMmaTimeout)) goto done;
+          const uint32_t si = step % L::kSteps, sph = (step / L::kSteps) & 1u;
+          if (!ptx::mbar_wait(ready0 + 8u * si, sph, ctl, kStatusMmaTimeout)) goto done;
           if (!ptx::mbar_wait(bar(L::kPFull), pp0, ctl, kStatusMmaTimeout)) goto done;
           ptx::tc_fence_after();
           issue_pv<D, E, true>(tO0, tS0, v_lo);
-          if (!ptx::mbar_wait(bar(L::kKVFull) + 8u * ks, kph, ctl, kStatusMmaTimeout)) goto done;
           issue_s<D, E>(tS0, q_lo0, k_lo);
           ptx::mma_commit(bar(L::kSFull));
           if (!ptx::mbar_wait(bar(L::kPFull + 1), pp1, ctl, kStatusMmaTimeout)) goto done;
@@ -292,26 +319,19 @@ __device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_
           issue_pv<D, E, true>(tO1, tS1, v_lo);
           issue_s<D, E>(tS1, q_lo1, k_lo);
           ptx::mma_commit(bar(L::kSFull + 1));
-          ptx::mma_commit(bar(L::kKVEmpty) + 8u * vs);
-          ptx::mma_commit(bar(L::kKVEmpty) + 8u * ks);
+          ptx::mma_commit(done0 + 8u * si);
           pp0 ^= 1u;
           pp1 ^= 1u;
-          ks = vs + 1;
-          kph = vph;
-          if (ks == L::kStages) { ks = 0; kph ^= 1u; }
+          ks = vs + 1 == L::kStages ? 0u : vs + 1;
         }
         p_uses[0] += steady_end - 2;
         p_uses[1] += steady_end - 2;
-        if (j > n) break;
       }
-      uint32_t kslot = 0, vslot = 0;
-      bool k_ready = false;
-      if (j >= 1) {
-        const uint32_t li = load_idx + v_pos(j - 1, n);
-        vslot = li % L::kStages;
-        if (!ptx::mbar_wait(bar(L::kKVFull + vslot), (li / L::kStages) & 1u, ctl, kStatusMmaTimeout))
-          goto done;
-      }
+      // every load of this step has landed
+      if (!ptx::mbar_wait(ready0 + 8u * (step % L::kSteps), (step / L::kSteps) & 1u, ctl, kStatusMmaTimeout))
+        goto done;
+      const uint32_t vslot = j >= 1 ? (load_idx + v_pos(j - 1, n)) % L::kStages : 0u;
+      const uint32_t kslot = j < n ? (load_idx + k_pos(j)) % L::kStages : 0u;
 #pragma unroll
       for (int t = 0; t < kQTiles; ++t) {
         const uint32_t tS = t ? tS1 : tS0;
@@ -327,13 +347,6 @@ __device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_
         }
         if (j < nt[t]) {
           // S_t = Q_t K_j^T
-          if (!k_ready) {
-            const uint32_t li = load_idx + k_pos(j);
-            kslot = li % L::kStages;
-            if (!ptx::mbar_wait(bar(L::kKVFull + kslot), (li / L::kStages) & 1u, ctl, kStatusMmaTimeout))
-              goto done;
-            k_ready = true;
-          }
           if (j == 0) {
             if (!ptx::mbar_wait(bar(L::kQFull + t), q_uses[t] & 1u, ctl, kStatusMmaTimeout)) goto done;
             ++q_uses[t];
@@ -343,8 +356,7 @@ __device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_
           if (j == nt[t] - 1) ptx::mma_commit(bar(L::kQEmpty + t));
         }
       }
-      if (j >= 1) ptx::mma_commit(bar(L::kKVEmpty + vslot));
-      if (k_ready) ptx::mma_commit(bar(L::kKVEmpty + kslot));
+      ptx::mma_commit(done0 + 8u * (step % L::kSteps));
     }
     load_idx += 2u * n;
   }
@@ -575,9 +587,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       ptx::mbar_init(bar(L::kPFull + t), 4);   // one arrival per softmax warp
       ptx::mbar_init(bar(L::kOFull + t), 1);
     }
-    for (int s = 0; s < L::kStages; ++s) {
-      ptx::mbar_init(bar(L::kKVFull + s), 1);
-      ptx::mbar_init(bar(L::kKVEmpty + s), 1);
+    for (int s = 0; s < L::kSteps; ++s) {
+      ptx::mbar_init(bar(L::kReady + s), 1);
+      ptx::mbar_init(bar(L::kDone + s), 1);
     }
     ptx::mbar_init(bar(L::kMmaDone), 1);
     *abort_flag = 0;
