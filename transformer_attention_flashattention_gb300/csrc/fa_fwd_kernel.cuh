@@ -100,16 +100,40 @@ struct FwdCfg {
   static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
-__device__ __forceinline__ void decode_unit(const FwdParams& p, int u, int& bh, int& qb) {
-  if (p.causal) {
-    // longest rows first: the last q-blocks of every head, then the next-to-last, ...
-    qb = p.n_qblk - 1 - u / p.BH;
-    bh = u % p.BH;
-  } else {
-    // consecutive units share a head, so concurrently running CTAs reuse K/V in L2
+// The k-th (b*h, q-block) unit of this CTA of the persistent grid; false once the
+// CTA has none left.  Every role of the CTA walks the same sequence.
+//  - Non-causal: units in head-major order, dealt round-robin, so the CTAs running at
+//    the same time share a few heads and their K/V re-reads hit L2.
+//  - Causal: the cost of q-block qb grows with qb, so qb and n_qblk-1-qb of one head
+//    form a pair of equal total cost.  A CTA takes whole pairs round-robin in
+//    head-major order (the longer half first), which balances the grid and keeps
+//    concurrent CTAs on few heads; the middle q-block of each head (odd n_qblk)
+//    comes after the pairs, dealt on with the same stride.
+__device__ __forceinline__ bool unit_at(const FwdParams& p, int k, int& bh, int& qb) {
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  if (!p.causal) {
+    const int u = c + k * G;
+    if (u >= p.num_units) return false;
     bh = u / p.n_qblk;
     qb = u % p.n_qblk;
+    return true;
   }
+  const int P = p.n_qblk / 2;                         // pairs per head
+  const int pairs = p.BH * P;
+  const int mine = c < pairs ? (pairs - c + G - 1) / G : 0;
+  if (k < 2 * mine) {
+    const int s = c + (k >> 1) * G;
+    bh = s / P;
+    const int i = s % P;
+    qb = (k & 1) ? i : p.n_qblk - 1 - i;
+    return true;
+  }
+  if ((p.n_qblk & 1) == 0) return false;
+  const int r = c + (mine + (k - 2 * mine)) * G - pairs;   // >= 0 by the choice of mine
+  if (r >= p.BH) return false;
+  bh = r;
+  qb = P;
+  return true;
 }
 
 // Number of K/V tiles Q tile t of q-block qb attends to (0 if the tile is past N).
@@ -145,9 +169,8 @@ __device__ __noinline__ void fwd_producer(const FwdParams& p, uint32_t sbase,
   for (int s = 0; s < L::kStages; ++s) slot_step[s] = 0;
   uint32_t armed = 0;                    // bit g % kSteps: step g's loads were issued
 
-  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-    int bh, qb;
-    decode_unit(p, u, bh, qb);
+  int bh, qb;
+  for (int k = 0; unit_at(p, k, bh, qb); ++k) {
     const int n0 = tile_nkv(p, qb, 0), n1 = tile_nkv(p, qb, 1);
     const int n = max(n0, n1);
 #pragma unroll
@@ -161,6 +184,19 @@ __device__ __noinline__ void fwd_producer(const FwdParams& p, uint32_t sbase,
         ptx::tma_load_3d(sbase + L::kQOff + t * L::kTileBytes + a * L::kAtomBytes, &p.tm_q,
                          bar(L::kQFull + t), a * L::kAtomElems, qb * kUnitRows + t * kBlockM, bh);
       ++q_fills[t];
+    }
+    {
+      // Q is read once, so its next load comes from HBM; start that unit's Q on its
+      // way into L2 now, a whole unit ahead of the load
+      int bhn, qbn;
+      if (unit_at(p, k + 1, bhn, qbn)) {
+#pragma unroll
+        for (int t = 0; t < kQTiles; ++t)
+          if (tile_nkv(p, qbn, t) > 0)
+#pragma unroll
+            for (int a = 0; a < L::kAtoms; ++a)
+              ptx::tma_prefetch_3d(&p.tm_q, a * L::kAtomElems, qbn * kUnitRows + t * kBlockM, bhn);
+      }
     }
     for (int j = 0; j <= n; ++j, ++step) {
       const uint32_t cnt = (j < n ? 1u : 0u) + (j >= 1 ? 1u : 0u);
@@ -292,9 +328,8 @@ __device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_
   uint32_t q_uses[kQTiles] = {0, 0};
   uint32_t p_uses[kQTiles] = {0, 0};
 
-  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-    int bh, qb;
-    decode_unit(p, u, bh, qb);
+  int bh, qb;
+  for (int k = 0; unit_at(p, k, bh, qb); ++k) {
     const int nt[kQTiles] = {tile_nkv(p, qb, 0), tile_nkv(p, qb, 1)};
     const int n = max(nt[0], nt[1]);
     // steps 2 .. steady_end - 1: both tiles run PV(j-1) and S(j), none of them is a
@@ -387,9 +422,8 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, int t, uint32_t 
   uint32_t s_uses = 0, o_uses = 0;
   const int lane = threadIdx.x & 31;
 
-  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-    int bh, qb;
-    decode_unit(p, u, bh, qb);
+  int bh, qb;
+  for (int k = 0; unit_at(p, k, bh, qb); ++k) {
     const int ntile = tile_nkv(p, qb, t);
     if (ntile == 0) continue;
     const int r0 = qb * kUnitRows + t * kBlockM;
@@ -541,15 +575,17 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, int t, uint32_t 
     const bool live = row < p.N;
     uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
                                            (static_cast<size_t>(bh) * p.N + (live ? row : 0)) * D);
+    // all of the row's O columns in one TMEM round trip
+    uint32_t orr[D / 32][32];
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) ptx::tmem_ld32(tO + 32 * c, orr[c]);
+    ptx::tmem_wait_ld();
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
-      uint32_t orr[32];
-      ptx::tmem_ld32(tO + 32 * c, orr);
-      ptx::tmem_wait_ld();
       uint32_t pk[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const float2 v = ptx::mul2(make_float2(__uint_as_float(orr[2 * i]), __uint_as_float(orr[2 * i + 1])),
+        const float2 v = ptx::mul2(make_float2(__uint_as_float(orr[c][2 * i]), __uint_as_float(orr[c][2 * i + 1])),
                                    make_float2(inv_l, inv_l));
         pk[i] = ptx::pack2<L::kBf16Out>(v.x, v.y);
       }
