@@ -329,13 +329,21 @@ __device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_
   uint32_t p_uses[kQTiles] = {0, 0};
 
   int bh, qb;
-  for (int k = 0; unit_at(p, k, bh, qb); ++k) {
+  bool have = unit_at(p, 0, bh, qb);
+  int j0 = 0;                            // 1 once a unit's step 0 ran inside the previous unit
+  for (int k = 0; have; ++k) {
     const int nt[kQTiles] = {tile_nkv(p, qb, 0), tile_nkv(p, qb, 1)};
     const int n = max(nt[0], nt[1]);
     // steps 2 .. steady_end - 1: both tiles run PV(j-1) and S(j), none of them is a
     // tile's last PV or last S, and V_{j-1} sits right after K_j in the ring
     const int steady_end = min(nt[0], nt[1]) - 1;
-    for (int j = 0; j <= n; ++j, ++step) {
+    // The next unit's step 0 (S_t = Q_t K_0^T) is issued inside this unit's last step,
+    // right after tile t's last PV, so each softmax group finds its next S as soon as
+    // its epilogue ends instead of after both tiles' last PVs.
+    int bhn = 0, qbn = 0;
+    const bool has_next = unit_at(p, k + 1, bhn, qbn);
+    const int ntn[kQTiles] = {has_next ? tile_nkv(p, qbn, 0) : 0, has_next ? tile_nkv(p, qbn, 1) : 0};
+    for (int j = j0; j <= n; ++j, ++step) {
       if (j == 2 && steady_end > 2) {
         uint32_t ks = (load_idx + 2u * j - 1u) % L::kStages;     // ring slot of K_j
         uint32_t pp0 = p_uses[0] & 1u, pp1 = p_uses[1] & 1u;
@@ -362,11 +370,15 @@ __device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_
         p_uses[0] += steady_end - 2;
         p_uses[1] += steady_end - 2;
       }
-      // every load of this step has landed
+      // every load of this step (and of the next unit's step 0, when fused) has landed
+      const bool fuse = j == n && has_next;
       if (!ptx::mbar_wait(ready0 + 8u * (step % L::kSteps), (step / L::kSteps) & 1u, ctl, kStatusMmaTimeout))
         goto done;
+      if (fuse && !ptx::mbar_wait(ready0 + 8u * ((step + 1) % L::kSteps), ((step + 1) / L::kSteps) & 1u, ctl,
+                                  kStatusMmaTimeout))
+        goto done;
       const uint32_t vslot = j >= 1 ? (load_idx + v_pos(j - 1, n)) % L::kStages : 0u;
-      const uint32_t kslot = j < n ? (load_idx + k_pos(j)) % L::kStages : 0u;
+      const uint32_t kslot = j < n ? (load_idx + k_pos(j)) % L::kStages : (load_idx + 2u * n) % L::kStages;
 #pragma unroll
       for (int t = 0; t < kQTiles; ++t) {
         const uint32_t tS = t ? tS1 : tS0;
@@ -389,11 +401,25 @@ __device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_
           issue_s<D, E>(tS, t == 0 ? q_lo0 : q_lo1, k_lo0 + kslot * kSlotDesc);
           ptx::mma_commit(bar(L::kSFull + t));
           if (j == nt[t] - 1) ptx::mma_commit(bar(L::kQEmpty + t));
+        } else if (fuse && ntn[t] > 0) {
+          // the next unit's S_t = Q_t K_0^T (kslot holds its K_0)
+          if (!ptx::mbar_wait(bar(L::kQFull + t), q_uses[t] & 1u, ctl, kStatusMmaTimeout)) goto done;
+          ++q_uses[t];
+          issue_s<D, E>(tS, t == 0 ? q_lo0 : q_lo1, k_lo0 + kslot * kSlotDesc);
+          ptx::mma_commit(bar(L::kSFull + t));
+          if (ntn[t] == 1) ptx::mma_commit(bar(L::kQEmpty + t));
         }
       }
       ptx::mma_commit(done0 + 8u * (step % L::kSteps));
+      if (fuse) ptx::mma_commit(done0 + 8u * ((step + 1) % L::kSteps));
     }
     load_idx += 2u * n;
+    // the next unit's step 0 has been issued: it starts at step 1
+    if (has_next) ++step;
+    j0 = has_next ? 1 : 0;
+    have = has_next;
+    bh = bhn;
+    qb = qbn;
   }
 done:
   // Every MMA issued so far must finish before TMEM is released.
@@ -420,6 +446,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, int t, uint32_t 
   const uint32_t tO = tmem + (lane_base << 16) + L::kTmemO + t * D;
   const float sl2 = p.scale_log2;
   uint32_t s_uses = 0, o_uses = 0;
+  const bool o_v8 = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
   const int lane = threadIdx.x & 31;
 
   int bh, qb;
@@ -590,9 +617,15 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, int t, uint32_t 
         pk[i] = ptx::pack2<L::kBf16Out>(v.x, v.y);
       }
       if (live) {
+        if (o_v8) {
+          // 32-byte stores fill whole sectors (rows are 128 or 256 bytes; base 32-aligned)
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          orow[c * 4 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          for (int i = 0; i < 2; ++i) ptx::st_global_v8(orow + c * 4 + 2 * i, pk + 8 * i);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            orow[c * 4 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
       }
     }
     if (live && p.lse != nullptr)
