@@ -19,6 +19,10 @@ Recipe (one reading, stated once): ``g = torch.Generator().manual_seed(seed)``;
 workload, per tensor in the order q, k, v: ``pos = randperm(numel)[:round(1e-3 *
 numel)]`` then ``vals = 20 * randn(len(pos))``, written at those flat positions;
 finally each tensor is cast to the workload dtype.
+
+The upstream gradient dO of the backward pass is one more tensor shaped like Q:
+``randn(shape)`` in float32 from its own generator seeded with ``seed + 100``,
+cast to the workload dtype (``make_dout``).
 """
 from __future__ import annotations
 
@@ -35,6 +39,7 @@ __all__ = [
     "sweep_workload",
     "make_qkv",
     "make_inputs",
+    "make_dout",
     "sample_rows",
 ]
 
@@ -99,6 +104,12 @@ def make_qkv(shape, dtype: torch.dtype, seed: int, outliers: bool = False):
         for t in (q, k, v):
             _add_outliers(t, g)
     return q.to(dtype), k.to(dtype), v.to(dtype)
+
+
+def make_dout(shape, dtype: torch.dtype, seed: int) -> torch.Tensor:
+    """Upstream gradient dO for a workload drawn with ``seed`` (own generator, seed + 100)."""
+    g = torch.Generator().manual_seed(seed + 100)
+    return torch.randn(tuple(shape), generator=g, dtype=torch.float32).to(dtype)
 
 
 def make_inputs(w: Workload):

@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for the attention forward pass.
+"""fp64 CPU oracle for the attention forward pass and its gradient.
 
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU
 baseline leg of ``bench.py`` may import this package; the CUDA product path
@@ -11,6 +11,11 @@ from .sdpa import (  # noqa: F401
     brute_force_attention,
     online_softmax_attention,
     rel_rms,
+)
+from .backward import (  # noqa: F401
+    attention_backward,
+    attention_backward_delta,
+    brute_force_attention_backward,
 )
 from .fp8 import (  # noqa: F401
     E4M3_MAX,
