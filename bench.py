@@ -11,6 +11,7 @@ Other workloads (for profiling; the default is the headline):
   --workload fp8         [4, 16, 4096, 128] E4M3 forward (Hadamard on), quantisation excluded
   --workload tiny        [1, 1, 128, 64] fp16, both masks
   --workload decode      one query row per head against a [8, 32, 32768, 128] bf16 key cache
+  --workload bwd         backward pass (dQ, dK, dV) on [16, 16, 2048, 128] bf16, both masks
                          (split-KV on the CUDA cores; HBM roofline)
 
 Multi-GPU (torchrun, one rank per GPU): every rank runs the same per-GPU
@@ -78,7 +79,15 @@ def aggregate_tflops(step_flops: float, steps: int, world: int, max_total_ms: fl
 DECODE = dict(B=8, H=32, Nq=1, Nk=32768, d=128)
 
 
+# the backward pass is timed on the headline forward shape, both masks
+BWD = dict(B=16, H=16, N=2048, d=128, seed=1)
+BWD_FLOP_RATIO = 2.5   # five N x N x d products against the forward's two
+
+
 def _workload(name: str):
+    if name == "bwd":
+        from fa_inputs import Workload
+        return Workload("bwd", BWD["B"], BWD["H"], BWD["N"], BWD["d"], torch.bfloat16, BWD["seed"], (False, True))
     if name == "decode":
         from fa_inputs import Workload
         return Workload("decode", DECODE["B"], DECODE["H"], DECODE["Nk"], DECODE["d"], torch.bfloat16, 5, (False,))
@@ -159,6 +168,10 @@ def _oracle_sample(w, budget_s: float, max_units=None):
     import numpy as np  # noqa: F401
     import oracle
     q, k, v = make_qkv((1, min(w.H, 4), w.N, w.d), w.dtype, w.seed, w.outliers)
+    bwd = w.name == "bwd"
+    if bwd:
+        from fa_inputs import make_dout
+        do = make_dout(q.shape, w.dtype, w.seed)
     flops = 0.0
     done = 0
     t0 = time.perf_counter()
@@ -167,14 +180,17 @@ def _oracle_sample(w, budget_s: float, max_units=None):
     while True:
         causal, h = pairs[i % len(pairs)]
         sl = (slice(0, 1), slice(h, h + 1))
-        oracle.attention(q[sl], k[sl], v[sl], w.scale, causal)
-        flops += (4.0 * w.N * w.N * w.d) / (2.0 if causal else 1.0)
+        if bwd:
+            oracle.attention_backward(q[sl], k[sl], v[sl], do[sl], w.scale, causal)
+        else:
+            oracle.attention(q[sl], k[sl], v[sl], w.scale, causal)
+        flops += (4.0 * w.N * w.N * w.d) / (2.0 if causal else 1.0) * (BWD_FLOP_RATIO if bwd else 1.0)
         done += 1
         i += 1
         el = time.perf_counter() - t0
         if el >= budget_s or (max_units is not None and done >= max_units):
             break
-    desc = (f"{done} full (b,h) heads of [{w.B},{w.H},{w.N},{w.d}] "
+    desc = (f"{done} full (b,h) heads of [{w.B},{w.H},{w.N},{w.d}]{' (gradient)' if bwd else ''} "
             f"({'/'.join('causal' if c else 'non-causal' for c in w.causal_modes)} alternating), fp64 numpy")
     return flops, time.perf_counter() - t0, desc
 
@@ -232,6 +248,7 @@ def run_gpu(args):
     w = _workload(args.workload)
     fp8 = args.workload == "fp8"
     dec = args.workload == "decode"
+    bwd = args.workload == "bwd"
     # Each rank draws its own shard (same shape, seed offset by rank): weak scaling.
     if dec:
         q, _, _ = make_qkv((w.B, w.H, DECODE["Nq"], w.d), w.dtype, shard_seed(w, rank))
@@ -248,6 +265,16 @@ def run_gpu(args):
     o = torch.empty(q.shape, device=dev, dtype=torch.bfloat16 if fp8 else w.dtype)
     lse = torch.empty(q.shape[:3], device=dev, dtype=torch.float32)
     ws = None
+    if bwd:
+        # the backward consumes the forward's O and LSE (computed once, outside the timing)
+        from fa_inputs import make_dout
+        dod = make_dout(w.shape, w.dtype, shard_seed(w, rank)).to(dev)
+        saved = {c: fa.attention(qd, kd, vd, causal=c) for c in masks}
+        grads = tuple(torch.empty_like(qd) for _ in range(3))
+        import ctypes
+        need = ctypes.c_ulonglong(0)
+        fa.load_library().fa_bwd_workspace_size(w.B, w.H, w.N, w.d, ctypes.byref(need))
+        ws = torch.empty(max(need.value, 256), device=dev, dtype=torch.uint8)
     if dec:
         import ctypes
         need = ctypes.c_ulonglong(0)
@@ -255,14 +282,17 @@ def run_gpu(args):
         ws = torch.empty(max(need.value, 256), device=dev, dtype=torch.uint8)
 
     def one(causal):
-        if dec:
+        if bwd:
+            fa.attention_backward(qd, kd, vd, saved[causal][0], saved[causal][1], dod, causal=causal,
+                                  dq=grads[0], dk=grads[1], dv=grads[2], workspace=ws)
+        elif dec:
             fa.decode(qd, kd, vd, causal=causal, out=o, lse=lse, workspace=ws)
         elif fp8:
             fa.attention_fp8(q8, k8, v8, qs, ks, vs, causal=causal, hadamard=True, out=o, lse=lse)
         else:
             fa.attention(qd, kd, vd, causal=causal, out=o, lse=lse)
 
-    step_flops = sum(w.flops(c) for c in masks)
+    step_flops = sum(w.flops(c) for c in masks) * (BWD_FLOP_RATIO if bwd else 1.0)
     if dec:
         step_flops = 4.0 * w.B * w.H * DECODE["Nq"] * w.N * w.d * len(masks)
     for _ in range(args.warmup):
@@ -308,7 +338,7 @@ def run_gpu(args):
 
     # End-to-end through the public API with pinned host buffers (this rank's shard).
     e2e = None
-    if not fp8 and not dec:
+    if not fp8 and not dec and not bwd:
         qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
         e_steps = max(1, min(args.steps, 5))
         for _ in range(2):
@@ -358,8 +388,12 @@ def run_gpu(args):
         roof = {"bound": "tensor", "achieved": kern_tflops, "peak": peak, "unit": "TFLOP/s",
                 "frac": kern_tflops / peak, "traffic": traffic, "peak_source": peak_note,
                 "kernel": "fa_fwd_fp8_kernel" if fp8 else "fa_fwd_kernel"}
+        if bwd:
+            roof["kernel"] = "fa_bwd_prep_kernel + fa_bwd_kernel (dQ) + fa_bwd_kernel (dK, dV)"
+            roof["note"] = ("algorithmic FLOPs = 2.5 x forward (five products); the two-kernel scheme "
+                            "runs seven, recomputing S and dP once more instead of reducing dQ")
     def mask_flops(c):
-        return step_flops / len(masks) if dec else w.flops(c)
+        return step_flops / len(masks) if dec else w.flops(c) * (BWD_FLOP_RATIO if bwd else 1.0)
     variants = {("causal" if c else "non_causal"): {
         "tflops": mask_flops(c) / (statistics.median(per_mask_ms[c]) * 1e-3) / 1e12,
         "median_ms": statistics.median(per_mask_ms[c]),
@@ -388,7 +422,7 @@ def run_gpu(args):
         "variants": variants,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": n_ev * (2 if dec else 1),
+        "gpu_launches": n_ev * (3 if bwd else (2 if dec else 1)),
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)

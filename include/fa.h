@@ -116,6 +116,31 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, 
 int fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits,
                              unsigned long long* bytes);
 
+/*
+ * Backward pass: dQ, dK, dV of fa_fwd's output for an upstream gradient dO.  The
+ * pages name the backward pass as where FlashAttention-2 parallelises better (the
+ * concept card "FlashAttention 2 + 3 — speicherbewusste Attention-Kernels", section
+ * "Kernpunkte") but print no formula: the gradient is the calculus of fa_fwd's
+ * definition, with P recomputed tile by tile from the saved LSE,
+ *   P = exp(scale * Q K^T - LSE),  D_i = sum_c dO_ic O_ic,  dS = P * (dO V^T - D),
+ *   dV = P^T dO,  dQ = scale * dS K,  dK = scale * dS^T Q.
+ *   q, k, v, o, dout : [B, H, N, d] of `dtype`; o and lse are fa_fwd's outputs for
+ *                      the same q, k, v, scale and causal (lse must not be NULL there)
+ *   dq, dk, dv       : [B, H, N, d] of `dtype`, written
+ *   workspace        : device scratch of at least fa_bwd_workspace_size() bytes,
+ *                      256-byte aligned, owned by the caller; contents on entry do not
+ *                      matter; calls sharing one workspace must not overlap on the GPU
+ * Same support as fa_fwd (d in {64, 128}, f16/bf16, causal 0 or 1, any N >= 1).  P
+ * and dS are rounded to `dtype` before their MMAs and the results once at the end;
+ * accumulation is fp32.  No atomics: results are bitwise reproducible.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+           void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, int dtype,
+           void* workspace, unsigned long long workspace_bytes, void* stream);
+
+/* Scratch bytes fa_bwd needs for these sizes (8 * B * H * N rounded up to 128 per head). */
+int fa_bwd_workspace_size(int B, int H, int N, int d, unsigned long long* bytes);
+
 /* Size of the static scratch area behind fa_decode_noalloc, per device (8 MiB). */
 #define FA_DECODE_NOALLOC_SCRATCH_BYTES (8ull << 20)
 

@@ -33,7 +33,8 @@ def lib():
 def test_header_declares_the_boundary():
     assert _declared() == sorted(["fa_fwd", "fa_quantize_fp8", "fa_fwd_fp8", "fa_strerror",
                                   "fa_last_device_status", "fa_debug_inject_stall", "fa_version",
-                                  "fa_decode", "fa_decode_workspace_size", "fa_decode_noalloc"])
+                                  "fa_decode", "fa_decode_workspace_size", "fa_decode_noalloc",
+                                  "fa_bwd", "fa_bwd_workspace_size"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -97,3 +98,19 @@ def test_decode_rejects_bad_arguments_on_the_host(lib, args, want):
 ])
 def test_decode_noalloc_rejects_bad_shapes_on_the_host(lib, Nq, Nk, d, want):
     assert lib.fa_decode_noalloc(A, A, A, A, None, 1, 1, Nq, Nk, d, 0.125, 0, 1, 0, None) == want
+
+
+def test_bwd_rejects_bad_arguments_on_the_host(lib):
+    args = [A] * 9
+    ws = 0x100000
+    call = lambda a, B=1, H=1, N=128, d=64, scale=0.125, causal=0, dtype=1, wsp=ws, wsb=1 << 20: lib.fa_bwd(
+        *a, B, H, N, d, scale, causal, dtype, wsp, wsb, None)
+    assert call([0] + args[1:]) == fa.FA_ERR_NULL
+    assert call(args, d=96) == fa.FA_ERR_UNSUPPORTED
+    assert call(args, causal=2) == fa.FA_ERR_UNSUPPORTED
+    assert call(args, scale=-1.0) == fa.FA_ERR_UNSUPPORTED
+    assert call(args, N=0) == fa.FA_ERR_SHAPE
+    assert call(args, wsp=ws + 16) == fa.FA_ERR_ALIGN
+    assert call(args, wsb=512) == fa.FA_ERR_WORKSPACE     # 1 x 1 x 128 needs 1024
+    n = ctypes.c_ulonglong(0)
+    assert lib.fa_bwd_workspace_size(2, 3, 200, 64, ctypes.byref(n)) == fa.FA_OK and n.value == 2 * 2 * 3 * 256 * 4

@@ -26,6 +26,7 @@ __all__ = [
     "attention_fp8",
     "decode",
     "decode_noalloc",
+    "attention_backward",
     "DECODE_NOALLOC_SCRATCH_BYTES",
     "last_device_status",
     "inject_stall",
@@ -68,6 +69,8 @@ _SIGNATURES = {
     "fa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _vp, ctypes.c_ulonglong, _vp]),
     "fa_decode_workspace_size": (_i, [_i, _i, _i, _i, _i, _i, ctypes.POINTER(ctypes.c_ulonglong)]),
     "fa_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _vp]),
+    "fa_bwd": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _i, _vp, ctypes.c_ulonglong, _vp]),
+    "fa_bwd_workspace_size": (_i, [_i, _i, _i, _i, ctypes.POINTER(ctypes.c_ulonglong)]),
     "fa_strerror": (ctypes.c_char_p, [_i]),
     "fa_last_device_status": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),
     "fa_debug_inject_stall": (_i, [_i, _i]),
@@ -307,6 +310,42 @@ def decode_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bo
                           f"{DECODE_NOALLOC_SCRATCH_BYTES}-byte static scratch: lower num_splits or use decode)")
     _check(st, "fa_decode_noalloc")
     return out, lse
+
+
+def attention_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                       lse: torch.Tensor, dout: torch.Tensor, causal: bool = False,
+                       scale: Optional[float] = None, dq: Optional[torch.Tensor] = None,
+                       dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None,
+                       stream: Optional[torch.cuda.Stream] = None):
+    """(dQ, dK, dV) of ``attention``'s output for the upstream gradient ``dout``.
+
+    ``o`` and ``lse`` are ``attention``'s outputs for the same inputs, scale and
+    mask.  A scratch workspace is allocated with torch unless one is given.
+    """
+    lib = load_library()
+    _check_qkv(q, k, v)
+    for name, t in (("o", o), ("dout", dout)):
+        if t.shape != q.shape or t.dtype != q.dtype or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor shaped and typed like q")
+    B, H, N, d = q.shape
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = ctypes.c_ulonglong(0)
+    _check(lib.fa_bwd_workspace_size(B, H, N, d, ctypes.byref(need)), "fa_bwd_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(max(need.value, 256), device=q.device, dtype=torch.uint8)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    with torch.cuda.device(q.device):
+        st = lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                        B, H, N, d, float(scale), int(bool(causal)), _DTYPES[q.dtype], _ptr(workspace),
+                        workspace.numel() * workspace.element_size(), _stream_handle(stream, q.device))
+    _check(st, "fa_bwd")
+    return dq, dk, dv
 
 
 def last_device_status(stream: Optional[torch.cuda.Stream] = None) -> Tuple[int, int]:

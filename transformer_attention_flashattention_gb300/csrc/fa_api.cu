@@ -342,6 +342,68 @@ extern "C" int fa_decode(const void* q, const void* k, const void* v, void* o, f
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
+extern "C" int fa_bwd_workspace_size(int B, int H, int N, int d, unsigned long long* bytes) {
+  if (!bytes) return FA_ERR_NULL;
+  const int st = check_shape(B, H, N, d);
+  if (st != FA_OK) return st;
+  const unsigned long long n_pad = (static_cast<unsigned long long>(N) + 127) / 128 * 128;
+  *bytes = 2ull * static_cast<unsigned long long>(B) * H * n_pad * 4ull;
+  return FA_OK;
+}
+
+extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                      const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                      int causal, int dtype, void* workspace, unsigned long long workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return FA_ERR_NULL;
+  if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+  if (causal != 0 && causal != 1) return FA_ERR_UNSUPPORTED;
+  int st = check_shape(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) || !aligned(workspace, 256))
+    return FA_ERR_ALIGN;
+  unsigned long long need = 0;
+  fa_bwd_workspace_size(B, H, N, d, &need);
+  if (workspace_bytes < need) return FA_ERR_WORKSPACE;
+  const DeviceInfo* di = current_device(&st);
+  if (!di) return st;
+
+  BwdParams p;
+  const CUtensorMapDataType dt = dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const uint64_t BH = static_cast<uint64_t>(B) * H;
+  if (!encode_3d(&p.tm_q, dt, 2, q, d, N, BH, 64, 128) || !encode_3d(&p.tm_k, dt, 2, k, d, N, BH, 64, 128) ||
+      !encode_3d(&p.tm_v, dt, 2, v, d, N, BH, 64, 128) || !encode_3d(&p.tm_do, dt, 2, dout, d, N, BH, 64, 128))
+    return FA_ERR_CUDA;
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.N = N;
+  p.n_pad = (N + 127) / 128 * 128;
+  p.n_blk = p.n_pad / 128;
+  p.BH = static_cast<int>(BH);
+  p.lse2 = static_cast<float*>(workspace);
+  p.delta = p.lse2 + BH * static_cast<uint64_t>(p.n_pad);
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.status = di->status;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.44269504088896340736f;
+  p.causal = causal;
+  const long long units = static_cast<long long>(p.n_blk) * p.BH;
+  if (units >= (1ll << 31)) return FA_ERR_SHAPE;
+  p.num_units = static_cast<int>(units);
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    p.timeout_ns = timeout_ns_for_call();
+  }
+  const int grid = static_cast<int>(units < di->sm_count ? units : di->sm_count);
+  const cudaError_t e = launch_bwd(d, dtype == FA_BF16, p, grid, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
 extern "C" int fa_last_device_status(void* stream, unsigned int* bits) {
   int st = FA_OK;
   const DeviceInfo* di = current_device(&st);

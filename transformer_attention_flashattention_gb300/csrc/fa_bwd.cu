@@ -1,0 +1,538 @@
+// Attention backward for sm_103a (f16/bf16, head dim 64 or 128): dQ, dK, dV of
+// O = softmax(scale * Q K^T [+ causal mask]) V for an upstream gradient dO, from the
+// forward pass's O and natural-log LSE.
+//
+// The pages name the backward pass as the place FlashAttention-2 parallelises better
+// (concept card "FlashAttention 2 + 3 — speicherbewusste Attention-Kernels", section
+// "Kernpunkte") but print no formula; the gradient is the calculus of the forward
+// definition, recomputing P tile by tile from the saved LSE so that no N x N matrix
+// reaches HBM:
+//   P = 2^(scale*log2(e) * Q K^T - LSE*log2(e)),  D_i = sum_c dO_ic O_ic,
+//   dS = P * (dO V^T - D),  dV = P^T dO,  dQ = scale * dS K,  dK = scale * dS^T Q.
+//
+// Three kernels on the caller's stream, no atomics (results are deterministic):
+//   prep   D and LSE*log2(e) into a workspace padded to 128 rows per head (padding:
+//          D = 0, LSE*log2(e) = +inf, so padded queries get P = 0)
+//   dq     Q-stationary: per 128-row Q tile, stream K_j, V_j;
+//          S = Q K^T and dP = dO V^T (two SS MMAs into TMEM), dS in registers,
+//          packed back over S, then dQ += dS K (TS MMA, K as an MN-major operand)
+//   dkdv   K/V-stationary: per 128-key tile, stream Q_i, dO_i (+ their LSE, D);
+//          S^T = K Q^T and dP^T = V dO^T, then P^T and dS^T per key row, then
+//          dV += P^T dO and dK += dS^T Q (both TS MMAs)
+// S and dP are computed twice (once per kernel) in exchange for no dQ reduction.
+//
+// Each main kernel is a persistent grid with four roles:
+//   warps 0-3  compute: thread i owns TMEM lane i (a Q row, or a key row)
+//   warp 4     TMA producer: the unit's two stationary tiles, then a 2-stage ring
+//   warp 5     MMA issuer (one thread) and TMEM owner
+// TMEM (512 columns): S (or S^T) | dP (or dP^T) | accumulator 0 | accumulator 1.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "fa_fwd_kernel.cuh"
+#include "fa_launch.h"
+
+namespace fa {
+namespace {
+
+constexpr int kBwdThreads = 192;
+constexpr int kBwdLoadWarp = 4;
+constexpr int kBwdMmaWarp = 5;
+constexpr int kBwdStages = 2;
+constexpr uint32_t kTmS = 0, kTmDP = 128, kTmAcc = 256;
+constexpr float kLog2e = 1.44269504088896340736f;
+
+template <int D>
+struct BwdCfg {
+  using L = FwdCfg<D, Elem::BF16>;                    // tile geometry (same for f16)
+  static constexpr int kTile = L::kTileBytes;         // 128 rows x D, 128-byte swizzle atoms
+  static constexpr int kStatOff = 0;                  // the unit's two stationary tiles
+  static constexpr int kRingOff = 2 * kTile;
+  static constexpr int kVecBytes = 128 * 4;           // one tile's LSE*log2(e) (or D) values
+  static constexpr int kStageBytes = 2 * kTile + 2 * kVecBytes;
+  static_assert(kStageBytes % 1024 == 0, "stages keep the tiles 1 KB aligned");
+  static constexpr int kBarOff = kRingOff + kBwdStages * kStageBytes;
+  // barriers
+  static constexpr int kStFull = 0, kStEmpty = 1, kReady = 2, kDone = kReady + kBwdStages;
+  static constexpr int kSdpFull = kDone + kBwdStages, kDsFull = kSdpFull + 1, kAccFull = kDsFull + 1;
+  static constexpr int kMmaDone = kAccFull + 1, kNumBars = kMmaDone + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kBytes = kMiscOff + 16;
+  static constexpr int kAlloc = kBytes + 1024;
+  static_assert(kAlloc <= 232448, "shared memory budget");
+};
+
+// Unit u of the dq kernel: (b*h, Q tile i).  Causal costs grow with i, so the last
+// tiles of every head go first.
+__device__ __forceinline__ void dq_unit(const BwdParams& p, int u, int& bh, int& i) {
+  if (p.causal) {
+    i = p.n_blk - 1 - u / p.BH;
+    bh = u % p.BH;
+  } else {
+    bh = u / p.n_blk;
+    i = u % p.n_blk;
+  }
+}
+// Unit u of the dkdv kernel: (b*h, K/V tile j).  Causal costs shrink with j.
+__device__ __forceinline__ void dkdv_unit(const BwdParams& p, int u, int& bh, int& j) {
+  if (p.causal) {
+    j = u / p.BH;
+    bh = u % p.BH;
+  } else {
+    bh = u / p.n_blk;
+    j = u % p.n_blk;
+  }
+}
+
+// ---------------------------------------------------------------------------- prep
+
+// D_i = sum_c dO_ic O_ic and LSE_i * log2(e), one row per group of D/8 lanes.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __grid_constant__ BwdParams p) {
+  constexpr int kLanes = D / 8;                      // 8 elements (16 bytes) per lane
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long grow = t / kLanes;                 // row over [B*H, n_pad]
+  const int part = static_cast<int>(t % kLanes);
+  // no early exit: every lane takes part in the shuffles below
+  const bool valid = grow < static_cast<long long>(p.BH) * p.n_pad;
+  const int bh = valid ? static_cast<int>(grow / p.n_pad) : 0;
+  const int row = valid ? static_cast<int>(grow % p.n_pad) : p.n_pad;
+  float acc = 0.f;
+  if (row < p.N) {
+    const size_t off = (static_cast<size_t>(bh) * p.N + row) * D + part * 8;
+    const uint4 ov = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.o) + off);
+    const uint4 dv = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.dout) + off);
+    const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float2 a, b;
+      if constexpr (BF16) {
+        a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[e]));
+        b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dw[e]));
+      } else {
+        a = __half22float2(*reinterpret_cast<const __half2*>(&ow[e]));
+        b = __half22float2(*reinterpret_cast<const __half2*>(&dw[e]));
+      }
+      acc = fmaf(a.x, b.x, fmaf(a.y, b.y, acc));
+    }
+  }
+#pragma unroll
+  for (int m = kLanes / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, m);
+  if (valid && part == 0) {
+    const size_t w = static_cast<size_t>(bh) * p.n_pad + row;
+    p.delta[w] = row < p.N ? acc : 0.f;
+    p.lse2[w] = row < p.N ? p.lse[static_cast<size_t>(bh) * p.N + row] * kLog2e : INFINITY;
+  }
+}
+
+// ---------------------------------------------------------------------------- shared pieces
+
+template <int D, Elem E>
+__device__ __forceinline__ void load_tile(const CUtensorMap* map, uint32_t dst, uint32_t bar, int row0, int bh) {
+  using L = FwdCfg<D, E>;
+#pragma unroll
+  for (int a = 0; a < L::kAtoms; ++a)
+    ptx::tma_load_3d(dst + a * L::kAtomBytes, map, bar, a * L::kAtomElems, row0, bh);
+}
+
+// Bounded wait for every copy issued so far on the ring and stationary barriers.
+template <int D>
+__device__ void producer_drain(uint32_t sbase, const uint32_t (&last_fill)[kBwdStages], uint32_t st_fills,
+                               const ptx::WaitCtl& ctl, unsigned code) {
+  using C = BwdCfg<D>;
+  for (int s = 0; s < kBwdStages; ++s)
+    if (last_fill[s] != 0xFFFFFFFFu &&
+        !ptx::mbar_wait_drain(sbase + C::kBarOff + 8u * (C::kReady + s), last_fill[s] & 1u, ctl.timeout_ns))
+      atomicOr(ctl.status, code);
+  if (st_fills > 0 &&
+      !ptx::mbar_wait_drain(sbase + C::kBarOff + 8u * C::kStFull, (st_fills - 1u) & 1u, ctl.timeout_ns))
+    atomicOr(ctl.status, code);
+}
+
+// Packs the 32 floats a[0..31] into 16 words of two 16-bit values each.
+template <bool BF16>
+__device__ __forceinline__ void pack16(const float (&a)[32], uint32_t (&w)[16]) {
+#pragma unroll
+  for (int x = 0; x < 16; ++x) w[x] = ptx::pack2<BF16>(a[2 * x], a[2 * x + 1]);
+}
+
+// Writes one 128-row-tile row of D accumulator columns, times `mul`, as 16-bit values.
+template <int D, bool BF16>
+__device__ __forceinline__ void store_acc_row(uint32_t taddr, float mul, void* out, size_t row_off, bool live) {
+  uint32_t r[D / 32][32];
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) ptx::tmem_ld32(taddr + 32 * c, r[c]);
+  ptx::tmem_wait_ld();
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + row_off);
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      pk[i] = ptx::pack2<BF16>(__uint_as_float(r[c][2 * i]) * mul, __uint_as_float(r[c][2 * i + 1]) * mul);
+    if (live) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) dst[c * 4 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------- dq kernel
+
+template <int D, Elem E>
+__device__ __noinline__ void dq_producer(const BwdParams& p, uint32_t sbase, const ptx::WaitCtl& ctl) {
+  using C = BwdCfg<D>;
+  auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
+  uint32_t tile = 0, units = 0;
+  uint32_t last_fill[kBwdStages] = {0xFFFFFFFFu, 0xFFFFFFFFu};
+  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    int bh, i;
+    dq_unit(p, u, bh, i);
+    const int n = p.causal ? i + 1 : p.n_blk;
+    if (!ptx::mbar_wait(bar(C::kStEmpty), (units & 1u) ^ 1u, ctl, 1u)) goto drain;
+    ptx::mbar_arrive_expect_tx(bar(C::kStFull), 2 * C::kTile);
+    load_tile<D, E>(&p.tm_q, sbase + C::kStatOff, bar(C::kStFull), i * 128, bh);
+    load_tile<D, E>(&p.tm_do, sbase + C::kStatOff + C::kTile, bar(C::kStFull), i * 128, bh);
+    ++units;
+    for (int j = 0; j < n; ++j, ++tile) {
+      const uint32_t s = tile % kBwdStages, f = tile / kBwdStages;
+      if (!ptx::mbar_wait(bar(C::kDone + s), (f & 1u) ^ 1u, ctl, 1u)) goto drain;
+      const uint32_t dst = sbase + C::kRingOff + s * C::kStageBytes;
+      ptx::mbar_arrive_expect_tx(bar(C::kReady + s), 2 * C::kTile);
+      load_tile<D, E>(&p.tm_k, dst, bar(C::kReady + s), j * 128, bh);
+      load_tile<D, E>(&p.tm_v, dst + C::kTile, bar(C::kReady + s), j * 128, bh);
+      last_fill[s] = f;
+    }
+  }
+drain:
+  producer_drain<D>(sbase, last_fill, units, ctl, 8u);
+}
+
+template <int D, Elem E>
+__device__ __noinline__ void dq_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const ptx::WaitCtl& ctl) {
+  using C = BwdCfg<D>;
+  auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
+  const uint32_t q_lo = ptx::sdesc_lo(sbase + C::kStatOff, 16);
+  const uint32_t do_lo = ptx::sdesc_lo(sbase + C::kStatOff + C::kTile, 16);
+  constexpr uint32_t kStageDesc = C::kStageBytes >> 4;
+  const uint32_t k_lo0 = ptx::sdesc_lo(sbase + C::kRingOff, 16);                 // K as K-major B of S
+  const uint32_t v_lo0 = ptx::sdesc_lo(sbase + C::kRingOff + C::kTile, 16);      // V as K-major B of dP
+  const uint32_t kmn_lo0 = ptx::sdesc_lo(sbase + C::kRingOff, v_lbo<D, E>());    // K as MN-major B of dQ
+  const uint32_t tS = tmem + kTmS, tDP = tmem + kTmDP, tAcc = tmem + kTmAcc;
+  uint32_t tile = 0, units = 0;
+  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    int bh, i;
+    dq_unit(p, u, bh, i);
+    const int n = p.causal ? i + 1 : p.n_blk;
+    if (!ptx::mbar_wait(bar(C::kStFull), units & 1u, ctl, 2u)) goto done;
+    for (int j = 0; j < n; ++j, ++tile) {
+      const uint32_t s = tile % kBwdStages, f = tile / kBwdStages;
+      if (!ptx::mbar_wait(bar(C::kReady + s), f & 1u, ctl, 2u)) goto done;
+      issue_s<D, E>(tS, q_lo, k_lo0 + s * kStageDesc);       // S = Q K_j^T
+      issue_s<D, E>(tDP, do_lo, v_lo0 + s * kStageDesc);     // dP = dO V_j^T
+      ptx::mma_commit(bar(C::kSdpFull));
+      if (!ptx::mbar_wait(bar(C::kDsFull), tile & 1u, ctl, 2u)) goto done;
+      ptx::tc_fence_after();
+      if (j == 0) issue_pv<D, E, false>(tAcc, tS, kmn_lo0 + s * kStageDesc);   // dQ = dS K_j
+      else issue_pv<D, E, true>(tAcc, tS, kmn_lo0 + s * kStageDesc);          // dQ += dS K_j
+      ptx::mma_commit(bar(C::kDone + s));
+    }
+    ptx::mma_commit(bar(C::kStEmpty));
+    ptx::mma_commit(bar(C::kAccFull));
+    ++units;
+  }
+done:
+  ptx::mma_commit(bar(C::kMmaDone));
+  if (!ptx::mbar_wait_drain(bar(C::kMmaDone), 0, ctl.timeout_ns)) atomicOr(ctl.status, 8u);
+}
+
+template <int D, Elem E>
+__device__ __forceinline__ void dq_compute(const BwdParams& p, uint32_t sbase, uint32_t tmem,
+                                           const ptx::WaitCtl& ctl) {
+  using C = BwdCfg<D>;
+  constexpr bool kBf16 = E == Elem::BF16;
+  auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
+  const int r = threadIdx.x;                                   // row in the Q tile = TMEM lane
+  const uint32_t lane_base = static_cast<uint32_t>((threadIdx.x / 32) * 32) << 16;
+  const uint32_t tS = tmem + lane_base + kTmS, tDP = tmem + lane_base + kTmDP, tAcc = tmem + lane_base + kTmAcc;
+  const int lane = threadIdx.x & 31;
+  uint32_t tile = 0, units = 0;
+  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    int bh, i;
+    dq_unit(p, u, bh, i);
+    const int n = p.causal ? i + 1 : p.n_blk;
+    const int row = i * 128 + r;
+    const size_t wrow = static_cast<size_t>(bh) * p.n_pad + row;
+    const float lse2 = p.lse2[wrow], dlt = p.delta[wrow];
+    for (int j = 0; j < n; ++j, ++tile) {
+      const bool got = ptx::mbar_wait(bar(C::kSdpFull), tile & 1u, ctl, 4u);
+      if (!__all_sync(0xFFFFFFFFu, got)) return;
+      ptx::tc_fence_after();
+      const int col0 = j * 128;
+      // keys past N, and (causal) past this row, get P = 0
+      const int visible = min(p.N, p.causal ? row + 1 : p.N) - col0;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sr[32], dr[32];
+        ptx::tmem_ld32(tS + 32 * c, sr);
+        ptx::tmem_ld32(tDP + 32 * c, dr);
+        ptx::tmem_wait_ld();
+        float ds[32];
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          const float pv = (32 * c + x < visible) ? ptx::ex2(fmaf(__uint_as_float(sr[x]), p.scale_log2, -lse2)) : 0.f;
+          ds[x] = pv * (__uint_as_float(dr[x]) - dlt);
+        }
+        uint32_t w[16];
+        pack16<kBf16>(ds, w);
+        // packed dS overwrites S columns 16c..16c+15, already read (chunks <= c)
+        ptx::tmem_st16(tS + 16 * c, w);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(C::kDsFull));
+    }
+    const bool got = ptx::mbar_wait(bar(C::kAccFull), units & 1u, ctl, 4u);
+    if (!__all_sync(0xFFFFFFFFu, got)) return;
+    ++units;
+    ptx::tc_fence_after();
+    store_acc_row<D, kBf16>(tAcc, p.scale, p.dq, (static_cast<size_t>(bh) * p.N + (row < p.N ? row : 0)) * D,
+                            row < p.N);
+    ptx::tc_fence_before();
+  }
+}
+
+// ---------------------------------------------------------------------------- dkdv kernel
+
+template <int D, Elem E>
+__device__ __noinline__ void dkdv_producer(const BwdParams& p, uint32_t sbase, const ptx::WaitCtl& ctl) {
+  using C = BwdCfg<D>;
+  auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
+  uint32_t tile = 0, units = 0;
+  uint32_t last_fill[kBwdStages] = {0xFFFFFFFFu, 0xFFFFFFFFu};
+  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    int bh, j;
+    dkdv_unit(p, u, bh, j);
+    const int i0 = p.causal ? j : 0;
+    if (!ptx::mbar_wait(bar(C::kStEmpty), (units & 1u) ^ 1u, ctl, 1u)) goto drain;
+    ptx::mbar_arrive_expect_tx(bar(C::kStFull), 2 * C::kTile);
+    load_tile<D, E>(&p.tm_k, sbase + C::kStatOff, bar(C::kStFull), j * 128, bh);
+    load_tile<D, E>(&p.tm_v, sbase + C::kStatOff + C::kTile, bar(C::kStFull), j * 128, bh);
+    ++units;
+    for (int i = i0; i < p.n_blk; ++i, ++tile) {
+      const uint32_t s = tile % kBwdStages, f = tile / kBwdStages;
+      if (!ptx::mbar_wait(bar(C::kDone + s), (f & 1u) ^ 1u, ctl, 1u)) goto drain;
+      const uint32_t dst = sbase + C::kRingOff + s * C::kStageBytes;
+      ptx::mbar_arrive_expect_tx(bar(C::kReady + s), 2 * C::kTile + 2 * C::kVecBytes);
+      load_tile<D, E>(&p.tm_q, dst, bar(C::kReady + s), i * 128, bh);
+      load_tile<D, E>(&p.tm_do, dst + C::kTile, bar(C::kReady + s), i * 128, bh);
+      const size_t w = static_cast<size_t>(bh) * p.n_pad + i * 128;
+      ptx::bulk_load(dst + 2 * C::kTile, p.lse2 + w, C::kVecBytes, bar(C::kReady + s));
+      ptx::bulk_load(dst + 2 * C::kTile + C::kVecBytes, p.delta + w, C::kVecBytes, bar(C::kReady + s));
+      last_fill[s] = f;
+    }
+  }
+drain:
+  producer_drain<D>(sbase, last_fill, units, ctl, 8u);
+}
+
+template <int D, Elem E>
+__device__ __noinline__ void dkdv_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const ptx::WaitCtl& ctl) {
+  using C = BwdCfg<D>;
+  auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
+  const uint32_t k_lo = ptx::sdesc_lo(sbase + C::kStatOff, 16);                  // K as K-major A of S^T
+  const uint32_t v_lo = ptx::sdesc_lo(sbase + C::kStatOff + C::kTile, 16);       // V as K-major A of dP^T
+  constexpr uint32_t kStageDesc = C::kStageBytes >> 4;
+  const uint32_t q_lo0 = ptx::sdesc_lo(sbase + C::kRingOff, 16);                 // Q as K-major B of S^T
+  const uint32_t do_lo0 = ptx::sdesc_lo(sbase + C::kRingOff + C::kTile, 16);     // dO as K-major B of dP^T
+  const uint32_t qmn_lo0 = ptx::sdesc_lo(sbase + C::kRingOff, v_lbo<D, E>());    // Q as MN-major B of dK
+  const uint32_t domn_lo0 = ptx::sdesc_lo(sbase + C::kRingOff + C::kTile, v_lbo<D, E>());  // dO, of dV
+  const uint32_t tS = tmem + kTmS, tDP = tmem + kTmDP, tDV = tmem + kTmAcc, tDK = tmem + kTmAcc + D;
+  uint32_t tile = 0, units = 0;
+  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    int bh, j;
+    dkdv_unit(p, u, bh, j);
+    const int i0 = p.causal ? j : 0;
+    if (!ptx::mbar_wait(bar(C::kStFull), units & 1u, ctl, 2u)) goto done;
+    for (int i = i0; i < p.n_blk; ++i, ++tile) {
+      const uint32_t s = tile % kBwdStages, f = tile / kBwdStages;
+      if (!ptx::mbar_wait(bar(C::kReady + s), f & 1u, ctl, 2u)) goto done;
+      issue_s<D, E>(tS, k_lo, q_lo0 + s * kStageDesc);       // S^T = K Q_i^T
+      issue_s<D, E>(tDP, v_lo, do_lo0 + s * kStageDesc);     // dP^T = V dO_i^T
+      ptx::mma_commit(bar(C::kSdpFull));
+      if (!ptx::mbar_wait(bar(C::kDsFull), tile & 1u, ctl, 2u)) goto done;
+      ptx::tc_fence_after();
+      if (i == i0) {
+        issue_pv<D, E, false>(tDV, tS, domn_lo0 + s * kStageDesc);   // dV = P^T dO_i
+        issue_pv<D, E, false>(tDK, tDP, qmn_lo0 + s * kStageDesc);   // dK = dS^T Q_i
+      } else {
+        issue_pv<D, E, true>(tDV, tS, domn_lo0 + s * kStageDesc);
+        issue_pv<D, E, true>(tDK, tDP, qmn_lo0 + s * kStageDesc);
+      }
+      ptx::mma_commit(bar(C::kDone + s));
+    }
+    ptx::mma_commit(bar(C::kStEmpty));
+    ptx::mma_commit(bar(C::kAccFull));
+    ++units;
+  }
+done:
+  ptx::mma_commit(bar(C::kMmaDone));
+  if (!ptx::mbar_wait_drain(bar(C::kMmaDone), 0, ctl.timeout_ns)) atomicOr(ctl.status, 8u);
+}
+
+template <int D, Elem E>
+__device__ __forceinline__ void dkdv_compute(const BwdParams& p, uint32_t sbase, uint8_t* smem, uint32_t tmem,
+                                             const ptx::WaitCtl& ctl) {
+  using C = BwdCfg<D>;
+  constexpr bool kBf16 = E == Elem::BF16;
+  auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
+  const int kr = threadIdx.x;                                  // key row in the K/V tile = TMEM lane
+  const uint32_t lane_base = static_cast<uint32_t>((threadIdx.x / 32) * 32) << 16;
+  const uint32_t tS = tmem + lane_base + kTmS, tDP = tmem + lane_base + kTmDP;
+  const uint32_t tDV = tmem + lane_base + kTmAcc, tDK = tDV + D;
+  const int lane = threadIdx.x & 31;
+  uint32_t tile = 0, units = 0;
+  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    int bh, j;
+    dkdv_unit(p, u, bh, j);
+    const int i0 = p.causal ? j : 0;
+    const int key = j * 128 + kr;
+    for (int i = i0; i < p.n_blk; ++i, ++tile) {
+      const bool got = ptx::mbar_wait(bar(C::kSdpFull), tile & 1u, ctl, 4u);
+      if (!__all_sync(0xFFFFFFFFu, got)) return;
+      ptx::tc_fence_after();
+      const uint32_t s = tile % kBwdStages;
+      const float* lse2 = reinterpret_cast<const float*>(smem + C::kRingOff + s * C::kStageBytes + 2 * C::kTile);
+      const float* dlt = lse2 + 128;
+      // causal diagonal tile: query i*128 + c sees this key iff c >= kr (padded queries
+      // have LSE*log2(e) = +inf and so P = 0 already)
+      const int first = (p.causal && i == j) ? kr : 0;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sr[32], dr[32];
+        ptx::tmem_ld32(tS + 32 * c, sr);
+        ptx::tmem_ld32(tDP + 32 * c, dr);
+        ptx::tmem_wait_ld();
+        float pv[32], ds[32];
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          const int q = 32 * c + x;
+          pv[x] = q >= first ? ptx::ex2(fmaf(__uint_as_float(sr[x]), p.scale_log2, -lse2[q])) : 0.f;
+          ds[x] = pv[x] * (__uint_as_float(dr[x]) - dlt[q]);
+        }
+        uint32_t wp[16], wd[16];
+        pack16<kBf16>(pv, wp);
+        pack16<kBf16>(ds, wd);
+        // packed P^T / dS^T overwrite S^T / dP^T columns 16c..16c+15, already read
+        ptx::tmem_st16(tS + 16 * c, wp);
+        ptx::tmem_st16(tDP + 16 * c, wd);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(C::kDsFull));
+    }
+    const bool got = ptx::mbar_wait(bar(C::kAccFull), units & 1u, ctl, 4u);
+    if (!__all_sync(0xFFFFFFFFu, got)) return;
+    ++units;
+    ptx::tc_fence_after();
+    const size_t off = (static_cast<size_t>(bh) * p.N + (key < p.N ? key : 0)) * D;
+    store_acc_row<D, kBf16>(tDV, 1.f, p.dv, off, key < p.N);
+    store_acc_row<D, kBf16>(tDK, p.scale, p.dk, off, key < p.N);
+    ptx::tc_fence_before();
+  }
+}
+
+// ---------------------------------------------------------------------------- kernels
+
+template <int D, Elem E, bool DKDV>
+__global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_constant__ BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = ptx::smem_u32(smem);
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
+  auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kNumBars; ++i) ptx::mbar_init(bar(i), i == C::kDsFull ? 4 : 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == kBwdLoadWarp && lane == 0) {
+    ptx::prefetch_tensormap(&p.tm_q);
+    ptx::prefetch_tensormap(&p.tm_k);
+    ptx::prefetch_tensormap(&p.tm_v);
+    ptx::prefetch_tensormap(&p.tm_do);
+  }
+  if (warp == kBwdMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const ptx::WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+
+  if (warp == kBwdLoadWarp) {
+    if (lane == 0) {
+      if constexpr (DKDV) dkdv_producer<D, E>(p, sbase, ctl);
+      else dq_producer<D, E>(p, sbase, ctl);
+    }
+  } else if (warp == kBwdMmaWarp) {
+    if (lane == 0) {
+      if constexpr (DKDV) dkdv_mma<D, E>(p, sbase, tmem, ctl);
+      else dq_mma<D, E>(p, sbase, tmem, ctl);
+    }
+  } else {
+    if constexpr (DKDV) dkdv_compute<D, E>(p, sbase, smem, tmem, ctl);
+    else dq_compute<D, E>(p, sbase, tmem, ctl);
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kBwdMmaWarp) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D, Elem E>
+cudaError_t launch_bwd_kernels(const BwdParams& p, int grid, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  constexpr bool kBf16 = E == Elem::BF16;
+  const long long rows = static_cast<long long>(p.BH) * p.n_pad;
+  const long long threads = rows * (D / 8);
+  fa_bwd_prep_kernel<D, kBf16><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  auto dq = fa_bwd_kernel<D, E, false>;
+  auto dkdv = fa_bwd_kernel<D, E, true>;
+  for (auto k : {dq, dkdv}) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc);
+    if (e != cudaSuccess) return e;
+  }
+  dq<<<grid, kBwdThreads, C::kAlloc, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dkdv<<<grid, kBwdThreads, C::kAlloc, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(int d, bool bf16, const BwdParams& p, int grid, cudaStream_t stream) {
+  if (d == 128)
+    return bf16 ? launch_bwd_kernels<128, Elem::BF16>(p, grid, stream)
+                : launch_bwd_kernels<128, Elem::F16>(p, grid, stream);
+  return bf16 ? launch_bwd_kernels<64, Elem::BF16>(p, grid, stream)
+              : launch_bwd_kernels<64, Elem::F16>(p, grid, stream);
+}
+
+}  // namespace fa

@@ -65,4 +65,30 @@ struct DecodeParams {
   int causal;
 };
 
+// Attention backward: dQ, dK, dV from Q, K, V, O, LSE and dO.
+struct BwdParams {
+  CUtensorMap tm_q;   // 3-D {d, N, B*H}, box {128 bytes of d, 128 rows, 1}, 128-byte swizzle
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  CUtensorMap tm_do;
+  const void* o;      // [B*H, N, d] (prep kernel)
+  const void* dout;   // [B*H, N, d] (prep kernel)
+  const float* lse;   // [B*H, N] natural-log LSE of the forward pass
+  float* lse2;        // workspace [B*H, n_pad]: lse * log2(e), +inf on padded rows
+  float* delta;       // workspace [B*H, n_pad]: sum_c dO_ic O_ic, 0 on padded rows
+  void* dq;           // [B*H, N, d], same type as the inputs
+  void* dk;
+  void* dv;
+  unsigned int* status;
+  unsigned long long timeout_ns;
+  float scale;
+  float scale_log2;   // scale * log2(e)
+  int N;
+  int n_pad;          // N rounded up to 128
+  int BH;
+  int n_blk;          // ceil(N / 128): Q tiles = K/V tiles per head
+  int num_units;      // BH * n_blk (each kernel)
+  int causal;
+};
+
 }  // namespace fa
