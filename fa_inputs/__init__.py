@@ -22,7 +22,8 @@ finally each tensor is cast to the workload dtype.
 
 The upstream gradient dO of the backward pass is one more tensor shaped like Q:
 ``randn(shape)`` in float32 from its own generator seeded with ``seed + 100``,
-cast to the workload dtype (``make_dout``).
+cast to the workload dtype (``make_dout``).  The randomised Hadamard rotation's
+signs are d bits drawn the same way (``make_sign_flips``).
 """
 from __future__ import annotations
 
@@ -40,6 +41,7 @@ __all__ = [
     "make_qkv",
     "make_inputs",
     "make_dout",
+    "make_sign_flips",
     "sample_rows",
 ]
 
@@ -110,6 +112,14 @@ def make_dout(shape, dtype: torch.dtype, seed: int) -> torch.Tensor:
     """Upstream gradient dO for a workload drawn with ``seed`` (own generator, seed + 100)."""
     g = torch.Generator().manual_seed(seed + 100)
     return torch.randn(tuple(shape), generator=g, dtype=torch.float32).to(dtype)
+
+
+def make_sign_flips(d: int, seed: int) -> int:
+    """Sign mask of the randomised Hadamard rotation: bit c set with probability 1/2,
+    from ``torch.randint(0, 2, (d,))`` on a generator seeded with ``seed``."""
+    g = torch.Generator().manual_seed(seed)
+    bits = torch.randint(0, 2, (d,), generator=g)
+    return sum(1 << c for c in range(d) if bits[c])
 
 
 def make_inputs(w: Workload):

@@ -26,5 +26,6 @@ from .fp8 import (  # noqa: F401
     hadamard_rotate,
     quantize_fp8_blocks,
     round_to_e4m3,
+    sign_vector,
     sylvester_hadamard,
 )

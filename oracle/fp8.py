@@ -20,6 +20,16 @@ the 8-bit format nor the transform size; the readings used here:
   applied along the head dimension to Q and K (the same matrix for both, so
   (QH)(KH)^T = QK^T); V is never rotated.
 
+Variants (the next steps after the plain path, not on the pages beyond the words
+"Hadamard-Transformation" and "Absmax"):
+
+* randomised rotation: ``x -> (x * sigma) @ H_d / sqrt(d)`` with a +-1 sign vector
+  sigma, the same for Q and K, so scores are still unchanged; sigma is an input
+  (drawn by the caller from a seeded generator), given as a bit mask where bit c
+  set means sigma_c = -1;
+* per-head scale: one absmax over all N rows of a (b, h) instead of one per block,
+  stored in every block entry of the scale array.
+
 The e4m3 grid is written out from the format definition: a normal value is
 ``(1 + m/8) * 2^(E-7)`` for exponent field E in 1..15 (E=15, m=7 is NaN) and a
 subnormal is ``m * 2^-9``.
@@ -32,6 +42,7 @@ from .sdpa import _f64, attention
 
 __all__ = [
     "E4M3_MAX",
+    "sign_vector",
     "sylvester_hadamard",
     "hadamard_rotate",
     "round_to_e4m3",
@@ -59,13 +70,20 @@ def sylvester_hadamard(d: int) -> np.ndarray:
     return h
 
 
-def hadamard_rotate(x) -> np.ndarray:
-    """x @ H_d / sqrt(d) along the last axis, in fp64.
+def sign_vector(flips: int, d: int) -> np.ndarray:
+    """+-1 vector of length d: entry c is -1 where bit c of the integer mask is set."""
+    return np.array([-1.0 if (flips >> c) & 1 else 1.0 for c in range(d)])
+
+
+def hadamard_rotate(x, signs=None) -> np.ndarray:
+    """(x * signs) @ H_d / sqrt(d) along the last axis, in fp64 (signs: None or +-1 of length d).
 
     The +-1 matrix is applied first (sums of the inputs, exact in fp64 for
     bf16 data) and the result divided by sqrt(d) once."""
     x = _f64(x)
     d = x.shape[-1]
+    if signs is not None:
+        x = x * np.asarray(signs, dtype=np.float64)
     return (x @ sylvester_hadamard(d)) / np.sqrt(d)
 
 
@@ -108,20 +126,23 @@ def e4m3_decode(codes) -> np.ndarray:
     return sign * val
 
 
-def quantize_fp8_blocks(x, block: int = 64, hadamard: bool = False):
+def quantize_fp8_blocks(x, block: int = 64, hadamard: bool = False, signs=None, per_head: bool = False):
     """Block absmax quantisation of ``x [B,H,N,d]`` to E4M3.
 
     Returns ``(codes uint8 [B,H,N,d], scales fp64 [B,H,ceil(N/block)])``; the
-    rotation, when asked for, is applied before the absmax is taken.
+    rotation (with ``signs`` if given), when asked for, is applied before the
+    absmax is taken.  With ``per_head`` the absmax runs over the whole head and
+    every block of it gets that one scale.
     """
-    y = hadamard_rotate(x) if hadamard else _f64(x)
+    y = hadamard_rotate(x, signs) if hadamard else _f64(x)
     B, H, N, d = y.shape
     nb = -(-N // block)
     scales = np.empty((B, H, nb))
     codes = np.empty((B, H, N, d), dtype=np.uint8)
+    head_amax = np.abs(y).max(axis=(2, 3))
     for i in range(nb):
         blk = y[:, :, i * block:(i + 1) * block, :]
-        amax = np.abs(blk).max(axis=(2, 3))
+        amax = head_amax if per_head else np.abs(blk).max(axis=(2, 3))
         s = np.where(amax > 0, amax / E4M3_MAX, 1.0)
         scales[:, :, i] = s
         codes[:, :, i * block:(i + 1) * block, :] = e4m3_encode(round_to_e4m3(blk / s[:, :, None, None]))
@@ -137,7 +158,7 @@ def dequantize_fp8_blocks(codes, scales, block: int = 64) -> np.ndarray:
 
 
 def emulate_fp8_attention(q, k, v, scale: float, causal: bool, hadamard: bool, block: int = 64,
-                          round_p: bool = False):
+                          round_p: bool = False, signs=None, v_per_head: bool = False):
     """Predictor, not a reference: fp64 attention on dequantised E4M3 inputs.
 
     The reference for the FP8 path is ``attention`` on the unquantised inputs;
@@ -147,11 +168,13 @@ def emulate_fp8_attention(q, k, v, scale: float, causal: bool, hadamard: bool, b
     scales folded into them relative to the head's largest V scale:
     ``P~_ij = e4m3(p_ij * s_v(j) / max s_v)`` and
     ``O_i = max s_v * sum_j P~_ij * v8_j / sum_j p_ij``.
+    ``signs`` randomises the rotation of Q and K; ``v_per_head`` gives V one scale
+    per head.
     Returns ``(O, LSE)`` (the LSE is that of the dequantised scores).
     """
-    qc, qs = quantize_fp8_blocks(q, block, hadamard)
-    kc, ks = quantize_fp8_blocks(k, block, hadamard)
-    vc, vs = quantize_fp8_blocks(v, block, False)
+    qc, qs = quantize_fp8_blocks(q, block, hadamard, signs)
+    kc, ks = quantize_fp8_blocks(k, block, hadamard, signs)
+    vc, vs = quantize_fp8_blocks(v, block, False, per_head=v_per_head)
     qd, kd = dequantize_fp8_blocks(qc, qs, block), dequantize_fp8_blocks(kc, ks, block)
     if not round_p:
         return attention(qd, kd, dequantize_fp8_blocks(vc, vs, block), scale, causal)

@@ -357,3 +357,38 @@ def test_decode_causal_first_row_sees_the_prefix():
     o, _ = oracle.attention_decode(q, k2, v2, 0.5, True)
     ref, _ = oracle.attention_decode(q[:, :, :1], k2[:, :, :8], v2[:, :, :8], 0.5, False)
     assert np.abs(o[0, 0, 0] - ref[0, 0, 0]).max() < 1e-13
+
+
+# ----------------------------------------------------------------------------- FP8 variants
+
+def test_sign_vector_reads_the_mask_bit_by_bit():
+    assert list(oracle.sign_vector(0b1011, 6)) == [-1, -1, 1, -1, 1, 1]
+    assert list(oracle.sign_vector(1 << 127, 128))[-1] == -1
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_signed_rotation_is_orthogonal_and_keeps_scores(d):
+    from fa_inputs import make_sign_flips
+    sv = oracle.sign_vector(make_sign_flips(d, 11), d)
+    r = np.diag(sv) @ oracle.sylvester_hadamard(d) / np.sqrt(d)
+    assert np.abs(r @ r.T - np.eye(d)).max() < 1e-14
+    q, k, _ = _rand((1, 2, 9, d), 12)
+    s0 = q.numpy() @ np.swapaxes(k.numpy(), -1, -2)
+    s1 = oracle.hadamard_rotate(q, sv) @ np.swapaxes(oracle.hadamard_rotate(k, sv), -1, -2)
+    assert np.abs(s1 - s0).max() < 1e-12
+    # all-positive signs are the plain rotation
+    assert np.array_equal(oracle.hadamard_rotate(q, np.ones(d)), oracle.hadamard_rotate(q))
+
+
+def test_per_head_scale_is_the_largest_block_scale():
+    x, _, _ = make_qkv((2, 3, 200, 64), torch.bfloat16, 13, outliers=True)
+    for had in (False, True):
+        _, sb = oracle.quantize_fp8_blocks(x, 64, had)
+        codes, sh = oracle.quantize_fp8_blocks(x, 64, had, per_head=True)
+        assert np.array_equal(sh, np.broadcast_to(sb.max(axis=2, keepdims=True), sh.shape))
+        y = oracle.hadamard_rotate(x) if had else x.double().numpy()
+        deq = oracle.dequantize_fp8_blocks(codes, sh)
+        # E4M3 keeps 3 mantissa bits: error <= 2^-4 relative (normals) or half the
+        # subnormal quantum 2^-9 times the scale
+        bound = np.maximum(2.0 ** -4 * np.abs(y), 2.0 ** -10 * sh.max())
+        assert (np.abs(deq - y) <= bound + 1e-12).all()
