@@ -78,6 +78,24 @@ int fa_quantize_fp8(const void* x, void* x8, float* scale, int B, int H, int N, 
                     int transpose_out, void* stream);
 
 /*
+ * fa_quantize_fp8 with two variants of the prologue (steps beyond the pages, which
+ * name only a "Hadamard-Transformation" and "Absmax" scaling):
+ *   sign_flips_lo/hi : randomised rotation x -> (x * sigma) H_d / sqrt(d), where bit c
+ *                      of the 128-bit mask (lo = bits 0..63, hi = bits 64..127) sets
+ *                      sigma_c = -1.  Use the same mask for Q and K: scores are
+ *                      unchanged, so fa_fwd_fp8 needs nothing else.  Must be 0 when
+ *                      hadamard = 0, and hi must be 0 for d = 64 (FA_ERR_UNSUPPORTED).
+ *   per_head         : 1 takes one absmax over all N rows of each (b, h) and writes it
+ *                      to every block entry of `scale` (the layout fa_fwd_fp8 reads);
+ *                      0 is the per-64-row-block scale of fa_quantize_fp8.  Per-head
+ *                      reads x twice (absmax pass, then quantisation pass).
+ * Other arguments and errors as fa_quantize_fp8.
+ */
+int fa_quantize_fp8_ex(const void* x, void* x8, float* scale, int B, int H, int N, int d, int hadamard,
+                       unsigned long long sign_flips_lo, unsigned long long sign_flips_hi, int per_head,
+                       int transpose_out, void* stream);
+
+/*
  * Attention forward from E4M3 inputs produced by fa_quantize_fp8.
  *   q8, k8   : [B, H, N, d] E4M3 (rotated by the same Hadamard matrix, or both not)
  *   v8t      : [B, H, d, N] E4M3 (V quantised with transpose_out = 1, not rotated)

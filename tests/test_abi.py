@@ -34,7 +34,7 @@ def test_header_declares_the_boundary():
     assert _declared() == sorted(["fa_fwd", "fa_quantize_fp8", "fa_fwd_fp8", "fa_strerror",
                                   "fa_last_device_status", "fa_debug_inject_stall", "fa_version",
                                   "fa_decode", "fa_decode_workspace_size", "fa_decode_noalloc",
-                                  "fa_bwd", "fa_bwd_workspace_size"])
+                                  "fa_bwd", "fa_bwd_workspace_size", "fa_quantize_fp8_ex"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -114,3 +114,11 @@ def test_bwd_rejects_bad_arguments_on_the_host(lib):
     assert call(args, wsb=512) == fa.FA_ERR_WORKSPACE     # 1 x 1 x 128 needs 1024
     n = ctypes.c_ulonglong(0)
     assert lib.fa_bwd_workspace_size(2, 3, 200, 64, ctypes.byref(n)) == fa.FA_OK and n.value == 2 * 2 * 3 * 256 * 4
+
+
+def test_quantize_ex_rejects_bad_options_on_the_host(lib):
+    call = lambda had=1, lo=0, hi=0, ph=0, d=128: lib.fa_quantize_fp8_ex(A, A, A, 1, 1, 64, d, had, lo, hi, ph, 0, None)
+    assert call(had=0, lo=1) == fa.FA_ERR_UNSUPPORTED          # signs without the rotation
+    assert call(d=64, hi=1) == fa.FA_ERR_UNSUPPORTED           # sign bit past d
+    assert call(ph=2) == fa.FA_ERR_UNSUPPORTED
+    assert call(d=96) == fa.FA_ERR_UNSUPPORTED

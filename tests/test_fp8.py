@@ -4,7 +4,8 @@ Quantisation is compared code by code with the fp64 oracle.  Where the two
 differ, the exact scaled value must sit on a rounding midpoint between the two
 codes, up to the fp32 rounding of the kernel's rotation (a few units of 2^-24
 times the row's L1 norm, in scaled units): the fp32 kernel and the fp64 oracle
-may decide such a near-tie differently; anything else fails.  Scales must agree
+may decide such a near-tie differently; anything else fails.  Ties are rare with
+the rotation and about 1 % of values without it (bf16 data over a bf16 absmax).  Scales must agree
 to 1e-6 relative.
 
 The FP8 forward is compared with the fp64 attention oracle on the UNQUANTISED
@@ -28,14 +29,14 @@ import pytest
 import torch
 
 import oracle
-from fa_inputs import WORKLOADS, make_inputs, make_qkv
+from fa_inputs import WORKLOADS, make_inputs, make_qkv, make_sign_flips
 
 pytestmark = pytest.mark.gpu
 
 
-def _codes_match(gpu_codes, x, hadamard):
-    oc, osc = oracle.quantize_fp8_blocks(x, 64, hadamard)
-    y = oracle.hadamard_rotate(x) if hadamard else x.double().numpy()
+def _codes_match(gpu_codes, x, hadamard, signs=None, per_head=False):
+    oc, osc = oracle.quantize_fp8_blocks(x, 64, hadamard, signs, per_head)
+    y = oracle.hadamard_rotate(x, signs) if hadamard else x.double().numpy()
     mism = oracle.e4m3_decode(gpu_codes) != oracle.e4m3_decode(oc)     # +0 and -0 are one value
     if mism.any():
         N = y.shape[2]
@@ -47,7 +48,11 @@ def _codes_match(gpu_codes, x, hadamard):
         mid = 0.5 * (gv + ov)
         off_tie = np.abs(scaled - mid) > 2.0 ** -18 * (np.abs(scaled) + l1)
         assert not off_tie.any(), f"{int(off_tie.sum())} codes differ away from a rounding tie"
-    assert mism.mean() <= 1e-3
+    # Only codes on ties may differ.  Without the rotation, x and its absmax are both
+    # bf16 numbers, so 448 x / absmax falls exactly on an E4M3 midpoint for about 1 %
+    # of values (0.9-1.5 % measured at N=200, d=64; none with the rotation), and the
+    # kernel, which forms 448 / absmax in fp32 first, breaks some of them the other way.
+    assert mism.mean() <= 2e-2
     return osc
 
 
@@ -135,3 +140,39 @@ def test_fp8_rejections(gpu_lib):
     with pytest.raises(gpu_lib.FAError) as e:
         gpu_lib.attention_fp8(q8, q8, v8, s, s, s)
     assert e.value.status == gpu_lib.FA_ERR_SHAPE
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [200, 1000])
+@pytest.mark.parametrize("hadamard,signed,per_head", [(True, True, False), (True, True, True), (False, False, True),
+                                                      (True, False, True)])
+def test_quantize_variants_match_oracle(gpu_lib, d, N, hadamard, signed, per_head):
+    x, _, _ = make_qkv((2, 3, N, d), torch.bfloat16, 7 + N, outliers=True)
+    flips = make_sign_flips(d, 5) if signed else 0
+    x8, sc = gpu_lib.quantize_fp8(x.cuda(), hadamard=hadamard, sign_flips=flips, per_head=per_head)
+    torch.cuda.synchronize()
+    signs = oracle.sign_vector(flips, d) if signed else None
+    osc = _codes_match(x8.cpu().numpy(), x, hadamard, signs, per_head)
+    assert np.abs(sc.cpu().numpy() / osc - 1).max() <= 1e-6
+    if per_head:
+        assert bool((sc == sc[:, :, :1]).all())
+
+
+def test_fp8_randomised_rotation_and_per_head_v_track_the_predictor(gpu_lib):
+    q, k, v = make_qkv((1, 2, 1040, 128), torch.bfloat16, 77, outliers=True)
+    scale = 1 / math.sqrt(128)
+    flips = make_sign_flips(128, 9)
+    ro, _ = oracle.attention(q, k, v, scale, False)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    q8, qs = gpu_lib.quantize_fp8(qd, hadamard=True, sign_flips=flips)
+    k8, ks = gpu_lib.quantize_fp8(kd, hadamard=True, sign_flips=flips)
+    v8, vs = gpu_lib.quantize_fp8(vd, transpose_out=True, per_head=True)
+    o, lse = gpu_lib.attention_fp8(q8, k8, v8, qs, ks, vs, hadamard=True)
+    torch.cuda.synchronize()
+    st, bits = gpu_lib.last_device_status()
+    assert st == gpu_lib.FA_OK, f"device status {bits:#x}"
+    pred_o, pred_lse = oracle.emulate_fp8_attention(q, k, v, scale, False, True, round_p=True,
+                                                    signs=oracle.sign_vector(flips, 128), v_per_head=True)
+    got, want = oracle.rel_rms(o.float().cpu().numpy(), ro), oracle.rel_rms(pred_o, ro)
+    assert got <= 1.1 * want + 2e-3, f"{got:.4f} vs predicted {want:.4f}"
+    assert np.median(np.abs(lse.cpu().numpy() - pred_lse)) < 1e-4

@@ -65,6 +65,8 @@ _f = ctypes.c_float
 _SIGNATURES = {
     "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _vp]),
     "fa_quantize_fp8": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]),
+    "fa_quantize_fp8_ex": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_ulonglong, ctypes.c_ulonglong,
+                                _i, _i, _vp]),
     "fa_fwd_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _i, _vp]),
     "fa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _vp, ctypes.c_ulonglong, _vp]),
     "fa_decode_workspace_size": (_i, [_i, _i, _i, _i, _i, _i, ctypes.POINTER(ctypes.c_ulonglong)]),
@@ -191,9 +193,12 @@ def attention_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bo
 
 
 def quantize_fp8(x: torch.Tensor, hadamard: bool = False, transpose_out: bool = False,
-                 stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+                 stream: Optional[torch.cuda.Stream] = None, sign_flips: int = 0,
+                 per_head: bool = False) -> Tuple[torch.Tensor, torch.Tensor]:
     """Block absmax E4M3 quantisation of bf16 ``x [B,H,N,d]`` (optionally Hadamard-rotated).
 
+    ``sign_flips`` (an integer bit mask, bit c negates coordinate c before the
+    rotation) randomises the rotation; ``per_head`` takes one scale per (b, h).
     Returns (codes as uint8 [B,H,N,d] or [B,H,d,N] when transposed, scales fp32 [B,H,ceil(N/64)]).
     """
     lib = load_library()
@@ -203,6 +208,14 @@ def quantize_fp8(x: torch.Tensor, hadamard: bool = False, transpose_out: bool = 
     shape = (B, H, d, N) if transpose_out else (B, H, N, d)
     x8 = torch.empty(shape, device=x.device, dtype=torch.uint8)
     sc = torch.empty((B, H, (N + 63) // 64), device=x.device, dtype=torch.float32)
+    if sign_flips or per_head:
+        if not 0 <= int(sign_flips) < (1 << 128):
+            raise ValueError("sign_flips must be a 128-bit mask")
+        st = lib.fa_quantize_fp8_ex(_ptr(x), _ptr(x8), _ptr(sc), B, H, N, d, int(bool(hadamard)),
+                                    int(sign_flips) & ((1 << 64) - 1), int(sign_flips) >> 64, int(bool(per_head)),
+                                    int(bool(transpose_out)), _stream_handle(stream, x.device))
+        _check(st, "fa_quantize_fp8_ex")
+        return x8, sc
     st = lib.fa_quantize_fp8(_ptr(x), _ptr(x8), _ptr(sc), B, H, N, d, int(bool(hadamard)),
                              int(bool(transpose_out)), _stream_handle(stream, x.device))
     _check(st, "fa_quantize_fp8")

@@ -172,13 +172,20 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
-extern "C" int fa_quantize_fp8(const void* x, void* x8, float* scale, int B, int H, int N, int d,
-                               int hadamard, int transpose_out, void* stream) {
+namespace fa {
+namespace {
+
+int quantize_fp8(const void* x, void* x8, float* scale, int B, int H, int N, int d, int hadamard,
+                 unsigned long long flips_lo, unsigned long long flips_hi, int per_head, int transpose_out,
+                 void* stream) {
   if (!x || !x8 || !scale) return FA_ERR_NULL;
-  if ((hadamard != 0 && hadamard != 1) || (transpose_out != 0 && transpose_out != 1))
+  if ((hadamard != 0 && hadamard != 1) || (transpose_out != 0 && transpose_out != 1) ||
+      (per_head != 0 && per_head != 1))
     return FA_ERR_UNSUPPORTED;
   int st = check_shape(B, H, N, d);
   if (st != FA_OK) return st;
+  // sign flips only make sense with the rotation, and only on the d coordinates
+  if ((flips_lo | flips_hi) != 0 && (!hadamard || (d == 64 && flips_hi != 0))) return FA_ERR_UNSUPPORTED;
   if (transpose_out && N % 16 != 0) return FA_ERR_SHAPE;
   if (!aligned(x, 16) || !aligned(x8, 16) || !aligned(scale, 4)) return FA_ERR_ALIGN;
   const DeviceInfo* di = current_device(&st);
@@ -193,8 +200,28 @@ extern "C" int fa_quantize_fp8(const void* x, void* x8, float* scale, int B, int
   p.n_sblk = (N + 63) / 64;
   p.hadamard = hadamard;
   p.transpose_out = transpose_out;
+  p.flips_lo = flips_lo;
+  p.flips_hi = flips_hi;
+  p.per_head = per_head;
+  p.amax_mode = 0;
   const cudaError_t e = launch_quant_fp8(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" int fa_quantize_fp8(const void* x, void* x8, float* scale, int B, int H, int N, int d,
+                               int hadamard, int transpose_out, void* stream) {
+  return fa::quantize_fp8(x, x8, scale, B, H, N, d, hadamard, 0, 0, 0, transpose_out, stream);
+}
+
+extern "C" int fa_quantize_fp8_ex(const void* x, void* x8, float* scale, int B, int H, int N, int d,
+                                  int hadamard, unsigned long long sign_flips_lo,
+                                  unsigned long long sign_flips_hi, int per_head, int transpose_out,
+                                  void* stream) {
+  return fa::quantize_fp8(x, x8, scale, B, H, N, d, hadamard, sign_flips_lo, sign_flips_hi, per_head,
+                          transpose_out, stream);
 }
 
 extern "C" int fa_fwd_fp8(const void* q8, const void* k8, const void* v8t, void* o, float* lse, int B,

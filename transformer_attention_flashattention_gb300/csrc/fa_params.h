@@ -41,6 +41,11 @@ struct QuantParams {
   int n_sblk;
   int hadamard;
   int transpose_out;
+  unsigned long long flips_lo;   // randomised rotation: bit c negates coordinate c (c < 64) ...
+  unsigned long long flips_hi;   // ... and c - 64 (64 <= c < 128) before the transform
+  int per_head;                  // one absmax per (b, h) instead of per 64-row block
+  int amax_mode;                 // 0: own block absmax; 1: write the block absmax only;
+                                 // 2: quantise with the absmax already in `scale`
 };
 
 // Split-KV attention of N_q query rows against N_k cached keys.

@@ -11,6 +11,11 @@
 // shuffles.  It is left unnormalised: with y = x H and a = max |y| over the
 // block, the stored codes e4m3(y * 448 / a) equal e4m3((y / sqrt d) / s) for the
 // normalised rotation, and the stored scale is s = a / (448 sqrt d).
+//
+// Variants: a sign mask negates chosen coordinates before the transform (the
+// randomised rotation x D H); with one scale per head, the kernel first runs in a
+// mode that only writes each block's absmax, a small kernel takes the head's
+// maximum into every block entry, and a second pass quantises with it.
 #include <cstdint>
 
 #include <cuda_bf16.h>
@@ -67,6 +72,12 @@ __global__ void __launch_bounds__(kQuantThreads) fa_quant_fp8_kernel(const __gri
       for (int e = 0; e < E; ++e) y[rr][e] = 0.f;
     }
     if (p.hadamard) {
+      // randomised rotation: this lane's coordinates lane*E .. lane*E+E-1 of the sign mask
+      const int c0 = lane * E;
+      const unsigned long long word = c0 < 64 ? p.flips_lo : p.flips_hi;
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        if ((word >> ((c0 + e) & 63)) & 1ull) y[rr][e] = -y[rr][e];
       // strides 1 .. E/2 inside the thread
 #pragma unroll
       for (int h = 1; h < E; h <<= 1) {
@@ -99,16 +110,24 @@ __global__ void __launch_bounds__(kQuantThreads) fa_quant_fp8_kernel(const __gri
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
   if (lane == 0) s_wmax[warp] = amax;
   __syncthreads();
+  const size_t sidx = static_cast<size_t>(bh) * p.n_sblk + blk;
   if (threadIdx.x == 0) {
     float a = 0.f;
 #pragma unroll
     for (int w = 0; w < kQuantWarps; ++w) a = fmaxf(a, s_wmax[w]);
-    s_factor = a > 0.f ? kE4m3Max / a : 0.f;
-    float s = 1.f;
-    if (a > 0.f) s = p.hadamard ? a * (1.f / (kE4m3Max * sqrtf(static_cast<float>(D)))) : a / kE4m3Max;
-    p.scale[static_cast<size_t>(bh) * p.n_sblk + blk] = s;
+    if (p.amax_mode == 1) {
+      p.scale[sidx] = a;                 // first pass of a per-head scale: absmax only
+      s_factor = 0.f;
+    } else {
+      if (p.amax_mode == 2) a = p.scale[sidx];   // the head's absmax
+      s_factor = a > 0.f ? kE4m3Max / a : 0.f;
+      float s = 1.f;
+      if (a > 0.f) s = p.hadamard ? a * (1.f / (kE4m3Max * sqrtf(static_cast<float>(D)))) : a / kE4m3Max;
+      p.scale[sidx] = s;
+    }
   }
   __syncthreads();
+  if (p.amax_mode == 1) return;
   const float f = s_factor;
 
 #pragma unroll
@@ -144,16 +163,48 @@ __global__ void __launch_bounds__(kQuantThreads) fa_quant_fp8_kernel(const __gri
   }
 }
 
+// Per-head scale, between the two passes: the largest block absmax of each (b, h)
+// into every block entry.  One warp per head.
+__global__ void __launch_bounds__(256) fa_quant_head_max_kernel(const __grid_constant__ QuantParams p) {
+  const long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
+  const int lane = threadIdx.x & 31;
+  if (w >= p.BH) return;                 // whole warps leave together
+  float* row = p.scale + static_cast<size_t>(w) * p.n_sblk;
+  float m = 0.f;
+  for (int i = lane; i < p.n_sblk; i += 32) m = fmaxf(m, row[i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  for (int i = lane; i < p.n_sblk; i += 32) row[i] = m;
+}
+
+cudaError_t launch_quant_pass(const QuantParams& p, unsigned grid, cudaStream_t stream) {
+  if (p.d == 128) fa_quant_fp8_kernel<128><<<grid, kQuantThreads, 0, stream>>>(p);
+  else if (p.d == 64) fa_quant_fp8_kernel<64><<<grid, kQuantThreads, 0, stream>>>(p);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_quant_fp8(const QuantParams& p, cudaStream_t stream) {
   const long long blocks = static_cast<long long>(p.n_sblk) * p.BH;
   if (blocks >= (1ll << 31)) return cudaErrorInvalidConfiguration;
   const unsigned grid = static_cast<unsigned>(blocks);
-  if (p.d == 128) fa_quant_fp8_kernel<128><<<grid, kQuantThreads, 0, stream>>>(p);
-  else if (p.d == 64) fa_quant_fp8_kernel<64><<<grid, kQuantThreads, 0, stream>>>(p);
-  else return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  if (!p.per_head) {
+    QuantParams q = p;
+    q.amax_mode = 0;
+    return launch_quant_pass(q, grid, stream);
+  }
+  QuantParams q = p;
+  q.amax_mode = 1;
+  cudaError_t e = launch_quant_pass(q, grid, stream);
+  if (e != cudaSuccess) return e;
+  const long long warps_threads = static_cast<long long>(p.BH) * 32;
+  fa_quant_head_max_kernel<<<static_cast<unsigned>((warps_threads + 255) / 256), 256, 0, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  q.amax_mode = 2;
+  return launch_quant_pass(q, grid, stream);
 }
 
 }  // namespace fa
