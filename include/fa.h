@@ -65,6 +65,29 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
            int d, float scale, int causal, int dtype, void* stream);
 
 /*
+ * fa_fwd on HOST buffers, end to end: copies Q, K, V to the device, computes, and copies
+ * O (and LSE) back, with the copies of one chunk of heads overlapped with the
+ * computation of the next (a runtime convenience; the pages' operation is fa_fwd's).
+ *   q, k, v, o : [B, H, N, d] of `dtype` in host memory (pinned memory lets the copies
+ *                run asynchronously; pageable memory works, without overlap)
+ *   lse        : [B, H, N] float32 in host memory, or NULL
+ *   chunks     : number of head chunks (0 picks 8; at most 32 and B*H)
+ *   workspace  : DEVICE scratch of at least fa_fwd_host_workspace_size() bytes,
+ *                256-byte aligned, owned by the caller; calls sharing one workspace must
+ *                be on one stream (the copies wait for earlier work on `stream`)
+ * Asynchronous: the results are on the host once `stream` reaches this point
+ * (synchronise it).  Two copy streams and a few events per device are created on the
+ * first call there; concurrent calls from several host threads are serialised while
+ * they enqueue.  Errors as fa_fwd, plus FA_ERR_WORKSPACE.
+ */
+int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                float scale, int causal, int dtype, int chunks, void* workspace,
+                unsigned long long workspace_bytes, void* stream);
+
+/* Device scratch fa_fwd_host needs: Q, K, V, O and LSE on the device, 256-byte aligned each. */
+int fa_fwd_host_workspace_size(int B, int H, int N, int d, unsigned long long* bytes);
+
+/*
  * FP8 prologue: optional Hadamard rotation along d, block absmax, E4M3 quantisation.
  *   x        : [B, H, N, d] bfloat16 input
  *   x8       : E4M3 output, [B, H, N, d]; with transpose_out = 1 it is [B, H, d, N]

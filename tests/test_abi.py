@@ -34,7 +34,8 @@ def test_header_declares_the_boundary():
     assert _declared() == sorted(["fa_fwd", "fa_quantize_fp8", "fa_fwd_fp8", "fa_strerror",
                                   "fa_last_device_status", "fa_debug_inject_stall", "fa_version",
                                   "fa_decode", "fa_decode_workspace_size", "fa_decode_noalloc",
-                                  "fa_bwd", "fa_bwd_workspace_size", "fa_quantize_fp8_ex"])
+                                  "fa_bwd", "fa_bwd_workspace_size", "fa_quantize_fp8_ex",
+                                  "fa_fwd_host", "fa_fwd_host_workspace_size"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -122,3 +123,17 @@ def test_quantize_ex_rejects_bad_options_on_the_host(lib):
     assert call(d=64, hi=1) == fa.FA_ERR_UNSUPPORTED           # sign bit past d
     assert call(ph=2) == fa.FA_ERR_UNSUPPORTED
     assert call(d=96) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_fwd_host_rejects_bad_arguments_on_the_host(lib):
+    n = ctypes.c_ulonglong(0)
+    assert lib.fa_fwd_host_workspace_size(2, 3, 100, 64, ctypes.byref(n)) == fa.FA_OK
+    assert n.value == 4 * ((2 * 2 * 3 * 100 * 64 + 255) // 256 * 256) + (4 * 2 * 3 * 100 + 255) // 256 * 256
+    ws = 0x100000
+    call = lambda wsp=ws, wsb=1 << 30, chunks=0, dtype=1, d=64: lib.fa_fwd_host(
+        A, A, A, A, None, 2, 3, 100, d, 0.125, 0, dtype, chunks, wsp, wsb, None)
+    assert call(wsb=1024) == fa.FA_ERR_WORKSPACE
+    assert call(wsp=ws + 64) == fa.FA_ERR_ALIGN
+    assert call(chunks=-1) == fa.FA_ERR_UNSUPPORTED
+    assert call(dtype=5) == fa.FA_ERR_UNSUPPORTED
+    assert call(d=80) == fa.FA_ERR_UNSUPPORTED

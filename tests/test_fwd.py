@@ -201,6 +201,19 @@ def test_host_buffers_end_to_end(gpu_lib):
     _assert_close(o.float().numpy(), lse.numpy(), ro, rl, "host buffers")
 
 
+@pytest.mark.parametrize("chunks", [0, 1, 3, 64])
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_pipeline_matches_device_call_bitwise(gpu_lib, chunks, pinned):
+    # chunking over heads changes no arithmetic: every head is computed the same way
+    q, k, v = make_qkv((3, 5, 333, 64), torch.float16, 14)
+    if pinned:
+        q, k, v = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    o, lse = gpu_lib.attention_host(q, k, v, causal=True, chunks=chunks)
+    od, ld = gpu_lib.attention(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o, od.cpu()) and torch.equal(lse, ld.cpu())
+
+
 def test_device_rejections(gpu_lib):
     q = torch.zeros((1, 1, 64, 96), device="cuda", dtype=torch.bfloat16)
     with pytest.raises(gpu_lib.FAError) as e:

@@ -73,6 +73,8 @@ _SIGNATURES = {
     "fa_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _vp]),
     "fa_bwd": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _i, _vp, ctypes.c_ulonglong, _vp]),
     "fa_bwd_workspace_size": (_i, [_i, _i, _i, _i, ctypes.POINTER(ctypes.c_ulonglong)]),
+    "fa_fwd_host": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _i, _vp, ctypes.c_ulonglong, _vp]),
+    "fa_fwd_host_workspace_size": (_i, [_i, _i, _i, _i, ctypes.POINTER(ctypes.c_ulonglong)]),
     "fa_strerror": (ctypes.c_char_p, [_i]),
     "fa_last_device_status": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),
     "fa_debug_inject_stall": (_i, [_i, _i]),
@@ -171,25 +173,46 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = 
     return out, lse
 
 
+_HOST_WS = {}
+
+
 def attention_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
                    scale: Optional[float] = None, device: Optional[torch.device] = None,
-                   stream: Optional[torch.cuda.Stream] = None):
-    """End-to-end call on HOST tensors (pinned for best speed): copy Q, K, V to the
-    GPU, run ``fa_fwd``, copy O and LSE back.  Returns host tensors."""
+                   stream: Optional[torch.cuda.Stream] = None, out: Optional[torch.Tensor] = None,
+                   lse_out: Optional[torch.Tensor] = None, chunks: int = 0):
+    """End-to-end call on HOST tensors through ``fa_fwd_host``: the library copies Q, K,
+    V to the GPU, computes and copies O and LSE back, overlapping the copies of one chunk
+    of heads with the computation of another.  Pinned host tensors let the copies run
+    asynchronously.  Returns host tensors (``out``/``lse_out`` if given)."""
+    lib = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.is_cuda or t.dim() != 4 or t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous host tensor shaped and typed like q")
+    if q.dtype not in _DTYPES:
+        raise ValueError(f"dtype must be float16 or bfloat16, got {q.dtype}")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
     dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    pin = q.is_pinned()
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=pin)
+    if lse_out is None:
+        lse_out = torch.empty((B, H, N), dtype=torch.float32, pin_memory=pin)
+    need = ctypes.c_ulonglong(0)
+    _check(lib.fa_fwd_host_workspace_size(B, H, N, d, ctypes.byref(need)), "fa_fwd_host_workspace_size")
+    ws = _HOST_WS.get(dev)
+    if ws is None or ws.numel() < need.value:
+        ws = torch.empty(need.value, device=dev, dtype=torch.uint8)
+        _HOST_WS[dev] = ws
     s = stream if stream is not None else torch.cuda.current_stream(dev)
-    with torch.cuda.stream(s):
-        qd = q.to(dev, non_blocking=True)
-        kd = k.to(dev, non_blocking=True)
-        vd = v.to(dev, non_blocking=True)
-        o, lse = attention(qd, kd, vd, causal=causal, scale=scale, stream=s)
-        pin = q.is_pinned()
-        oh = torch.empty(o.shape, dtype=o.dtype, pin_memory=pin)
-        lh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=pin)
-        oh.copy_(o, non_blocking=True)
-        lh.copy_(lse, non_blocking=True)
+    with torch.cuda.device(dev):
+        st = lib.fa_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse_out), B, H, N, d, float(scale),
+                             int(bool(causal)), _DTYPES[q.dtype], int(chunks), _ptr(ws), ws.numel(),
+                             s.cuda_stream)
+    _check(st, "fa_fwd_host")
     s.synchronize()
-    return oh, lh
+    return out, lse_out
 
 
 def quantize_fp8(x: torch.Tensor, hadamard: bool = False, transpose_out: bool = False,

@@ -19,7 +19,8 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libfa.so")
 SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd_fp8.cu", "fa_quant.cu", "fa_decode.cu",
-           "fa_decode_noalloc.cu", "fa_bwd.cu"]
+           "fa_decode_noalloc.cu", "fa_bwd.cu",
+           "fa_host.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
           "-I" + os.path.join(ROOT, "include")]
