@@ -470,6 +470,16 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, int t, uint32_t 
       for (int i = lane; i < p.n_sblk; i += 32) mx = fmaxf(mx, __ldg(vs + i));
       sv_max = warp_max(mx);
     }
+    // E4M3: the K and V scales of the tile about to be processed, loaded one tile
+    // ahead so that their latency stays off the softmax's critical path
+    const float inv_sv_max = 1.f / sv_max;
+    float nk0 = 1.f, nk1 = 1.f, nv0 = 1.f, nv1 = 1.f;
+    if constexpr (L::kFp8) {
+      nk0 = __ldg(ks);
+      nk1 = __ldg(ks + min(1, p.n_sblk - 1));
+      nv0 = __ldg(vs);
+      nv1 = __ldg(vs + min(1, p.n_sblk - 1));
+    }
 
     for (int j = 0; j < ntile; ++j) {
       const bool got = ptx::mbar_wait(bar(L::kSFull + t), s_uses & 1u, ctl, kStatusSoftmaxTimeout);
@@ -485,11 +495,15 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, int t, uint32_t 
       // per-half factors (E4M3: one K and one V scale per 64 keys)
       float f0 = sl2, f1 = sl2, b0 = 0.f, b1 = 0.f;
       if constexpr (L::kFp8) {
-        const int kb0 = min(2 * j, p.n_sblk - 1), kb1 = min(2 * j + 1, p.n_sblk - 1);
-        f0 = c_row * __ldg(ks + kb0);
-        f1 = c_row * __ldg(ks + kb1);
-        b0 = ptx::lg2(__ldg(vs + kb0) / sv_max);      // log2 of V's relative block scale (<= 0)
-        b1 = ptx::lg2(__ldg(vs + kb1) / sv_max);
+        f0 = c_row * nk0;
+        f1 = c_row * nk1;
+        b0 = ptx::lg2(nv0 * inv_sv_max);              // log2 of V's relative block scale (<= 0)
+        b1 = ptx::lg2(nv1 * inv_sv_max);
+        const int kb0 = min(2 * j + 2, p.n_sblk - 1), kb1 = min(2 * j + 3, p.n_sblk - 1);
+        nk0 = __ldg(ks + kb0);
+        nk1 = __ldg(ks + kb1);
+        nv0 = __ldg(vs + kb0);
+        nv1 = __ldg(vs + kb1);
       }
       ptx::tmem_wait_ld();
 
