@@ -271,17 +271,23 @@ __device__ __forceinline__ void dq_compute(const BwdParams& p, uint32_t sbase, u
       const int col0 = j * 128;
       // keys past N, and (causal) past this row, get P = 0
       const int visible = min(p.N, p.causal ? row + 1 : p.N) - col0;
+      // chunk c+1's TMEM loads fly while chunk c is computed
+      uint32_t sr[2][32], dr[2][32];
+      ptx::tmem_ld32(tS, sr[0]);
+      ptx::tmem_ld32(tDP, dr[0]);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t sr[32], dr[32];
-        ptx::tmem_ld32(tS + 32 * c, sr);
-        ptx::tmem_ld32(tDP + 32 * c, dr);
         ptx::tmem_wait_ld();
+        if (c + 1 < 4) {
+          ptx::tmem_ld32(tS + 32 * (c + 1), sr[(c + 1) & 1]);
+          ptx::tmem_ld32(tDP + 32 * (c + 1), dr[(c + 1) & 1]);
+        }
         float ds[32];
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
-          const float pv = (32 * c + x < visible) ? ptx::ex2(fmaf(__uint_as_float(sr[x]), p.scale_log2, -lse2)) : 0.f;
-          ds[x] = pv * (__uint_as_float(dr[x]) - dlt);
+          const float pv = (32 * c + x < visible)
+                               ? ptx::ex2(fmaf(__uint_as_float(sr[c & 1][x]), p.scale_log2, -lse2)) : 0.f;
+          ds[x] = pv * (__uint_as_float(dr[c & 1][x]) - dlt);
         }
         uint32_t w[16];
         pack16<kBf16>(ds, w);
@@ -408,18 +414,23 @@ __device__ __forceinline__ void dkdv_compute(const BwdParams& p, uint32_t sbase,
       // causal diagonal tile: query i*128 + c sees this key iff c >= kr (padded queries
       // have LSE*log2(e) = +inf and so P = 0 already)
       const int first = (p.causal && i == j) ? kr : 0;
+      // chunk c+1's TMEM loads fly while chunk c is computed
+      uint32_t sr[2][32], dr[2][32];
+      ptx::tmem_ld32(tS, sr[0]);
+      ptx::tmem_ld32(tDP, dr[0]);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t sr[32], dr[32];
-        ptx::tmem_ld32(tS + 32 * c, sr);
-        ptx::tmem_ld32(tDP + 32 * c, dr);
         ptx::tmem_wait_ld();
+        if (c + 1 < 4) {
+          ptx::tmem_ld32(tS + 32 * (c + 1), sr[(c + 1) & 1]);
+          ptx::tmem_ld32(tDP + 32 * (c + 1), dr[(c + 1) & 1]);
+        }
         float pv[32], ds[32];
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
           const int q = 32 * c + x;
-          pv[x] = q >= first ? ptx::ex2(fmaf(__uint_as_float(sr[x]), p.scale_log2, -lse2[q])) : 0.f;
-          ds[x] = pv[x] * (__uint_as_float(dr[x]) - dlt[q]);
+          pv[x] = q >= first ? ptx::ex2(fmaf(__uint_as_float(sr[c & 1][x]), p.scale_log2, -lse2[q])) : 0.f;
+          ds[x] = pv[x] * (__uint_as_float(dr[c & 1][x]) - dlt[q]);
         }
         uint32_t wp[16], wd[16];
         pack16<kBf16>(pv, wp);
