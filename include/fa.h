@@ -142,7 +142,8 @@ int fa_fwd_fp8(const void* q8, const void* k8, const void* v8t, void* o, float* 
  *   k, v       : [B, H, N_k, d] of `dtype`
  *   o, lse     : [B, H, N_q, d] of `dtype` and [B, H, N_q] float32 (lse may be NULL)
  *   num_splits : key chunks per head processed in parallel and merged by log-sum-exp;
- *                0 picks a count from the SM count and N_k
+ *                0 picks the count that best fills whole waves of CTAs on this GPU
+ *                (chunks of at least 256 keys, at most 4 MiB of scratch)
  *   workspace  : device scratch of at least fa_decode_workspace_size() bytes, 256-byte
  *                aligned, owned by the caller; may be NULL when that size is 0.  Its
  *                contents on entry do not matter; calls sharing one workspace must not
@@ -197,9 +198,9 @@ int fa_bwd_workspace_size(int B, int H, int N, int d, unsigned long long* bytes)
  * memory inside this library (one per device, reserved when the library's device
  * code is loaded there).  The call allocates nothing: no cudaMalloc, no pool, no
  * allocating library routine.
- *   - Limit: with num_splits = 0 the scratch fa_decode needs is at most 5,003,136
- *     bytes (under 4.8 MiB) for every supported shape on a GB300 (152 SMs), so
- *     only an explicit large num_splits can exceed the area.  When fa_decode_workspace_size reports more
+ *   - Limit: with num_splits = 0 fa_decode never picks a split count that needs
+ *     more than 4 MiB of scratch, so only an explicit large num_splits can exceed
+ *     the area.  When fa_decode_workspace_size reports more
  *     than FA_DECODE_NOALLOC_SCRATCH_BYTES for these sizes, the call returns
  *     FA_ERR_WORKSPACE and launches nothing; use a smaller num_splits, or
  *     fa_decode with a workspace of your own.

@@ -276,26 +276,53 @@ namespace {
 
 constexpr int kDecodeMaxQ = 16;
 
-// Key chunks per head: enough CTAs for about two per SM, at least 256 keys each.
-void decode_split(int BH, int Nk, int requested, int sm_count, int* splits, int* chunk) {
-  int s = requested;
-  if (s <= 0) {
-    s = (2 * sm_count + BH - 1) / BH;
-    const int by_len = (Nk + 255) / 256;
-    if (s > by_len) s = by_len;
-  }
-  if (s < 1) s = 1;
-  int c = (Nk + s - 1) / s;
-  c = (c + 63) / 64 * 64;
-  *chunk = c;
-  *splits = (Nk + c - 1) / c;
-}
-
 unsigned long long decode_workspace(int BH, int Nq, int d, int splits) {
   if (splits <= 1) return 0;
   const unsigned long long o = static_cast<unsigned long long>(BH) * splits * Nq * d * 4;
   const unsigned long long l = static_cast<unsigned long long>(BH) * splits * Nq * 4;
   return (o + 255) / 256 * 256 + l;
+}
+
+// Key chunks per head.  One split CTA fills an SM at d = 128 and half of one at d = 64
+// (shared memory), so B*H*splits CTAs run in waves of `slots`.  With splits = 0 the
+// count minimises  waves * (64-key tiles per chunk + 4 tiles of per-CTA overhead),
+// taking the fewest splits within 2 % of the best, with chunks of at least 256 keys
+// and at most 4 MiB of split scratch (so that every automatic choice also fits the
+// static area of fa_decode_noalloc).
+constexpr unsigned long long kAutoSplitScratch = 4ull << 20;
+
+void decode_split(int BH, int Nq, int Nk, int d, int requested, int sm_count, int* splits, int* chunk) {
+  auto shape = [&](int s, int* c_out) {
+    int c = (Nk + s - 1) / s;
+    c = (c + 63) / 64 * 64;
+    *c_out = c;
+    return (Nk + c - 1) / c;
+  };
+  if (requested > 0) {
+    *splits = shape(requested, chunk);
+    return;
+  }
+  const long long slots = static_cast<long long>(sm_count) * (d == 64 ? 2 : 1);
+  int s_max = Nk / 256;
+  if (s_max > 128) s_max = 128;
+  if (s_max < 1) s_max = 1;
+  long long cost[129];
+  long long best = -1;
+  for (int s = 1; s <= s_max; ++s) {
+    int c;
+    const int sp = shape(s, &c);
+    cost[s] = -1;
+    if (sp > 1 && decode_workspace(BH, Nq, d, sp) > kAutoSplitScratch) continue;
+    cost[s] = ((static_cast<long long>(BH) * sp + slots - 1) / slots) * (c / 64 + 4);
+    if (best < 0 || cost[s] < best) best = cost[s];
+  }
+  for (int s = 1; s <= s_max; ++s) {
+    if (cost[s] >= 0 && cost[s] * 50 <= best * 51) {
+      *splits = shape(s, chunk);
+      return;
+    }
+  }
+  *splits = shape(1, chunk);
 }
 
 int check_decode(int B, int H, int Nq, int Nk, int d) {
@@ -318,7 +345,7 @@ extern "C" int fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d, int
   const DeviceInfo* di = current_device(&st);
   if (!di) return st;
   int splits, chunk;
-  decode_split(B * H, Nk, num_splits, di->sm_count, &splits, &chunk);
+  decode_split(B * H, Nq, Nk, d, num_splits, di->sm_count, &splits, &chunk);
   *bytes = decode_workspace(B * H, Nq, d, splits);
   return FA_OK;
 }
@@ -343,7 +370,7 @@ extern "C" int fa_decode(const void* q, const void* k, const void* v, void* o, f
   if (!encode_3d(&p.tm_k, dt, 2, k, d, Nk, static_cast<uint64_t>(B) * H, 64, 64) ||
       !encode_3d(&p.tm_v, dt, 2, v, d, Nk, static_cast<uint64_t>(B) * H, 64, 64))
     return FA_ERR_CUDA;
-  decode_split(B * H, Nk, num_splits, di->sm_count, &p.splits, &p.chunk);
+  decode_split(B * H, Nq, Nk, d, num_splits, di->sm_count, &p.splits, &p.chunk);
   const unsigned long long need = decode_workspace(B * H, Nq, d, p.splits);
   if (need > 0 && (!workspace || workspace_bytes < need)) return FA_ERR_WORKSPACE;
   p.q = q;
