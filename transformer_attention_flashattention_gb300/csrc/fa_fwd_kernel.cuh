@@ -173,18 +173,6 @@ __device__ __noinline__ void fwd_producer(const FwdParams& p, uint32_t sbase,
   for (int k = 0; unit_at(p, k, bh, qb); ++k) {
     const int n0 = tile_nkv(p, qb, 0), n1 = tile_nkv(p, qb, 1);
     const int n = max(n0, n1);
-#pragma unroll
-    for (int t = 0; t < kQTiles; ++t) {
-      if ((t == 0 ? n0 : n1) == 0) continue;
-      if (!ptx::mbar_wait(bar(L::kQEmpty + t), (q_fills[t] & 1u) ^ 1u, ctl, kStatusLoadTimeout))
-        goto drain;
-      ptx::mbar_arrive_expect_tx(bar(L::kQFull + t), L::kTileBytes);
-#pragma unroll
-      for (int a = 0; a < L::kAtoms; ++a)
-        ptx::tma_load_3d(sbase + L::kQOff + t * L::kTileBytes + a * L::kAtomBytes, &p.tm_q,
-                         bar(L::kQFull + t), a * L::kAtomElems, qb * kUnitRows + t * kBlockM, bh);
-      ++q_fills[t];
-    }
     {
       // Q is read once, so its next load comes from HBM; start that unit's Q on its
       // way into L2 now, a whole unit ahead of the load
@@ -240,6 +228,23 @@ __device__ __noinline__ void fwd_producer(const FwdParams& p, uint32_t sbase,
       }
       if (!skip) armed |= bit;
       load_idx += cnt;
+      if (j == 0) {
+        // The unit's Q tiles go out after its K_0: the MMA thread issues this unit's
+        // S_t(0) at the end of the previous unit, tile 0's possibly a step before
+        // tile 1's last S frees Q buffer 1, so K_0 must not queue behind that wait.
+#pragma unroll
+        for (int t = 0; t < kQTiles; ++t) {
+          if ((t == 0 ? n0 : n1) == 0) continue;
+          if (!ptx::mbar_wait(bar(L::kQEmpty + t), (q_fills[t] & 1u) ^ 1u, ctl, kStatusLoadTimeout))
+            goto drain;
+          ptx::mbar_arrive_expect_tx(bar(L::kQFull + t), L::kTileBytes);
+#pragma unroll
+          for (int a = 0; a < L::kAtoms; ++a)
+            ptx::tma_load_3d(sbase + L::kQOff + t * L::kTileBytes + a * L::kAtomBytes, &p.tm_q,
+                             bar(L::kQFull + t), a * L::kAtomElems, qb * kUnitRows + t * kBlockM, bh);
+          ++q_fills[t];
+        }
+      }
     }
   }
 drain:
@@ -337,12 +342,13 @@ __device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_
     // steps 2 .. steady_end - 1: both tiles run PV(j-1) and S(j), none of them is a
     // tile's last PV or last S, and V_{j-1} sits right after K_j in the ring
     const int steady_end = min(nt[0], nt[1]) - 1;
-    // The next unit's step 0 (S_t = Q_t K_0^T) is issued inside this unit's last step,
-    // right after tile t's last PV, so each softmax group finds its next S as soon as
-    // its epilogue ends instead of after both tiles' last PVs.
+    // The next unit's step 0 (S_t = Q_t K_0^T) is issued inside this unit, right after
+    // tile t's last PV (in the last step for a tile with no PV), so each softmax group
+    // finds its next S as soon as its epilogue ends.
     int bhn = 0, qbn = 0;
     const bool has_next = unit_at(p, k + 1, bhn, qbn);
     const int ntn[kQTiles] = {has_next ? tile_nkv(p, qbn, 0) : 0, has_next ? tile_nkv(p, qbn, 1) : 0};
+    bool next_ready = false;
     for (int j = j0; j <= n; ++j, ++step) {
       if (j == 2 && steady_end > 2) {
         uint32_t ks = (load_idx + 2u * j - 1u) % L::kStages;     // ring slot of K_j
@@ -370,15 +376,13 @@ __device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_
         p_uses[0] += steady_end - 2;
         p_uses[1] += steady_end - 2;
       }
-      // every load of this step (and of the next unit's step 0, when fused) has landed
-      const bool fuse = j == n && has_next;
+      // every load of this step has landed
       if (!ptx::mbar_wait(ready0 + 8u * (step % L::kSteps), (step / L::kSteps) & 1u, ctl, kStatusMmaTimeout))
         goto done;
-      if (fuse && !ptx::mbar_wait(ready0 + 8u * ((step + 1) % L::kSteps), ((step + 1) / L::kSteps) & 1u, ctl,
-                                  kStatusMmaTimeout))
-        goto done;
       const uint32_t vslot = j >= 1 ? (load_idx + v_pos(j - 1, n)) % L::kStages : 0u;
-      const uint32_t kslot = j < n ? (load_idx + k_pos(j)) % L::kStages : (load_idx + 2u * n) % L::kStages;
+      const uint32_t kslot = j < n ? (load_idx + k_pos(j)) % L::kStages : 0u;
+      const uint32_t next0 = step - j + n + 1;                        // the next unit's step 0
+      const uint32_t kslot_next = (load_idx + 2u * n) % L::kStages;   // and its K_0
 #pragma unroll
       for (int t = 0; t < kQTiles; ++t) {
         const uint32_t tS = t ? tS1 : tS0;
@@ -401,17 +405,25 @@ __device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_
           issue_s<D, E>(tS, t == 0 ? q_lo0 : q_lo1, k_lo0 + kslot * kSlotDesc);
           ptx::mma_commit(bar(L::kSFull + t));
           if (j == nt[t] - 1) ptx::mma_commit(bar(L::kQEmpty + t));
-        } else if (fuse && ntn[t] > 0) {
-          // the next unit's S_t = Q_t K_0^T (kslot holds its K_0)
+        }
+        if (has_next && ntn[t] > 0 && j == (nt[t] > 0 ? nt[t] : n)) {
+          // the next unit's S_t = Q_t K_0^T, right after this tile's last P.V (its O is
+          // then ready for the epilogue before anything waits on the next unit's loads)
+          if (!next_ready) {
+            if (!ptx::mbar_wait(ready0 + 8u * (next0 % L::kSteps), (next0 / L::kSteps) & 1u, ctl,
+                                kStatusMmaTimeout))
+              goto done;
+            next_ready = true;
+          }
           if (!ptx::mbar_wait(bar(L::kQFull + t), q_uses[t] & 1u, ctl, kStatusMmaTimeout)) goto done;
           ++q_uses[t];
-          issue_s<D, E>(tS, t == 0 ? q_lo0 : q_lo1, k_lo0 + kslot * kSlotDesc);
+          issue_s<D, E>(tS, t == 0 ? q_lo0 : q_lo1, k_lo0 + kslot_next * kSlotDesc);
           ptx::mma_commit(bar(L::kSFull + t));
           if (ntn[t] == 1) ptx::mma_commit(bar(L::kQEmpty + t));
         }
       }
       ptx::mma_commit(done0 + 8u * (step % L::kSteps));
-      if (fuse) ptx::mma_commit(done0 + 8u * ((step + 1) % L::kSteps));
+      if (j == n && has_next) ptx::mma_commit(done0 + 8u * (next0 % L::kSteps));
     }
     load_idx += 2u * n;
     // the next unit's step 0 has been issued: it starts at step 1
