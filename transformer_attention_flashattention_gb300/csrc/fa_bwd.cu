@@ -62,26 +62,41 @@ struct BwdCfg {
   static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
-// Unit u of the dq kernel: (b*h, Q tile i).  Causal costs grow with i, so the last
-// tiles of every head go first.
-__device__ __forceinline__ void dq_unit(const BwdParams& p, int u, int& bh, int& i) {
-  if (p.causal) {
-    i = p.n_blk - 1 - u / p.BH;
-    bh = u % p.BH;
-  } else {
+// The k-th unit of this CTA of the persistent grid, (b*h, tile blk); false once it
+// has none left.  The dq kernel's units are Q tiles, the dkdv kernel's K/V tiles.
+//  - Non-causal: head-major, dealt round-robin, so concurrent CTAs share a few heads
+//    and the streamed tiles hit L2.
+//  - Causal: a unit's cost grows with its Q tile (dq: tile i sees i + 1 key tiles) or
+//    shrinks with its K/V tile (dkdv: tile j is seen by n - j Q tiles), so tiles b and
+//    n-1-b of one head form a pair of equal cost.  A CTA takes whole pairs, longer half
+//    first, in head-major order; the middle tile of an odd count comes after the pairs.
+__device__ __forceinline__ bool bwd_unit_at(const BwdParams& p, int k, bool cost_grows, int& bh, int& blk) {
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  if (!p.causal) {
+    const int u = c + k * G;
+    if (u >= p.num_units) return false;
     bh = u / p.n_blk;
-    i = u % p.n_blk;
+    blk = u % p.n_blk;
+    return true;
   }
-}
-// Unit u of the dkdv kernel: (b*h, K/V tile j).  Causal costs shrink with j.
-__device__ __forceinline__ void dkdv_unit(const BwdParams& p, int u, int& bh, int& j) {
-  if (p.causal) {
-    j = u / p.BH;
-    bh = u % p.BH;
-  } else {
-    bh = u / p.n_blk;
-    j = u % p.n_blk;
+  const int P = p.n_blk / 2;
+  const int pairs = p.BH * P;
+  const int mine = c < pairs ? (pairs - c + G - 1) / G : 0;
+  if (k < 2 * mine) {
+    const int s = c + (k >> 1) * G;
+    bh = s / P;
+    const int i = s % P;
+    const int lo = i, hi = p.n_blk - 1 - i;
+    const int longer = cost_grows ? hi : lo, shorter = cost_grows ? lo : hi;
+    blk = (k & 1) ? shorter : longer;
+    return true;
   }
+  if ((p.n_blk & 1) == 0) return false;
+  const int r = c + (mine + (k - 2 * mine)) * G - pairs;
+  if (r >= p.BH) return false;
+  bh = r;
+  blk = P;
+  return true;
 }
 
 // ---------------------------------------------------------------------------- prep
@@ -185,9 +200,8 @@ __device__ __noinline__ void dq_producer(const BwdParams& p, uint32_t sbase, con
   auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
   uint32_t tile = 0, units = 0;
   uint32_t last_fill[kBwdStages] = {0xFFFFFFFFu, 0xFFFFFFFFu};
-  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-    int bh, i;
-    dq_unit(p, u, bh, i);
+  int bh, i;
+  for (int k = 0; bwd_unit_at(p, k, true, bh, i); ++k) {
     const int n = p.causal ? i + 1 : p.n_blk;
     if (!ptx::mbar_wait(bar(C::kStEmpty), (units & 1u) ^ 1u, ctl, 1u)) goto drain;
     ptx::mbar_arrive_expect_tx(bar(C::kStFull), 2 * C::kTile);
@@ -220,9 +234,8 @@ __device__ __noinline__ void dq_mma(const BwdParams& p, uint32_t sbase, uint32_t
   const uint32_t kmn_lo0 = ptx::sdesc_lo(sbase + C::kRingOff, v_lbo<D, E>());    // K as MN-major B of dQ
   const uint32_t tS = tmem + kTmS, tDP = tmem + kTmDP, tAcc = tmem + kTmAcc;
   uint32_t tile = 0, units = 0;
-  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-    int bh, i;
-    dq_unit(p, u, bh, i);
+  int bh, i;
+  for (int k = 0; bwd_unit_at(p, k, true, bh, i); ++k) {
     const int n = p.causal ? i + 1 : p.n_blk;
     if (!ptx::mbar_wait(bar(C::kStFull), units & 1u, ctl, 2u)) goto done;
     for (int j = 0; j < n; ++j, ++tile) {
@@ -257,9 +270,8 @@ __device__ __forceinline__ void dq_compute(const BwdParams& p, uint32_t sbase, u
   const uint32_t tS = tmem + lane_base + kTmS, tDP = tmem + lane_base + kTmDP, tAcc = tmem + lane_base + kTmAcc;
   const int lane = threadIdx.x & 31;
   uint32_t tile = 0, units = 0;
-  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-    int bh, i;
-    dq_unit(p, u, bh, i);
+  int bh, i;
+  for (int k = 0; bwd_unit_at(p, k, true, bh, i); ++k) {
     const int n = p.causal ? i + 1 : p.n_blk;
     const int row = i * 128 + r;
     const size_t wrow = static_cast<size_t>(bh) * p.n_pad + row;
@@ -317,9 +329,8 @@ __device__ __noinline__ void dkdv_producer(const BwdParams& p, uint32_t sbase, c
   auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
   uint32_t tile = 0, units = 0;
   uint32_t last_fill[kBwdStages] = {0xFFFFFFFFu, 0xFFFFFFFFu};
-  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-    int bh, j;
-    dkdv_unit(p, u, bh, j);
+  int bh, j;
+  for (int k = 0; bwd_unit_at(p, k, false, bh, j); ++k) {
     const int i0 = p.causal ? j : 0;
     if (!ptx::mbar_wait(bar(C::kStEmpty), (units & 1u) ^ 1u, ctl, 1u)) goto drain;
     ptx::mbar_arrive_expect_tx(bar(C::kStFull), 2 * C::kTile);
@@ -356,9 +367,8 @@ __device__ __noinline__ void dkdv_mma(const BwdParams& p, uint32_t sbase, uint32
   const uint32_t domn_lo0 = ptx::sdesc_lo(sbase + C::kRingOff + C::kTile, v_lbo<D, E>());  // dO, of dV
   const uint32_t tS = tmem + kTmS, tDP = tmem + kTmDP, tDV = tmem + kTmAcc, tDK = tmem + kTmAcc + D;
   uint32_t tile = 0, units = 0;
-  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-    int bh, j;
-    dkdv_unit(p, u, bh, j);
+  int bh, j;
+  for (int k = 0; bwd_unit_at(p, k, false, bh, j); ++k) {
     const int i0 = p.causal ? j : 0;
     if (!ptx::mbar_wait(bar(C::kStFull), units & 1u, ctl, 2u)) goto done;
     for (int i = i0; i < p.n_blk; ++i, ++tile) {
@@ -399,9 +409,8 @@ __device__ __forceinline__ void dkdv_compute(const BwdParams& p, uint32_t sbase,
   const uint32_t tDV = tmem + lane_base + kTmAcc, tDK = tDV + D;
   const int lane = threadIdx.x & 31;
   uint32_t tile = 0, units = 0;
-  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-    int bh, j;
-    dkdv_unit(p, u, bh, j);
+  int bh, j;
+  for (int k = 0; bwd_unit_at(p, k, false, bh, j); ++k) {
     const int i0 = p.causal ? j : 0;
     const int key = j * 128 + kr;
     for (int i = i0; i < p.n_blk; ++i, ++tile) {
