@@ -385,7 +385,7 @@ def run_gpu(args):
     if dec:
         roof = {"bound": "hbm", "achieved": dec_gbs, "peak": peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]),
                 "unit": "GB/s", "frac": dec_gbs / peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]),
-                "traffic": None, "peak_source": f"{peak_src} HBM copy bandwidth",
+                "traffic": traffic, "peak_source": f"{peak_src} HBM copy bandwidth",
                 "kernel": "fa_decode_split_kernel + fa_decode_merge_kernel", "bytes_per_step": dec_bytes}
     else:
         roof = {"bound": "tensor", "achieved": kern_tflops, "peak": peak, "unit": "TFLOP/s",
