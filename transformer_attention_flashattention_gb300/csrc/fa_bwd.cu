@@ -21,11 +21,15 @@
 //          dV += P^T dO and dK += dS^T Q (both TS MMAs)
 // S and dP are computed twice (once per kernel) in exchange for no dQ reduction.
 //
-// Each main kernel is a persistent grid with four roles:
-//   warps 0-3  compute: thread i owns TMEM lane i (a Q row, or a key row)
-//   warp 4     TMA producer: the unit's two stationary tiles, then a 2-stage ring
-//   warp 5     MMA issuer (one thread) and TMEM owner
+// Each main kernel is a persistent grid with these roles (320 threads):
+//   warps 0-7  compute: warp w takes TMEM lanes 32*(w%4).. (Q rows, or key rows) and
+//              column half w/4, so every row is shared by two threads
+//   warp 8     TMA producer: the unit's two stationary tiles, then a 2-stage ring
+//   warp 9     MMA issuer (one thread) and TMEM owner
 // TMEM (512 columns): S (or S^T) | dP (or dP^T) | accumulator 0 | accumulator 1.
+// A half-row thread packs its 16-bit results over the first 32 columns of its own half
+// of a region (never over the other half, which the other thread may still be
+// reading), so the TS MMAs read their A operand from columns 0..31 and 64..95.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -35,9 +39,10 @@
 namespace fa {
 namespace {
 
-constexpr int kBwdThreads = 192;
-constexpr int kBwdLoadWarp = 4;
-constexpr int kBwdMmaWarp = 5;
+constexpr int kBwdComputeWarps = 8;
+constexpr int kBwdThreads = kBwdComputeWarps * 32 + 64;
+constexpr int kBwdLoadWarp = 8;
+constexpr int kBwdMmaWarp = 9;
 constexpr int kBwdStages = 2;
 constexpr uint32_t kTmS = 0, kTmDP = 128, kTmAcc = 256;
 constexpr float kLog2e = 1.44269504088896340736f;
@@ -171,16 +176,17 @@ __device__ __forceinline__ void pack16(const float (&a)[32], uint32_t (&w)[16]) 
   for (int x = 0; x < 16; ++x) w[x] = ptx::pack2<BF16>(a[2 * x], a[2 * x + 1]);
 }
 
-// Writes one 128-row-tile row of D accumulator columns, times `mul`, as 16-bit values.
-template <int D, bool BF16>
-__device__ __forceinline__ void store_acc_row(uint32_t taddr, float mul, void* out, size_t row_off, bool live) {
-  uint32_t r[D / 32][32];
+// Writes COLS accumulator columns of one row, times `mul`, as 16-bit values at
+// element offset `off` of `out`.
+template <int COLS, bool BF16>
+__device__ __forceinline__ void store_acc_row(uint32_t taddr, float mul, void* out, size_t off, bool live) {
+  uint32_t r[COLS / 32][32];
 #pragma unroll
-  for (int c = 0; c < D / 32; ++c) ptx::tmem_ld32(taddr + 32 * c, r[c]);
+  for (int c = 0; c < COLS / 32; ++c) ptx::tmem_ld32(taddr + 32 * c, r[c]);
   ptx::tmem_wait_ld();
-  uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + row_off);
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + off);
 #pragma unroll
-  for (int c = 0; c < D / 32; ++c) {
+  for (int c = 0; c < COLS / 32; ++c) {
     uint32_t pk[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i)
@@ -189,6 +195,23 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, float mul, void* o
 #pragma unroll
       for (int i = 0; i < 4; ++i) dst[c * 4 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
     }
+  }
+}
+
+// The 8 TS MMAs of one 128-key (or 128-query) reduction whose A operand was packed by
+// the two half-row threads: steps 0-3 at TMEM columns 0..31, steps 4-7 at 64..95.
+template <int D, Elem E, bool ACC, int KK = 0>
+__device__ __forceinline__ void issue_pv_halves(uint32_t tO, uint32_t tA, uint32_t b_lo) {
+  using L = FwdCfg<D, E>;
+  static_assert(!L::kFp8 && L::kPvSteps == 8, "16-bit operands, 16 keys per step");
+  if constexpr (KK < L::kPvSteps) {
+    constexpr uint32_t idesc = ptx::idesc_make(kBlockM, D, L::kAbType, false, true);
+    constexpr uint32_t desc_hi = ptx::sdesc_hi(1024);
+    constexpr int kAcc = (ACC || KK > 0) ? 1 : 0;
+    constexpr uint32_t kOt = KK < 4 ? KK * 8 : 64 + (KK - 4) * 8;
+    constexpr uint32_t kOb = (KK * 16 * 128) >> 4;
+    ptx::mma_f16_ts_o<kAcc, kOt, kOb>(tO, tA, b_lo, desc_hi, idesc);
+    issue_pv_halves<D, E, ACC, KK + 1>(tO, tA, b_lo);
   }
 }
 
@@ -246,8 +269,9 @@ __device__ __noinline__ void dq_mma(const BwdParams& p, uint32_t sbase, uint32_t
       ptx::mma_commit(bar(C::kSdpFull));
       if (!ptx::mbar_wait(bar(C::kDsFull), tile & 1u, ctl, 2u)) goto done;
       ptx::tc_fence_after();
-      if (j == 0) issue_pv<D, E, false>(tAcc, tS, kmn_lo0 + s * kStageDesc);   // dQ = dS K_j
-      else issue_pv<D, E, true>(tAcc, tS, kmn_lo0 + s * kStageDesc);          // dQ += dS K_j
+      // dS was packed over the dP region
+      if (j == 0) issue_pv_halves<D, E, false>(tAcc, tDP, kmn_lo0 + s * kStageDesc);   // dQ = dS K_j
+      else issue_pv_halves<D, E, true>(tAcc, tDP, kmn_lo0 + s * kStageDesc);          // dQ += dS K_j
       ptx::mma_commit(bar(C::kDone + s));
     }
     ptx::mma_commit(bar(C::kStEmpty));
@@ -265,10 +289,12 @@ __device__ __forceinline__ void dq_compute(const BwdParams& p, uint32_t sbase, u
   using C = BwdCfg<D>;
   constexpr bool kBf16 = E == Elem::BF16;
   auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
-  const int r = threadIdx.x;                                   // row in the Q tile = TMEM lane
-  const uint32_t lane_base = static_cast<uint32_t>((threadIdx.x / 32) * 32) << 16;
-  const uint32_t tS = tmem + lane_base + kTmS, tDP = tmem + lane_base + kTmDP, tAcc = tmem + lane_base + kTmAcc;
-  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+  const int r = (warp & 3) * 32 + lane;                        // row in the Q tile = TMEM lane
+  const int half = warp >> 2;                                  // key columns 64*half .. +63
+  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  const uint32_t tS = tmem + lane_base + kTmS + 64 * half, tDP = tmem + lane_base + kTmDP + 64 * half;
+  const uint32_t tAcc = tmem + lane_base + kTmAcc + (D / 2) * half;
   uint32_t tile = 0, units = 0;
   int bh, i;
   for (int k = 0; bwd_unit_at(p, k, true, bh, i); ++k) {
@@ -280,31 +306,28 @@ __device__ __forceinline__ void dq_compute(const BwdParams& p, uint32_t sbase, u
       const bool got = ptx::mbar_wait(bar(C::kSdpFull), tile & 1u, ctl, 4u);
       if (!__all_sync(0xFFFFFFFFu, got)) return;
       ptx::tc_fence_after();
-      const int col0 = j * 128;
-      // keys past N, and (causal) past this row, get P = 0
-      const int visible = min(p.N, p.causal ? row + 1 : p.N) - col0;
-      // chunk c+1's TMEM loads fly while chunk c is computed
+      // keys past N, and (causal) past this row, get P = 0 (counted from this half's first key)
+      const int visible = min(p.N, p.causal ? row + 1 : p.N) - (j * 128 + 64 * half);
       uint32_t sr[2][32], dr[2][32];
-      ptx::tmem_ld32(tS, sr[0]);
-      ptx::tmem_ld32(tDP, dr[0]);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        ptx::tmem_wait_ld();
-        if (c + 1 < 4) {
-          ptx::tmem_ld32(tS + 32 * (c + 1), sr[(c + 1) & 1]);
-          ptx::tmem_ld32(tDP + 32 * (c + 1), dr[(c + 1) & 1]);
-        }
+      for (int c = 0; c < 2; ++c) {
+        ptx::tmem_ld32(tS + 32 * c, sr[c]);
+        ptx::tmem_ld32(tDP + 32 * c, dr[c]);
+      }
+      ptx::tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
         float ds[32];
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
           const float pv = (32 * c + x < visible)
-                               ? ptx::ex2(fmaf(__uint_as_float(sr[c & 1][x]), p.scale_log2, -lse2)) : 0.f;
-          ds[x] = pv * (__uint_as_float(dr[c & 1][x]) - dlt);
+                               ? ptx::ex2(fmaf(__uint_as_float(sr[c][x]), p.scale_log2, -lse2)) : 0.f;
+          ds[x] = pv * (__uint_as_float(dr[c][x]) - dlt);
         }
         uint32_t w[16];
         pack16<kBf16>(ds, w);
-        // packed dS overwrites S columns 16c..16c+15, already read (chunks <= c)
-        ptx::tmem_st16(tS + 16 * c, w);
+        // packed dS goes over this half's first 32 dP columns, already read
+        ptx::tmem_st16(tDP + 16 * c, w);
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
@@ -315,8 +338,9 @@ __device__ __forceinline__ void dq_compute(const BwdParams& p, uint32_t sbase, u
     if (!__all_sync(0xFFFFFFFFu, got)) return;
     ++units;
     ptx::tc_fence_after();
-    store_acc_row<D, kBf16>(tAcc, p.scale, p.dq, (static_cast<size_t>(bh) * p.N + (row < p.N ? row : 0)) * D,
-                            row < p.N);
+    store_acc_row<D / 2, kBf16>(tAcc, p.scale, p.dq,
+                                (static_cast<size_t>(bh) * p.N + (row < p.N ? row : 0)) * D + (D / 2) * half,
+                                row < p.N);
     ptx::tc_fence_before();
   }
 }
@@ -380,11 +404,11 @@ __device__ __noinline__ void dkdv_mma(const BwdParams& p, uint32_t sbase, uint32
       if (!ptx::mbar_wait(bar(C::kDsFull), tile & 1u, ctl, 2u)) goto done;
       ptx::tc_fence_after();
       if (i == i0) {
-        issue_pv<D, E, false>(tDV, tS, domn_lo0 + s * kStageDesc);   // dV = P^T dO_i
-        issue_pv<D, E, false>(tDK, tDP, qmn_lo0 + s * kStageDesc);   // dK = dS^T Q_i
+        issue_pv_halves<D, E, false>(tDV, tS, domn_lo0 + s * kStageDesc);   // dV = P^T dO_i
+        issue_pv_halves<D, E, false>(tDK, tDP, qmn_lo0 + s * kStageDesc);   // dK = dS^T Q_i
       } else {
-        issue_pv<D, E, true>(tDV, tS, domn_lo0 + s * kStageDesc);
-        issue_pv<D, E, true>(tDK, tDP, qmn_lo0 + s * kStageDesc);
+        issue_pv_halves<D, E, true>(tDV, tS, domn_lo0 + s * kStageDesc);
+        issue_pv_halves<D, E, true>(tDK, tDP, qmn_lo0 + s * kStageDesc);
       }
       ptx::mma_commit(bar(C::kDone + s));
     }
@@ -403,11 +427,12 @@ __device__ __forceinline__ void dkdv_compute(const BwdParams& p, uint32_t sbase,
   using C = BwdCfg<D>;
   constexpr bool kBf16 = E == Elem::BF16;
   auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
-  const int kr = threadIdx.x;                                  // key row in the K/V tile = TMEM lane
-  const uint32_t lane_base = static_cast<uint32_t>((threadIdx.x / 32) * 32) << 16;
-  const uint32_t tS = tmem + lane_base + kTmS, tDP = tmem + lane_base + kTmDP;
-  const uint32_t tDV = tmem + lane_base + kTmAcc, tDK = tDV + D;
-  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+  const int kr = (warp & 3) * 32 + lane;                       // key row in the K/V tile = TMEM lane
+  const int half = warp >> 2;                                  // query columns 64*half .. +63
+  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  const uint32_t tS = tmem + lane_base + kTmS + 64 * half, tDP = tmem + lane_base + kTmDP + 64 * half;
+  const uint32_t tDV = tmem + lane_base + kTmAcc + (D / 2) * half, tDK = tmem + lane_base + kTmAcc + D + (D / 2) * half;
   uint32_t tile = 0, units = 0;
   int bh, j;
   for (int k = 0; bwd_unit_at(p, k, false, bh, j); ++k) {
@@ -418,33 +443,31 @@ __device__ __forceinline__ void dkdv_compute(const BwdParams& p, uint32_t sbase,
       if (!__all_sync(0xFFFFFFFFu, got)) return;
       ptx::tc_fence_after();
       const uint32_t s = tile % kBwdStages;
-      const float* lse2 = reinterpret_cast<const float*>(smem + C::kRingOff + s * C::kStageBytes + 2 * C::kTile);
+      const float* lse2 = reinterpret_cast<const float*>(smem + C::kRingOff + s * C::kStageBytes + 2 * C::kTile) +
+                          64 * half;
       const float* dlt = lse2 + 128;
-      // causal diagonal tile: query i*128 + c sees this key iff c >= kr (padded queries
-      // have LSE*log2(e) = +inf and so P = 0 already)
-      const int first = (p.causal && i == j) ? kr : 0;
-      // chunk c+1's TMEM loads fly while chunk c is computed
-      uint32_t sr[2][32], dr[2][32];
-      ptx::tmem_ld32(tS, sr[0]);
-      ptx::tmem_ld32(tDP, dr[0]);
+      // causal diagonal tile: query i*128 + 64*half + q sees this key iff 64*half + q >= kr
+      // (padded queries have LSE*log2(e) = +inf and so P = 0 already)
+      const int first = (p.causal && i == j) ? kr - 64 * half : 0;
+      // one 32-column chunk at a time: with 10 warps an SMSP holds 3, which caps a
+      // thread at 168 registers
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
+        uint32_t sr[32], dr[32];
+        ptx::tmem_ld32(tS + 32 * c, sr);
+        ptx::tmem_ld32(tDP + 32 * c, dr);
         ptx::tmem_wait_ld();
-        if (c + 1 < 4) {
-          ptx::tmem_ld32(tS + 32 * (c + 1), sr[(c + 1) & 1]);
-          ptx::tmem_ld32(tDP + 32 * (c + 1), dr[(c + 1) & 1]);
-        }
         float pv[32], ds[32];
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
           const int q = 32 * c + x;
-          pv[x] = q >= first ? ptx::ex2(fmaf(__uint_as_float(sr[c & 1][x]), p.scale_log2, -lse2[q])) : 0.f;
-          ds[x] = pv[x] * (__uint_as_float(dr[c & 1][x]) - dlt[q]);
+          pv[x] = q >= first ? ptx::ex2(fmaf(__uint_as_float(sr[x]), p.scale_log2, -lse2[q])) : 0.f;
+          ds[x] = pv[x] * (__uint_as_float(dr[x]) - dlt[q]);
         }
         uint32_t wp[16], wd[16];
         pack16<kBf16>(pv, wp);
         pack16<kBf16>(ds, wd);
-        // packed P^T / dS^T overwrite S^T / dP^T columns 16c..16c+15, already read
+        // packed P^T / dS^T go over this half's first 32 S^T / dP^T columns, already read
         ptx::tmem_st16(tS + 16 * c, wp);
         ptx::tmem_st16(tDP + 16 * c, wd);
       }
@@ -457,9 +480,9 @@ __device__ __forceinline__ void dkdv_compute(const BwdParams& p, uint32_t sbase,
     if (!__all_sync(0xFFFFFFFFu, got)) return;
     ++units;
     ptx::tc_fence_after();
-    const size_t off = (static_cast<size_t>(bh) * p.N + (key < p.N ? key : 0)) * D;
-    store_acc_row<D, kBf16>(tDV, 1.f, p.dv, off, key < p.N);
-    store_acc_row<D, kBf16>(tDK, p.scale, p.dk, off, key < p.N);
+    const size_t off = (static_cast<size_t>(bh) * p.N + (key < p.N ? key : 0)) * D + (D / 2) * half;
+    store_acc_row<D / 2, kBf16>(tDV, 1.f, p.dv, off, key < p.N);
+    store_acc_row<D / 2, kBf16>(tDK, p.scale, p.dk, off, key < p.N);
     ptx::tc_fence_before();
   }
 }
@@ -479,7 +502,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
   auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kNumBars; ++i) ptx::mbar_init(bar(i), i == C::kDsFull ? 4 : 1);
+    for (int i = 0; i < C::kNumBars; ++i) ptx::mbar_init(bar(i), i == C::kDsFull ? kBwdComputeWarps : 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
