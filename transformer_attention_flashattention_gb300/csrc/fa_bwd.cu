@@ -26,10 +26,13 @@
 //              column half w/4, so every row is shared by two threads
 //   warp 8     TMA producer: the unit's two stationary tiles, then a 2-stage ring
 //   warp 9     MMA issuer (one thread) and TMEM owner
-// TMEM (512 columns): S (or S^T) | dP (or dP^T) | accumulator 0 | accumulator 1.
-// A half-row thread packs its 16-bit results over the first 32 columns of its own half
-// of a region (never over the other half, which the other thread may still be
-// reading), so the TS MMAs read their A operand from columns 0..31 and 64..95.
+// Each 128-row streamed tile is processed as two 64-row halves a and b with their own
+// S and dP buffers, so the compute warps work on one half while the tensor pipe runs
+// the other half's (or the next tile's) MMAs.
+// TMEM (512 columns): S_a | dP_a | S_b | dP_b (64 columns each) | accumulator 0 | 1.
+// A compute thread handles 32 of a half's 64 columns and packs its 16-bit results over
+// the first 16 columns of its own 32 (never over the other thread's, which may still be
+// unread), so a half's TS MMAs read their A operand from columns {0, 8, 32, 40}.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -44,7 +47,7 @@ constexpr int kBwdThreads = kBwdComputeWarps * 32 + 64;
 constexpr int kBwdLoadWarp = 8;
 constexpr int kBwdMmaWarp = 9;
 constexpr int kBwdStages = 2;
-constexpr uint32_t kTmS = 0, kTmDP = 128, kTmAcc = 256;
+constexpr uint32_t kTmHalf = 128, kTmDP = 64, kTmAcc = 256;   // half h: S at 128h, dP at 128h + 64
 constexpr float kLog2e = 1.44269504088896340736f;
 
 template <int D>
@@ -59,7 +62,7 @@ struct BwdCfg {
   static constexpr int kBarOff = kRingOff + kBwdStages * kStageBytes;
   // barriers
   static constexpr int kStFull = 0, kStEmpty = 1, kReady = 2, kDone = kReady + kBwdStages;
-  static constexpr int kSdpFull = kDone + kBwdStages, kDsFull = kSdpFull + 1, kAccFull = kDsFull + 1;
+  static constexpr int kSdpFull = kDone + kBwdStages, kDsFull = kSdpFull + 2, kAccFull = kDsFull + 2;   // per half
   static constexpr int kMmaDone = kAccFull + 1, kNumBars = kMmaDone + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
@@ -198,22 +201,38 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, float mul, void* o
   }
 }
 
-// The 8 TS MMAs of one 128-key (or 128-query) reduction whose A operand was packed by
-// the two half-row threads: steps 0-3 at TMEM columns 0..31, steps 4-7 at 64..95.
-template <int D, Elem E, bool ACC, int KK = 0>
-__device__ __forceinline__ void issue_pv_halves(uint32_t tO, uint32_t tA, uint32_t b_lo) {
+// SS MMAs over d with N = 64: one 64-row half of a 128-row B tile (its descriptor
+// starts 64 rows = 8 KB, a whole number of swizzle atoms, into the tile).
+template <int D, Elem E, int KK = 0>
+__device__ __forceinline__ void issue_s64(uint32_t tD, uint32_t a_lo, uint32_t b_lo) {
   using L = FwdCfg<D, E>;
-  static_assert(!L::kFp8 && L::kPvSteps == 8, "16-bit operands, 16 keys per step");
-  if constexpr (KK < L::kPvSteps) {
+  if constexpr (KK < D / L::kMmaK) {
+    constexpr uint32_t idesc = ptx::idesc_make(kBlockM, 64, L::kAbType, false, false);
+    constexpr uint32_t desc_hi = ptx::sdesc_hi(1024);
+    constexpr uint32_t kOff = ((KK * 32 / 128) * L::kAtomBytes + (KK * 32) % 128) >> 4;
+    ptx::mma_f16_ss_o<KK ? 1 : 0, kOff, kOff>(tD, a_lo, b_lo, desc_hi, idesc);
+    issue_s64<D, E, KK + 1>(tD, a_lo, b_lo);
+  }
+}
+
+// The 4 TS MMAs of one 64-key (or 64-query) half: A packed by the two compute threads
+// of a row at TMEM columns {0, 8} and {32, 40}, B 64 MN-major rows (16 per step).
+template <int D, Elem E, bool ACC, int KK = 0>
+__device__ __forceinline__ void issue_pv64(uint32_t tO, uint32_t tA, uint32_t b_lo) {
+  using L = FwdCfg<D, E>;
+  static_assert(!L::kFp8, "16-bit operands");
+  if constexpr (KK < 4) {
     constexpr uint32_t idesc = ptx::idesc_make(kBlockM, D, L::kAbType, false, true);
     constexpr uint32_t desc_hi = ptx::sdesc_hi(1024);
     constexpr int kAcc = (ACC || KK > 0) ? 1 : 0;
-    constexpr uint32_t kOt = KK < 4 ? KK * 8 : 64 + (KK - 4) * 8;
+    constexpr uint32_t kOt = (KK & 1) * 8 + (KK >> 1) * 32;
     constexpr uint32_t kOb = (KK * 16 * 128) >> 4;
     ptx::mma_f16_ts_o<kAcc, kOt, kOb>(tO, tA, b_lo, desc_hi, idesc);
-    issue_pv_halves<D, E, ACC, KK + 1>(tO, tA, b_lo);
+    issue_pv64<D, E, ACC, KK + 1>(tO, tA, b_lo);
   }
 }
+
+constexpr uint32_t kHalfDesc = (64 * 128) >> 4;    // 64 rows of 128-byte swizzle atoms
 
 // ---------------------------------------------------------------------------- dq kernel
 
@@ -255,24 +274,44 @@ __device__ __noinline__ void dq_mma(const BwdParams& p, uint32_t sbase, uint32_t
   const uint32_t k_lo0 = ptx::sdesc_lo(sbase + C::kRingOff, 16);                 // K as K-major B of S
   const uint32_t v_lo0 = ptx::sdesc_lo(sbase + C::kRingOff + C::kTile, 16);      // V as K-major B of dP
   const uint32_t kmn_lo0 = ptx::sdesc_lo(sbase + C::kRingOff, v_lbo<D, E>());    // K as MN-major B of dQ
-  const uint32_t tS = tmem + kTmS, tDP = tmem + kTmDP, tAcc = tmem + kTmAcc;
+  const uint32_t tAcc = tmem + kTmAcc;
+  // S_h = Q K_h^T and dP_h = dO V_h^T for key half h of the tile in ring stage s
+  auto sdp = [&](uint32_t s, int h) {
+    const uint32_t tS = tmem + kTmHalf * h;
+    issue_s64<D, E>(tS, q_lo, k_lo0 + s * kStageDesc + kHalfDesc * h);
+    issue_s64<D, E>(tS + kTmDP, do_lo, v_lo0 + s * kStageDesc + kHalfDesc * h);
+    ptx::mma_commit(bar(C::kSdpFull + h));
+  };
   uint32_t tile = 0, units = 0;
   int bh, i;
   for (int k = 0; bwd_unit_at(p, k, true, bh, i); ++k) {
     const int n = p.causal ? i + 1 : p.n_blk;
     if (!ptx::mbar_wait(bar(C::kStFull), units & 1u, ctl, 2u)) goto done;
+    {
+      const uint32_t s0 = tile % kBwdStages;
+      if (!ptx::mbar_wait(bar(C::kReady + s0), (tile / kBwdStages) & 1u, ctl, 2u)) goto done;
+      sdp(s0, 0);
+      sdp(s0, 1);
+    }
     for (int j = 0; j < n; ++j, ++tile) {
-      const uint32_t s = tile % kBwdStages, f = tile / kBwdStages;
-      if (!ptx::mbar_wait(bar(C::kReady + s), f & 1u, ctl, 2u)) goto done;
-      issue_s<D, E>(tS, q_lo, k_lo0 + s * kStageDesc);       // S = Q K_j^T
-      issue_s<D, E>(tDP, do_lo, v_lo0 + s * kStageDesc);     // dP = dO V_j^T
-      ptx::mma_commit(bar(C::kSdpFull));
+      const uint32_t s = tile % kBwdStages;
+      const bool more = j + 1 < n;
+      const uint32_t sn = (tile + 1) % kBwdStages;
+      // half a: dQ += dS_a K_a, then the next tile's half a
       if (!ptx::mbar_wait(bar(C::kDsFull), tile & 1u, ctl, 2u)) goto done;
       ptx::tc_fence_after();
-      // dS was packed over the dP region
-      if (j == 0) issue_pv_halves<D, E, false>(tAcc, tDP, kmn_lo0 + s * kStageDesc);   // dQ = dS K_j
-      else issue_pv_halves<D, E, true>(tAcc, tDP, kmn_lo0 + s * kStageDesc);          // dQ += dS K_j
+      if (j == 0) issue_pv64<D, E, false>(tAcc, tmem + kTmDP, kmn_lo0 + s * kStageDesc);
+      else issue_pv64<D, E, true>(tAcc, tmem + kTmDP, kmn_lo0 + s * kStageDesc);
+      if (more) {
+        if (!ptx::mbar_wait(bar(C::kReady + sn), ((tile + 1) / kBwdStages) & 1u, ctl, 2u)) goto done;
+        sdp(sn, 0);
+      }
+      // half b
+      if (!ptx::mbar_wait(bar(C::kDsFull + 1), tile & 1u, ctl, 2u)) goto done;
+      ptx::tc_fence_after();
+      issue_pv64<D, E, true>(tAcc, tmem + kTmHalf + kTmDP, kmn_lo0 + s * kStageDesc + kHalfDesc);
       ptx::mma_commit(bar(C::kDone + s));
+      if (more) sdp(sn, 1);
     }
     ptx::mma_commit(bar(C::kStEmpty));
     ptx::mma_commit(bar(C::kAccFull));
@@ -291,10 +330,9 @@ __device__ __forceinline__ void dq_compute(const BwdParams& p, uint32_t sbase, u
   auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const int r = (warp & 3) * 32 + lane;                        // row in the Q tile = TMEM lane
-  const int half = warp >> 2;                                  // key columns 64*half .. +63
+  const int sub = warp >> 2;                                   // keys 32*sub .. +31 of each 64-key half
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-  const uint32_t tS = tmem + lane_base + kTmS + 64 * half, tDP = tmem + lane_base + kTmDP + 64 * half;
-  const uint32_t tAcc = tmem + lane_base + kTmAcc + (D / 2) * half;
+  const uint32_t tAcc = tmem + lane_base + kTmAcc + (D / 2) * sub;
   uint32_t tile = 0, units = 0;
   int bh, i;
   for (int k = 0; bwd_unit_at(p, k, true, bh, i); ++k) {
@@ -302,44 +340,40 @@ __device__ __forceinline__ void dq_compute(const BwdParams& p, uint32_t sbase, u
     const int row = i * 128 + r;
     const size_t wrow = static_cast<size_t>(bh) * p.n_pad + row;
     const float lse2 = p.lse2[wrow], dlt = p.delta[wrow];
+    const int limit = min(p.N, p.causal ? row + 1 : p.N);      // keys >= limit get P = 0
     for (int j = 0; j < n; ++j, ++tile) {
-      const bool got = ptx::mbar_wait(bar(C::kSdpFull), tile & 1u, ctl, 4u);
-      if (!__all_sync(0xFFFFFFFFu, got)) return;
-      ptx::tc_fence_after();
-      // keys past N, and (causal) past this row, get P = 0 (counted from this half's first key)
-      const int visible = min(p.N, p.causal ? row + 1 : p.N) - (j * 128 + 64 * half);
-      uint32_t sr[2][32], dr[2][32];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        ptx::tmem_ld32(tS + 32 * c, sr[c]);
-        ptx::tmem_ld32(tDP + 32 * c, dr[c]);
-      }
-      ptx::tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int h = 0; h < 2; ++h) {
+        const bool got = ptx::mbar_wait(bar(C::kSdpFull + h), tile & 1u, ctl, 4u);
+        if (!__all_sync(0xFFFFFFFFu, got)) return;
+        ptx::tc_fence_after();
+        const uint32_t tS = tmem + lane_base + kTmHalf * h + 32 * sub, tDP = tS + kTmDP;
+        const int visible = limit - (j * 128 + 64 * h + 32 * sub);
+        uint32_t sr[32], dr[32];
+        ptx::tmem_ld32(tS, sr);
+        ptx::tmem_ld32(tDP, dr);
+        ptx::tmem_wait_ld();
         float ds[32];
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
-          const float pv = (32 * c + x < visible)
-                               ? ptx::ex2(fmaf(__uint_as_float(sr[c][x]), p.scale_log2, -lse2)) : 0.f;
-          ds[x] = pv * (__uint_as_float(dr[c][x]) - dlt);
+          const float pv = x < visible ? ptx::ex2(fmaf(__uint_as_float(sr[x]), p.scale_log2, -lse2)) : 0.f;
+          ds[x] = pv * (__uint_as_float(dr[x]) - dlt);
         }
         uint32_t w[16];
         pack16<kBf16>(ds, w);
-        // packed dS goes over this half's first 32 dP columns, already read
-        ptx::tmem_st16(tDP + 16 * c, w);
+        ptx::tmem_st16(tDP, w);                                // over this thread's first 16 dP columns
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar(C::kDsFull + h));
       }
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(C::kDsFull));
     }
     const bool got = ptx::mbar_wait(bar(C::kAccFull), units & 1u, ctl, 4u);
     if (!__all_sync(0xFFFFFFFFu, got)) return;
     ++units;
     ptx::tc_fence_after();
     store_acc_row<D / 2, kBf16>(tAcc, p.scale, p.dq,
-                                (static_cast<size_t>(bh) * p.N + (row < p.N ? row : 0)) * D + (D / 2) * half,
+                                (static_cast<size_t>(bh) * p.N + (row < p.N ? row : 0)) * D + (D / 2) * sub,
                                 row < p.N);
     ptx::tc_fence_before();
   }
@@ -389,28 +423,50 @@ __device__ __noinline__ void dkdv_mma(const BwdParams& p, uint32_t sbase, uint32
   const uint32_t do_lo0 = ptx::sdesc_lo(sbase + C::kRingOff + C::kTile, 16);     // dO as K-major B of dP^T
   const uint32_t qmn_lo0 = ptx::sdesc_lo(sbase + C::kRingOff, v_lbo<D, E>());    // Q as MN-major B of dK
   const uint32_t domn_lo0 = ptx::sdesc_lo(sbase + C::kRingOff + C::kTile, v_lbo<D, E>());  // dO, of dV
-  const uint32_t tS = tmem + kTmS, tDP = tmem + kTmDP, tDV = tmem + kTmAcc, tDK = tmem + kTmAcc + D;
+  const uint32_t tDV = tmem + kTmAcc, tDK = tmem + kTmAcc + D;
+  // S^T_h = K Q_h^T and dP^T_h = V dO_h^T for query half h of the tile in ring stage s
+  auto sdp = [&](uint32_t s, int h) {
+    const uint32_t tS = tmem + kTmHalf * h;
+    issue_s64<D, E>(tS, k_lo, q_lo0 + s * kStageDesc + kHalfDesc * h);
+    issue_s64<D, E>(tS + kTmDP, v_lo, do_lo0 + s * kStageDesc + kHalfDesc * h);
+    ptx::mma_commit(bar(C::kSdpFull + h));
+  };
   uint32_t tile = 0, units = 0;
   int bh, j;
   for (int k = 0; bwd_unit_at(p, k, false, bh, j); ++k) {
     const int i0 = p.causal ? j : 0;
     if (!ptx::mbar_wait(bar(C::kStFull), units & 1u, ctl, 2u)) goto done;
+    {
+      const uint32_t s0 = tile % kBwdStages;
+      if (!ptx::mbar_wait(bar(C::kReady + s0), (tile / kBwdStages) & 1u, ctl, 2u)) goto done;
+      sdp(s0, 0);
+      sdp(s0, 1);
+    }
     for (int i = i0; i < p.n_blk; ++i, ++tile) {
-      const uint32_t s = tile % kBwdStages, f = tile / kBwdStages;
-      if (!ptx::mbar_wait(bar(C::kReady + s), f & 1u, ctl, 2u)) goto done;
-      issue_s<D, E>(tS, k_lo, q_lo0 + s * kStageDesc);       // S^T = K Q_i^T
-      issue_s<D, E>(tDP, v_lo, do_lo0 + s * kStageDesc);     // dP^T = V dO_i^T
-      ptx::mma_commit(bar(C::kSdpFull));
+      const uint32_t s = tile % kBwdStages;
+      const bool more = i + 1 < p.n_blk;
+      const uint32_t sn = (tile + 1) % kBwdStages;
+      // half a: dV += P^T_a dO_a, dK += dS^T_a Q_a, then the next tile's half a
       if (!ptx::mbar_wait(bar(C::kDsFull), tile & 1u, ctl, 2u)) goto done;
       ptx::tc_fence_after();
       if (i == i0) {
-        issue_pv_halves<D, E, false>(tDV, tS, domn_lo0 + s * kStageDesc);   // dV = P^T dO_i
-        issue_pv_halves<D, E, false>(tDK, tDP, qmn_lo0 + s * kStageDesc);   // dK = dS^T Q_i
+        issue_pv64<D, E, false>(tDV, tmem, domn_lo0 + s * kStageDesc);
+        issue_pv64<D, E, false>(tDK, tmem + kTmDP, qmn_lo0 + s * kStageDesc);
       } else {
-        issue_pv_halves<D, E, true>(tDV, tS, domn_lo0 + s * kStageDesc);
-        issue_pv_halves<D, E, true>(tDK, tDP, qmn_lo0 + s * kStageDesc);
+        issue_pv64<D, E, true>(tDV, tmem, domn_lo0 + s * kStageDesc);
+        issue_pv64<D, E, true>(tDK, tmem + kTmDP, qmn_lo0 + s * kStageDesc);
       }
+      if (more) {
+        if (!ptx::mbar_wait(bar(C::kReady + sn), ((tile + 1) / kBwdStages) & 1u, ctl, 2u)) goto done;
+        sdp(sn, 0);
+      }
+      // half b
+      if (!ptx::mbar_wait(bar(C::kDsFull + 1), tile & 1u, ctl, 2u)) goto done;
+      ptx::tc_fence_after();
+      issue_pv64<D, E, true>(tDV, tmem + kTmHalf, domn_lo0 + s * kStageDesc + kHalfDesc);
+      issue_pv64<D, E, true>(tDK, tmem + kTmHalf + kTmDP, qmn_lo0 + s * kStageDesc + kHalfDesc);
       ptx::mma_commit(bar(C::kDone + s));
+      if (more) sdp(sn, 1);
     }
     ptx::mma_commit(bar(C::kStEmpty));
     ptx::mma_commit(bar(C::kAccFull));
@@ -429,58 +485,55 @@ __device__ __forceinline__ void dkdv_compute(const BwdParams& p, uint32_t sbase,
   auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const int kr = (warp & 3) * 32 + lane;                       // key row in the K/V tile = TMEM lane
-  const int half = warp >> 2;                                  // query columns 64*half .. +63
+  const int sub = warp >> 2;                                   // queries 32*sub .. +31 of each 64-query half
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-  const uint32_t tS = tmem + lane_base + kTmS + 64 * half, tDP = tmem + lane_base + kTmDP + 64 * half;
-  const uint32_t tDV = tmem + lane_base + kTmAcc + (D / 2) * half, tDK = tmem + lane_base + kTmAcc + D + (D / 2) * half;
+  const uint32_t tDV = tmem + lane_base + kTmAcc + (D / 2) * sub, tDK = tDV + D;
   uint32_t tile = 0, units = 0;
   int bh, j;
   for (int k = 0; bwd_unit_at(p, k, false, bh, j); ++k) {
     const int i0 = p.causal ? j : 0;
     const int key = j * 128 + kr;
     for (int i = i0; i < p.n_blk; ++i, ++tile) {
-      const bool got = ptx::mbar_wait(bar(C::kSdpFull), tile & 1u, ctl, 4u);
-      if (!__all_sync(0xFFFFFFFFu, got)) return;
-      ptx::tc_fence_after();
       const uint32_t s = tile % kBwdStages;
-      const float* lse2 = reinterpret_cast<const float*>(smem + C::kRingOff + s * C::kStageBytes + 2 * C::kTile) +
-                          64 * half;
-      const float* dlt = lse2 + 128;
-      // causal diagonal tile: query i*128 + 64*half + q sees this key iff 64*half + q >= kr
-      // (padded queries have LSE*log2(e) = +inf and so P = 0 already)
-      const int first = (p.causal && i == j) ? kr - 64 * half : 0;
-      // one 32-column chunk at a time: with 10 warps an SMSP holds 3, which caps a
-      // thread at 168 registers
+      const float* vec = reinterpret_cast<const float*>(smem + C::kRingOff + s * C::kStageBytes + 2 * C::kTile);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int h = 0; h < 2; ++h) {
+        const bool got = ptx::mbar_wait(bar(C::kSdpFull + h), tile & 1u, ctl, 4u);
+        if (!__all_sync(0xFFFFFFFFu, got)) return;
+        ptx::tc_fence_after();
+        const int q0 = 64 * h + 32 * sub;                      // first query of this thread's 32
+        const float* lse2 = vec + q0;
+        const float* dlt = vec + 128 + q0;
+        // causal diagonal tile: query i*128 + q0 + x sees this key iff q0 + x >= kr (padded
+        // queries have LSE*log2(e) = +inf and so P = 0 already)
+        const int first = (p.causal && i == j) ? kr - q0 : 0;
+        const uint32_t tS = tmem + lane_base + kTmHalf * h + 32 * sub, tDP = tS + kTmDP;
         uint32_t sr[32], dr[32];
-        ptx::tmem_ld32(tS + 32 * c, sr);
-        ptx::tmem_ld32(tDP + 32 * c, dr);
+        ptx::tmem_ld32(tS, sr);
+        ptx::tmem_ld32(tDP, dr);
         ptx::tmem_wait_ld();
         float pv[32], ds[32];
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
-          const int q = 32 * c + x;
-          pv[x] = q >= first ? ptx::ex2(fmaf(__uint_as_float(sr[x]), p.scale_log2, -lse2[q])) : 0.f;
-          ds[x] = pv[x] * (__uint_as_float(dr[x]) - dlt[q]);
+          pv[x] = x >= first ? ptx::ex2(fmaf(__uint_as_float(sr[x]), p.scale_log2, -lse2[x])) : 0.f;
+          ds[x] = pv[x] * (__uint_as_float(dr[x]) - dlt[x]);
         }
         uint32_t wp[16], wd[16];
         pack16<kBf16>(pv, wp);
         pack16<kBf16>(ds, wd);
-        // packed P^T / dS^T go over this half's first 32 S^T / dP^T columns, already read
-        ptx::tmem_st16(tS + 16 * c, wp);
-        ptx::tmem_st16(tDP + 16 * c, wd);
+        ptx::tmem_st16(tS, wp);                                // over this thread's first 16 columns
+        ptx::tmem_st16(tDP, wd);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar(C::kDsFull + h));
       }
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(C::kDsFull));
     }
     const bool got = ptx::mbar_wait(bar(C::kAccFull), units & 1u, ctl, 4u);
     if (!__all_sync(0xFFFFFFFFu, got)) return;
     ++units;
     ptx::tc_fence_after();
-    const size_t off = (static_cast<size_t>(bh) * p.N + (key < p.N ? key : 0)) * D + (D / 2) * half;
+    const size_t off = (static_cast<size_t>(bh) * p.N + (key < p.N ? key : 0)) * D + (D / 2) * sub;
     store_acc_row<D / 2, kBf16>(tDV, 1.f, p.dv, off, key < p.N);
     store_acc_row<D / 2, kBf16>(tDK, p.scale, p.dk, off, key < p.N);
     ptx::tc_fence_before();
@@ -502,7 +555,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
   auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kNumBars; ++i) ptx::mbar_init(bar(i), i == C::kDsFull ? kBwdComputeWarps : 1);
+    for (int i = 0; i < C::kNumBars; ++i)
+      ptx::mbar_init(bar(i), (i == C::kDsFull || i == C::kDsFull + 1) ? kBwdComputeWarps : 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
