@@ -390,16 +390,22 @@ def run_gpu(args):
     else:
         roof = {"bound": "tensor", "achieved": kern_tflops, "peak": peak, "unit": "TFLOP/s",
                 "frac": kern_tflops / peak, "traffic": traffic, "peak_source": peak_note,
-                "kernel": "fa_fwd_fp8_kernel" if fp8 else "fa_fwd_kernel"}
+                "kernel": "fa_fwd_kernel<128, e4m3>" if fp8 else "fa_fwd_kernel"}
         if bwd:
             roof["kernel"] = "fa_bwd_prep_kernel + fa_bwd_kernel (dQ) + fa_bwd_kernel (dK, dV)"
             roof["note"] = ("algorithmic FLOPs = 2.5 x forward (five products); the two-kernel scheme "
                             "runs seven, recomputing S and dP once more instead of reducing dQ")
     def mask_flops(c):
         return step_flops / len(masks) if dec else w.flops(c) * (BWD_FLOP_RATIO if bwd else 1.0)
+    def pct(xs, q):
+        # q-th quantile of the per-launch times (nearest rank)
+        ys = sorted(xs)
+        return ys[min(len(ys) - 1, max(0, int(round(q * (len(ys) - 1)))))]
     variants = {("causal" if c else "non_causal"): {
         "tflops": mask_flops(c) / (statistics.median(per_mask_ms[c]) * 1e-3) / 1e12,
         "median_ms": statistics.median(per_mask_ms[c]),
+        "p10_ms": pct(per_mask_ms[c], 0.1),
+        "p90_ms": pct(per_mask_ms[c], 0.9),
         "pct_of_spec_peak": 100.0 * mask_flops(c) / (statistics.median(per_mask_ms[c]) * 1e-3) / 1e12
         / SPEC_PEAK_TFLOPS[dtype_name]} for c in masks}
 
