@@ -143,3 +143,27 @@ def test_rejections(gpu_lib):
     with pytest.raises(gpu_lib.FAError) as e:
         gpu_lib.attention_backward(q, q, q, q, lse, q, workspace=ws)
     assert e.value.status == gpu_lib.FA_ERR_WORKSPACE
+
+
+def test_outputs_16_byte_aligned_match_aligned_outputs(gpu_lib):
+    # dQ, dK, dV at a 16-byte (not 32-byte) offset take the 16-byte store path; the
+    # values must be the same bits as with 32-byte aligned outputs
+    fa = gpu_lib
+    shape = (1, 2, 300, 128)
+    q, k, v = (t.cuda() for t in make_qkv(shape, torch.bfloat16, 13))
+    do = make_dout(shape, torch.bfloat16, 13).cuda()
+    o, lse = fa.attention(q, k, v, causal=True)
+    ref = fa.attention_backward(q, k, v, o, lse, do, causal=True)
+    n = q.numel()
+    outs = []
+    for _ in range(3):
+        buf = torch.empty(n + 64, device="cuda", dtype=torch.bfloat16)
+        view = buf[8:8 + n].view(shape)          # 16 bytes past a 256-byte aligned base
+        assert view.data_ptr() % 32 == 16
+        outs.append(view)
+    got = fa.attention_backward(q, k, v, o, lse, do, causal=True, dq=outs[0], dk=outs[1], dv=outs[2])
+    torch.cuda.synchronize()
+    st, bits = fa.last_device_status()
+    assert st == fa.FA_OK, f"device status {bits:#x}"
+    for a, b in zip(ref, got):
+        assert torch.equal(a, b)

@@ -195,8 +195,15 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, float mul, void* o
     for (int i = 0; i < 16; ++i)
       pk[i] = ptx::pack2<BF16>(__uint_as_float(r[c][2 * i]) * mul, __uint_as_float(r[c][2 * i + 1]) * mul);
     if (live) {
+      if ((reinterpret_cast<uintptr_t>(dst) & 31u) == 0) {
+        // 32-byte stores fill whole sectors: half as many scattered row writes, and
+        // those slow the MMA issue of the steps they overlap
 #pragma unroll
-      for (int i = 0; i < 4; ++i) dst[c * 4 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        for (int i = 0; i < 2; ++i) ptx::st_global_v8(dst + c * 4 + 2 * i, pk + 8 * i);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[c * 4 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      }
     }
   }
 }
