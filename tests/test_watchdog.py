@@ -19,9 +19,10 @@ from fa_inputs import make_qkv
 pytestmark = pytest.mark.gpu
 
 
-def test_stalled_stage_reports_timeout_and_context_recovers(gpu_lib):
+@pytest.mark.parametrize("d", [64, 128])
+def test_stalled_stage_reports_timeout_and_context_recovers(gpu_lib, d):
     fa = gpu_lib
-    q, k, v = make_qkv((1, 4, 1024, 128), torch.bfloat16, 40)
+    q, k, v = make_qkv((1, 4, 1024, d), torch.bfloat16, 40)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     st, _ = fa.last_device_status()
     assert st == fa.FA_OK
@@ -35,6 +36,6 @@ def test_stalled_stage_reports_timeout_and_context_recovers(gpu_lib):
     o, lse = fa.attention(qd, kd, vd, causal=False)
     st, bits = fa.last_device_status()
     assert st == fa.FA_OK and bits == 0
-    ro, rl = oracle.attention(q, k, v, 1 / math.sqrt(128), False)
+    ro, rl = oracle.attention(q, k, v, 1 / math.sqrt(d), False)
     assert float(np.abs(o.float().cpu().numpy() - ro).max()) <= 1.2e-2
     assert float(np.abs(lse.cpu().numpy() - rl).max()) <= 1e-3
