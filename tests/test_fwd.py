@@ -107,6 +107,29 @@ def test_ragged_shapes(gpu_lib, B, H, N, d, dtype, causal):
     _compare_full(gpu_lib, q, k, v, causal, what=f"{B}x{H}x{N}x{d} {dtype}")
 
 
+@pytest.mark.parametrize("d,dtype", [(64, torch.float16), (128, torch.bfloat16)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_equal_scores_closed_form(gpu_lib, d, dtype, causal):
+    """Q = 0 makes every visible score 0: every P is exactly 1, so O is the plain mean of
+    the visible V rows and LSE = ln(number of visible keys), with no oracle involved.  Left
+    over are the fp32 sums of the P.V MMA and the final rounding of O."""
+    B, H, N = 1, 2, 333
+    _, k, v = make_qkv((B, H, N, d), dtype, 60)
+    q = torch.zeros((B, H, N, d), dtype=dtype)
+    o, lse = _run(gpu_lib, q, k, v, causal)
+    vd = v.double().numpy()
+    count = np.arange(1, N + 1, dtype=np.float64) if causal else np.full(N, float(N))
+    ref_o = (np.cumsum(vd, axis=2) if causal else np.broadcast_to(vd.sum(axis=2, keepdims=True), vd.shape))
+    ref_o = ref_o / count[None, None, :, None]
+    ref_lse = np.broadcast_to(np.log(count), lse.shape)
+    mant = 10 if dtype == torch.float16 else 7
+    bound = half_ulp(ref_o, mant) + 1e-5 * np.abs(vd).max()
+    assert (np.abs(o - ref_o) <= bound).all(), f"max|dO| {np.abs(o - ref_o).max():.3e}"
+    assert np.abs(lse - ref_lse).max() <= 1e-5
+    if causal:
+        assert np.array_equal(o[:, :, 0], v[:, :, 0].float().numpy())     # row 0 sees one key
+
+
 def test_explicit_scale(gpu_lib):
     q, k, v = make_qkv((1, 2, 300, 64), torch.bfloat16, 7)
     _compare_full(gpu_lib, q, k, v, False, scale=0.3, what="scale 0.3")
