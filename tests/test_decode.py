@@ -83,3 +83,28 @@ def test_decode_workspace_too_small(gpu_lib):
     with pytest.raises(gpu_lib.FAError) as e:
         gpu_lib.decode(q, k, v, num_splits=8, workspace=ws)
     assert e.value.status == gpu_lib.FA_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("num_splits", [1, 7])
+@pytest.mark.parametrize("causal", [False, True])
+def test_equal_scores_closed_form(gpu_lib, causal, num_splits):
+    """Q = 0: every visible score is 0, so O is the mean of the visible V rows and
+    LSE = ln(number of visible keys); query row i sees keys 0 .. Nk - Nq + i when causal.
+    With several splits the partial results meet in the log-sum-exp merge."""
+    fa = gpu_lib
+    B, H, Nq, Nk, d = 1, 2, 4, 999, 128
+    _, k, v = _inputs(B, H, Nq, Nk, d, torch.bfloat16, 70)
+    q = torch.zeros((B, H, Nq, d), dtype=torch.bfloat16)
+    o, lse = fa.decode(q.cuda(), k.cuda(), v.cuda(), causal=causal, num_splits=num_splits)
+    torch.cuda.synchronize()
+    st, bits = fa.last_device_status()
+    assert st == fa.FA_OK, f"status {bits:#x}"
+    vd = v.double().numpy()
+    count = (Nk - Nq + 1 + np.arange(Nq)) if causal else np.full(Nq, Nk)
+    csum = np.cumsum(vd, axis=2)
+    ref_o = np.stack([csum[:, :, c - 1] / c for c in count], axis=2)
+    ref_lse = np.broadcast_to(np.log(count.astype(np.float64)), (B, H, Nq))
+    on, ln = o.float().cpu().numpy(), lse.cpu().numpy()
+    bound = _half_ulp(ref_o, 7) + 1e-5 * np.abs(vd).max()
+    assert (np.abs(on - ref_o) <= bound).all(), f"max|dO| {np.abs(on - ref_o).max():.3e}"
+    assert np.abs(ln - ref_lse).max() <= 1e-5
