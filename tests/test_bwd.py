@@ -167,3 +167,27 @@ def test_outputs_16_byte_aligned_match_aligned_outputs(gpu_lib):
     assert st == fa.FA_OK, f"device status {bits:#x}"
     for a, b in zip(ref, got):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_equal_scores_closed_form(gpu_lib, causal):
+    """Q = 0 makes every visible score 0, so P_ij = 1 / count_i (count_i = visible keys of
+    row i): dK = scale * dS^T Q is exactly zero, and dV_j = sum_i P_ij dO_i needs no
+    oracle.  The only rounding in dV is that of P and of dV to bf16 before and after the
+    fp32 MMA sums (P = 1/count is not a bf16 number in general)."""
+    fa = gpu_lib
+    B, H, N, d = 1, 2, 300, 128
+    _, k, v = make_qkv((B, H, N, d), torch.bfloat16, 80)
+    q = torch.zeros((B, H, N, d), dtype=torch.bfloat16)
+    do = make_dout((B, H, N, d), torch.bfloat16, 80)
+    _, _, (dq, dk, dv) = _run(fa, q, k, v, do, causal)
+    assert torch.count_nonzero(dk).item() == 0
+    count = np.arange(1, N + 1, dtype=np.float64) if causal else np.full(N, float(N))
+    w = do.double().numpy() / count[None, None, :, None]           # dO_i / count_i
+    if causal:
+        ref = np.flip(np.cumsum(np.flip(w, axis=2), axis=2), axis=2)   # sum over i >= j
+    else:
+        ref = np.broadcast_to(w.sum(axis=2, keepdims=True), w.shape)
+    got = dv.double().cpu().numpy()
+    scale_ref = np.abs(ref).max()
+    assert np.abs(got - ref).max() <= 4 * 2.0 ** -8 * scale_ref, f"max|ddV| {np.abs(got - ref).max():.3e}"
