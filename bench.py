@@ -30,6 +30,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import torch
@@ -100,12 +101,14 @@ def _workload(name: str):
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi sampled every 100 ms during the timed region."""
+    """nvidia-smi sampled every 100 ms during the timed region.  The raw samples go to
+    FA_CLOCKS_DIR (to keep them) or else the system temporary directory."""
 
     def __init__(self, device_index: int):
         self.idx = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        out_dir = os.environ.get("FA_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"fa_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
