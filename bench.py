@@ -107,6 +107,7 @@ class ClockSampler:
     def __init__(self, device_index: int):
         self.idx = device_index
         self.proc = None
+        self.keep = bool(os.environ.get("FA_CLOCKS_DIR"))
         out_dir = os.environ.get("FA_CLOCKS_DIR") or tempfile.gettempdir()
         self.path = os.path.join(out_dir, f"fa_clocks_{os.getpid()}.csv")
 
@@ -144,6 +145,11 @@ class ClockSampler:
                         rows.append(parts)
         except OSError:
             pass
+        if not self.keep:
+            try:
+                os.remove(self.path)
+            except OSError:
+                pass
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
 
