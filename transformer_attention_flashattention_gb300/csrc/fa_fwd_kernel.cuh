@@ -52,6 +52,7 @@ constexpr uint32_t kTmemCols = 512;
 // rescaled far less often.  Exact in real arithmetic; the final division uses the
 // same stale maximum for numerator and denominator.
 constexpr float kRescaleThreshold = 8.0f;
+constexpr int kHoldStoresMinTiles = 16;   // units longer than this hold SMSP-shared O stores
 constexpr float kLn2 = 0.693147180559945309f;
 
 // Bits of the device status word.
@@ -628,30 +629,41 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, int t, uint32_t 
     const bool live = row < p.N;
     uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
                                            (static_cast<size_t>(bh) * p.N + (live ? row : 0)) * D);
-    // all of the row's O columns in one TMEM round trip
-    uint32_t orr[D / 32][32];
+    // all of the row's O columns in one TMEM round trip, scaled and packed
+    uint32_t pk[D / 2];
+    {
+      uint32_t orr[D / 32][32];
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) ptx::tmem_ld32(tO + 32 * c, orr[c]);
-    ptx::tmem_wait_ld();
+      for (int c = 0; c < D / 32; ++c) ptx::tmem_ld32(tO + 32 * c, orr[c]);
+      ptx::tmem_wait_ld();
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t pk[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float2 v = ptx::mul2(make_float2(__uint_as_float(orr[c][2 * i]), __uint_as_float(orr[c][2 * i + 1])),
-                                   make_float2(inv_l, inv_l));
+      for (int i = 0; i < D / 2; ++i) {
+        const float2 v = ptx::mul2(
+            make_float2(__uint_as_float(orr[i / 16][(2 * i) % 32]), __uint_as_float(orr[i / 16][(2 * i + 1) % 32])),
+            make_float2(inv_l, inv_l));
         pk[i] = ptx::pack2<L::kBf16Out>(v.x, v.y);
       }
-      if (live) {
-        if (o_v8) {
-          // 32-byte stores fill whole sectors (rows are 128 or 256 bytes; base 32-aligned)
+    }
+    // In long 16-bit units, the warps that share an SMSP with the MMA-issuing warp hold their O
+    // stores until the next unit's S_t(0) is in (the wait step 0 of that unit does anyway):
+    // their row-scattered stores queue ahead of that warp's tcgen05 instructions, and by
+    // then the MMA thread has issued this unit boundary's MMAs.  In short units the held
+    // stores would delay the next unit more than they save.
+    if (!L::kFp8 && ntile > kHoldStoresMinTiles && ((threadIdx.x / 32) & 3) == (kMmaWarp & 3)) {
+      int bhn, qbn;
+      if (unit_at(p, k + 1, bhn, qbn) && tile_nkv(p, qbn, t) > 0) {
+        const bool held = ptx::mbar_wait(bar(L::kSFull + t), s_uses & 1u, ctl, kStatusSoftmaxTimeout);
+        if (!__all_sync(0xFFFFFFFFu, held)) return;
+      }
+    }
+    if (live) {
+      if (o_v8) {
+        // 32-byte stores fill whole sectors (rows are 128 or 256 bytes; base 32-aligned)
 #pragma unroll
-          for (int i = 0; i < 2; ++i) ptx::st_global_v8(orow + c * 4 + 2 * i, pk + 8 * i);
-        } else {
+        for (int i = 0; i < D / 16; ++i) ptx::st_global_v8(orow + 2 * i, pk + 8 * i);
+      } else {
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            orow[c * 4 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-        }
+        for (int i = 0; i < D / 8; ++i) orow[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
       }
     }
     if (live && p.lse != nullptr)
