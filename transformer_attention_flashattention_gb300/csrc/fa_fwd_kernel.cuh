@@ -52,7 +52,7 @@ constexpr uint32_t kTmemCols = 512;
 // rescaled far less often.  Exact in real arithmetic; the final division uses the
 // same stale maximum for numerator and denominator.
 constexpr float kRescaleThreshold = 8.0f;
-constexpr int kHoldStoresMinTiles = 16;   // units longer than this hold SMSP-shared O stores
+constexpr int kHoldStoresMinTiles = 15;   // units longer than this hold SMSP-shared O stores
 constexpr float kLn2 = 0.693147180559945309f;
 
 // Bits of the device status word.
