@@ -97,6 +97,10 @@ RAGGED = [
     (1, 2, 1000, 128, torch.bfloat16),
     (1, 1, 1536, 64, torch.bfloat16),
     (3, 5, 333, 128, torch.bfloat16),
+    # 17 key tiles per unit and 288 units: the epilogue's held O stores run, and some
+    # CTAs' next unit is a last q-block whose second Q tile lies past N
+    (4, 8, 2100, 128, torch.bfloat16),
+    (4, 8, 2100, 64, torch.float16),
 ]
 
 
