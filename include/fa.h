@@ -96,6 +96,10 @@ int fa_fwd_host_workspace_size(int B, int H, int N, int d, unsigned long long* b
  *              64-row block, 1 for an all-zero block; x8 = e4m3_rn_satfinite(x/s)
  *   hadamard : 1 applies x -> x H_d / sqrt(d) (Sylvester order) before the absmax;
  *              0 does not.  Use 1 for Q and K only, never for V.
+ * Errors: FA_ERR_NULL, FA_ERR_SHAPE, FA_ERR_UNSUPPORTED, FA_ERR_ALIGN (x, x8 16-byte
+ * aligned, scale 4-byte), FA_ERR_ARCH, FA_ERR_LAUNCH.  The kernel's waits for its
+ * bulk copies are bounded; one that gives up ORs 1 into the device status word (and
+ * 8 if a copy had still not landed when its CTA left); see fa_last_device_status.
  */
 int fa_quantize_fp8(const void* x, void* x8, float* scale, int B, int H, int N, int d, int hadamard,
                     int transpose_out, void* stream);
@@ -227,7 +231,8 @@ const char* fa_strerror(int status);
  * Synchronises `stream`, then reads and clears the current device's status
  * word, which kernels set when a bounded pipeline wait gives up.  Returns FA_OK
  * or FA_ERR_DEVICE_TIMEOUT; *bits (if not NULL) receives the raw word
- * (1 load warp, 2 MMA warp, 4 softmax warps, 8 drain of in-flight copies).
+ * (1 load warp, or a quantisation load wait; 2 MMA warp; 4 softmax warps; 8 drain
+ * of in-flight copies; 16 a decode load wait).
  */
 int fa_last_device_status(void* stream, unsigned int* bits);
 

@@ -204,6 +204,9 @@ int quantize_fp8(const void* x, void* x8, float* scale, int B, int H, int N, int
   p.flips_hi = flips_hi;
   p.per_head = per_head;
   p.amax_mode = 0;
+  p.sm_count = di->sm_count;
+  p.status = di->status;
+  p.timeout_ns = timeout_ns_for_call();
   const cudaError_t e = launch_quant_fp8(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }

@@ -46,6 +46,9 @@ struct QuantParams {
   int per_head;                  // one absmax per (b, h) instead of per 64-row block
   int amax_mode;                 // 0: own block absmax; 1: write the block absmax only;
                                  // 2: quantise with the absmax already in `scale`
+  int sm_count;                  // SMs of the device; the persistent grid is a multiple of it
+  unsigned int* status;
+  unsigned long long timeout_ns;
 };
 
 // Split-KV attention of N_q query rows against N_k cached keys.
