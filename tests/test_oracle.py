@@ -221,6 +221,24 @@ def test_e4m3_rounding_matches_torch_cast():
     assert np.array_equal(oracle.round_to_e4m3(x.to(torch.float64)), want)
 
 
+def _golden_fraction(x):
+    if isinstance(x, str):
+        num, _, den = x.partition("/")
+        return float(num) / float(den) if den else float(num)
+    return float(x)
+
+
+@pytest.mark.parametrize("part", ["rotated", "plain"])
+def test_hand_worked_fp8_golden(part):
+    with open(os.path.join(GOLDEN, "hand_worked_fp8_blocks.json")) as f:
+        g = json.load(f)[part]
+    x = np.array(g["x"], dtype=np.float64)[None, None]
+    codes, scales = oracle.quantize_fp8_blocks(x, g["block"], hadamard=(part == "rotated"))
+    want = np.array([[int(c, 16) for c in row] for row in g["codes"]], dtype=np.uint8)
+    assert np.array_equal(codes[0, 0], want)
+    assert np.array_equal(scales[0, 0], np.array([_golden_fraction(s) for s in g["scales"]]))
+
+
 @pytest.mark.parametrize("hadamard", [False, True])
 def test_block_quantisation_properties(hadamard):
     q, _, _ = make_qkv((2, 3, 200, 128), torch.bfloat16, 3, outliers=True)
@@ -325,6 +343,72 @@ def test_pins_reject_planted_mistakes(kind, monkeypatch):
     assert _pins_pass()
     monkeypatch.setattr(oracle_attention_mod, "_rows_of_head", _mutant(kind))
     assert not _pins_pass(), f"no pin caught the planted mistake {kind!r}"
+
+
+# ----------------------------------------------------------------------------- planted FP8 mistakes
+
+def _fp8_mutant(kind):
+    """(attribute of oracle.fp8, replacement) carrying one plausible mistake."""
+    fp8 = oracle.fp8
+    if kind == "ties_away":
+        def round_ties_away(x):
+            x = fp8._f64(x)
+            a = np.abs(x)
+            _, e2 = np.frexp(a)
+            quantum = np.where(a >= 2.0 ** -6, np.exp2((e2 - 1).astype(np.float64) - 3), 2.0 ** -9)
+            return np.copysign(np.minimum(quantum * np.floor(a / quantum + 0.5), 448.0), x)
+        return "round_to_e4m3", round_ties_away
+    if kind == "walsh_order":
+        sylvester = fp8.sylvester_hadamard
+        def walsh(d):
+            h = sylvester(d)
+            return h[np.argsort((np.diff(h, axis=1) != 0).sum(axis=1), kind="stable")]
+        return "sylvester_hadamard", walsh
+    if kind == "no_sqrt_d":
+        def rotate_unnormalised(x, signs=None):
+            x = fp8._f64(x)
+            if signs is not None:
+                x = x * np.asarray(signs, dtype=np.float64)
+            return x @ fp8.sylvester_hadamard(x.shape[-1])
+        return "hadamard_rotate", rotate_unnormalised
+    if kind == "max_240":
+        return "E4M3_MAX", 240.0
+    if kind == "row_absmax":
+        def quantize_per_row(x, block=64, hadamard=False, signs=None, per_head=False):
+            y = fp8.hadamard_rotate(x, signs) if hadamard else fp8._f64(x)
+            amax = np.abs(y).max(axis=3, keepdims=True)
+            s = np.where(amax > 0, amax / 448.0, 1.0)
+            codes = fp8.e4m3_encode(fp8.round_to_e4m3(y / s))
+            return codes, s[:, :, ::block, 0]
+        return "quantize_fp8_blocks", quantize_per_row
+    raise ValueError(kind)
+
+
+def _fp8_pins_pass():
+    """Run the FP8 pins above against whatever the oracle's FP8 functions are."""
+    try:
+        for part in ("rotated", "plain"):
+            test_hand_worked_fp8_golden(part)
+        test_e4m3_grid_from_definition()
+        test_e4m3_rounding_ties_to_even_and_saturates()
+        test_sylvester_matches_scipy_and_is_orthogonal(128)
+        test_rotation_preserves_scores()
+        for hadamard in (False, True):
+            test_block_quantisation_properties(hadamard)
+        test_zero_block_gets_unit_scale()
+    except AssertionError:
+        return False
+    return True
+
+
+@pytest.mark.parametrize("kind", ["ties_away", "walsh_order", "no_sqrt_d", "max_240", "row_absmax"])
+def test_fp8_pins_reject_planted_mistakes(kind, monkeypatch):
+    assert _fp8_pins_pass()
+    name, value = _fp8_mutant(kind)
+    # the package re-exports the module's names: replace both, so that every caller sees it
+    monkeypatch.setattr(oracle.fp8, name, value)
+    monkeypatch.setattr(oracle, name, value)
+    assert not _fp8_pins_pass(), f"no pin caught the planted mistake {kind!r}"
 
 
 # ----------------------------------------------------------------------------- decode (N_q < N_k)
