@@ -345,6 +345,31 @@ def test_pins_reject_planted_mistakes(kind, monkeypatch):
     assert not _pins_pass(), f"no pin caught the planted mistake {kind!r}"
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_predictor_equal_scores_closed_form(causal):
+    # Q = 0 makes every visible score 0 and every weight 1.  V lies on the E4M3 grid in two
+    # 64-row blocks with absmax 224 and 112 (scales 1/2 and 1/4), so its codes decode to 2 V
+    # and 4 V, the second block's weights fold to exactly 1/2, the largest scale (1/2) comes
+    # back out at the end, and every product and sum is exact in fp64: O is the plain mean
+    # of the visible V rows and LSE = ln(count).
+    rng = np.random.default_rng(31)
+    grid = oracle.e4m3_decode(np.arange(256, dtype=np.uint8))
+    finite = grid[~np.isnan(grid)]
+    N, d = 128, 64
+    v = np.empty((N, d))
+    v[:64] = rng.choice(finite[np.abs(finite) <= 224.0], size=(64, d))
+    v[0, 0] = 224.0
+    v[64:] = rng.choice(finite[np.abs(finite) <= 112.0], size=(64, d))
+    v[64, 0] = -112.0
+    q = np.zeros((1, 1, N, d))
+    k = rng.standard_normal((1, 1, N, d))
+    o, lse = oracle.emulate_fp8_attention(q, k, v[None, None], 0.125, causal, False, round_p=True)
+    count = np.arange(1, N + 1) if causal else np.full(N, N)
+    want = np.stack([v[:c].sum(axis=0) / c for c in count])
+    assert np.array_equal(o[0, 0], want)
+    assert np.array_equal(lse[0, 0], np.log(count.astype(np.float64)))
+
+
 # ----------------------------------------------------------------------------- planted FP8 mistakes
 
 def _fp8_mutant(kind):
