@@ -501,3 +501,64 @@ def test_per_head_scale_is_the_largest_block_scale():
         # subnormal quantum 2^-9 times the scale
         bound = np.maximum(2.0 ** -4 * np.abs(y), 2.0 ** -10 * sh.max())
         assert (np.abs(deq - y) <= bound + 1e-12).all()
+
+
+# ----------------------------------------------------------------------------- the error metric
+
+def test_rel_rms_hand_worked():
+    """relRMS = ||x - ref||_F / ||ref||_F, worked by hand on 3-4-5 triangles."""
+    ref = np.array([3.0, 4.0])                                    # ||ref|| = 5
+    assert oracle.rel_rms(ref, ref) == 0.0
+    assert oracle.rel_rms(np.zeros(2), ref) == 1.0                # ||0 - ref|| / ||ref||
+    assert abs(oracle.rel_rms([3.3, 4.4], ref) - 0.1) < 1e-15     # error (0.3, 0.4): 0.5 / 5
+    assert abs(oracle.rel_rms([4.0, 4.0], ref) - 0.2) < 1e-15     # error (1, 0): 1 / 5
+    # the norm is that of ref, not of x: x = 2 ref gives ||ref|| / ||ref|| = 1 (not 5 / 10)
+    assert abs(oracle.rel_rms([6.0, 8.0], ref) - 1.0) < 1e-15
+    # one norm over all elements, not a mean of per-row ratios: rows of norm 5 and 1 with
+    # an error of 1 in the second row only give 1 / sqrt(26) (per-row mean: 0.5)
+    ref2 = np.array([[3.0, 4.0], [0.0, 1.0]])
+    x2 = np.array([[3.0, 4.0], [1.0, 1.0]])
+    assert abs(oracle.rel_rms(x2, ref2) - 1.0 / math.sqrt(26.0)) < 1e-15
+
+
+def test_rel_rms_scale_invariance_and_direction():
+    rng = np.random.default_rng(3)
+    ref = rng.standard_normal((4, 5, 6))
+    x = ref + 0.01 * rng.standard_normal(ref.shape)
+    r = oracle.rel_rms(x, ref)
+    assert abs(oracle.rel_rms(7.5 * x, 7.5 * ref) - r) < 1e-15
+    # x = ref (1 + eps) gives exactly eps
+    assert abs(oracle.rel_rms(ref * 1.25, ref) - 0.25) < 1e-15
+
+
+def _rel_rms_mutant(kind):
+    def rel_rms(x, ref):
+        x, ref = np.asarray(x, np.float64), np.asarray(ref, np.float64)
+        if kind == "norm_of_x":
+            return float(np.linalg.norm(x - ref) / np.linalg.norm(x))
+        if kind == "no_root":
+            return float(((x - ref) ** 2).sum() / (ref ** 2).sum())
+        if kind == "per_row":
+            rr = ref.reshape(-1, ref.shape[-1])
+            return float(np.mean(np.linalg.norm((x - ref).reshape(rr.shape), axis=1) / np.linalg.norm(rr, axis=1)))
+        if kind == "max_abs":
+            return float(np.abs(x - ref).max() / np.abs(ref).max())
+        raise ValueError(kind)
+    return rel_rms
+
+
+def _rel_rms_pins_pass():
+    try:
+        test_rel_rms_hand_worked()
+        test_rel_rms_scale_invariance_and_direction()
+    except AssertionError:
+        return False
+    return True
+
+
+@pytest.mark.parametrize("kind", ["norm_of_x", "no_root", "per_row", "max_abs"])
+def test_rel_rms_pins_reject_planted_mistakes(kind, monkeypatch):
+    assert _rel_rms_pins_pass()
+    monkeypatch.setattr(oracle_attention_mod, "rel_rms", _rel_rms_mutant(kind))
+    monkeypatch.setattr(oracle, "rel_rms", _rel_rms_mutant(kind))
+    assert not _rel_rms_pins_pass(), f"no pin caught the planted mistake {kind!r}"
