@@ -21,6 +21,28 @@ against the predictor's (same dequantised scores): the median row within 1e-4;
 the tail is looser because a few codes per head fall on near-ties that the
 kernel and the oracle break differently, and one such code on an outlier
 coordinate moves a dominant score by a few hundredths.
+
+That comparison alone is loose: an independent kernel error of up to about
+0.038 relative RMS (a wrong V block scale, a P fold off by a constant) would
+hide inside 1.1x the predictor's distance.  So the kernel is also checked
+element by element against a CPU replay of its own roundings
+(``fp8_replay.py``) on E4M3 codes that the oracle's quantiser made on the CPU and
+both sides read.  What separates the two is then only:
+
+* the final bf16 rounding of O, at most half a bf16 ulp per element (about 1e-3
+  relative RMS);
+* the fp32 arithmetic of the exponent, of ex2 and of the MMA accumulation,
+  relative 1e-6 to 1e-5 on each weight: at most 2^-12 of W_ic, the magnitude
+  sum_j |P~_ij| |v_jc| s_v,max / l_i behind the element;
+* where that fp32 error moves a weight's E4M3 rounding to the neighbouring code
+  (its exact value lies within about 1e-5 relative of a midpoint, a few in 10^5
+  weights), one E4M3 step of that weight, at most 2^-3 of its share of W_ic.
+
+The bounds: relative RMS over the heads <= 3e-3; at most 1e-3 of the elements
+beyond half an ulp + 2^-12 W_ic, none beyond half an ulp + 2^-3 W_ic; the LSE (a
+sum of unrounded weights) within 1e-5 at the median row and 1e-3 at worst.  The
+CPU tests of the replay show that a V block scale 5 % off, or P scaled by 1.01,
+fails these by a wide margin while passing the comparison above.
 """
 import math
 
@@ -30,6 +52,7 @@ import torch
 
 import oracle
 from fa_inputs import WORKLOADS, make_inputs, make_qkv, make_sign_flips
+from fp8_replay import quantize_for_both, replay_fp8_attention
 
 pytestmark = pytest.mark.gpu
 
@@ -176,3 +199,90 @@ def test_fp8_randomised_rotation_and_per_head_v_track_the_predictor(gpu_lib):
     got, want = oracle.rel_rms(o.float().cpu().numpy(), ro), oracle.rel_rms(pred_o, ro)
     assert got <= 1.1 * want + 2e-3, f"{got:.4f} vs predicted {want:.4f}"
     assert np.median(np.abs(lse.cpu().numpy() - pred_lse)) < 1e-4
+
+
+# ----------------------------------------------------------------------------- element-wise vs the replay
+
+REPLAY_REL = 3e-3           # relative RMS, kernel vs replay
+W_SLACK = 2.0 ** -12        # fp32 arithmetic, per element, as a fraction of W
+FLIP_SLACK = 2.0 ** -3      # one E4M3 step of a weight, as a fraction of W
+FLIP_FRACTION = 1e-3        # share of elements allowed past the fp32 slack
+
+
+def _bf16_half_ulp(x):
+    a = np.maximum(np.abs(x), 2.0 ** -126)
+    _, e2 = np.frexp(a)
+    return np.exp2(e2 - 1 - 7 - 1)
+
+
+def _oracle_codes(q, k, v, hadamard):
+    q8, qs = quantize_for_both(q, hadamard)
+    k8, ks = quantize_for_both(k, hadamard)
+    v8, vs = quantize_for_both(v, False)
+    return q8, k8, v8, qs, ks, vs
+
+
+def _gpu_on_codes(fa, codes, causal, hadamard):
+    q8, k8, v8, qs, ks, vs = codes
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    o, lse = fa.attention_fp8(t(q8), t(k8), t(np.swapaxes(v8, -1, -2)), t(qs), t(ks), t(vs), causal=causal,
+                              hadamard=hadamard)
+    torch.cuda.synchronize()
+    st, bits = fa.last_device_status()
+    assert st == fa.FA_OK, f"device status {bits:#x}"
+    return o.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def _assert_tracks_replay(o, lse, ro, rl, w, what):
+    assert np.isfinite(o).all() and np.isfinite(lse).all(), what
+    err = np.abs(o - ro)
+    hb = _bf16_half_ulp(ro)
+    rel = oracle.rel_rms(o, ro)
+    past = float((err > hb + W_SLACK * w).mean())
+    worst = float(((err - hb) / np.maximum(w, 1e-30)).max())
+    dl = np.abs(lse - rl)
+    msg = (f"{what}: relRMS vs replay {rel:.2e}, share past fp32 slack {past:.2e}, worst (|dO|-hulp)/W "
+           f"{worst:.2e}, LSE median {np.median(dl):.2e} max {dl.max():.2e}")
+    assert rel <= REPLAY_REL, msg
+    assert past <= FLIP_FRACTION, msg
+    assert worst <= FLIP_SLACK, msg
+    assert np.median(dl) <= 1e-5 and dl.max() <= 1e-3, msg
+
+
+@pytest.mark.parametrize("N,causal", [(128, False), (208, True), (512, True), (1040, False), (2048, True)])
+@pytest.mark.parametrize("hadamard", [False, True])
+def test_fp8_kernel_tracks_the_replay_elementwise(gpu_lib, N, causal, hadamard):
+    q, k, v = make_qkv((1, 2, N, 128), torch.bfloat16, 30 + N, outliers=True)
+    codes = _oracle_codes(q, k, v, hadamard)
+    o, lse = _gpu_on_codes(gpu_lib, codes, causal, hadamard)
+    ro, rl, w = replay_fp8_attention(*codes, 1 / math.sqrt(128), causal)
+    _assert_tracks_replay(o, lse, ro, rl, w, f"N={N} causal={causal} hadamard={hadamard}")
+
+
+def test_fp8_workload_tracks_the_replay_elementwise(gpu_lib):
+    """The fp8 workload at full size, in the launch the benchmark times; the first and
+    the last head are replayed."""
+    w = WORKLOADS["fp8"]
+    q, k, v = make_inputs(w)
+    codes = _oracle_codes(q, k, v, True)
+    o, lse = _gpu_on_codes(gpu_lib, codes, False, True)
+    for (b, h) in [(0, 0), (w.B - 1, w.H - 1)]:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ro, rl, ww = replay_fp8_attention(*(c[sl] for c in codes), w.scale, False)
+        _assert_tracks_replay(o[sl], lse[sl], ro, rl, ww, f"fp8 workload head ({b},{h})")
+
+
+@pytest.mark.parametrize("chunks", [0, 3])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_host_end_to_end_matches_the_device_path_bitwise(gpu_lib, chunks, causal):
+    # quantising per chunk of heads changes nothing: every block scale is per (b, h)
+    q, k, v = (t.pin_memory() for t in make_qkv((2, 3, 320, 128), torch.bfloat16, 15, outliers=True))
+    o, lse = gpu_lib.attention_fp8_host(q, k, v, causal=causal, hadamard=True, chunks=chunks)
+    assert o.device.type == "cpu" and o.dtype == torch.bfloat16
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    q8, qs = gpu_lib.quantize_fp8(qd, hadamard=True)
+    k8, ks = gpu_lib.quantize_fp8(kd, hadamard=True)
+    v8, vs = gpu_lib.quantize_fp8(vd, transpose_out=True)
+    od, ld = gpu_lib.attention_fp8(q8, k8, v8, qs, ks, vs, causal=causal, hadamard=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o, od.cpu()) and torch.equal(lse, ld.cpu())
