@@ -27,6 +27,17 @@
  *     detected on the host before any device work is enqueued.
  *   - Causal masking is top-left aligned: query row i sees keys 0..i.
  *   - Supported: B, H, N >= 1; d in {64, 128}; B*H*N*d < 2^40.
+ *   - Every pipeline wait inside a kernel is bounded (2 s by default, the
+ *     environment variable FA_TIMEOUT_MS overrides it).  A kernel whose wait gives
+ *     up sets a bit in the device status word and leaves early: its outputs are
+ *     then UNDEFINED, yet the call that launched it has already returned FA_OK.
+ *     Callers that must know call fa_last_device_status after the work they care
+ *     about (it synchronises and returns FA_ERR_DEVICE_TIMEOUT if any wait gave up).
+ *   - Per-device state (the status word's address, fa_decode_noalloc's scratch
+ *     address, fa_fwd_host's copy streams) is looked up once per device in the
+ *     context current at the first call, normally the device's primary context.
+ *     Do not call the library after cudaDeviceReset, or from another context on
+ *     a device it has already been used on.
  */
 #ifndef FA_GB300_H_
 #define FA_GB300_H_
@@ -135,6 +146,30 @@ int fa_quantize_fp8_ex(const void* x, void* x8, float* scale, int B, int H, int 
 int fa_fwd_fp8(const void* q8, const void* k8, const void* v8t, void* o, float* lse, int B, int H,
                int N, int d, float scale, int causal, const float* q_scale, const float* k_scale,
                const float* v_scale, int hadamard, void* stream);
+
+/*
+ * The FP8 mode end to end on HOST buffers: bf16 Q, K, V in, bf16 O (and LSE) out.  On the
+ * device, each chunk of heads runs the whole FP8 path of the news piece ("Drei
+ * technische Hebel", item 3): fa_quantize_fp8 of Q and K (rotated when `hadamard` is 1),
+ * of V (transposed, never rotated), then fa_fwd_fp8.  The copies of one chunk overlap
+ * the computation of the next, as in fa_fwd_host (a runtime convenience).
+ *   q, k, v, o : [B, H, N, d] bfloat16 in host memory (pinned lets the copies overlap)
+ *   lse        : [B, H, N] float32 in host memory, or NULL
+ *   hadamard   : 0 or 1
+ *   chunks     : number of head chunks (0 picks 8; at most 32 and B*H)
+ *   workspace  : DEVICE scratch of at least fa_fwd_fp8_host_workspace_size() bytes,
+ *                256-byte aligned, owned by the caller; calls sharing one workspace must
+ *                be on one stream
+ * Supported: d == 128, N % 16 == 0.  Asynchronous like fa_fwd_host; errors as
+ * fa_fwd_fp8 and fa_quantize_fp8, plus FA_ERR_WORKSPACE.
+ */
+int fa_fwd_fp8_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                    int d, float scale, int causal, int hadamard, int chunks, void* workspace,
+                    unsigned long long workspace_bytes, void* stream);
+
+/* Device scratch fa_fwd_fp8_host needs: the bf16 inputs and output, the E4M3 codes, the
+ * block scales and the LSE, 256-byte aligned each. */
+int fa_fwd_fp8_host_workspace_size(int B, int H, int N, int d, unsigned long long* bytes);
 
 /*
  * Attention of a few query rows against a long key cache (one decode step): the
@@ -248,6 +283,11 @@ int fa_debug_inject_stall(int load_index, int timeout_ms);
 
 /* Library ABI version (major * 10000 + minor * 100 + patch). */
 int fa_version(void);
+
+/* Identity of the sources this library was compiled from: 16 hex digits of a SHA-256
+ * over the CUDA sources, this header, the build script and the compiler flags
+ * ("unknown" if built without the build script).  Static storage, never NULL. */
+const char* fa_build_id(void);
 
 #ifdef __cplusplus
 }

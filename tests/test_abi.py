@@ -35,13 +35,28 @@ def test_header_declares_the_boundary():
                                   "fa_last_device_status", "fa_debug_inject_stall", "fa_version",
                                   "fa_decode", "fa_decode_workspace_size", "fa_decode_noalloc",
                                   "fa_bwd", "fa_bwd_workspace_size", "fa_quantize_fp8_ex",
-                                  "fa_fwd_host", "fa_fwd_host_workspace_size"])
+                                  "fa_fwd_host", "fa_fwd_host_workspace_size", "fa_fwd_fp8_host",
+                                  "fa_fwd_fp8_host_workspace_size", "fa_build_id"])
 
 
 def test_every_declared_symbol_is_exported(lib):
     for name in _declared():
         assert hasattr(lib, name), name
     assert sorted(fa.exported_symbols()) == _declared()
+
+
+def test_library_carries_the_build_id_of_these_sources(lib, tmp_path, capsys):
+    from transformer_attention_flashattention_gb300 import _build
+    sid = _build.source_id()
+    assert lib.fa_build_id().decode() == sid == _build.built_id()
+    _build.build()                                  # up to date: nothing is compiled
+    assert "up to date" in capsys.readouterr().out
+    # a library file carrying another id is stale; one with no id at all too
+    other = tmp_path / "libfa.so"
+    other.write_bytes(b"\x7fELF..." + _build.BUILD_ID_TAG + b"0123456789abcdef" + b"\0")
+    assert _build.built_id(str(other)) == "0123456789abcdef" != sid
+    other.write_bytes(b"\x7fELF...")
+    assert _build.built_id(str(other)) is None
 
 
 def test_strerror_and_version(lib):
@@ -101,6 +116,23 @@ def test_decode_noalloc_rejects_bad_shapes_on_the_host(lib, Nq, Nk, d, want):
     assert lib.fa_decode_noalloc(A, A, A, A, None, 1, 1, Nq, Nk, d, 0.125, 0, 1, 0, None) == want
 
 
+def test_decode_noalloc_checks_arguments_before_the_scratch_limit(lib):
+    """With a num_splits far past the scratch area, a call that is also malformed reports
+    what fa_decode would report, not FA_ERR_WORKSPACE."""
+    call = lambda q=A, o=A, lse=0, scale=0.125, causal=0, dtype=1: lib.fa_decode_noalloc(
+        q or None, A, A, o or None, lse or None, 1, 1, 1, 128, 64, scale, causal, dtype, 1 << 20, None)
+    assert call(q=0) == fa.FA_ERR_NULL
+    assert call(o=0) == fa.FA_ERR_NULL
+    assert call(dtype=9) == fa.FA_ERR_UNSUPPORTED
+    assert call(causal=2) == fa.FA_ERR_UNSUPPORTED
+    assert call(scale=float("inf")) == fa.FA_ERR_UNSUPPORTED
+    assert call(scale=0.0) == fa.FA_ERR_UNSUPPORTED
+    assert call(q=A + 8) == fa.FA_ERR_ALIGN
+    assert call(lse=A + 2) == fa.FA_ERR_ALIGN
+    # fa_decode checks the shape before the scale
+    assert lib.fa_decode_noalloc(A, A, A, A, None, 1, 1, 0, 128, 64, 0.0, 0, 1, 1 << 20, None) == fa.FA_ERR_SHAPE
+
+
 def test_bwd_rejects_bad_arguments_on_the_host(lib):
     args = [A] * 9
     ws = 0x100000
@@ -137,3 +169,23 @@ def test_fwd_host_rejects_bad_arguments_on_the_host(lib):
     assert call(chunks=-1) == fa.FA_ERR_UNSUPPORTED
     assert call(dtype=5) == fa.FA_ERR_UNSUPPORTED
     assert call(d=80) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_fwd_fp8_host_rejects_bad_arguments_on_the_host(lib):
+    n = ctypes.c_ulonglong(0)
+    assert lib.fa_fwd_fp8_host_workspace_size(2, 3, 96, 128, ctypes.byref(n)) == fa.FA_OK
+    r = lambda x: (x + 255) // 256 * 256
+    e = 2 * 3 * 96 * 128
+    assert n.value == 4 * r(2 * e) + 3 * r(e) + 3 * r(4 * 2 * 3 * 2) + r(4 * 2 * 3 * 96)
+    assert lib.fa_fwd_fp8_host_workspace_size(2, 3, 96, 64, ctypes.byref(n)) == fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_fwd_fp8_host_workspace_size(2, 3, 100, 128, ctypes.byref(n)) == fa.FA_ERR_SHAPE
+    ws = 0x100000
+    call = lambda wsp=ws, wsb=1 << 30, chunks=0, had=1, causal=0, N=96, q=A: lib.fa_fwd_fp8_host(
+        q or None, A, A, A, None, 2, 3, N, 128, 0.125, causal, had, chunks, wsp, wsb, None)
+    assert call(q=0) == fa.FA_ERR_NULL
+    assert call(wsb=1024) == fa.FA_ERR_WORKSPACE
+    assert call(wsp=ws + 64) == fa.FA_ERR_ALIGN
+    assert call(chunks=-1) == fa.FA_ERR_UNSUPPORTED
+    assert call(had=2) == fa.FA_ERR_UNSUPPORTED
+    assert call(causal=3) == fa.FA_ERR_UNSUPPORTED
+    assert call(N=100) == fa.FA_ERR_SHAPE

@@ -22,6 +22,7 @@ __all__ = [
     "exported_symbols",
     "attention",
     "attention_host",
+    "attention_fp8_host",
     "quantize_fp8",
     "attention_fp8",
     "decode",
@@ -75,9 +76,13 @@ _SIGNATURES = {
     "fa_bwd_workspace_size": (_i, [_i, _i, _i, _i, ctypes.POINTER(ctypes.c_ulonglong)]),
     "fa_fwd_host": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _i, _vp, ctypes.c_ulonglong, _vp]),
     "fa_fwd_host_workspace_size": (_i, [_i, _i, _i, _i, ctypes.POINTER(ctypes.c_ulonglong)]),
+    "fa_fwd_fp8_host": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _i, _vp, ctypes.c_ulonglong,
+                             _vp]),
+    "fa_fwd_fp8_host_workspace_size": (_i, [_i, _i, _i, _i, ctypes.POINTER(ctypes.c_ulonglong)]),
     "fa_strerror": (ctypes.c_char_p, [_i]),
     "fa_last_device_status": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),
     "fa_debug_inject_stall": (_i, [_i, _i]),
+    "fa_build_id": (ctypes.c_char_p, []),
     "fa_version": (_i, []),
 }
 
@@ -109,6 +114,13 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
+    # the in-tree library must be built from the sources as they are now
+    if path == library_path() and os.path.isdir(os.path.join(_PKG_DIR, "csrc")):
+        from . import _build
+        have, want = lib.fa_build_id().decode(), _build.source_id()
+        if have != want:
+            raise RuntimeError(f"libfa.so carries build id {have}, but the sources are {want}: rebuild it "
+                               "with `python -m transformer_attention_flashattention_gb300._build`")
     _LIB = lib
     return lib
 
@@ -150,11 +162,17 @@ def _check_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor):
 def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
               scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
               lse: Optional[torch.Tensor] = None, return_lse: bool = True,
-              stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+              stream: Optional[torch.cuda.Stream] = None,
+              check: bool = False) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """O = softmax(scale * Q K^T [+ causal mask]) V and the natural-log LSE.
 
     q, k, v: contiguous CUDA tensors [B, H, N, d], float16 or bfloat16, d in {64, 128}.
     Returns (O [B, H, N, d] of q's dtype, LSE [B, H, N] float32 or None).
+
+    The kernel's pipeline waits are bounded.  One that gives up (a stalled or heavily
+    preempted GPU) leaves O and LSE undefined while the call itself still succeeds;
+    only the device status word records it.  ``check=True`` synchronises the stream
+    after the launch and raises ``FAError(FA_ERR_DEVICE_TIMEOUT)`` if the word is set.
     """
     lib = load_library()
     _check_qkv(q, k, v)
@@ -170,6 +188,9 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = 
     st = lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, float(scale),
                     int(bool(causal)), _DTYPES[q.dtype], _stream_handle(stream, q.device))
     _check(st, "fa_fwd")
+    if check:
+        with torch.cuda.device(q.device):
+            _check(lib.fa_last_device_status(_stream_handle(stream, q.device), None), "fa_fwd (device status)")
     return out, lse
 
 
@@ -215,13 +236,53 @@ def attention_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bo
     return out, lse_out
 
 
+def attention_fp8_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+                       scale: Optional[float] = None, hadamard: bool = True,
+                       device: Optional[torch.device] = None, stream: Optional[torch.cuda.Stream] = None,
+                       out: Optional[torch.Tensor] = None, lse_out: Optional[torch.Tensor] = None,
+                       chunks: int = 0):
+    """The FP8 mode end to end on bf16 HOST tensors through ``fa_fwd_fp8_host``: the
+    library copies Q, K, V to the GPU, quantises them there (Q and K rotated when
+    ``hadamard``), runs the E4M3 forward and copies the bf16 O and the LSE back, chunk
+    by chunk.  Returns host tensors (``out``/``lse_out`` if given)."""
+    lib = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.is_cuda or t.dim() != 4 or t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bfloat16 host tensor shaped like q")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    pin = q.is_pinned()
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=pin)
+    if lse_out is None:
+        lse_out = torch.empty((B, H, N), dtype=torch.float32, pin_memory=pin)
+    need = ctypes.c_ulonglong(0)
+    _check(lib.fa_fwd_fp8_host_workspace_size(B, H, N, d, ctypes.byref(need)), "fa_fwd_fp8_host_workspace_size")
+    ws = _HOST_WS.get(dev)
+    if ws is None or ws.numel() < need.value:
+        ws = torch.empty(need.value, device=dev, dtype=torch.uint8)
+        _HOST_WS[dev] = ws
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        st = lib.fa_fwd_fp8_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse_out), B, H, N, d, float(scale),
+                                 int(bool(causal)), int(bool(hadamard)), int(chunks), _ptr(ws), ws.numel(),
+                                 s.cuda_stream)
+    _check(st, "fa_fwd_fp8_host")
+    s.synchronize()
+    return out, lse_out
+
+
 def quantize_fp8(x: torch.Tensor, hadamard: bool = False, transpose_out: bool = False,
                  stream: Optional[torch.cuda.Stream] = None, sign_flips: int = 0,
-                 per_head: bool = False) -> Tuple[torch.Tensor, torch.Tensor]:
+                 per_head: bool = False,
+                 out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Block absmax E4M3 quantisation of bf16 ``x [B,H,N,d]`` (optionally Hadamard-rotated).
 
     ``sign_flips`` (an integer bit mask, bit c negates coordinate c before the
     rotation) randomises the rotation; ``per_head`` takes one scale per (b, h).
+    ``out`` = (codes, scales) to write into instead of new tensors.
     Returns (codes as uint8 [B,H,N,d] or [B,H,d,N] when transposed, scales fp32 [B,H,ceil(N/64)]).
     """
     lib = load_library()
@@ -229,8 +290,14 @@ def quantize_fp8(x: torch.Tensor, hadamard: bool = False, transpose_out: bool = 
         raise ValueError("x must be a contiguous CUDA bfloat16 tensor [B, H, N, d]")
     B, H, N, d = x.shape
     shape = (B, H, d, N) if transpose_out else (B, H, N, d)
-    x8 = torch.empty(shape, device=x.device, dtype=torch.uint8)
-    sc = torch.empty((B, H, (N + 63) // 64), device=x.device, dtype=torch.float32)
+    if out is not None:
+        x8, sc = out
+        if (tuple(x8.shape) != shape or x8.dtype != torch.uint8 or tuple(sc.shape) != (B, H, (N + 63) // 64)
+                or sc.dtype != torch.float32 or not x8.is_contiguous() or not sc.is_contiguous()):
+            raise ValueError("out must be (uint8 codes, float32 scales) shaped for x")
+    else:
+        x8 = torch.empty(shape, device=x.device, dtype=torch.uint8)
+        sc = torch.empty((B, H, (N + 63) // 64), device=x.device, dtype=torch.float32)
     if sign_flips or per_head:
         if not 0 <= int(sign_flips) < (1 << 128):
             raise ValueError("sign_flips must be a 128-bit mask")

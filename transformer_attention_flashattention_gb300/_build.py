@@ -4,9 +4,16 @@ Each translation unit is compiled in parallel into ``_build/``, then linked with
 the static CUDA runtime into ``transformer_attention_flashattention_gb300/libfa.so``.
 No libcuda link: the tensor-map encoder is fetched from the driver at run time.
 Run as ``python -m transformer_attention_flashattention_gb300._build``.
+
+The library carries the SHA-256 (first 16 hex digits) of everything it is built
+from: the CUDA sources, the C header, this script and the compiler flags.  It is
+compiled into ``libfa.so`` as a string and returned by ``fa_build_id()``.  A
+library is rebuilt unless it carries the id of the sources as they are now, and
+the binding refuses to load one that does not.
 """
 from __future__ import annotations
 
+import hashlib
 import os
 import shutil
 import subprocess
@@ -40,11 +47,35 @@ def _deps():
     return files
 
 
+BUILD_ID_TAG = b"fa-build-id:"
+
+
+def source_id() -> str:
+    """Hash of the sources, header, this script and the flags the library is built from."""
+    h = hashlib.sha256()
+    for f in sorted(_deps()):
+        h.update(os.path.relpath(f, ROOT).encode() + b"\0")
+        with open(f, "rb") as fh:
+            h.update(fh.read() + b"\0")
+    h.update(" ".join(ARCH_FLAGS + CFLAGS).encode())
+    return h.hexdigest()[:16]
+
+
+def built_id(path: str = LIB_PATH):
+    """The build id a library file carries (read from its bytes, without loading it), or None."""
+    try:
+        with open(path, "rb") as f:
+            data = f.read()
+    except OSError:
+        return None
+    i = data.find(BUILD_ID_TAG)
+    if i < 0:
+        return None
+    return data[i + len(BUILD_ID_TAG):i + len(BUILD_ID_TAG) + 16].decode("ascii", "replace")
+
+
 def _stale() -> bool:
-    if not os.path.exists(LIB_PATH):
-        return True
-    t = os.path.getmtime(LIB_PATH)
-    return any(os.path.getmtime(f) > t for f in _deps())
+    return built_id() != source_id()
 
 
 def _compile(src: str, extra) -> str:
@@ -56,12 +87,16 @@ def _compile(src: str, extra) -> str:
     return obj
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link libfa.so if any source is newer than it; returns its path."""
-    if not force and not _stale():
+def build(force: bool = False, verbose: bool = False, extra_flags=(), quiet: bool = False) -> str:
+    """Compile and link libfa.so unless it already carries the current sources' build id;
+    returns its path and says (unless ``quiet``) whether it compiled."""
+    sid = source_id()
+    if not force and not extra_flags and built_id() == sid:
+        if not quiet:
+            print(f"libfa.so: up to date (build id {sid})", flush=True)
         return LIB_PATH
     os.makedirs(BUILD_DIR, exist_ok=True)
-    extra = list(extra_flags) + (["-Xptxas", "-v"] if verbose else [])
+    extra = list(extra_flags) + (["-Xptxas", "-v"] if verbose else []) + [f'-DFA_BUILD_ID="{sid}"']
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(lambda s: _compile(s, extra), SOURCES))
     tmp = LIB_PATH + ".tmp"
@@ -70,6 +105,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB_PATH)
+    if not quiet:
+        print(f"libfa.so: compiled {len(SOURCES)} translation units (build id {sid})", flush=True)
     return LIB_PATH
 
 

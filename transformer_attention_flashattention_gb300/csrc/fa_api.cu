@@ -328,6 +328,8 @@ void decode_split(int BH, int Nq, int Nk, int d, int requested, int sm_count, in
   *splits = shape(1, chunk);
 }
 
+}  // namespace
+
 int check_decode(int B, int H, int Nq, int Nk, int d) {
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_SHAPE;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
@@ -337,7 +339,6 @@ int check_decode(int B, int H, int Nq, int Nk, int d) {
   return FA_OK;
 }
 
-}  // namespace
 }  // namespace fa
 
 extern "C" int fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits,
@@ -499,3 +500,11 @@ extern "C" const char* fa_strerror(int status) {
 }
 
 extern "C" int fa_version(void) { return 100; }
+
+#ifndef FA_BUILD_ID
+#define FA_BUILD_ID "unknown"
+#endif
+// The tag lets the build script read the id from the file without loading it.
+static const char kBuildIdTagged[] = "fa-build-id:" FA_BUILD_ID;
+
+extern "C" const char* fa_build_id(void) { return kBuildIdTagged + 12; }

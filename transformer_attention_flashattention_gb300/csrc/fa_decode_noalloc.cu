@@ -5,9 +5,12 @@
 // caller-provided workspace; everything else is fa_decode, called unchanged.
 #include <cuda_runtime.h>
 
+#include <cmath>
+#include <cstdint>
 #include <mutex>
 
 #include "fa.h"
+#include "fa_launch.h"
 
 namespace {
 
@@ -38,8 +41,19 @@ int scratch_address(void** addr) {
 extern "C" int fa_decode_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                                  int H, int Nq, int Nk, int d, float scale, int causal, int dtype,
                                  int num_splits, void* stream) {
+  // fa_decode's own argument checks, in its order, so that a bad call returns the code
+  // fa_decode would return rather than FA_ERR_WORKSPACE (and does no device set-up)
+  if (!q || !k || !v || !o) return FA_ERR_NULL;
+  if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+  if (causal != 0 && causal != 1) return FA_ERR_UNSUPPORTED;
+  int st = fa::check_decode(B, H, Nq, Nk, d);
+  if (st != FA_OK) return st;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_UNSUPPORTED;
+  auto misaligned = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; };
+  if (misaligned(q, 16) || misaligned(k, 16) || misaligned(v, 16) || misaligned(o, 16) || (lse && misaligned(lse, 4)))
+    return FA_ERR_ALIGN;
   unsigned long long need = 0;
-  int st = fa_decode_workspace_size(B, H, Nq, Nk, d, num_splits, &need);
+  st = fa_decode_workspace_size(B, H, Nq, Nk, d, num_splits, &need);
   if (st != FA_OK) return st;
   if (need > FA_DECODE_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
   // the look-up runs on the first call on a device whatever `need` is, so that

@@ -1,5 +1,5 @@
-// fa_fwd_host: the attention forward on HOST buffers, with the host<->device copies
-// overlapped with the computation.
+// fa_fwd_host and fa_fwd_fp8_host: the attention forward on HOST buffers, with the
+// host<->device copies overlapped with the computation.
 //
 // The heads are cut into chunks.  Chunk c's Q, K, V go to the device on one copy
 // stream, its fa_fwd runs on the caller's stream once they have landed, and its O
@@ -7,7 +7,8 @@
 // c+1 in while chunk c computes and chunk c-1 goes out, so a call costs about one
 // pass of the inputs over the link instead of inputs + compute + outputs in a row.
 // The device copies live in a caller-provided workspace; the copy streams and
-// events are created once per device and reused.
+// events are created once per device and reused.  The FP8 variant runs the E4M3
+// prologue (three quantisation launches) and the E4M3 forward on each chunk.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -58,6 +59,53 @@ int engine(CopyEngine** out) {
 
 unsigned long long round256(unsigned long long x) { return (x + 255) / 256 * 256; }
 
+// The chunked schedule shared by both entry points.  `compute(h0, hn)` enqueues the
+// work on heads h0 .. h0+hn-1 on the caller's stream, after their inputs landed; the
+// three inputs are `in_bytes` per head from the host to `dev_in[i]`, and `out_bytes` per
+// head of O (plus N floats of LSE when `lse`) come back from `dev_o` / `dev_lse`.
+template <class Compute>
+int run_chunked(const void* const host_in[3], uint8_t* const dev_in[3], unsigned long long in_bytes,
+                void* host_o, const uint8_t* dev_o, unsigned long long out_bytes, float* host_lse,
+                const float* dev_lse, long long BH, int N, int chunks, cudaStream_t s, Compute compute) {
+  int nc = chunks == 0 ? kAutoChunks : chunks;
+  if (nc > kMaxChunks) nc = kMaxChunks;
+  if (nc > BH) nc = static_cast<int>(BH);
+  const long long per_chunk = (BH + nc - 1) / nc;
+  // one call's enqueue at a time per process: the events are shared
+  std::lock_guard<std::mutex> lock(g_host_mu);
+  CopyEngine* e = nullptr;
+  int st = engine(&e);
+  if (st != FA_OK) return st;
+  // the workspace may still be in use by earlier work on the caller's stream
+  if (cudaEventRecord(e->start, s) != cudaSuccess || cudaStreamWaitEvent(e->h2d, e->start, 0) != cudaSuccess)
+    return FA_ERR_CUDA;
+  for (int c = 0; c < nc; ++c) {
+    const long long h0 = c * per_chunk;
+    const long long hn = BH - h0 < per_chunk ? BH - h0 : per_chunk;
+    if (hn <= 0) break;
+    for (int i = 0; i < 3; ++i)
+      if (cudaMemcpyAsync(dev_in[i] + h0 * in_bytes, static_cast<const uint8_t*>(host_in[i]) + h0 * in_bytes,
+                          hn * in_bytes, cudaMemcpyHostToDevice, e->h2d) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (cudaEventRecord(e->in[c], e->h2d) != cudaSuccess || cudaStreamWaitEvent(s, e->in[c], 0) != cudaSuccess)
+      return FA_ERR_CUDA;
+    st = compute(h0, hn);
+    if (st != FA_OK) return st;
+    if (cudaEventRecord(e->computed[c], s) != cudaSuccess ||
+        cudaStreamWaitEvent(e->d2h, e->computed[c], 0) != cudaSuccess ||
+        cudaMemcpyAsync(static_cast<uint8_t*>(host_o) + h0 * out_bytes, dev_o + h0 * out_bytes, hn * out_bytes,
+                        cudaMemcpyDeviceToHost, e->d2h) != cudaSuccess)
+      return FA_ERR_CUDA;
+    if (host_lse && cudaMemcpyAsync(host_lse + h0 * N, dev_lse + h0 * N, static_cast<size_t>(hn) * N * sizeof(float),
+                                    cudaMemcpyDeviceToHost, e->d2h) != cudaSuccess)
+      return FA_ERR_CUDA;
+  }
+  // the caller's stream resumes once the last result is on the host
+  if (cudaEventRecord(e->out_done, e->d2h) != cudaSuccess || cudaStreamWaitEvent(s, e->out_done, 0) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
+}
+
 }  // namespace
 
 extern "C" int fa_fwd_host_workspace_size(int B, int H, int N, int d, unsigned long long* bytes) {
@@ -83,57 +131,76 @@ extern "C" int fa_fwd_host(const void* q, const void* k, const void* v, void* o,
       !(scale > 0.f) || !(scale < 3.4e38f))
     return FA_ERR_UNSUPPORTED;
   const long long BH = static_cast<long long>(B) * H;
-  int nc = chunks == 0 ? kAutoChunks : chunks;
-  if (nc > kMaxChunks) nc = kMaxChunks;
-  if (nc > BH) nc = static_cast<int>(BH);
-  const long long per_chunk = (BH + nc - 1) / nc;
-
   const unsigned long long head_bytes = 2ull * N * d;
   const unsigned long long tensor_bytes = round256(BH * head_bytes);
   uint8_t* base = static_cast<uint8_t*>(workspace);
-  uint8_t* dq = base;
-  uint8_t* dk = base + tensor_bytes;
-  uint8_t* dv = base + 2 * tensor_bytes;
+  uint8_t* const dev_in[3] = {base, base + tensor_bytes, base + 2 * tensor_bytes};
   uint8_t* dO = base + 3 * tensor_bytes;
   float* dl = reinterpret_cast<float*>(base + 4 * tensor_bytes);
-  const uint8_t* hq = static_cast<const uint8_t*>(q);
-  const uint8_t* hk = static_cast<const uint8_t*>(k);
-  const uint8_t* hv = static_cast<const uint8_t*>(v);
-  uint8_t* ho = static_cast<uint8_t*>(o);
+  const void* const host_in[3] = {q, k, v};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return run_chunked(host_in, dev_in, head_bytes, o, dO, head_bytes, lse, dl, BH, N, chunks, s,
+                     [&](long long h0, long long hn) {
+                       const unsigned long long off = static_cast<unsigned long long>(h0) * head_bytes;
+                       return fa_fwd(dev_in[0] + off, dev_in[1] + off, dev_in[2] + off, dO + off,
+                                     lse ? dl + h0 * N : nullptr, 1, static_cast<int>(hn), N, d, scale, causal,
+                                     dtype, s);
+                     });
+}
 
-  // one call's enqueue at a time per process: the events are shared
-  std::lock_guard<std::mutex> lock(g_host_mu);
-  CopyEngine* e = nullptr;
-  st = engine(&e);
-  if (st != FA_OK) return st;
-  // the workspace may still be in use by earlier work on the caller's stream
-  if (cudaEventRecord(e->start, s) != cudaSuccess || cudaStreamWaitEvent(e->h2d, e->start, 0) != cudaSuccess)
-    return FA_ERR_CUDA;
-  for (int c = 0; c < nc; ++c) {
-    const long long h0 = c * per_chunk;
-    const long long hn = BH - h0 < per_chunk ? BH - h0 : per_chunk;
-    if (hn <= 0) break;
-    const unsigned long long off = static_cast<unsigned long long>(h0) * head_bytes;
-    const unsigned long long len = static_cast<unsigned long long>(hn) * head_bytes;
-    if (cudaMemcpyAsync(dq + off, hq + off, len, cudaMemcpyHostToDevice, e->h2d) != cudaSuccess ||
-        cudaMemcpyAsync(dk + off, hk + off, len, cudaMemcpyHostToDevice, e->h2d) != cudaSuccess ||
-        cudaMemcpyAsync(dv + off, hv + off, len, cudaMemcpyHostToDevice, e->h2d) != cudaSuccess ||
-        cudaEventRecord(e->in[c], e->h2d) != cudaSuccess || cudaStreamWaitEvent(s, e->in[c], 0) != cudaSuccess)
-      return FA_ERR_CUDA;
-    st = fa_fwd(dq + off, dk + off, dv + off, dO + off, lse ? dl + h0 * N : nullptr, 1, static_cast<int>(hn), N,
-                d, scale, causal, dtype, s);
-    if (st != FA_OK) return st;
-    if (cudaEventRecord(e->computed[c], s) != cudaSuccess ||
-        cudaStreamWaitEvent(e->d2h, e->computed[c], 0) != cudaSuccess ||
-        cudaMemcpyAsync(ho + off, dO + off, len, cudaMemcpyDeviceToHost, e->d2h) != cudaSuccess)
-      return FA_ERR_CUDA;
-    if (lse && cudaMemcpyAsync(lse + h0 * N, dl + h0 * N, static_cast<size_t>(hn) * N * sizeof(float),
-                               cudaMemcpyDeviceToHost, e->d2h) != cudaSuccess)
-      return FA_ERR_CUDA;
-  }
-  // the caller's stream resumes once the last result is on the host
-  if (cudaEventRecord(e->out_done, e->d2h) != cudaSuccess || cudaStreamWaitEvent(s, e->out_done, 0) != cudaSuccess)
-    return FA_ERR_CUDA;
+extern "C" int fa_fwd_fp8_host_workspace_size(int B, int H, int N, int d, unsigned long long* bytes) {
+  if (!bytes) return FA_ERR_NULL;
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (N % 16 != 0) return FA_ERR_SHAPE;
+  const unsigned long long elems = static_cast<unsigned long long>(B) * H * N * d;
+  const unsigned long long rows = static_cast<unsigned long long>(B) * H * N;
+  const unsigned long long nsb = static_cast<unsigned long long>(B) * H * ((N + 63) / 64);
+  // bf16 Q, K, V and O; E4M3 Q, K, V^T; three scale arrays; LSE
+  *bytes = 4 * round256(2 * elems) + 3 * round256(elems) + 3 * round256(4 * nsb) + round256(4 * rows);
   return FA_OK;
+}
+
+extern "C" int fa_fwd_fp8_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                               int N, int d, float scale, int causal, int hadamard, int chunks, void* workspace,
+                               unsigned long long workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !workspace) return FA_ERR_NULL;
+  unsigned long long need = 0;
+  int st = fa_fwd_fp8_host_workspace_size(B, H, N, d, &need);
+  if (st != FA_OK) return st;
+  if (workspace_bytes < need) return FA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return FA_ERR_ALIGN;
+  if (chunks < 0 || (causal != 0 && causal != 1) || (hadamard != 0 && hadamard != 1) || !(scale > 0.f) ||
+      !(scale < 3.4e38f))
+    return FA_ERR_UNSUPPORTED;
+  const long long BH = static_cast<long long>(B) * H;
+  const int nsb = (N + 63) / 64;
+  const unsigned long long head_elems = static_cast<unsigned long long>(N) * d;
+  const unsigned long long t16 = round256(BH * 2 * head_elems), t8 = round256(BH * head_elems);
+  const unsigned long long ts = round256(4ull * BH * nsb);
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  uint8_t* const dev_in[3] = {base, base + t16, base + 2 * t16};
+  uint8_t* dO = base + 3 * t16;
+  uint8_t* x8[3];
+  float* sc[3];
+  for (int i = 0; i < 3; ++i) {
+    x8[i] = base + 4 * t16 + i * t8;
+    sc[i] = reinterpret_cast<float*>(base + 4 * t16 + 3 * t8 + i * ts);
+  }
+  float* dl = reinterpret_cast<float*>(base + 4 * t16 + 3 * t8 + 3 * ts);
+  const void* const host_in[3] = {q, k, v};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return run_chunked(host_in, dev_in, 2 * head_elems, o, dO, 2 * head_elems, lse, dl, BH, N, chunks, s,
+                     [&](long long h0, long long hn) {
+                       const unsigned long long o16 = h0 * 2 * head_elems, o8 = h0 * head_elems;
+                       const long long os = h0 * nsb;
+                       const int n = static_cast<int>(hn);
+                       int r = FA_OK;
+                       for (int i = 0; i < 3 && r == FA_OK; ++i)   // Q, K rotated; V transposed, not rotated
+                         r = fa_quantize_fp8(dev_in[i] + o16, x8[i] + o8, sc[i] + os, 1, n, N, d,
+                                             i < 2 ? hadamard : 0, i == 2 ? 1 : 0, s);
+                       if (r != FA_OK) return r;
+                       return fa_fwd_fp8(x8[0] + o8, x8[1] + o8, x8[2] + o8, dO + o16, lse ? dl + h0 * N : nullptr,
+                                         1, n, N, d, scale, causal, sc[0] + os, sc[1] + os, sc[2] + os, hadamard, s);
+                     });
 }

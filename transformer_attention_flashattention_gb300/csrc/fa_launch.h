@@ -19,4 +19,7 @@ cudaError_t launch_decode(int d, bool bf16, const DecodeParams& p, cudaStream_t 
 // Prep (D, LSE*log2e), then the dQ kernel, then the dK/dV kernel, all on `stream`.
 cudaError_t launch_bwd(int d, bool bf16, const BwdParams& p, int grid, cudaStream_t stream);
 
+// fa_decode's shape and size checks (FA_OK, FA_ERR_SHAPE or FA_ERR_UNSUPPORTED).
+int check_decode(int B, int H, int Nq, int Nk, int d);
+
 }  // namespace fa
