@@ -1,18 +1,27 @@
 """Attention forward benchmark: one JSON line on rank 0.
 
 A step is one pass of the forward over one batch of synthetic inputs already
-resident in HBM.  Default workload: bf16 Q/K/V [16, 16, 2048, 128], scale
-1/sqrt(128), one non-causal and one causal forward per step (both masks of that
-workload), TFLOP/s = algorithmic FLOPs (4*B*H*N^2*d, halved for causal) / time.
+resident in HBM.  TFLOP/s = algorithmic FLOPs (4*B*H*N^2*d, halved for causal) /
+time.  Default workload: the long-context forward, bf16 Q/K/V [1, 32, 32768, 128],
+causal, scale 1/sqrt(128) (the largest single-GPU configuration).  After its
+timed region the same process times, as ``variants`` of the line (each launch
+bracketed by CUDA events, L2 flushed before each launch whose inputs fit in it):
 
-Other workloads (for profiling; the default is the headline):
-  --workload sweep:N:d   B*N = 16384, H = 16, both masks
-  --workload long        [1, 32, 32768, 128], causal
-  --workload fp8         [4, 16, 4096, 128] E4M3 forward (Hadamard on), quantisation excluded
-  --workload tiny        [1, 1, 128, 64] fp16, both masks
-  --workload decode      one query row per head against a [8, 32, 32768, 128] bf16 key cache
-  --workload bwd         backward pass (dQ, dK, dV) on [16, 16, 2048, 128] bf16, both masks
-                         (split-KV on the CUDA cores; HBM roofline)
+  * 2x16x8192x128 and 1x16x16384x128 bf16, non-causal (the throughput bar's points);
+  * 16x16x2048x128 bf16, both masks, and 2x16x8192x64 bf16, non-causal;
+  * the E4M3 forward on [4, 16, 4096, 128] (Hadamard on): the forward alone, the
+    quantisation prologue (three launches, in GB/s against HBM), both together,
+    and end to end from host bf16 Q/K/V to host bf16 O through ``fa_fwd_fp8_host``.
+
+Single workloads (``--workload``; the line then carries that workload alone):
+  bf16            [16, 16, 2048, 128], both masks
+  sweep:N:d       B*N = 16384, H = 16, both masks
+  long            [1, 32, 32768, 128], causal (the default, without the variants)
+  fp8             [4, 16, 4096, 128] E4M3 forward, with the prologue and end-to-end figures
+  tiny            [1, 1, 128, 64] fp16, both masks
+  decode          one query row per head against a [8, 32, 32768, 128] bf16 key cache
+                  (split-KV on the CUDA cores; HBM roofline)
+  bwd             backward pass (dQ, dK, dV) on [16, 16, 2048, 128] bf16, both masks
 
 Multi-GPU (torchrun, one rank per GPU): every rank runs the same per-GPU
 workload on its own shard of heads (weak scaling, no collective on the data
@@ -104,12 +113,15 @@ class ClockSampler:
     """nvidia-smi sampled every 100 ms during the timed region.  The raw samples go to
     FA_CLOCKS_DIR (to keep them) or else the system temporary directory."""
 
+    _count = 0
+
     def __init__(self, device_index: int):
         self.idx = device_index
         self.proc = None
         self.keep = bool(os.environ.get("FA_CLOCKS_DIR"))
         out_dir = os.environ.get("FA_CLOCKS_DIR") or tempfile.gettempdir()
-        self.path = os.path.join(out_dir, f"fa_clocks_{os.getpid()}.csv")
+        ClockSampler._count += 1      # one file per sampler: a process may run several
+        self.path = os.path.join(out_dir, f"fa_clocks_{os.getpid()}_{ClockSampler._count}.csv")
 
     def __enter__(self):
         try:
@@ -171,13 +183,20 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- CPU oracle
 
+SAMPLED_ROWS_FROM_N = 8192   # above this the oracle computes 64 sampled query rows per head
+
+
 def _oracle_sample(w, budget_s: float, max_units=None):
     """Times the fp64 oracle over (mask, head) pairs of workload ``w`` until
-    ``budget_s`` seconds have passed; returns (flops, seconds, description)."""
-    import numpy as np  # noqa: F401
+    ``budget_s`` seconds have passed; returns (flops, seconds, description).  Long
+    sequences are sampled: 64 seeded query rows per head (always the first and the
+    last), counted at their visible keys."""
+    import numpy as np
     import oracle
+    from fa_inputs import sample_rows
     q, k, v = make_qkv((1, min(w.H, 4), w.N, w.d), w.dtype, w.seed, w.outliers)
     bwd = w.name == "bwd"
+    rows = sample_rows(w.N) if (w.N > SAMPLED_ROWS_FROM_N and not bwd) else None
     if bwd:
         from fa_inputs import make_dout
         do = make_dout(q.shape, w.dtype, w.seed)
@@ -192,14 +211,19 @@ def _oracle_sample(w, budget_s: float, max_units=None):
         if bwd:
             oracle.attention_backward(q[sl], k[sl], v[sl], do[sl], w.scale, causal)
         else:
-            oracle.attention(q[sl], k[sl], v[sl], w.scale, causal)
-        flops += (4.0 * w.N * w.N * w.d) / (2.0 if causal else 1.0) * (BWD_FLOP_RATIO if bwd else 1.0)
+            oracle.attention(q[sl], k[sl], v[sl], w.scale, causal, rows=rows)
+        if rows is None:
+            flops += (4.0 * w.N * w.N * w.d) / (2.0 if causal else 1.0) * (BWD_FLOP_RATIO if bwd else 1.0)
+        else:
+            vis = np.asarray(rows, dtype=np.float64) + 1.0 if causal else np.full(len(rows), float(w.N))
+            flops += 4.0 * w.d * float(vis.sum())
         done += 1
         i += 1
         el = time.perf_counter() - t0
         if el >= budget_s or (max_units is not None and done >= max_units):
             break
-    desc = (f"{done} full (b,h) heads of [{w.B},{w.H},{w.N},{w.d}]{' (gradient)' if bwd else ''} "
+    what = f"{len(rows)} sampled query rows of" if rows is not None else "full"
+    desc = (f"{done} x {what} (b,h) heads of [{w.B},{w.H},{w.N},{w.d}]{' (gradient)' if bwd else ''} "
             f"({'/'.join('causal' if c else 'non-causal' for c in w.causal_modes)} alternating), fp64 numpy")
     return flops, time.perf_counter() - t0, desc
 
@@ -239,6 +263,143 @@ def run_reference(args):
     return 0
 
 
+# ----------------------------------------------------------------------------- GPU timing helpers
+
+L2_BYTES = 129 << 20         # GB300 L2
+L2_FLUSH_BYTES = 256 << 20   # about twice the L2
+
+
+def _needs_flush(input_bytes: int) -> bool:
+    """Inputs under twice the L2 size could still be partly cached from the previous launch."""
+    return input_bytes < 2 * L2_BYTES
+
+
+class Timer:
+    """CUDA events around single launches on one stream, with an optional L2 flush
+    (a write of a buffer twice the L2's size) before each, outside the events."""
+
+    def __init__(self, dev, stream):
+        self.stream = stream
+        self.flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def launches(self, fn, n: int, warmup: int = 3, flush: bool = False):
+        for _ in range(warmup):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        torch.cuda.synchronize()
+        for a, b in ev:
+            if flush:
+                self.flush_buf.zero_()
+            a.record(self.stream)
+            fn()
+            b.record(self.stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in ev]
+
+
+def _quantile(xs, q):
+    ys = sorted(xs)
+    return ys[min(len(ys) - 1, max(0, int(round(q * (len(ys) - 1)))))]
+
+
+def _perf(ms, flops, dtype_name, peaks, kernel):
+    """Throughput figures of one variant from its per-launch times."""
+    med = statistics.median(ms)
+    mean = sum(ms) / len(ms)
+    bf16 = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    sus = peaks.get("bf16_tflops_sustained", bf16)
+    ratio = 2.0 if dtype_name == "e4m3" else 1.0
+    tf = flops / (med * 1e-3) / 1e12
+    return {"tflops": tf, "median_ms": med, "mean_ms": mean, "p10_ms": _quantile(ms, 0.1),
+            "p90_ms": _quantile(ms, 0.9), "launches": len(ms), "kernel": kernel,
+            "pct_of_spec_peak": 100.0 * tf / SPEC_PEAK_TFLOPS[dtype_name],
+            "roofline_frac": (flops / (mean * 1e-3) / 1e12) / (ratio * bf16),
+            "roofline_frac_sustained": (flops / (mean * 1e-3) / 1e12) / (ratio * sus)}
+
+
+def _fp8_inputs(fa, w, dev, seed):
+    q, k, v = make_qkv(w.shape, w.dtype, seed, w.outliers)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    q8, qs = fa.quantize_fp8(qd, hadamard=True)
+    k8, ks = fa.quantize_fp8(kd, hadamard=True)
+    v8, vs = fa.quantize_fp8(vd, hadamard=False, transpose_out=True)
+    return (q, k, v), (qd, kd, vd), (q8, k8, v8, qs, ks, vs)
+
+
+def _fp8_figures(fa, w, dev, timer, n, peaks, seed, e2e_steps):
+    """The E4M3 forward alone, its quantisation prologue, both, and host to host."""
+    host, (qd, kd, vd), (q8, k8, v8, qs, ks, vs) = _fp8_inputs(fa, w, dev, seed)
+    o = torch.empty(w.shape, device=dev, dtype=torch.bfloat16)
+    lse = torch.empty(w.shape[:3], device=dev, dtype=torch.float32)
+    flops = w.flops(False)
+    fwd = lambda: fa.attention_fp8(q8, k8, v8, qs, ks, vs, hadamard=True, out=o, lse=lse)
+
+    def prologue():
+        fa.quantize_fp8(qd, hadamard=True, out=(q8, qs))
+        fa.quantize_fp8(kd, hadamard=True, out=(k8, ks))
+        fa.quantize_fp8(vd, hadamard=False, transpose_out=True, out=(v8, vs))
+
+    def both():
+        prologue()
+        fwd()
+    out = {}
+    out["fp8_4x16x4096x128_forward"] = _perf(timer.launches(fwd, n, flush=True), flops, "e4m3", peaks,
+                                             "fa_fwd_kernel<128, e4m3>")
+    pro_ms = timer.launches(prologue, n, flush=True)
+    elems = q8.numel()
+    pro_bytes = 3 * (3 * elems + 4 * qs.numel())     # 2 B read + 1 B written per element, and the scales
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    med = statistics.median(pro_ms)
+    out["fp8_4x16x4096x128_prologue"] = {
+        "gbs": pro_bytes / (med * 1e-3) / 1e9, "median_ms": med, "p10_ms": _quantile(pro_ms, 0.1),
+        "p90_ms": _quantile(pro_ms, 0.9), "launches": len(pro_ms), "bytes": pro_bytes,
+        "roofline_frac": pro_bytes / (sum(pro_ms) / len(pro_ms) * 1e-3) / 1e9 / hbm, "bound": "hbm",
+        "kernel": "fa_quant_fp8_kernel<128> x 3 (Q and K rotated, V transposed)"}
+    out["fp8_4x16x4096x128_prologue_and_forward"] = _perf(timer.launches(both, n, flush=True), flops, "e4m3",
+                                                          peaks, "3 x fa_quant_fp8_kernel + fa_fwd_kernel<128, e4m3>")
+    qh, kh, vh = (t.pin_memory() for t in host)
+    oh = torch.empty(w.shape, dtype=torch.bfloat16, pin_memory=True)
+    lh = torch.empty(w.shape[:3], dtype=torch.float32, pin_memory=True)
+    for _ in range(2):
+        fa.attention_fp8_host(qh, kh, vh, hadamard=True, out=oh, lse_out=lh)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        fa.attention_fp8_host(qh, kh, vh, hadamard=True, out=oh, lse_out=lh)
+    e_s = time.perf_counter() - t0
+    h2d = 3 * qh.numel() * qh.element_size()
+    d2h = oh.numel() * oh.element_size() + 4 * lh.numel()
+    out["fp8_4x16x4096x128_end_to_end"] = {
+        "tflops": flops * e2e_steps / e_s / 1e12, "ms_per_call": 1e3 * e_s / e2e_steps, "calls": e2e_steps,
+        "h2d_bytes_per_call": h2d, "d2h_bytes_per_call": d2h,
+        "note": "fa.attention_fp8_host (fa_fwd_fp8_host), synchronised: pinned bf16 Q/K/V in, quantised and "
+                "attended on the device chunk by chunk, bf16 O and LSE out"}
+    return out
+
+
+def _variants(fa, dev, timer, n, peaks, e2e_steps):
+    """The other configurations of the throughput claim, timed in the same process."""
+    from fa_inputs import Workload
+    out = {}
+    specs = [("2x16x8192x128_non_causal", Workload("v8192", 2, 16, 8192, 128, torch.bfloat16, 2), False),
+             ("1x16x16384x128_non_causal", Workload("v16384", 1, 16, 16384, 128, torch.bfloat16, 2), False),
+             ("16x16x2048x128_non_causal", WORKLOADS["bf16"], False),
+             ("16x16x2048x128_causal", WORKLOADS["bf16"], True),
+             ("2x16x8192x64_non_causal", Workload("v8192d64", 2, 16, 8192, 64, torch.bfloat16, 2), False)]
+    cache = {}
+    for name, w, causal in specs:
+        if w.name not in cache:
+            cache.clear()
+            q, k, v = (t.to(dev) for t in make_inputs(w))
+            cache[w.name] = (q, k, v, torch.empty_like(q), torch.empty(w.shape[:3], device=dev))
+        q, k, v, o, lse = cache[w.name]
+        ms = timer.launches(lambda: fa.attention(q, k, v, causal=causal, out=o, lse=lse), n,
+                            flush=_needs_flush(3 * q.numel() * q.element_size()))
+        out[name] = _perf(ms, w.flops(causal), "bf16", peaks, f"fa_fwd_kernel<{w.d}, bf16>")
+    cache.clear()
+    out.update(_fp8_figures(fa, WORKLOADS["fp8"], dev, timer, n, peaks, WORKLOADS["fp8"].seed, e2e_steps))
+    return out
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 def run_gpu(args):
@@ -254,10 +415,11 @@ def run_gpu(args):
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
     fa.load_library()
-    w = _workload(args.workload)
-    fp8 = args.workload == "fp8"
-    dec = args.workload == "decode"
-    bwd = args.workload == "bwd"
+    default = args.workload == "default"
+    w = _workload("long" if default else args.workload)
+    fp8 = w.name == "fp8"
+    dec = w.name == "decode"
+    bwd = w.name == "bwd"
     # Each rank draws its own shard (same shape, seed offset by rank): weak scaling.
     if dec:
         q, _, _ = make_qkv((w.B, w.H, DECODE["Nq"], w.d), w.dtype, shard_seed(w, rank))
@@ -266,6 +428,7 @@ def run_gpu(args):
         q, k, v = make_qkv(w.shape, w.dtype, shard_seed(w, rank), w.outliers)
     masks = list(w.causal_modes)
     stream = torch.cuda.current_stream(dev)
+    timer = Timer(dev, stream)
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     if fp8:
         q8, qs = fa.quantize_fp8(qd, hadamard=True)
@@ -304,6 +467,8 @@ def run_gpu(args):
     step_flops = sum(w.flops(c) for c in masks) * (BWD_FLOP_RATIO if bwd else 1.0)
     if dec:
         step_flops = 4.0 * w.B * w.H * DECODE["Nq"] * w.N * w.d * len(masks)
+    in_bytes = (q.numel() + k.numel() + v.numel()) * (1 if fp8 else q.element_size())
+    flush = _needs_flush(in_bytes)
     for _ in range(args.warmup):
         for c in masks:
             one(c)
@@ -317,17 +482,21 @@ def run_gpu(args):
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local) as clk:
+    smi_idx = torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local
+    with ClockSampler(smi_idx) as clk:
         t_start.record(stream)
         i = 0
         for _ in range(args.steps):
             for c in masks:
+                if flush:
+                    timer.flush_buf.zero_()
                 ev[i][0].record(stream)
                 one(c)
                 ev[i][1].record(stream)
                 i += 1
         t_end.record(stream)
         torch.cuda.synchronize()
+    clocks = clk.summary()
     if pg:
         pg.barrier()
     total_ms = t_start.elapsed_time(t_end)
@@ -343,45 +512,66 @@ def run_gpu(args):
         total_ms, kern_ms = float(t[0]), float(t[1])
     else:
         kern_ms = sum(launch_ms)
+    if flush:
+        # the flush writes between launches are not the workload's: the step time is the launches'
+        total_ms = kern_ms
     value = aggregate_tflops(step_flops, args.steps, world, total_ms)
 
     # End-to-end through the public API with pinned host buffers (this rank's shard).
     e2e = None
-    if not fp8 and not dec and not bwd:
+    e_steps = max(1, min(args.steps, 5))
+    if not dec and not bwd:
         qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
-        oh = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+        oh = torch.empty(q.shape, dtype=torch.bfloat16 if fp8 else q.dtype, pin_memory=True)
         lh = torch.empty(q.shape[:3], dtype=torch.float32, pin_memory=True)
-        e_steps = max(1, min(args.steps, 5))
+        if fp8:
+            host_call = lambda c: fa.attention_fp8_host(qh, kh, vh, causal=c, hadamard=True, out=oh, lse_out=lh)
+            note = ("fa.attention_fp8_host (fa_fwd_fp8_host) per mask, synchronised: pinned bf16 Q/K/V in, "
+                    "quantised (the three prologue launches) and attended on the device chunk by chunk, bf16 O "
+                    "and LSE out")
+        else:
+            host_call = lambda c: fa.attention_host(qh, kh, vh, causal=c, out=oh, lse_out=lh)
+            note = ("fa.attention_host (fa_fwd_host) per mask, synchronised: pinned Q/K/V in and O/LSE out, "
+                    "copies of one chunk of heads overlapped with the computation of the next")
         for _ in range(2):
             for c in masks:
-                fa.attention_host(qh, kh, vh, causal=c, out=oh, lse_out=lh)
+                host_call(c)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for _ in range(e_steps):
             for c in masks:
-                fa.attention_host(qh, kh, vh, causal=c, out=oh, lse_out=lh)
+                host_call(c)
         e_s = time.perf_counter() - t0
         if pg:
             t = torch.tensor([e_s], device=dev, dtype=torch.float64)
             pg.all_reduce(t, op=pg.ReduceOp.MAX)
             e_s = float(t[0])
         h2d = len(masks) * 3 * q.numel() * q.element_size()
-        d2h = len(masks) * (q.numel() * q.element_size() + 4 * q.numel() // w.d)
+        d2h = len(masks) * (oh.numel() * oh.element_size() + 4 * lh.numel())
         e2e = {"value": world * step_flops * e_steps / e_s / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "note": "fa.attention_host (fa_fwd_host) per mask, synchronised: pinned Q/K/V in and O/LSE out, "
-                       "copies of one chunk of heads overlapped with the computation of the next"}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "note": note}
+
+    peaks, peak_src = _peaks()
+    variants_extra = {}
+    clk_var = None
+    if default and not args.no_variants and rank == 0:
+        with ClockSampler(smi_idx) as cv:
+            variants_extra = _variants(fa, dev, timer, max(10, min(args.steps, 50)), peaks, e_steps)
+        clk_var = cv.summary()
+    if fp8:
+        variants_extra = {k: v for k, v in _fp8_figures(fa, w, dev, timer, max(10, min(args.steps, 50)), peaks,
+                                                         shard_seed(w, rank), e_steps).items()
+                          if not k.endswith("_forward")}
 
     if rank != 0:
         if pg:
             pg.destroy_process_group()
         return 0
 
-    peaks, peak_src = _peaks()
     dtype_name = "e4m3" if fp8 else ("bf16" if w.dtype == torch.bfloat16 else "fp16")
     if fp8:
         peak = 2.0 * peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-        peak_note = f"2 x {peak_src} bf16 peak (nominal e4m3:bf16 ratio)"
+        peak_note = f"2 x {peak_src} bf16 burst peak (nominal e4m3:bf16 ratio)"
     else:
         peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
         peak_note = f"{peak_src} bf16 burst peak"
@@ -391,32 +581,32 @@ def run_gpu(args):
         dec_bytes = (2 * k.numel() + q.numel() + o.numel()) * k.element_size() + 4 * lse.numel()
         dec_gbs = dec_bytes * args.steps * len(masks) / (kern_ms * 1e-3) / 1e9
     traffic = _committed_traffic(w.name, fp8)
+    traffic_note = ("DRAM bytes per launch from the ncu capture summarised under profiles/ "
+                    "(not measured in this run)") if traffic is not None else "no committed capture for this workload"
     if dec:
         roof = {"bound": "hbm", "achieved": dec_gbs, "peak": peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]),
                 "unit": "GB/s", "frac": dec_gbs / peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]),
-                "traffic": traffic, "peak_source": f"{peak_src} HBM copy bandwidth",
+                "traffic": traffic, "traffic_source": traffic_note, "peak_source": f"{peak_src} HBM copy bandwidth",
                 "kernel": "fa_decode_split_kernel + fa_decode_merge_kernel", "bytes_per_step": dec_bytes}
     else:
         roof = {"bound": "tensor", "achieved": kern_tflops, "peak": peak, "unit": "TFLOP/s",
-                "frac": kern_tflops / peak, "traffic": traffic, "peak_source": peak_note,
-                "kernel": "fa_fwd_kernel<128, e4m3>" if fp8 else "fa_fwd_kernel"}
+                "frac": kern_tflops / peak, "traffic": traffic, "traffic_source": traffic_note,
+                "peak_source": peak_note,
+                "kernel": "fa_fwd_kernel<128, e4m3>" if fp8 else f"fa_fwd_kernel<{w.d}, {dtype_name}>"}
         if bwd:
             roof["kernel"] = "fa_bwd_prep_kernel + fa_bwd_kernel (dQ) + fa_bwd_kernel (dK, dV)"
             roof["note"] = ("algorithmic FLOPs = 2.5 x forward (five products); the two-kernel scheme "
                             "runs seven, recomputing S and dP once more instead of reducing dQ")
+
     def mask_flops(c):
         return step_flops / len(masks) if dec else w.flops(c) * (BWD_FLOP_RATIO if bwd else 1.0)
-    def pct(xs, q):
-        # q-th quantile of the per-launch times (nearest rank)
-        ys = sorted(xs)
-        return ys[min(len(ys) - 1, max(0, int(round(q * (len(ys) - 1)))))]
-    variants = {("causal" if c else "non_causal"): {
-        "tflops": mask_flops(c) / (statistics.median(per_mask_ms[c]) * 1e-3) / 1e12,
-        "median_ms": statistics.median(per_mask_ms[c]),
-        "p10_ms": pct(per_mask_ms[c], 0.1),
-        "p90_ms": pct(per_mask_ms[c], 0.9),
-        "pct_of_spec_peak": 100.0 * mask_flops(c) / (statistics.median(per_mask_ms[c]) * 1e-3) / 1e12
-        / SPEC_PEAK_TFLOPS[dtype_name]} for c in masks}
+    variants = {}
+    for c in masks:
+        key = ("causal" if c else "non_causal")
+        if default:
+            key = f"{w.B}x{w.H}x{w.N}x{w.d}_{key} (headline)"
+        variants[key] = _perf(per_mask_ms[c], mask_flops(c), dtype_name, peaks, roof["kernel"])
+    variants.update(variants_extra)
 
     cpu = None
     if world == 1 or rank == 0:
@@ -432,8 +622,10 @@ def run_gpu(args):
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
                    "masks": ["causal" if c else "non-causal" for c in masks],
                    "scale": "1/sqrt(d)", "global_batch_heads": world * w.B * w.H,
-                   "l2": "inputs larger than L2 (no flush): Q/K/V = %d MB per rank" %
-                         ((q.numel() + k.numel() + v.numel()) * q.element_size() // 2**20),
+                   "l2": ("L2 flushed (a %d MB write) before every launch, outside the timed launches: "
+                          "inputs are %d MB" if flush else
+                          "inputs larger than L2 (no flush): %d MB of Q/K/V per rank, L2 %d MB") %
+                         ((L2_FLUSH_BYTES >> 20, in_bytes >> 20) if flush else (in_bytes >> 20, L2_BYTES >> 20)),
                    "parallelism": f"dp{world} (independent head shards, no data-path collective)"},
         "pct_of_spec_peak": 100.0 * value / world / SPEC_PEAK_TFLOPS[dtype_name],
         "roofline": roof,
@@ -441,8 +633,10 @@ def run_gpu(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": n_ev * (3 if bwd else (2 if dec else 1)),
-        "clocks": clk.summary(),
+        "clocks": clocks,
     }
+    if clk_var is not None:
+        line["clocks_variants"] = clk_var
     print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
@@ -463,10 +657,11 @@ def _committed_traffic(workload: str, fp8: bool):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="bf16")
+    ap.add_argument("--workload", default="default")
+    ap.add_argument("--no-variants", action="store_true", help="default workload: skip the other configurations")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=6.0)
     ap.add_argument("--skip-cpu-baseline", action="store_true")
@@ -474,6 +669,8 @@ def main(argv=None):
     if args.warmup < 3:
         raise SystemExit("bench.py: at least 3 warm-up steps")
     if args.impl == "reference":
+        if args.workload == "default":
+            args.workload = "long"
         return run_reference(args)
     return run_gpu(args)
 

@@ -38,3 +38,22 @@ def test_our_arm_prints_the_contract_line(gpu_lib):
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
     for v in d["variants"].values():
         assert v["p10_ms"] <= v["median_ms"] <= v["p90_ms"]
+
+
+def test_default_line_carries_the_variants(gpu_lib):
+    """The default workload (long context) with its in-process variants: the throughput
+    bar's points, the bf16 and d=64 points and the E4M3 figures, each with its own numbers."""
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        rc = bench.main(["--steps", "3", "--warmup", "3", "--skip-cpu-baseline"])
+    assert rc == 0
+    d = json.loads([l for l in buf.getvalue().splitlines() if l.strip()][-1])
+    assert d["config"]["workload"] == "long" and d["dtype"] == "bf16"
+    v = d["variants"]
+    for name in ("2x16x8192x128_non_causal", "1x16x16384x128_non_causal", "16x16x2048x128_non_causal",
+                 "16x16x2048x128_causal", "2x16x8192x64_non_causal", "fp8_4x16x4096x128_forward",
+                 "fp8_4x16x4096x128_prologue_and_forward"):
+        assert v[name]["tflops"] > 0 and 0 < v[name]["roofline_frac"], name
+    assert v["fp8_4x16x4096x128_prologue"]["gbs"] > 0
+    assert v["fp8_4x16x4096x128_end_to_end"]["tflops"] > 0
+    assert d["e2e"]["value"] > 0 and d["roofline"]["traffic_source"]
