@@ -15,7 +15,8 @@
 //          D = 0, LSE*log2(e) = +inf, so padded queries get P = 0)
 //   dq     Q-stationary: per 128-row Q tile, stream K_j, V_j;
 //          S = Q K^T and dP = dO V^T (two SS MMAs into TMEM), dS in registers,
-//          packed back over S, then dQ += dS K (TS MMA, K as an MN-major operand)
+//          packed into a TMEM region of its own, then dQ += dS K (TS MMA, K as an
+//          MN-major operand)
 //   dkdv   K/V-stationary: per 128-key tile, stream Q_i, dO_i (+ their LSE, D);
 //          S^T = K Q^T and dP^T = V dO^T, then P^T and dS^T per key row, then
 //          dV += P^T dO and dK += dS^T Q (both TS MMAs)
@@ -26,13 +27,19 @@
 //              column half w/4, so every row is shared by two threads
 //   warp 8     TMA producer: the unit's two stationary tiles, then a 2-stage ring
 //   warp 9     MMA issuer (one thread) and TMEM owner
-// Each 128-row streamed tile is processed as two 64-row halves a and b with their own
-// S and dP buffers, so the compute warps work on one half while the tensor pipe runs
-// the other half's (or the next tile's) MMAs.
-// TMEM (512 columns): S_a | dP_a | S_b | dP_b (64 columns each) | accumulator 0 | 1.
-// A compute thread handles 32 of a half's 64 columns and packs its 16-bit results over
-// the first 16 columns of its own 32 (never over the other thread's, which may still be
-// unread), so a half's TS MMAs read their A operand from columns {0, 8, 32, 40}.
+// dq kernel: whole 128-key tiles, S and dP with N = 128.  The compute threads signal as
+// soon as S(j) and dP(j) are in their registers, and the MMA thread then issues S(j+1)
+// and dP(j+1) into the same TMEM columns while dS(j) is being computed; dS goes to a
+// region of its own, read by dQ += dS K.  24 MMA instructions a key tile (d = 128).
+// TMEM: S (128 columns) | dP (128) | dS (64, two 16-bit values a column) | dQ (D).
+// dkdv kernel: each 128-row streamed tile is processed as two 64-row halves a and b with
+// their own S and dP buffers, so the compute warps work on one half while the tensor
+// pipe runs the other half's (or the next tile's) MMAs (its TMEM holds two accumulators
+// and has no room for a separate P/dS region).
+// TMEM (512 columns): S_a | dP_a | S_b | dP_b (64 columns each) | dV | dK.
+// A dkdv compute thread handles 32 of a half's 64 columns and packs its 16-bit results
+// over the first 16 columns of its own 32 (never over the other thread's, which may still
+// be unread), so a half's TS MMAs read their A operand from columns {0, 8, 32, 40}.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -47,7 +54,8 @@ constexpr int kBwdThreads = kBwdComputeWarps * 32 + 64;
 constexpr int kBwdLoadWarp = 8;
 constexpr int kBwdMmaWarp = 9;
 constexpr int kBwdStages = 2;
-constexpr uint32_t kTmHalf = 128, kTmDP = 64, kTmAcc = 256;   // half h: S at 128h, dP at 128h + 64
+constexpr uint32_t kTmHalf = 128, kTmDP = 64, kTmAcc = 256;   // dkdv, half h: S at 128h, dP at 128h + 64
+constexpr uint32_t kQS = 0, kQDP = 128, kQDS = 256, kQAcc = 320;  // dq: S | dP | dS | dQ
 constexpr float kLog2e = 1.44269504088896340736f;
 
 template <int D>
@@ -59,11 +67,25 @@ struct BwdCfg {
   static constexpr int kVecBytes = 128 * 4;           // one tile's LSE*log2(e) (or D) values
   static constexpr int kStageBytes = 2 * kTile + 2 * kVecBytes;
   static_assert(kStageBytes % 1024 == 0, "stages keep the tiles 1 KB aligned");
-  static constexpr int kBarOff = kRingOff + kBwdStages * kStageBytes;
+  // dq kernel: the stationary Q and dO tiles, then K in a ring of kDqKSlots tiles and V in
+  // one of kDqVSlots.  V_j is free once dP(j) has run, K_j only after dQ += dS(j) K_j, so
+  // the two rings release at different points and K needs the deeper one.
+  static constexpr int kDqKSlots = 3, kDqVSlots = 2;
+  static constexpr int kDqKOff = 2 * kTile;
+  static constexpr int kDqVOff = kDqKOff + kDqKSlots * kTile;
+  static constexpr int kDqEnd = kDqVOff + kDqVSlots * kTile;
+  static constexpr int kDkdvEnd = kRingOff + kBwdStages * kStageBytes;
+  static constexpr int kBarOff = kDqEnd > kDkdvEnd ? kDqEnd : kDkdvEnd;
   // barriers
   static constexpr int kStFull = 0, kStEmpty = 1, kReady = 2, kDone = kReady + kBwdStages;
   static constexpr int kSdpFull = kDone + kBwdStages, kDsFull = kSdpFull + 2, kAccFull = kDsFull + 2;   // per half
-  static constexpr int kMmaDone = kAccFull + 1, kNumBars = kMmaDone + 1;
+  static constexpr int kMmaDone = kAccFull + 1;
+  // dq kernel only: S/dP read into registers (compute arrives), dS region free again (commit),
+  // and the K and V rings' full / free barriers per slot
+  static constexpr int kSdpFree = kMmaDone + 1, kDsFree = kSdpFree + 1;
+  static constexpr int kKFull = kDsFree + 1, kKFree = kKFull + kDqKSlots;
+  static constexpr int kVFull = kKFree + kDqKSlots, kVFree = kVFull + kDqVSlots;
+  static constexpr int kNumBars = kVFree + kDqVSlots;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -247,8 +269,7 @@ template <int D, Elem E>
 __device__ __noinline__ void dq_producer(const BwdParams& p, uint32_t sbase, const ptx::WaitCtl& ctl) {
   using C = BwdCfg<D>;
   auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
-  uint32_t tile = 0, units = 0;
-  uint32_t last_fill[kBwdStages] = {0xFFFFFFFFu, 0xFFFFFFFFu};
+  uint32_t nk = 0, nv = 0, units = 0;     // K and V loads issued so far, stationary fills
   int bh, i;
   for (int k = 0; bwd_unit_at(p, k, true, bh, i); ++k) {
     const int n = p.causal ? i + 1 : p.n_blk;
@@ -257,18 +278,30 @@ __device__ __noinline__ void dq_producer(const BwdParams& p, uint32_t sbase, con
     load_tile<D, E>(&p.tm_q, sbase + C::kStatOff, bar(C::kStFull), i * 128, bh);
     load_tile<D, E>(&p.tm_do, sbase + C::kStatOff + C::kTile, bar(C::kStFull), i * 128, bh);
     ++units;
-    for (int j = 0; j < n; ++j, ++tile) {
-      const uint32_t s = tile % kBwdStages, f = tile / kBwdStages;
-      if (!ptx::mbar_wait(bar(C::kDone + s), (f & 1u) ^ 1u, ctl, 1u)) goto drain;
-      const uint32_t dst = sbase + C::kRingOff + s * C::kStageBytes;
-      ptx::mbar_arrive_expect_tx(bar(C::kReady + s), 2 * C::kTile);
-      load_tile<D, E>(&p.tm_k, dst, bar(C::kReady + s), j * 128, bh);
-      load_tile<D, E>(&p.tm_v, dst + C::kTile, bar(C::kReady + s), j * 128, bh);
-      last_fill[s] = f;
+    for (int j = 0; j < n; ++j) {
+      const uint32_t ks = nk % C::kDqKSlots, kf = nk / C::kDqKSlots;
+      if (!ptx::mbar_wait(bar(C::kKFree + ks), (kf & 1u) ^ 1u, ctl, 1u)) goto drain;
+      ptx::mbar_arrive_expect_tx(bar(C::kKFull + ks), C::kTile);
+      load_tile<D, E>(&p.tm_k, sbase + C::kDqKOff + ks * C::kTile, bar(C::kKFull + ks), j * 128, bh);
+      ++nk;
+      const uint32_t vs = nv % C::kDqVSlots, vf = nv / C::kDqVSlots;
+      if (!ptx::mbar_wait(bar(C::kVFree + vs), (vf & 1u) ^ 1u, ctl, 1u)) goto drain;
+      ptx::mbar_arrive_expect_tx(bar(C::kVFull + vs), C::kTile);
+      load_tile<D, E>(&p.tm_v, sbase + C::kDqVOff + vs * C::kTile, bar(C::kVFull + vs), j * 128, bh);
+      ++nv;
     }
   }
 drain:
-  producer_drain<D>(sbase, last_fill, units, ctl, 8u);
+  // Copies still in flight must land before the CTA may exit: the last fill of every slot
+  // issued so far (immediate on the normal path).
+  for (uint32_t t = nk > static_cast<uint32_t>(C::kDqKSlots) ? nk - C::kDqKSlots : 0; t < nk; ++t)
+    if (!ptx::mbar_wait_drain(bar(C::kKFull + t % C::kDqKSlots), (t / C::kDqKSlots) & 1u, ctl.timeout_ns))
+      atomicOr(ctl.status, 8u);
+  for (uint32_t t = nv > static_cast<uint32_t>(C::kDqVSlots) ? nv - C::kDqVSlots : 0; t < nv; ++t)
+    if (!ptx::mbar_wait_drain(bar(C::kVFull + t % C::kDqVSlots), (t / C::kDqVSlots) & 1u, ctl.timeout_ns))
+      atomicOr(ctl.status, 8u);
+  if (units > 0 && !ptx::mbar_wait_drain(bar(C::kStFull), (units - 1u) & 1u, ctl.timeout_ns))
+    atomicOr(ctl.status, 8u);
 }
 
 template <int D, Elem E>
@@ -277,48 +310,43 @@ __device__ __noinline__ void dq_mma(const BwdParams& p, uint32_t sbase, uint32_t
   auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
   const uint32_t q_lo = ptx::sdesc_lo(sbase + C::kStatOff, 16);
   const uint32_t do_lo = ptx::sdesc_lo(sbase + C::kStatOff + C::kTile, 16);
-  constexpr uint32_t kStageDesc = C::kStageBytes >> 4;
-  const uint32_t k_lo0 = ptx::sdesc_lo(sbase + C::kRingOff, 16);                 // K as K-major B of S
-  const uint32_t v_lo0 = ptx::sdesc_lo(sbase + C::kRingOff + C::kTile, 16);      // V as K-major B of dP
-  const uint32_t kmn_lo0 = ptx::sdesc_lo(sbase + C::kRingOff, v_lbo<D, E>());    // K as MN-major B of dQ
-  const uint32_t tAcc = tmem + kTmAcc;
-  // S_h = Q K_h^T and dP_h = dO V_h^T for key half h of the tile in ring stage s
-  auto sdp = [&](uint32_t s, int h) {
-    const uint32_t tS = tmem + kTmHalf * h;
-    issue_s64<D, E>(tS, q_lo, k_lo0 + s * kStageDesc + kHalfDesc * h);
-    issue_s64<D, E>(tS + kTmDP, do_lo, v_lo0 + s * kStageDesc + kHalfDesc * h);
-    ptx::mma_commit(bar(C::kSdpFull + h));
+  constexpr uint32_t kTileDesc = C::kTile >> 4;
+  const uint32_t k_lo0 = ptx::sdesc_lo(sbase + C::kDqKOff, 16);                 // K as K-major B of S
+  const uint32_t kmn_lo0 = ptx::sdesc_lo(sbase + C::kDqKOff, v_lbo<D, E>());    // K as MN-major B of dQ
+  const uint32_t v_lo0 = ptx::sdesc_lo(sbase + C::kDqVOff, 16);                 // V as K-major B of dP
+  const uint32_t tS = tmem + kQS, tDP = tmem + kQDP, tDS = tmem + kQDS, tAcc = tmem + kQAcc;
+  // S = Q K^T and dP = dO V^T for global tile number t (N = 128); V's slot is free once
+  // dP has run
+  auto sdp = [&](uint32_t t) -> bool {
+    const uint32_t ks = t % C::kDqKSlots, vs = t % C::kDqVSlots;
+    if (!ptx::mbar_wait(bar(C::kKFull + ks), (t / C::kDqKSlots) & 1u, ctl, 2u)) return false;
+    if (!ptx::mbar_wait(bar(C::kVFull + vs), (t / C::kDqVSlots) & 1u, ctl, 2u)) return false;
+    ptx::tc_fence_after();
+    issue_s<D, E>(tS, q_lo, k_lo0 + ks * kTileDesc);
+    issue_s<D, E>(tDP, do_lo, v_lo0 + vs * kTileDesc);
+    ptx::mma_commit(bar(C::kSdpFull));
+    ptx::mma_commit(bar(C::kVFree + vs));
+    return true;
   };
   uint32_t tile = 0, units = 0;
   int bh, i;
   for (int k = 0; bwd_unit_at(p, k, true, bh, i); ++k) {
     const int n = p.causal ? i + 1 : p.n_blk;
     if (!ptx::mbar_wait(bar(C::kStFull), units & 1u, ctl, 2u)) goto done;
-    {
-      const uint32_t s0 = tile % kBwdStages;
-      if (!ptx::mbar_wait(bar(C::kReady + s0), (tile / kBwdStages) & 1u, ctl, 2u)) goto done;
-      sdp(s0, 0);
-      sdp(s0, 1);
-    }
+    if (!sdp(tile)) goto done;
     for (int j = 0; j < n; ++j, ++tile) {
-      const uint32_t s = tile % kBwdStages;
-      const bool more = j + 1 < n;
-      const uint32_t sn = (tile + 1) % kBwdStages;
-      // half a: dQ += dS_a K_a, then the next tile's half a
+      // S(j) and dP(j) are in the compute threads' registers: the next tile's go into
+      // the same columns while dS(j) is formed
+      if (!ptx::mbar_wait(bar(C::kSdpFree), tile & 1u, ctl, 2u)) goto done;
+      if (j + 1 < n && !sdp(tile + 1)) goto done;
+      // dQ += dS(j) K_j, after which K_j's slot and the dS region are free
       if (!ptx::mbar_wait(bar(C::kDsFull), tile & 1u, ctl, 2u)) goto done;
       ptx::tc_fence_after();
-      if (j == 0) issue_pv64<D, E, false>(tAcc, tmem + kTmDP, kmn_lo0 + s * kStageDesc);
-      else issue_pv64<D, E, true>(tAcc, tmem + kTmDP, kmn_lo0 + s * kStageDesc);
-      if (more) {
-        if (!ptx::mbar_wait(bar(C::kReady + sn), ((tile + 1) / kBwdStages) & 1u, ctl, 2u)) goto done;
-        sdp(sn, 0);
-      }
-      // half b
-      if (!ptx::mbar_wait(bar(C::kDsFull + 1), tile & 1u, ctl, 2u)) goto done;
-      ptx::tc_fence_after();
-      issue_pv64<D, E, true>(tAcc, tmem + kTmHalf + kTmDP, kmn_lo0 + s * kStageDesc + kHalfDesc);
-      ptx::mma_commit(bar(C::kDone + s));
-      if (more) sdp(sn, 1);
+      const uint32_t ks = tile % C::kDqKSlots;
+      if (j == 0) issue_pv<D, E, false>(tAcc, tDS, kmn_lo0 + ks * kTileDesc);
+      else issue_pv<D, E, true>(tAcc, tDS, kmn_lo0 + ks * kTileDesc);
+      ptx::mma_commit(bar(C::kDsFree));
+      ptx::mma_commit(bar(C::kKFree + ks));
     }
     ptx::mma_commit(bar(C::kStEmpty));
     ptx::mma_commit(bar(C::kAccFull));
@@ -337,9 +365,11 @@ __device__ __forceinline__ void dq_compute(const BwdParams& p, uint32_t sbase, u
   auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const int r = (warp & 3) * 32 + lane;                        // row in the Q tile = TMEM lane
-  const int sub = warp >> 2;                                   // keys 32*sub .. +31 of each 64-key half
+  const int sub = warp >> 2;                                   // keys 64*sub .. +63 of each tile
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-  const uint32_t tAcc = tmem + lane_base + kTmAcc + (D / 2) * sub;
+  const uint32_t tS = tmem + lane_base + kQS + 64 * sub, tDP = tmem + lane_base + kQDP + 64 * sub;
+  const uint32_t tDS = tmem + lane_base + kQDS + 32 * sub;     // this thread's 64 keys, packed
+  const uint32_t tAcc = tmem + lane_base + kQAcc + (D / 2) * sub;
   uint32_t tile = 0, units = 0;
   int bh, i;
   for (int k = 0; bwd_unit_at(p, k, true, bh, i); ++k) {
@@ -349,31 +379,44 @@ __device__ __forceinline__ void dq_compute(const BwdParams& p, uint32_t sbase, u
     const float lse2 = p.lse2[wrow], dlt = p.delta[wrow];
     const int limit = min(p.N, p.causal ? row + 1 : p.N);      // keys >= limit get P = 0
     for (int j = 0; j < n; ++j, ++tile) {
+      const bool got = ptx::mbar_wait(bar(C::kSdpFull), tile & 1u, ctl, 4u);
+      if (!__all_sync(0xFFFFFFFFu, got)) return;
+      ptx::tc_fence_after();
+      uint32_t sr[2][32], dr[2][32];
+      ptx::tmem_ld32(tS, sr[0]);
+      ptx::tmem_ld32(tS + 32, sr[1]);
+      ptx::tmem_ld32(tDP, dr[0]);
+      ptx::tmem_ld32(tDP + 32, dr[1]);
+      ptx::tmem_wait_ld();
+      // S and dP are read: the MMA thread may overwrite them with the next tile's
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(C::kSdpFree));
+      const int visible = limit - (j * 128 + 64 * sub);
+      uint32_t w[2][16];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const bool got = ptx::mbar_wait(bar(C::kSdpFull + h), tile & 1u, ctl, 4u);
-        if (!__all_sync(0xFFFFFFFFu, got)) return;
-        ptx::tc_fence_after();
-        const uint32_t tS = tmem + lane_base + kTmHalf * h + 32 * sub, tDP = tS + kTmDP;
-        const int visible = limit - (j * 128 + 64 * h + 32 * sub);
-        uint32_t sr[32], dr[32];
-        ptx::tmem_ld32(tS, sr);
-        ptx::tmem_ld32(tDP, dr);
-        ptx::tmem_wait_ld();
+      for (int c = 0; c < 2; ++c) {
         float ds[32];
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
-          const float pv = x < visible ? ptx::ex2(fmaf(__uint_as_float(sr[x]), p.scale_log2, -lse2)) : 0.f;
-          ds[x] = pv * (__uint_as_float(dr[x]) - dlt);
+          const float pv = 32 * c + x < visible
+                               ? ptx::ex2(fmaf(__uint_as_float(sr[c][x]), p.scale_log2, -lse2)) : 0.f;
+          ds[x] = pv * (__uint_as_float(dr[c][x]) - dlt);
         }
-        uint32_t w[16];
-        pack16<kBf16>(ds, w);
-        ptx::tmem_st16(tDP, w);                                // over this thread's first 16 dP columns
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar(C::kDsFull + h));
+        pack16<kBf16>(ds, w[c]);
       }
+      // the previous tile's dQ MMAs have read the dS region
+      if (j > 0 || units > 0) {
+        const bool fr = ptx::mbar_wait(bar(C::kDsFree), (tile - 1) & 1u, ctl, 4u);
+        if (!__all_sync(0xFFFFFFFFu, fr)) return;
+        ptx::tc_fence_after();
+      }
+      ptx::tmem_st16(tDS, w[0]);
+      ptx::tmem_st16(tDS + 16, w[1]);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(C::kDsFull));
     }
     const bool got = ptx::mbar_wait(bar(C::kAccFull), units & 1u, ctl, 4u);
     if (!__all_sync(0xFFFFFFFFu, got)) return;
@@ -563,7 +606,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumBars; ++i)
-      ptx::mbar_init(bar(i), (i == C::kDsFull || i == C::kDsFull + 1) ? kBwdComputeWarps : 1);
+      ptx::mbar_init(bar(i), (i == C::kDsFull || i == C::kDsFull + 1 || i == C::kSdpFree) ? kBwdComputeWarps : 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
