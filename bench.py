@@ -9,6 +9,8 @@ bracketed by CUDA events, L2 flushed before each launch whose inputs fit in it):
 
   * 2x16x8192x128 and 1x16x16384x128 bf16, non-causal (the throughput bar's points);
   * 16x16x2048x128 bf16, both masks, and 2x16x8192x64 bf16, non-causal;
+  * the CTA-pair kernel (fa_fwd_2cta) on 2x16x8192x128, both masks of 16x16x2048x128
+    and the long-context workload, beside the single-CTA kernel;
   * the E4M3 forward on [4, 16, 4096, 128] (Hadamard on): the forward alone, the
     quantisation prologue (three launches, in GB/s against HBM), both together,
     and end to end from host bf16 Q/K/V to host bf16 O through ``fa_fwd_fp8_host``.
@@ -377,24 +379,32 @@ def _fp8_figures(fa, w, dev, timer, n, peaks, seed, e2e_steps):
 
 
 def _variants(fa, dev, timer, n, peaks, e2e_steps):
-    """The other configurations of the throughput claim, timed in the same process."""
+    """The other configurations of the throughput claim, timed in the same process; the
+    CTA-pair kernel (fa_fwd_2cta) beside the single-CTA one where it applies (d = 128)."""
     from fa_inputs import Workload
     out = {}
-    specs = [("2x16x8192x128_non_causal", Workload("v8192", 2, 16, 8192, 128, torch.bfloat16, 2), False),
-             ("1x16x16384x128_non_causal", Workload("v16384", 1, 16, 16384, 128, torch.bfloat16, 2), False),
-             ("16x16x2048x128_non_causal", WORKLOADS["bf16"], False),
-             ("16x16x2048x128_causal", WORKLOADS["bf16"], True),
-             ("2x16x8192x64_non_causal", Workload("v8192d64", 2, 16, 8192, 64, torch.bfloat16, 2), False)]
+    w8k = Workload("v8192", 2, 16, 8192, 128, torch.bfloat16, 2)
+    specs = [("2x16x8192x128_non_causal", w8k, False, False),
+             ("2x16x8192x128_non_causal_2cta", w8k, False, True),
+             ("1x16x16384x128_non_causal", Workload("v16384", 1, 16, 16384, 128, torch.bfloat16, 2), False, False),
+             ("16x16x2048x128_non_causal", WORKLOADS["bf16"], False, False),
+             ("16x16x2048x128_causal", WORKLOADS["bf16"], True, False),
+             ("16x16x2048x128_non_causal_2cta", WORKLOADS["bf16"], False, True),
+             ("16x16x2048x128_causal_2cta", WORKLOADS["bf16"], True, True),
+             ("1x32x32768x128_causal_2cta", WORKLOADS["long"], True, True),
+             ("2x16x8192x64_non_causal", Workload("v8192d64", 2, 16, 8192, 64, torch.bfloat16, 2), False, False)]
     cache = {}
-    for name, w, causal in specs:
+    for name, w, causal, pair in specs:
         if w.name not in cache:
             cache.clear()
             q, k, v = (t.to(dev) for t in make_inputs(w))
             cache[w.name] = (q, k, v, torch.empty_like(q), torch.empty(w.shape[:3], device=dev))
         q, k, v, o, lse = cache[w.name]
-        ms = timer.launches(lambda: fa.attention(q, k, v, causal=causal, out=o, lse=lse), n,
+        call = fa.attention_2cta if pair else fa.attention
+        ms = timer.launches(lambda: call(q, k, v, causal=causal, out=o, lse=lse), n,
                             flush=_needs_flush(3 * q.numel() * q.element_size()))
-        out[name] = _perf(ms, w.flops(causal), "bf16", peaks, f"fa_fwd_kernel<{w.d}, bf16>")
+        kern = "fa_fwd2_kernel<bf16> (CTA pairs)" if pair else f"fa_fwd_kernel<{w.d}, bf16>"
+        out[name] = _perf(ms, w.flops(causal), "bf16", peaks, kern)
     cache.clear()
     out.update(_fp8_figures(fa, WORKLOADS["fp8"], dev, timer, n, peaks, WORKLOADS["fp8"].seed, e2e_steps))
     return out

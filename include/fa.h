@@ -76,6 +76,18 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
            int d, float scale, int causal, int dtype, void* stream);
 
 /*
+ * fa_fwd computed by pairs of CTAs on two SMs (a cluster of two), with M = 256 tensor-core
+ * tiles issued for both SMs by one thread (tcgen05 cta_group::2): each SM holds half of
+ * every K and V tile, so a key tile costs each SM half the shared memory.  This is the
+ * larger tile the FlashAttention-3 news piece's levers point at ("Drei technische
+ * Hebel", items 1-2); the operation and the results' accuracy are fa_fwd's.
+ * Arguments, layout, ownership and errors as fa_fwd; supported: d == 128 only (other
+ * head dims return FA_ERR_UNSUPPORTED).
+ */
+int fa_fwd_2cta(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                int d, float scale, int causal, int dtype, void* stream);
+
+/*
  * fa_fwd on HOST buffers, end to end: copies Q, K, V to the device, computes, and copies
  * O (and LSE) back, with the copies of one chunk of heads overlapped with the
  * computation of the next (a runtime convenience; the pages' operation is fa_fwd's).

@@ -36,7 +36,7 @@ def test_header_declares_the_boundary():
                                   "fa_decode", "fa_decode_workspace_size", "fa_decode_noalloc",
                                   "fa_bwd", "fa_bwd_workspace_size", "fa_quantize_fp8_ex",
                                   "fa_fwd_host", "fa_fwd_host_workspace_size", "fa_fwd_fp8_host",
-                                  "fa_fwd_fp8_host_workspace_size", "fa_build_id"])
+                                  "fa_fwd_fp8_host_workspace_size", "fa_build_id", "fa_fwd_2cta"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -189,3 +189,15 @@ def test_fwd_fp8_host_rejects_bad_arguments_on_the_host(lib):
     assert call(had=2) == fa.FA_ERR_UNSUPPORTED
     assert call(causal=3) == fa.FA_ERR_UNSUPPORTED
     assert call(N=100) == fa.FA_ERR_SHAPE
+
+
+def test_fwd_2cta_rejects_bad_arguments_on_the_host(lib):
+    call = lambda q=A, d=128, dtype=1, causal=0, scale=0.125, N=128: lib.fa_fwd_2cta(
+        q or None, A, A, A, None, 1, 1, N, d, scale, causal, dtype, None)
+    assert call(q=0) == fa.FA_ERR_NULL
+    assert call(d=64) == fa.FA_ERR_UNSUPPORTED          # head dim 128 only
+    assert call(dtype=3) == fa.FA_ERR_UNSUPPORTED
+    assert call(causal=2) == fa.FA_ERR_UNSUPPORTED
+    assert call(scale=-1.0) == fa.FA_ERR_UNSUPPORTED
+    assert call(N=0) == fa.FA_ERR_SHAPE
+    assert call(q=A + 8) == fa.FA_ERR_ALIGN

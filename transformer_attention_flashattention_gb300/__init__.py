@@ -22,6 +22,7 @@ __all__ = [
     "exported_symbols",
     "attention",
     "attention_host",
+    "attention_2cta",
     "attention_fp8_host",
     "quantize_fp8",
     "attention_fp8",
@@ -65,6 +66,7 @@ _i = ctypes.c_int
 _f = ctypes.c_float
 _SIGNATURES = {
     "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _vp]),
+    "fa_fwd_2cta": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _vp]),
     "fa_quantize_fp8": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]),
     "fa_quantize_fp8_ex": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_ulonglong, ctypes.c_ulonglong,
                                 _i, _i, _vp]),
@@ -191,6 +193,28 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = 
     if check:
         with torch.cuda.device(q.device):
             _check(lib.fa_last_device_status(_stream_handle(stream, q.device), None), "fa_fwd (device status)")
+    return out, lse
+
+
+def attention_2cta(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+                   scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                   lse: Optional[torch.Tensor] = None, return_lse: bool = True,
+                   stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """``attention`` computed by CTA pairs (``fa_fwd_2cta``; head dim 128 only)."""
+    lib = load_library()
+    _check_qkv(q, k, v)
+    if q.dtype not in _DTYPES:
+        raise ValueError(f"dtype must be float16 or bfloat16, got {q.dtype}")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    st = lib.fa_fwd_2cta(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, float(scale),
+                         int(bool(causal)), _DTYPES[q.dtype], _stream_handle(stream, q.device))
+    _check(st, "fa_fwd_2cta")
     return out, lse
 
 

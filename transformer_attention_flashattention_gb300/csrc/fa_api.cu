@@ -125,13 +125,18 @@ int check_shape(int B, int H, int N, int d) {
 
 using namespace fa;
 
-extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                      int N, int d, float scale, int causal, int dtype, void* stream) {
+namespace {
+
+// fa_fwd and fa_fwd_2cta: the same checks and parameters; `pair` selects the CTA-pair
+// kernel (head dim 128 only, 512-row units, two CTAs a cluster).
+int fwd_call(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+             float scale, int causal, int dtype, void* stream, bool pair) {
   if (!q || !k || !v || !o) return FA_ERR_NULL;
   if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
   if (causal != 0 && causal != 1) return FA_ERR_UNSUPPORTED;
   int st = check_shape(B, H, N, d);
   if (st != FA_OK) return st;
+  if (pair && d != 128) return FA_ERR_UNSUPPORTED;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
       (lse && !aligned(lse, 4)))
@@ -145,7 +150,7 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
                                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const uint64_t BH = static_cast<uint64_t>(B) * H;
   if (!encode_3d(&p.tm_q, dt, 2, q, d, N, BH, 64, 128) || !encode_3d(&p.tm_k, dt, 2, k, d, N, BH, 64, 128) ||
-      !encode_3d(&p.tm_v, dt, 2, v, d, N, BH, 64, 128))
+      !encode_3d(&p.tm_v, dt, 2, v, d, N, BH, 64, 128) || !encode_3d(&p.tm_kh, dt, 2, k, d, N, BH, 64, 64))
     return FA_ERR_CUDA;
   p.o = o;
   p.lse = lse;
@@ -153,7 +158,8 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   p.scale_log2 = scale * 1.44269504088896340736f;
   p.N = N;
   p.BH = static_cast<int>(BH);
-  p.n_qblk = (N + kUnitRows - 1) / kUnitRows;
+  const int unit_rows = pair ? 2 * kUnitRows : kUnitRows;
+  p.n_qblk = (N + unit_rows - 1) / unit_rows;
   const long long units = static_cast<long long>(p.n_qblk) * p.BH;
   if (units >= (1ll << 31)) return FA_ERR_SHAPE;
   p.num_units = static_cast<int>(units);
@@ -167,9 +173,28 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
     g_dbg_skip_load = -1;
     g_dbg_timeout_ms = 0;
   }
-  const int grid = static_cast<int>(units < di->sm_count ? units : di->sm_count);
-  const cudaError_t e = launch_fwd(d, dtype == FA_BF16, p, grid, static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  if (pair) {
+    const long long pairs = di->sm_count / 2;
+    const int grid = 2 * static_cast<int>(units < pairs ? units : pairs);
+    e = launch_fwd2(dtype == FA_BF16, p, grid, static_cast<cudaStream_t>(stream));
+  } else {
+    const int grid = static_cast<int>(units < di->sm_count ? units : di->sm_count);
+    e = launch_fwd(d, dtype == FA_BF16, p, grid, static_cast<cudaStream_t>(stream));
+  }
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                      int N, int d, float scale, int causal, int dtype, void* stream) {
+  return fwd_call(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream, false);
+}
+
+extern "C" int fa_fwd_2cta(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                           int N, int d, float scale, int causal, int dtype, void* stream) {
+  return fwd_call(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream, true);
 }
 
 namespace fa {

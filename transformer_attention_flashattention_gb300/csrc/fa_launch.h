@@ -14,6 +14,8 @@ struct BwdParams;
 // Launch one forward kernel instantiation on `stream`; returns the launch status.
 cudaError_t launch_fwd(int d, bool bf16, const FwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_fwd_fp8(const FwdParams& p, int grid, cudaStream_t stream);
+// CTA-pair forward (16-bit, head dim 128); `grid` is even (two CTAs a cluster).
+cudaError_t launch_fwd2(bool bf16, const FwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_quant_fp8(const QuantParams& p, cudaStream_t stream);
 cudaError_t launch_decode(int d, bool bf16, const DecodeParams& p, cudaStream_t stream);
 // Prep (D, LSE*log2e), then the dQ kernel, then the dK/dV kernel, all on `stream`.

@@ -12,6 +12,7 @@ struct FwdParams {
   CUtensorMap tm_q;   // 3-D {d, N, B*H}, box {128 bytes of d, 128 rows, 1}, 128-byte swizzle
   CUtensorMap tm_k;
   CUtensorMap tm_v;   // as Q for 16-bit inputs; E4M3: V^T, 3-D {N, d, B*H}, box {128, 128, 1}
+  CUtensorMap tm_kh;  // CTA-pair kernel only: K with a 64-row box (half a key tile per CTA)
   void* o;            // [B, H, N, d]: the input type for 16-bit inputs, bf16 for E4M3
   float* lse;         // [B, H, N] or nullptr
   unsigned int* status;
@@ -19,7 +20,7 @@ struct FwdParams {
   float scale_log2;   // scale * log2(e)
   int N;
   int BH;
-  int n_qblk;         // ceil(N / 256)
+  int n_qblk;         // ceil(N / 256); the CTA-pair kernel: ceil(N / 512)
   int num_units;      // BH * n_qblk
   int causal;
   int dbg_skip_load;  // K/V load index the producer leaves out (fault-path test), -1 = none
