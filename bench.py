@@ -471,9 +471,13 @@ def run_gpu(args):
             fa.decode(qd, kd, vd, causal=causal, out=o, lse=lse, workspace=ws)
         elif fp8:
             fa.attention_fp8(q8, k8, v8, qs, ks, vs, causal=causal, hadamard=True, out=o, lse=lse)
+        elif args.kernel == "pair":
+            fa.attention_2cta(qd, kd, vd, causal=causal, out=o, lse=lse)
         else:
             fa.attention(qd, kd, vd, causal=causal, out=o, lse=lse)
 
+    if args.kernel == "pair" and (fp8 or dec or bwd or w.d != 128):
+        raise SystemExit("bench.py: --kernel pair is the 16-bit head-dim-128 forward only")
     step_flops = sum(w.flops(c) for c in masks) * (BWD_FLOP_RATIO if bwd else 1.0)
     if dec:
         step_flops = 4.0 * w.B * w.H * DECODE["Nq"] * w.N * w.d * len(masks)
@@ -602,7 +606,9 @@ def run_gpu(args):
         roof = {"bound": "tensor", "achieved": kern_tflops, "peak": peak, "unit": "TFLOP/s",
                 "frac": kern_tflops / peak, "traffic": traffic, "traffic_source": traffic_note,
                 "peak_source": peak_note,
-                "kernel": "fa_fwd_kernel<128, e4m3>" if fp8 else f"fa_fwd_kernel<{w.d}, {dtype_name}>"}
+                "kernel": "fa_fwd_kernel<128, e4m3>" if fp8 else (
+                    f"fa_fwd2_kernel<{dtype_name}> (CTA pairs)" if args.kernel == "pair"
+                    else f"fa_fwd_kernel<{w.d}, {dtype_name}>")}
         if bwd:
             roof["kernel"] = "fa_bwd_prep_kernel + fa_bwd_kernel (dQ) + fa_bwd_kernel (dK, dV)"
             roof["note"] = ("algorithmic FLOPs = 2.5 x forward (five products); the two-kernel scheme "
@@ -672,6 +678,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="default")
     ap.add_argument("--no-variants", action="store_true", help="default workload: skip the other configurations")
+    ap.add_argument("--kernel", choices=["single", "pair"], default="single",
+                    help="16-bit d=128 forward: one CTA per SM (fa_fwd) or CTA pairs (fa_fwd_2cta)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=6.0)
     ap.add_argument("--skip-cpu-baseline", action="store_true")

@@ -286,3 +286,18 @@ def test_fp8_host_end_to_end_matches_the_device_path_bitwise(gpu_lib, chunks, ca
     od, ld = gpu_lib.attention_fp8(q8, k8, v8, qs, ks, vs, causal=causal, hadamard=True)
     torch.cuda.synchronize()
     assert torch.equal(o, od.cpu()) and torch.equal(lse, ld.cpu())
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_variants_track_the_replay_elementwise(gpu_lib, causal):
+    """The randomised rotation (a sign mask shared by Q and K) and per-head V scales, on
+    oracle-made codes, element by element against the replay."""
+    q, k, v = make_qkv((1, 2, 1040, 128), torch.bfloat16, 77, outliers=True)
+    signs = oracle.sign_vector(make_sign_flips(128, 9), 128)
+    q8, qs = quantize_for_both(q, True, signs)
+    k8, ks = quantize_for_both(k, True, signs)
+    v8, vs = quantize_for_both(v, False, per_head=True)
+    codes = (q8, k8, v8, qs, ks, vs)
+    o, lse = _gpu_on_codes(gpu_lib, codes, causal, True)
+    ro, rl, w = replay_fp8_attention(*codes, 1 / math.sqrt(128), causal)
+    _assert_tracks_replay(o, lse, ro, rl, w, f"signed rotation, per-head V, causal={causal}")

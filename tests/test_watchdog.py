@@ -39,3 +39,18 @@ def test_stalled_stage_reports_timeout_and_context_recovers(gpu_lib, d):
     ro, rl = oracle.attention(q, k, v, 1 / math.sqrt(d), False)
     assert float(np.abs(o.float().cpu().numpy() - ro).max()) <= 1.2e-2
     assert float(np.abs(lse.cpu().numpy() - rl).max()) <= 1e-3
+
+
+def test_checked_call_raises_when_a_wait_gives_up(gpu_lib):
+    """attention(check=True) reads the status word after the launch: a call whose wait gave
+    up (its outputs undefined) raises instead of returning quietly."""
+    fa = gpu_lib
+    q, k, v = (t.cuda() for t in make_qkv((1, 2, 512, 128), torch.bfloat16, 41))
+    fa.inject_stall(load_index=2, timeout_ms=100)
+    with pytest.raises(fa.FAError) as e:
+        fa.attention(q, k, v, check=True)
+    assert e.value.status == fa.FA_ERR_DEVICE_TIMEOUT
+    # the status word was read and cleared by the check; a checked call now succeeds
+    o, _ = fa.attention(q, k, v, check=True)
+    st, bits = fa.last_device_status()
+    assert st == fa.FA_OK and bits == 0 and torch.isfinite(o).all()
