@@ -25,7 +25,8 @@
 // Each main kernel is a persistent grid with these roles (320 threads):
 //   warps 0-7  compute: warp w takes TMEM lanes 32*(w%4).. (Q rows, or key rows) and
 //              column half w/4, so every row is shared by two threads
-//   warp 8     TMA producer: the unit's two stationary tiles, then a 2-stage ring
+//   warp 8     TMA producer: the unit's two stationary tiles, then the streamed tiles
+//              (dq: K in a 3-slot ring and V in a 2-slot ring; dkdv: a 2-stage ring)
 //   warp 9     MMA issuer (one thread) and TMEM owner
 // dq kernel: whole 128-key tiles, S and dP with N = 128.  The compute threads signal as
 // soon as S(j) and dP(j) are in their registers, and the MMA thread then issues S(j+1)
