@@ -146,6 +146,21 @@ int fa_quantize_fp8_ex(const void* x, void* x8, float* scale, int B, int H, int 
                        int transpose_out, void* stream);
 
 /*
+ * The whole FP8 prologue in one launch: Q and K quantised as fa_quantize_fp8 with
+ * `hadamard`, V quantised without rotation and written transposed (transpose_out = 1).
+ * The three tensors' blocks form one sequence of work for one persistent grid, so the
+ * launch has one ramp and one tail instead of three.  Codes and scales are bitwise those
+ * of the three separate calls.
+ *   q, k, v          : [B, H, N, d] bfloat16
+ *   q8, k8           : [B, H, N, d] E4M3;  v8t : [B, H, d, N] E4M3
+ *   q_scale, k_scale, v_scale : [B, H, ceil(N/64)] float32, written
+ * Needs N % 16 == 0.  Errors as fa_quantize_fp8.
+ */
+int fa_quantize_fp8_qkv(const void* q, const void* k, const void* v, void* q8, void* k8, void* v8t,
+                        float* q_scale, float* k_scale, float* v_scale, int B, int H, int N, int d,
+                        int hadamard, void* stream);
+
+/*
  * Attention forward from E4M3 inputs produced by fa_quantize_fp8.
  *   q8, k8   : [B, H, N, d] E4M3 (rotated by the same Hadamard matrix, or both not)
  *   v8t      : [B, H, d, N] E4M3 (V quantised with transpose_out = 1, not rotated)
@@ -162,8 +177,8 @@ int fa_fwd_fp8(const void* q8, const void* k8, const void* v8t, void* o, float* 
 /*
  * The FP8 mode end to end on HOST buffers: bf16 Q, K, V in, bf16 O (and LSE) out.  On the
  * device, each chunk of heads runs the whole FP8 path of the news piece ("Drei
- * technische Hebel", item 3): fa_quantize_fp8 of Q and K (rotated when `hadamard` is 1),
- * of V (transposed, never rotated), then fa_fwd_fp8.  The copies of one chunk overlap
+ * technische Hebel", item 3): fa_quantize_fp8_qkv (Q and K rotated when `hadamard` is 1,
+ * V transposed, never rotated), then fa_fwd_fp8.  The copies of one chunk overlap
  * the computation of the next, as in fa_fwd_host (a runtime convenience).
  *   q, k, v, o : [B, H, N, d] bfloat16 in host memory (pinned lets the copies overlap)
  *   lse        : [B, H, N] float32 in host memory, or NULL

@@ -36,7 +36,7 @@ def test_header_declares_the_boundary():
                                   "fa_decode", "fa_decode_workspace_size", "fa_decode_noalloc",
                                   "fa_bwd", "fa_bwd_workspace_size", "fa_quantize_fp8_ex",
                                   "fa_fwd_host", "fa_fwd_host_workspace_size", "fa_fwd_fp8_host",
-                                  "fa_fwd_fp8_host_workspace_size", "fa_build_id", "fa_fwd_2cta"])
+                                  "fa_fwd_fp8_host_workspace_size", "fa_build_id", "fa_fwd_2cta", "fa_quantize_fp8_qkv"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -201,3 +201,15 @@ def test_fwd_2cta_rejects_bad_arguments_on_the_host(lib):
     assert call(scale=-1.0) == fa.FA_ERR_UNSUPPORTED
     assert call(N=0) == fa.FA_ERR_SHAPE
     assert call(q=A + 8) == fa.FA_ERR_ALIGN
+
+
+def test_quantize_qkv_rejects_bad_arguments_on_the_host(lib):
+    call = lambda q=A, had=1, N=128, d=128, vs=A: lib.fa_quantize_fp8_qkv(q or None, A, A, A, A, A, A, A, vs or None,
+                                                                      1, 1, N, d, had, None)
+    assert call(q=0) == fa.FA_ERR_NULL
+    assert call(vs=0) == fa.FA_ERR_NULL
+    assert call(had=2) == fa.FA_ERR_UNSUPPORTED
+    assert call(d=80) == fa.FA_ERR_UNSUPPORTED
+    assert call(N=100) == fa.FA_ERR_SHAPE               # V is written transposed: N % 16 == 0
+    assert call(q=A + 8) == fa.FA_ERR_ALIGN
+    assert call(vs=A + 2) == fa.FA_ERR_ALIGN

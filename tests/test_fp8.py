@@ -301,3 +301,18 @@ def test_fp8_variants_track_the_replay_elementwise(gpu_lib, causal):
     o, lse = _gpu_on_codes(gpu_lib, codes, causal, True)
     ro, rl, w = replay_fp8_attention(*codes, 1 / math.sqrt(128), causal)
     _assert_tracks_replay(o, lse, ro, rl, w, f"signed rotation, per-head V, causal={causal}")
+
+
+@pytest.mark.parametrize("d,N", [(128, 64), (128, 1040), (64, 208), (128, 4096)])
+@pytest.mark.parametrize("hadamard", [False, True])
+def test_fused_prologue_is_bitwise_the_three_calls(gpu_lib, d, N, hadamard):
+    q, k, v = (t.cuda() for t in make_qkv((2, 3, N, d), torch.bfloat16, 90 + N, outliers=True))
+    q8, k8, v8t, qs, ks, vs = gpu_lib.quantize_fp8_qkv(q, k, v, hadamard=hadamard)
+    rq8, rqs = gpu_lib.quantize_fp8(q, hadamard=hadamard)
+    rk8, rks = gpu_lib.quantize_fp8(k, hadamard=hadamard)
+    rv8, rvs = gpu_lib.quantize_fp8(v, hadamard=False, transpose_out=True)
+    torch.cuda.synchronize()
+    st, bits = gpu_lib.last_device_status()
+    assert st == gpu_lib.FA_OK, f"device status {bits:#x}"
+    for a, b in ((q8, rq8), (k8, rk8), (v8t, rv8), (qs, rqs), (ks, rks), (vs, rvs)):
+        assert torch.equal(a, b)

@@ -25,6 +25,7 @@ __all__ = [
     "attention_2cta",
     "attention_fp8_host",
     "quantize_fp8",
+    "quantize_fp8_qkv",
     "attention_fp8",
     "decode",
     "decode_noalloc",
@@ -71,6 +72,7 @@ _SIGNATURES = {
     "fa_quantize_fp8_ex": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_ulonglong, ctypes.c_ulonglong,
                                 _i, _i, _vp]),
     "fa_fwd_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _i, _vp]),
+    "fa_quantize_fp8_qkv": (_i, [_vp] * 9 + [_i, _i, _i, _i, _i, _vp]),
     "fa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _vp, ctypes.c_ulonglong, _vp]),
     "fa_decode_workspace_size": (_i, [_i, _i, _i, _i, _i, _i, ctypes.POINTER(ctypes.c_ulonglong)]),
     "fa_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _vp]),
@@ -334,6 +336,29 @@ def quantize_fp8(x: torch.Tensor, hadamard: bool = False, transpose_out: bool = 
                              int(bool(transpose_out)), _stream_handle(stream, x.device))
     _check(st, "fa_quantize_fp8")
     return x8, sc
+
+
+def quantize_fp8_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, hadamard: bool = True,
+                     stream: Optional[torch.cuda.Stream] = None, out=None):
+    """The FP8 prologue in one launch (``fa_quantize_fp8_qkv``): Q and K quantised (rotated
+    when ``hadamard``), V quantised and transposed.  ``out`` = (q8, k8, v8t, qs, ks, vs) to
+    write into.  Returns (q8, k8, v8t, q_scale, k_scale, v_scale)."""
+    lib = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dim() != 4 or not t.is_cuda or not t.is_contiguous() or t.dtype != torch.bfloat16 or t.shape != q.shape:
+            raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor shaped like q")
+    B, H, N, d = q.shape
+    nb = (N + 63) // 64
+    if out is None:
+        out = (torch.empty((B, H, N, d), device=q.device, dtype=torch.uint8),
+               torch.empty((B, H, N, d), device=q.device, dtype=torch.uint8),
+               torch.empty((B, H, d, N), device=q.device, dtype=torch.uint8),
+               *(torch.empty((B, H, nb), device=q.device, dtype=torch.float32) for _ in range(3)))
+    q8, k8, v8t, qs, ks, vs = out
+    st = lib.fa_quantize_fp8_qkv(_ptr(q), _ptr(k), _ptr(v), _ptr(q8), _ptr(k8), _ptr(v8t), _ptr(qs), _ptr(ks),
+                                 _ptr(vs), B, H, N, d, int(bool(hadamard)), _stream_handle(stream, q.device))
+    _check(st, "fa_quantize_fp8_qkv")
+    return q8, k8, v8t, qs, ks, vs
 
 
 def attention_fp8(q8: torch.Tensor, k8: torch.Tensor, v8t: torch.Tensor, q_scale: torch.Tensor,

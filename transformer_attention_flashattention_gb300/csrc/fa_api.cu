@@ -215,16 +215,17 @@ int quantize_fp8(const void* x, void* x8, float* scale, int B, int H, int N, int
   if (!aligned(x, 16) || !aligned(x8, 16) || !aligned(scale, 4)) return FA_ERR_ALIGN;
   const DeviceInfo* di = current_device(&st);
   if (!di) return st;
-  QuantParams p;
-  p.x = x;
-  p.x8 = static_cast<uint8_t*>(x8);
-  p.scale = scale;
+  QuantParams p = {};
+  p.x[0] = x;
+  p.x8[0] = static_cast<uint8_t*>(x8);
+  p.scale[0] = scale;
+  p.hadamard[0] = hadamard;
+  p.transpose_out[0] = transpose_out;
+  p.ntens = 1;
   p.N = N;
   p.d = d;
   p.BH = B * H;
   p.n_sblk = (N + 63) / 64;
-  p.hadamard = hadamard;
-  p.transpose_out = transpose_out;
   p.flips_lo = flips_lo;
   p.flips_hi = flips_hi;
   p.per_head = per_head;
@@ -238,6 +239,42 @@ int quantize_fp8(const void* x, void* x8, float* scale, int B, int H, int N, int
 
 }  // namespace
 }  // namespace fa
+
+extern "C" int fa_quantize_fp8_qkv(const void* q, const void* k, const void* v, void* q8, void* k8, void* v8t,
+                                   float* q_scale, float* k_scale, float* v_scale, int B, int H, int N, int d,
+                                   int hadamard, void* stream) {
+  if (!q || !k || !v || !q8 || !k8 || !v8t || !q_scale || !k_scale || !v_scale) return FA_ERR_NULL;
+  if (hadamard != 0 && hadamard != 1) return FA_ERR_UNSUPPORTED;
+  int st = check_shape(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (N % 16 != 0) return FA_ERR_SHAPE;                    // V is written transposed
+  const void* xs[3] = {q, k, v};
+  void* x8s[3] = {q8, k8, v8t};
+  float* scs[3] = {q_scale, k_scale, v_scale};
+  for (int i = 0; i < 3; ++i)
+    if (!aligned(xs[i], 16) || !aligned(x8s[i], 16) || !aligned(scs[i], 4)) return FA_ERR_ALIGN;
+  const DeviceInfo* di = current_device(&st);
+  if (!di) return st;
+  QuantParams p = {};
+  for (int i = 0; i < 3; ++i) {
+    p.x[i] = xs[i];
+    p.x8[i] = static_cast<uint8_t*>(x8s[i]);
+    p.scale[i] = scs[i];
+    p.hadamard[i] = i < 2 ? hadamard : 0;                  // Q and K rotated, V never
+    p.transpose_out[i] = i == 2 ? 1 : 0;                   // V transposed for the P.V MMA
+  }
+  p.ntens = 3;
+  p.N = N;
+  p.d = d;
+  p.BH = B * H;
+  p.n_sblk = (N + 63) / 64;
+  p.amax_mode = 0;
+  p.sm_count = di->sm_count;
+  p.status = di->status;
+  p.timeout_ns = timeout_ns_for_call();
+  const cudaError_t e = launch_quant_fp8(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
 
 extern "C" int fa_quantize_fp8(const void* x, void* x8, float* scale, int B, int H, int N, int d,
                                int hadamard, int transpose_out, void* stream) {

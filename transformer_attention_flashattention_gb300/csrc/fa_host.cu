@@ -8,7 +8,7 @@
 // pass of the inputs over the link instead of inputs + compute + outputs in a row.
 // The device copies live in a caller-provided workspace; the copy streams and
 // events are created once per device and reused.  The FP8 variant runs the E4M3
-// prologue (three quantisation launches) and the E4M3 forward on each chunk.
+// prologue (one launch for Q, K and V) and the E4M3 forward on each chunk.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -195,10 +195,10 @@ extern "C" int fa_fwd_fp8_host(const void* q, const void* k, const void* v, void
                        const unsigned long long o16 = h0 * 2 * head_elems, o8 = h0 * head_elems;
                        const long long os = h0 * nsb;
                        const int n = static_cast<int>(hn);
-                       int r = FA_OK;
-                       for (int i = 0; i < 3 && r == FA_OK; ++i)   // Q, K rotated; V transposed, not rotated
-                         r = fa_quantize_fp8(dev_in[i] + o16, x8[i] + o8, sc[i] + os, 1, n, N, d,
-                                             i < 2 ? hadamard : 0, i == 2 ? 1 : 0, s);
+                       // Q, K rotated; V transposed, not rotated: one launch
+                       const int r = fa_quantize_fp8_qkv(dev_in[0] + o16, dev_in[1] + o16, dev_in[2] + o16,
+                                                         x8[0] + o8, x8[1] + o8, x8[2] + o8, sc[0] + os,
+                                                         sc[1] + os, sc[2] + os, 1, n, N, d, hadamard, s);
                        if (r != FA_OK) return r;
                        return fa_fwd_fp8(x8[0] + o8, x8[1] + o8, x8[2] + o8, dO + o16, lse ? dl + h0 * N : nullptr,
                                          1, n, N, d, scale, causal, sc[0] + os, sc[1] + os, sc[2] + os, hadamard, s);

@@ -31,20 +31,22 @@ struct FwdParams {
   int n_sblk;         // ceil(N / 64)
 };
 
-// FP8 prologue: block absmax E4M3 quantisation with an optional Hadamard rotation.
+// FP8 prologue: block absmax E4M3 quantisation with an optional Hadamard rotation, of
+// one tensor or of up to three tensors of the same shape in one launch (Q, K and V).
 struct QuantParams {
-  const void* x;      // bf16 [B*H, N, d]
-  uint8_t* x8;        // e4m3 [B*H, N, d], or [B*H, d, N] when transpose_out
-  float* scale;       // [B*H, n_sblk]
+  const void* x[3];       // bf16 [B*H, N, d] per tensor
+  uint8_t* x8[3];         // e4m3 [B*H, N, d], or [B*H, d, N] when that tensor's transpose_out
+  float* scale[3];        // [B*H, n_sblk] per tensor
+  int hadamard[3];
+  int transpose_out[3];
+  int ntens;              // tensors in this launch, 1..3
   int N;
   int d;
   int BH;
   int n_sblk;
-  int hadamard;
-  int transpose_out;
   unsigned long long flips_lo;   // randomised rotation: bit c negates coordinate c (c < 64) ...
   unsigned long long flips_hi;   // ... and c - 64 (64 <= c < 128) before the transform
-  int per_head;                  // one absmax per (b, h) instead of per 64-row block
+  int per_head;                  // one absmax per (b, h) instead of per 64-row block (one tensor)
   int amax_mode;                 // 0: own block absmax; 1: write the block absmax only;
                                  // 2: quantise with the absmax already in `scale`
   int sm_count;                  // SMs of the device; the persistent grid is a multiple of it

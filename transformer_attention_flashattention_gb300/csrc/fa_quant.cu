@@ -17,7 +17,9 @@
 // Variants: a sign mask negates chosen coordinates before the transform (the
 // randomised rotation x D H); with one scale per head, the kernel first runs in a
 // mode that only writes each block's absmax, a small kernel takes the head's
-// maximum into every block entry, and a second pass quantises with it.
+// maximum into every block entry, and a second pass quantises with it.  One launch
+// can take up to three tensors of the same shape (Q and K rotated, V transposed):
+// their blocks form one sequence, so the grid has one ramp and one tail, not three.
 #include <cstdint>
 
 #include <cuda_bf16.h>
@@ -100,17 +102,23 @@ __global__ void __launch_bounds__(kQuantThreads, kQuantCtasPerSm) fa_quant_fp8_k
   const int q = lane & 3;
   const int nl = warp * kRowsPerWarp + (lane >> 2);     // row within the block
   const int a = (q ^ (lane >> 2)) & (NC - 1);
-  const long long total = static_cast<long long>(p.BH) * p.n_sblk;
+  // blocks of one tensor, and of the launch (below 2^31, checked on the host)
+  const int per = p.BH * p.n_sblk;
+  const long long total = static_cast<long long>(per) * p.ntens;
   const long long G = gridDim.x;
-  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(p.x);
+  // the tensor of a block (selects, not a dynamic index into parameter space)
+  auto pick = [](int ti, auto a0, auto a1, auto a2) { return ti == 0 ? a0 : (ti == 1 ? a1 : a2); };
   const uint32_t full0 = ptx::smem_u32(&sm.full[0]);
   const ptx::WaitCtl ctl{&sm.abort, p.status, p.timeout_ns};
 
   // copy of block b (only its rows inside the head) into stage s
   auto issue = [&](long long b, int s) {
-    const int bh = static_cast<int>(b / p.n_sblk), blk = static_cast<int>(b % p.n_sblk);
+    const int ti = static_cast<int>(b) / per;
+    const int lb = static_cast<int>(b) - ti * per;
+    const int bh = lb / p.n_sblk, blk = lb % p.n_sblk;
     const uint32_t rows = static_cast<uint32_t>(min(kQuantRows, p.N - blk * kQuantRows));
     const uint32_t bar = full0 + 8u * static_cast<uint32_t>(s);
+    const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(pick(ti, p.x[0], p.x[1], p.x[2]));
     ptx::mbar_arrive_expect_tx(bar, rows * kRowBytes);
     ptx::bulk_load(ptx::smem_u32(sm.in[s]), x + (static_cast<size_t>(bh) * p.N + blk * kQuantRows) * D,
                    rows * kRowBytes, bar);
@@ -144,7 +152,9 @@ __global__ void __launch_bounds__(kQuantThreads, kQuantCtasPerSm) fa_quant_fp8_k
       return;
     }
 
-    const int bh = static_cast<int>(b / p.n_sblk), blk = static_cast<int>(b % p.n_sblk);
+    const int ti = static_cast<int>(b) / per;
+    const int lb = static_cast<int>(b) - ti * per;
+    const int bh = lb / p.n_sblk, blk = lb % p.n_sblk;
     const int n_base = blk * kQuantRows;
     const int valid = min(kQuantRows, p.N - n_base);
     float y[E];
@@ -180,7 +190,7 @@ __global__ void __launch_bounds__(kQuantThreads, kQuantCtasPerSm) fa_quant_fp8_k
       for (int e = 0; e < E; ++e) y[e] = 0.f;
     }
 
-    if (p.hadamard) {
+    if (pick(ti, p.hadamard[0], p.hadamard[1], p.hadamard[2])) {
       if ((p.flips_lo | p.flips_hi) != 0) {
         // randomised rotation: bit e of m negates this lane's coordinate q*E + e
         const int c0 = q * E;
@@ -239,18 +249,20 @@ __global__ void __launch_bounds__(kQuantThreads, kQuantCtasPerSm) fa_quant_fp8_k
     if (lane == 0) sm.wmax[warp] = amax;
     __syncthreads();   // every row of stage s has been read, and every warp's maximum written
     if (threadIdx.x == 0) {
+      float* const scale = pick(ti, p.scale[0], p.scale[1], p.scale[2]);
+      const int hadamard = pick(ti, p.hadamard[0], p.hadamard[1], p.hadamard[2]);
       float am = 0.f;
 #pragma unroll
       for (int w = 0; w < kQuantWarps; ++w) am = fmaxf(am, sm.wmax[w]);
       if (p.amax_mode == 1) {
-        p.scale[b] = am;                 // first pass of a per-head scale: absmax only
+        scale[lb] = am;                  // first pass of a per-head scale: absmax only
         sm.factor = 0.f;
       } else {
-        if (p.amax_mode == 2) am = p.scale[b];   // the head's absmax
+        if (p.amax_mode == 2) am = scale[lb];   // the head's absmax
         sm.factor = am > 0.f ? kE4m3Max / am : 0.f;
         float sc = 1.f;
-        if (am > 0.f) sc = p.hadamard ? am * (1.f / (kE4m3Max * sqrtf(static_cast<float>(D)))) : am / kE4m3Max;
-        p.scale[b] = sc;
+        if (am > 0.f) sc = hadamard ? am * (1.f / (kE4m3Max * sqrtf(static_cast<float>(D)))) : am / kE4m3Max;
+        scale[lb] = sc;
       }
     }
     __syncthreads();
@@ -265,9 +277,10 @@ __global__ void __launch_bounds__(kQuantThreads, kQuantCtasPerSm) fa_quant_fp8_k
       const float2 p23 = mul2_rn(make_float2(y[4 * w + 2], y[4 * w + 3]), f2);
       codes[w] = ptx::pack4_e4m3(p01.x, p01.y, p23.x, p23.y);
     }
-    if (!p.transpose_out) {
+    uint8_t* const x8 = pick(ti, p.x8[0], p.x8[1], p.x8[2]);
+    if (!pick(ti, p.transpose_out[0], p.transpose_out[1], p.transpose_out[2])) {
       if (nl < valid) {
-        uint8_t* dst = p.x8 + (static_cast<size_t>(bh) * p.N + n_base + nl) * D + q * E;
+        uint8_t* dst = x8 + (static_cast<size_t>(bh) * p.N + n_base + nl) * D + q * E;
 #pragma unroll
         for (int k = 0; k < E / 16; ++k)
           *reinterpret_cast<uint4*>(dst + 16 * k) =
@@ -298,7 +311,7 @@ __global__ void __launch_bounds__(kQuantThreads, kQuantCtasPerSm) fa_quant_fp8_k
         const uint32_t t2 = __byte_perm(r2, r3, 0x5140), t3 = __byte_perm(r2, r3, 0x7362);
         const uint32_t col[4] = {__byte_perm(t0, t2, 0x5410), __byte_perm(t0, t2, 0x7632),
                                  __byte_perm(t1, t3, 0x5410), __byte_perm(t1, t3, 0x7632)};
-        uint8_t* dst = p.x8 + (static_cast<size_t>(bh) * D + cg * 4) * p.N + n_base + rg * 4;
+        uint8_t* dst = x8 + (static_cast<size_t>(bh) * D + cg * 4) * p.N + n_base + rg * 4;
 #pragma unroll
         for (int e = 0; e < 4; ++e) *reinterpret_cast<uint32_t*>(dst + static_cast<size_t>(e) * p.N) = col[e];
       }
@@ -312,7 +325,7 @@ __global__ void __launch_bounds__(256) fa_quant_head_max_kernel(const __grid_con
   const long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x & 31;
   if (w >= p.BH) return;                 // whole warps leave together
-  float* row = p.scale + static_cast<size_t>(w) * p.n_sblk;
+  float* row = p.scale[0] + static_cast<size_t>(w) * p.n_sblk;
   float m = 0.f;
   for (int i = lane; i < p.n_sblk; i += 32) m = fmaxf(m, row[i]);
 #pragma unroll
@@ -330,7 +343,8 @@ cudaError_t launch_quant_pass(const QuantParams& p, unsigned grid, cudaStream_t 
 }  // namespace
 
 cudaError_t launch_quant_fp8(const QuantParams& p, cudaStream_t stream) {
-  const long long blocks = static_cast<long long>(p.n_sblk) * p.BH;
+  if (p.ntens < 1 || p.ntens > 3 || (p.per_head && p.ntens != 1)) return cudaErrorInvalidValue;
+  const long long blocks = static_cast<long long>(p.n_sblk) * p.BH * p.ntens;
   if (blocks >= (1ll << 31) || p.sm_count < 1) return cudaErrorInvalidConfiguration;
   const long long ctas = static_cast<long long>(p.sm_count) * kQuantCtasPerSm;
   const unsigned grid = static_cast<unsigned>(blocks < ctas ? blocks : ctas);
