@@ -9,8 +9,8 @@ bracketed by CUDA events, L2 flushed before each launch whose inputs fit in it):
 
   * 2x16x8192x128 and 1x16x16384x128 bf16, non-causal (the throughput bar's points);
   * 16x16x2048x128 bf16, both masks, and 2x16x8192x64 bf16, non-causal;
-  * the CTA-pair kernel (fa_fwd_2cta) on 2x16x8192x128, both masks of 16x16x2048x128
-    and the long-context workload, beside the single-CTA kernel;
+  * the CTA-pair kernel (fa_fwd_2cta) on 2x16x8192x128 and both masks of
+    16x16x2048x128, beside the single-CTA kernel;
   * the E4M3 forward on [4, 16, 4096, 128] (Hadamard on): the forward alone, the
     quantisation prologue (three launches, in GB/s against HBM), both together,
     and end to end from host bf16 Q/K/V to host bf16 O through ``fa_fwd_fp8_host``.
@@ -400,7 +400,6 @@ def _variants(fa, dev, timer, n, peaks, e2e_steps):
              ("16x16x2048x128_causal", WORKLOADS["bf16"], True, False),
              ("16x16x2048x128_non_causal_2cta", WORKLOADS["bf16"], False, True),
              ("16x16x2048x128_causal_2cta", WORKLOADS["bf16"], True, True),
-             ("1x32x32768x128_causal_2cta", WORKLOADS["long"], True, True),
              ("2x16x8192x64_non_causal", Workload("v8192d64", 2, 16, 8192, 64, torch.bfloat16, 2), False, False)]
     cache = {}
     for name, w, causal, pair in specs:
