@@ -503,8 +503,8 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   p.n_pad = (N + 127) / 128 * 128;
   p.n_blk = p.n_pad / 128;
   p.BH = static_cast<int>(BH);
-  p.lse2 = static_cast<float*>(workspace);
-  p.delta = p.lse2 + BH * static_cast<uint64_t>(p.n_pad);
+  p.nlse2 = static_cast<float*>(workspace);
+  p.ndelta = p.nlse2 + BH * static_cast<uint64_t>(p.n_pad);
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;

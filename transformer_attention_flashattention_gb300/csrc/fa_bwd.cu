@@ -11,8 +11,9 @@
 //   dS = P * (dO V^T - D),  dV = P^T dO,  dQ = scale * dS K,  dK = scale * dS^T Q.
 //
 // Three kernels on the caller's stream, no atomics (results are deterministic):
-//   prep   D and LSE*log2(e) into a workspace padded to 128 rows per head (padding:
-//          D = 0, LSE*log2(e) = +inf, so padded queries get P = 0)
+//   prep   -D and -LSE*log2(e) into a workspace padded to 128 rows per head (padding:
+//          0 and -inf, so padded queries get P = 0); negated so that both enter the
+//          packed-pair arithmetic below as addends
 //   dq     Q-stationary: per 128-row Q tile, stream K_j, V_j;
 //          S = Q K^T and dP = dO V^T (two SS MMAs into TMEM), dS in registers,
 //          packed into a TMEM region of its own, then dQ += dS K (TS MMA, K as an
@@ -132,7 +133,7 @@ __device__ __forceinline__ bool bwd_unit_at(const BwdParams& p, int k, bool cost
 
 // ---------------------------------------------------------------------------- prep
 
-// D_i = sum_c dO_ic O_ic and LSE_i * log2(e), one row per group of D/8 lanes.
+// -D_i = -sum_c dO_ic O_ic and -LSE_i * log2(e), one row per group of D/8 lanes.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __grid_constant__ BwdParams p) {
   constexpr int kLanes = D / 8;                      // 8 elements (16 bytes) per lane
@@ -166,8 +167,8 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __grid_constant_
   for (int m = kLanes / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, m);
   if (valid && part == 0) {
     const size_t w = static_cast<size_t>(bh) * p.n_pad + row;
-    p.delta[w] = row < p.N ? acc : 0.f;
-    p.lse2[w] = row < p.N ? p.lse[static_cast<size_t>(bh) * p.N + row] * kLog2e : INFINITY;
+    p.ndelta[w] = row < p.N ? -acc : 0.f;
+    p.nlse2[w] = row < p.N ? -(p.lse[static_cast<size_t>(bh) * p.N + row] * kLog2e) : -INFINITY;
   }
 }
 
@@ -195,11 +196,45 @@ __device__ void producer_drain(uint32_t sbase, const uint32_t (&last_fill)[kBwdS
     atomicOr(ctl.status, code);
 }
 
-// Packs the 32 floats a[0..31] into 16 words of two 16-bit values each.
-template <bool BF16>
-__device__ __forceinline__ void pack16(const float (&a)[32], uint32_t (&w)[16]) {
+// dS = P (dP - D) of 32 scores of one dq row, packed: P = 2^(s * c + nl) with the row's
+// nl = -LSE*log2(e) and nd = -D; with MASK, keys x >= visible get P = 0.  Pairs of columns
+// go through the packed fp32 forms (one instruction for two lanes of work).
+template <bool BF16, bool MASK>
+__device__ __forceinline__ void dq_row32(const uint32_t (&sr)[32], const uint32_t (&dr)[32], float2 cc, float2 nl,
+                                         float2 nd, int visible, uint32_t (&w)[16]) {
 #pragma unroll
-  for (int x = 0; x < 16; ++x) w[x] = ptx::pack2<BF16>(a[2 * x], a[2 * x + 1]);
+  for (int x = 0; x < 16; ++x) {
+    const float2 t = ptx::fma2(make_float2(__uint_as_float(sr[2 * x]), __uint_as_float(sr[2 * x + 1])), cc, nl);
+    float2 pv = make_float2(ptx::ex2(t.x), ptx::ex2(t.y));
+    if constexpr (MASK) {
+      if (2 * x >= visible) pv.x = 0.f;
+      if (2 * x + 1 >= visible) pv.y = 0.f;
+    }
+    const float2 ds =
+        ptx::mul2(pv, ptx::add2(make_float2(__uint_as_float(dr[2 * x]), __uint_as_float(dr[2 * x + 1])), nd));
+    w[x] = ptx::pack2<BF16>(ds.x, ds.y);
+  }
+}
+
+// P^T and dS^T of one key row against 32 queries, packed: the queries' -LSE*log2(e) and -D
+// come as pairs from shared memory (nl, nd); with MASK, queries x < first get P = 0.
+template <bool BF16, bool MASK>
+__device__ __forceinline__ void dkdv_row32(const uint32_t (&sr)[32], const uint32_t (&dr)[32], float2 cc,
+                                           const float2* nl, const float2* nd, int first, uint32_t (&wp)[16],
+                                           uint32_t (&wd)[16]) {
+#pragma unroll
+  for (int x = 0; x < 16; ++x) {
+    const float2 t = ptx::fma2(make_float2(__uint_as_float(sr[2 * x]), __uint_as_float(sr[2 * x + 1])), cc, nl[x]);
+    float2 pv = make_float2(ptx::ex2(t.x), ptx::ex2(t.y));
+    if constexpr (MASK) {
+      if (2 * x < first) pv.x = 0.f;
+      if (2 * x + 1 < first) pv.y = 0.f;
+    }
+    const float2 ds =
+        ptx::mul2(pv, ptx::add2(make_float2(__uint_as_float(dr[2 * x]), __uint_as_float(dr[2 * x + 1])), nd[x]));
+    wp[x] = ptx::pack2<BF16>(pv.x, pv.y);
+    wd[x] = ptx::pack2<BF16>(ds.x, ds.y);
+  }
 }
 
 // Writes COLS accumulator columns of one row, times `mul`, as 16-bit values at
@@ -377,7 +412,8 @@ __device__ __forceinline__ void dq_compute(const BwdParams& p, uint32_t sbase, u
     const int n = p.causal ? i + 1 : p.n_blk;
     const int row = i * 128 + r;
     const size_t wrow = static_cast<size_t>(bh) * p.n_pad + row;
-    const float lse2 = p.lse2[wrow], dlt = p.delta[wrow];
+    const float nl = p.nlse2[wrow], nd = p.ndelta[wrow];
+    const float2 cc = make_float2(p.scale_log2, p.scale_log2), nl2 = make_float2(nl, nl), nd2 = make_float2(nd, nd);
     const int limit = min(p.N, p.causal ? row + 1 : p.N);      // keys >= limit get P = 0
     for (int j = 0; j < n; ++j, ++tile) {
       const bool got = ptx::mbar_wait(bar(C::kSdpFull), tile & 1u, ctl, 4u);
@@ -395,16 +431,12 @@ __device__ __forceinline__ void dq_compute(const BwdParams& p, uint32_t sbase, u
       if (lane == 0) ptx::mbar_arrive(bar(C::kSdpFree));
       const int visible = limit - (j * 128 + 64 * sub);
       uint32_t w[2][16];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float ds[32];
-#pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          const float pv = 32 * c + x < visible
-                               ? ptx::ex2(fmaf(__uint_as_float(sr[c][x]), p.scale_log2, -lse2)) : 0.f;
-          ds[x] = pv * (__uint_as_float(dr[c][x]) - dlt);
-        }
-        pack16<kBf16>(ds, w[c]);
+      if (visible >= 64) {
+        dq_row32<kBf16, false>(sr[0], dr[0], cc, nl2, nd2, 0, w[0]);
+        dq_row32<kBf16, false>(sr[1], dr[1], cc, nl2, nd2, 0, w[1]);
+      } else {
+        dq_row32<kBf16, true>(sr[0], dr[0], cc, nl2, nd2, visible, w[0]);
+        dq_row32<kBf16, true>(sr[1], dr[1], cc, nl2, nd2, visible - 32, w[1]);
       }
       // the previous tile's dQ MMAs have read the dS region
       if (j > 0 || units > 0) {
@@ -454,8 +486,8 @@ __device__ __noinline__ void dkdv_producer(const BwdParams& p, uint32_t sbase, c
       load_tile<D, E>(&p.tm_q, dst, bar(C::kReady + s), i * 128, bh);
       load_tile<D, E>(&p.tm_do, dst + C::kTile, bar(C::kReady + s), i * 128, bh);
       const size_t w = static_cast<size_t>(bh) * p.n_pad + i * 128;
-      ptx::bulk_load(dst + 2 * C::kTile, p.lse2 + w, C::kVecBytes, bar(C::kReady + s));
-      ptx::bulk_load(dst + 2 * C::kTile + C::kVecBytes, p.delta + w, C::kVecBytes, bar(C::kReady + s));
+      ptx::bulk_load(dst + 2 * C::kTile, p.nlse2 + w, C::kVecBytes, bar(C::kReady + s));
+      ptx::bulk_load(dst + 2 * C::kTile + C::kVecBytes, p.ndelta + w, C::kVecBytes, bar(C::kReady + s));
       last_fill[s] = f;
     }
   }
@@ -544,6 +576,7 @@ __device__ __forceinline__ void dkdv_compute(const BwdParams& p, uint32_t sbase,
   for (int k = 0; bwd_unit_at(p, k, false, bh, j); ++k) {
     const int i0 = p.causal ? j : 0;
     const int key = j * 128 + kr;
+    const float2 cc = make_float2(p.scale_log2, p.scale_log2);
     for (int i = i0; i < p.n_blk; ++i, ++tile) {
       const uint32_t s = tile % kBwdStages;
       const float* vec = reinterpret_cast<const float*>(smem + C::kRingOff + s * C::kStageBytes + 2 * C::kTile);
@@ -553,25 +586,18 @@ __device__ __forceinline__ void dkdv_compute(const BwdParams& p, uint32_t sbase,
         if (!__all_sync(0xFFFFFFFFu, got)) return;
         ptx::tc_fence_after();
         const int q0 = 64 * h + 32 * sub;                      // first query of this thread's 32
-        const float* lse2 = vec + q0;
-        const float* dlt = vec + 128 + q0;
-        // causal diagonal tile: query i*128 + q0 + x sees this key iff q0 + x >= kr (padded
-        // queries have LSE*log2(e) = +inf and so P = 0 already)
-        const int first = (p.causal && i == j) ? kr - q0 : 0;
+        const float2* nl = reinterpret_cast<const float2*>(vec + q0);
+        const float2* nd = reinterpret_cast<const float2*>(vec + 128 + q0);
         const uint32_t tS = tmem + lane_base + kTmHalf * h + 32 * sub, tDP = tS + kTmDP;
         uint32_t sr[32], dr[32];
         ptx::tmem_ld32(tS, sr);
         ptx::tmem_ld32(tDP, dr);
         ptx::tmem_wait_ld();
-        float pv[32], ds[32];
-#pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          pv[x] = x >= first ? ptx::ex2(fmaf(__uint_as_float(sr[x]), p.scale_log2, -lse2[x])) : 0.f;
-          ds[x] = pv[x] * (__uint_as_float(dr[x]) - dlt[x]);
-        }
         uint32_t wp[16], wd[16];
-        pack16<kBf16>(pv, wp);
-        pack16<kBf16>(ds, wd);
+        // causal diagonal tile: query i*128 + q0 + x sees this key iff q0 + x >= kr (padded
+        // queries have -LSE*log2(e) = -inf and so P = 0 already)
+        if (p.causal && i == j) dkdv_row32<kBf16, true>(sr, dr, cc, nl, nd, kr - q0, wp, wd);
+        else dkdv_row32<kBf16, false>(sr, dr, cc, nl, nd, 0, wp, wd);
         ptx::tmem_st16(tS, wp);                                // over this thread's first 16 columns
         ptx::tmem_st16(tDP, wd);
         ptx::tmem_wait_st();

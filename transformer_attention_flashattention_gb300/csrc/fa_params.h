@@ -85,8 +85,8 @@ struct BwdParams {
   const void* o;      // [B*H, N, d] (prep kernel)
   const void* dout;   // [B*H, N, d] (prep kernel)
   const float* lse;   // [B*H, N] natural-log LSE of the forward pass
-  float* lse2;        // workspace [B*H, n_pad]: lse * log2(e), +inf on padded rows
-  float* delta;       // workspace [B*H, n_pad]: sum_c dO_ic O_ic, 0 on padded rows
+  float* nlse2;       // workspace [B*H, n_pad]: -lse * log2(e), -inf on padded rows
+  float* ndelta;      // workspace [B*H, n_pad]: -sum_c dO_ic O_ic, 0 on padded rows
   void* dq;           // [B*H, N, d], same type as the inputs
   void* dk;
   void* dv;
