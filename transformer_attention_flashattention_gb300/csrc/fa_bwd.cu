@@ -19,29 +19,32 @@
 //          packed into a TMEM region of its own, then dQ += dS K (TS MMA, K as an
 //          MN-major operand)
 //   dkdv   K/V-stationary: per 128-key tile, stream Q_i, dO_i (+ their LSE, D);
-//          S^T = K Q^T and dP^T = V dO^T, then P^T and dS^T per key row, then
-//          dV += P^T dO and dK += dS^T Q (both TS MMAs)
+//          S^T = K Q^T and dP^T = V dO^T (SS), then P^T (into TMEM) and dS^T (into
+//          shared memory) per key row, then dV += P^T dO (TS) and dK += dS^T Q (SS)
 // S and dP are computed twice (once per kernel) in exchange for no dQ reduction.
 //
 // Each main kernel is a persistent grid with these roles (320 threads):
 //   warps 0-7  compute: warp w takes TMEM lanes 32*(w%4).. (Q rows, or key rows) and
 //              column half w/4, so every row is shared by two threads
 //   warp 8     TMA producer: the unit's two stationary tiles, then the streamed tiles
-//              (dq: K in a 3-slot ring and V in a 2-slot ring; dkdv: a 2-stage ring)
+//              (dq: K in a 3-slot ring and V in a 2-slot ring; dkdv: Q and dO in
+//              2-slot rings)
 //   warp 9     MMA issuer (one thread) and TMEM owner
 // dq kernel: whole 128-key tiles, S and dP with N = 128.  The compute threads signal as
 // soon as S(j) and dP(j) are in their registers, and the MMA thread then issues S(j+1)
 // and dP(j+1) into the same TMEM columns while dS(j) is being computed; dS goes to a
 // region of its own, read by dQ += dS K.  24 MMA instructions a key tile (d = 128).
 // TMEM: S (128 columns) | dP (128) | dS (64, two 16-bit values a column) | dQ (D).
-// dkdv kernel: each 128-row streamed tile is processed as two 64-row halves a and b with
-// their own S and dP buffers, so the compute warps work on one half while the tensor
-// pipe runs the other half's (or the next tile's) MMAs (its TMEM holds two accumulators
-// and has no room for a separate P/dS region).
-// TMEM (512 columns): S_a | dP_a | S_b | dP_b (64 columns each) | dV | dK.
-// A dkdv compute thread handles 32 of a half's 64 columns and packs its 16-bit results
-// over the first 16 columns of its own 32 (never over the other thread's, which may still
-// be unread), so a half's TS MMAs read their A operand from columns {0, 8, 32, 40}.
+// dkdv kernel: whole 128-query tiles, S^T and dP^T with N = 128, in the tensor-pipe order
+//   ... S^T(i)  dP^T(i)  dV(i)  S^T(i+1)  dK(i)  dP^T(i+1)  dV(i+1) ...
+// The compute threads form P^T(i) as soon as S^T(i) is in, packed over the S^T columns
+// they have read (queries 0-63 at columns 0-31, 64-127 at 64-95), for dV += P^T dO; then,
+// once dP^T(i) is in, dS^T(i) from the P values they kept in registers, into shared memory
+// as a K-major tile for dK += dS^T Q.  So each half of their work overlaps two products
+// of the pipe.  The pipe runs its MMAs in order: S^T(i+1) overwrites P^T(i) only after
+// dV(i) has read it, and dP^T(i+1) completes only after dK(i) has read the dS^T tile.  32
+// MMA instructions a Q tile (d = 128).
+// TMEM (512 columns at d = 128): S^T | dP^T (128 columns each) | dV | dK.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -55,8 +58,8 @@ constexpr int kBwdComputeWarps = 8;
 constexpr int kBwdThreads = kBwdComputeWarps * 32 + 64;
 constexpr int kBwdLoadWarp = 8;
 constexpr int kBwdMmaWarp = 9;
-constexpr int kBwdStages = 2;
-constexpr uint32_t kTmHalf = 128, kTmDP = 64, kTmAcc = 256;   // dkdv, half h: S at 128h, dP at 128h + 64
+constexpr int kBwdStages = 2;                                      // dkdv: Q and dO ring slots
+constexpr uint32_t kTmS = 0, kTmDP = 128, kTmAcc = 256;            // dkdv: S^T | dP^T | dV | dK
 constexpr uint32_t kQS = 0, kQDP = 128, kQDS = 256, kQAcc = 320;  // dq: S | dP | dS | dQ
 constexpr float kLog2e = 1.44269504088896340736f;
 
@@ -65,10 +68,7 @@ struct BwdCfg {
   using L = FwdCfg<D, Elem::BF16>;                    // tile geometry (same for f16)
   static constexpr int kTile = L::kTileBytes;         // 128 rows x D, 128-byte swizzle atoms
   static constexpr int kStatOff = 0;                  // the unit's two stationary tiles
-  static constexpr int kRingOff = 2 * kTile;
-  static constexpr int kVecBytes = 128 * 4;           // one tile's LSE*log2(e) (or D) values
-  static constexpr int kStageBytes = 2 * kTile + 2 * kVecBytes;
-  static_assert(kStageBytes % 1024 == 0, "stages keep the tiles 1 KB aligned");
+  static constexpr int kVecBytes = 128 * 4;           // one tile's -LSE*log2(e) (or -D) values
   // dq kernel: the stationary Q and dO tiles, then K in a ring of kDqKSlots tiles and V in
   // one of kDqVSlots.  V_j is free once dP(j) has run, K_j only after dQ += dS(j) K_j, so
   // the two rings release at different points and K needs the deeper one.
@@ -76,7 +76,16 @@ struct BwdCfg {
   static constexpr int kDqKOff = 2 * kTile;
   static constexpr int kDqVOff = kDqKOff + kDqKSlots * kTile;
   static constexpr int kDqEnd = kDqVOff + kDqVSlots * kTile;
-  static constexpr int kDkdvEnd = kRingOff + kBwdStages * kStageBytes;
+  // dkdv kernel: the stationary K and V tiles, Q and dO in rings of kBwdStages slots (Q_i is
+  // free after dK += dS^T Q_i, dO_i after dV += P^T dO_i), each Q slot's -LSE*log2(e) and -D
+  // vectors, and the dS^T tile (128 keys x 128 queries, K-major, two 128-byte swizzle atoms)
+  static constexpr int kKvQOff = 2 * kTile;
+  static constexpr int kKvDoOff = kKvQOff + kBwdStages * kTile;
+  static constexpr int kKvVecOff = kKvDoOff + kBwdStages * kTile;
+  static constexpr int kKvDsOff = kKvVecOff + kBwdStages * 2 * kVecBytes;
+  static constexpr int kDsAtom = 128 * 128;           // 64 queries of all 128 key rows
+  static_assert(kKvDsOff % 1024 == 0, "the dS^T tile is 1 KB aligned");
+  static constexpr int kDkdvEnd = kKvDsOff + 2 * kDsAtom;
   static constexpr int kBarOff = kDqEnd > kDkdvEnd ? kDqEnd : kDkdvEnd;
   // barriers
   static constexpr int kStFull = 0, kStEmpty = 1, kReady = 2, kDone = kReady + kBwdStages;
@@ -87,10 +96,17 @@ struct BwdCfg {
   static constexpr int kSdpFree = kMmaDone + 1, kDsFree = kSdpFree + 1;
   static constexpr int kKFull = kDsFree + 1, kKFree = kKFull + kDqKSlots;
   static constexpr int kVFull = kKFree + kDqKSlots, kVFree = kVFull + kDqVSlots;
-  static constexpr int kNumBars = kVFree + kDqVSlots;
+  // dkdv kernel only: its dO slots' full / free barriers.  It also takes kReady / kDone as
+  // its Q slots' full / free barriers, kSdpFull / kSdpFull + 1 as "S^T in" / "dP^T in"
+  // (commits), and kDsFull / kDsFull + 1 as "dS^T written" / "P^T written" (compute arrives).
+  static constexpr int kDoFull = kVFree + kDqVSlots, kDoFree = kDoFull + kBwdStages;
+  static constexpr int kNumBars = kDoFree + kBwdStages;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
-  static constexpr int kAlloc = kBytes + 1024;
+  // No alignment slack: the kernel checks that its dynamic shared memory starts on a 1 KB
+  // boundary (which the 128-byte swizzle of TMA and the MMA descriptors needs) and does no
+  // work, setting a status bit, if it does not.
+  static constexpr int kAlloc = kBytes;
   static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
@@ -182,20 +198,6 @@ __device__ __forceinline__ void load_tile(const CUtensorMap* map, uint32_t dst, 
     ptx::tma_load_3d(dst + a * L::kAtomBytes, map, bar, a * L::kAtomElems, row0, bh);
 }
 
-// Bounded wait for every copy issued so far on the ring and stationary barriers.
-template <int D>
-__device__ void producer_drain(uint32_t sbase, const uint32_t (&last_fill)[kBwdStages], uint32_t st_fills,
-                               const ptx::WaitCtl& ctl, unsigned code) {
-  using C = BwdCfg<D>;
-  for (int s = 0; s < kBwdStages; ++s)
-    if (last_fill[s] != 0xFFFFFFFFu &&
-        !ptx::mbar_wait_drain(sbase + C::kBarOff + 8u * (C::kReady + s), last_fill[s] & 1u, ctl.timeout_ns))
-      atomicOr(ctl.status, code);
-  if (st_fills > 0 &&
-      !ptx::mbar_wait_drain(sbase + C::kBarOff + 8u * C::kStFull, (st_fills - 1u) & 1u, ctl.timeout_ns))
-    atomicOr(ctl.status, code);
-}
-
 // dS = P (dP - D) of 32 scores of one dq row, packed: P = 2^(s * c + nl) with the row's
 // nl = -LSE*log2(e) and nd = -D; with MASK, keys x >= visible get P = 0.  Pairs of columns
 // go through the packed fp32 forms (one instruction for two lanes of work).
@@ -216,24 +218,34 @@ __device__ __forceinline__ void dq_row32(const uint32_t (&sr)[32], const uint32_
   }
 }
 
-// P^T and dS^T of one key row against 32 queries, packed: the queries' -LSE*log2(e) and -D
-// come as pairs from shared memory (nl, nd); with MASK, queries x < first get P = 0.
+// P^T of one key row against 32 queries: P = 2^(s * c + nl) with the queries'
+// -LSE*log2(e) as pairs from shared memory; with MASK, queries x < first get P = 0.  The
+// values stay in pv for dS; w gets them packed.
 template <bool BF16, bool MASK>
-__device__ __forceinline__ void dkdv_row32(const uint32_t (&sr)[32], const uint32_t (&dr)[32], float2 cc,
-                                           const float2* nl, const float2* nd, int first, uint32_t (&wp)[16],
-                                           uint32_t (&wd)[16]) {
+__device__ __forceinline__ void dkdv_p32(const uint32_t (&sr)[32], float2 cc, const float2* nl, int first,
+                                         float2 (&pv)[16], uint32_t (&w)[16]) {
 #pragma unroll
   for (int x = 0; x < 16; ++x) {
     const float2 t = ptx::fma2(make_float2(__uint_as_float(sr[2 * x]), __uint_as_float(sr[2 * x + 1])), cc, nl[x]);
-    float2 pv = make_float2(ptx::ex2(t.x), ptx::ex2(t.y));
+    float2 v = make_float2(ptx::ex2(t.x), ptx::ex2(t.y));
     if constexpr (MASK) {
-      if (2 * x < first) pv.x = 0.f;
-      if (2 * x + 1 < first) pv.y = 0.f;
+      if (2 * x < first) v.x = 0.f;
+      if (2 * x + 1 < first) v.y = 0.f;
     }
+    pv[x] = v;
+    w[x] = ptx::pack2<BF16>(v.x, v.y);
+  }
+}
+
+// dS^T = P (dP - D) of one key row against 32 queries, packed (nd: the queries' -D pairs).
+template <bool BF16>
+__device__ __forceinline__ void dkdv_ds32(const uint32_t (&dr)[32], const float2 (&pv)[16], const float2* nd,
+                                          uint32_t (&w)[16]) {
+#pragma unroll
+  for (int x = 0; x < 16; ++x) {
     const float2 ds =
-        ptx::mul2(pv, ptx::add2(make_float2(__uint_as_float(dr[2 * x]), __uint_as_float(dr[2 * x + 1])), nd[x]));
-    wp[x] = ptx::pack2<BF16>(pv.x, pv.y);
-    wd[x] = ptx::pack2<BF16>(ds.x, ds.y);
+        ptx::mul2(pv[x], ptx::add2(make_float2(__uint_as_float(dr[2 * x]), __uint_as_float(dr[2 * x + 1])), nd[x]));
+    w[x] = ptx::pack2<BF16>(ds.x, ds.y);
   }
 }
 
@@ -266,38 +278,40 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, float mul, void* o
   }
 }
 
-// SS MMAs over d with N = 64: one 64-row half of a 128-row B tile (its descriptor
-// starts 64 rows = 8 KB, a whole number of swizzle atoms, into the tile).
-template <int D, Elem E, int KK = 0>
-__device__ __forceinline__ void issue_s64(uint32_t tD, uint32_t a_lo, uint32_t b_lo) {
-  using L = FwdCfg<D, E>;
-  if constexpr (KK < D / L::kMmaK) {
-    constexpr uint32_t idesc = ptx::idesc_make(kBlockM, 64, L::kAbType, false, false);
-    constexpr uint32_t desc_hi = ptx::sdesc_hi(1024);
-    constexpr uint32_t kOff = ((KK * 32 / 128) * L::kAtomBytes + (KK * 32) % 128) >> 4;
-    ptx::mma_f16_ss_o<KK ? 1 : 0, kOff, kOff>(tD, a_lo, b_lo, desc_hi, idesc);
-    issue_s64<D, E, KK + 1>(tD, a_lo, b_lo);
-  }
-}
-
-// The 4 TS MMAs of one 64-key (or 64-query) half: A packed by the two compute threads
-// of a row at TMEM columns {0, 8} and {32, 40}, B 64 MN-major rows (16 per step).
+// dV += P^T dO over a tile's 128 queries: A = P^T packed in TMEM by the two compute threads
+// of each key row (queries 0-63 at columns 0-31, 64-127 at columns 64-95), B = dO as an
+// MN-major operand (16 query rows, 2 KB, a step).
 template <int D, Elem E, bool ACC, int KK = 0>
-__device__ __forceinline__ void issue_pv64(uint32_t tO, uint32_t tA, uint32_t b_lo) {
+__device__ __forceinline__ void issue_dv(uint32_t tD, uint32_t tA, uint32_t b_lo) {
   using L = FwdCfg<D, E>;
   static_assert(!L::kFp8, "16-bit operands");
-  if constexpr (KK < 4) {
+  if constexpr (KK < 8) {
     constexpr uint32_t idesc = ptx::idesc_make(kBlockM, D, L::kAbType, false, true);
     constexpr uint32_t desc_hi = ptx::sdesc_hi(1024);
     constexpr int kAcc = (ACC || KK > 0) ? 1 : 0;
-    constexpr uint32_t kOt = (KK & 1) * 8 + (KK >> 1) * 32;
+    constexpr uint32_t kOt = 8 * KK + (KK >= 4 ? 32 : 0);
     constexpr uint32_t kOb = (KK * 16 * 128) >> 4;
-    ptx::mma_f16_ts_o<kAcc, kOt, kOb>(tO, tA, b_lo, desc_hi, idesc);
-    issue_pv64<D, E, ACC, KK + 1>(tO, tA, b_lo);
+    ptx::mma_f16_ts_o<kAcc, kOt, kOb>(tD, tA, b_lo, desc_hi, idesc);
+    issue_dv<D, E, ACC, KK + 1>(tD, tA, b_lo);
   }
 }
 
-constexpr uint32_t kHalfDesc = (64 * 128) >> 4;    // 64 rows of 128-byte swizzle atoms
+// dK += dS^T Q: A = the dS^T tile in shared memory (K-major, 32 bytes of queries a step
+// inside a 128-byte swizzle atom), B = Q as an MN-major operand.
+template <int D, Elem E, bool ACC, int KK = 0>
+__device__ __forceinline__ void issue_dk(uint32_t tD, uint32_t a_lo, uint32_t b_lo) {
+  using L = FwdCfg<D, E>;
+  static_assert(!L::kFp8, "16-bit operands");
+  if constexpr (KK < 8) {
+    constexpr uint32_t idesc = ptx::idesc_make(kBlockM, D, L::kAbType, false, true);
+    constexpr uint32_t desc_hi = ptx::sdesc_hi(1024);
+    constexpr int kAcc = (ACC || KK > 0) ? 1 : 0;
+    constexpr uint32_t kOa = ((KK * 32 / 128) * BwdCfg<D>::kDsAtom + (KK * 32) % 128) >> 4;
+    constexpr uint32_t kOb = (KK * 16 * 128) >> 4;
+    ptx::mma_f16_ss_o<kAcc, kOa, kOb>(tD, a_lo, b_lo, desc_hi, idesc);
+    issue_dk<D, E, ACC, KK + 1>(tD, a_lo, b_lo);
+  }
+}
 
 // ---------------------------------------------------------------------------- dq kernel
 
@@ -467,89 +481,110 @@ __device__ __forceinline__ void dq_compute(const BwdParams& p, uint32_t sbase, u
 template <int D, Elem E>
 __device__ __noinline__ void dkdv_producer(const BwdParams& p, uint32_t sbase, const ptx::WaitCtl& ctl) {
   using C = BwdCfg<D>;
+  using L = FwdCfg<D, E>;
   auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
-  uint32_t tile = 0, units = 0;
-  uint32_t last_fill[kBwdStages] = {0xFFFFFFFFu, 0xFFFFFFFFu};
+  uint32_t nd = 0, nq = 0, units = 0;   // dO and Q fills issued so far, stationary fills
   int bh, j;
   for (int k = 0; bwd_unit_at(p, k, false, bh, j); ++k) {
     const int i0 = p.causal ? j : 0;
+    // the next unit's stationary tiles into L2 while this unit runs
+    int bhn, jn;
+    if (bwd_unit_at(p, k + 1, false, bhn, jn)) {
+#pragma unroll
+      for (int a = 0; a < L::kAtoms; ++a) {
+        ptx::tma_prefetch_3d(&p.tm_k, a * L::kAtomElems, jn * 128, bhn);
+        ptx::tma_prefetch_3d(&p.tm_v, a * L::kAtomElems, jn * 128, bhn);
+      }
+    }
     if (!ptx::mbar_wait(bar(C::kStEmpty), (units & 1u) ^ 1u, ctl, 1u)) goto drain;
     ptx::mbar_arrive_expect_tx(bar(C::kStFull), 2 * C::kTile);
     load_tile<D, E>(&p.tm_k, sbase + C::kStatOff, bar(C::kStFull), j * 128, bh);
     load_tile<D, E>(&p.tm_v, sbase + C::kStatOff + C::kTile, bar(C::kStFull), j * 128, bh);
     ++units;
-    for (int i = i0; i < p.n_blk; ++i, ++tile) {
-      const uint32_t s = tile % kBwdStages, f = tile / kBwdStages;
+    for (int i = i0; i < p.n_blk; ++i) {
+      // tile number nq == nd: its ring slot and the slot's fill count
+      const uint32_t s = nq % kBwdStages, f = nq / kBwdStages;
+      // Q first: S^T is the first product of a tile
       if (!ptx::mbar_wait(bar(C::kDone + s), (f & 1u) ^ 1u, ctl, 1u)) goto drain;
-      const uint32_t dst = sbase + C::kRingOff + s * C::kStageBytes;
-      ptx::mbar_arrive_expect_tx(bar(C::kReady + s), 2 * C::kTile + 2 * C::kVecBytes);
-      load_tile<D, E>(&p.tm_q, dst, bar(C::kReady + s), i * 128, bh);
-      load_tile<D, E>(&p.tm_do, dst + C::kTile, bar(C::kReady + s), i * 128, bh);
+      ptx::mbar_arrive_expect_tx(bar(C::kReady + s), C::kTile + 2 * C::kVecBytes);
+      load_tile<D, E>(&p.tm_q, sbase + C::kKvQOff + s * C::kTile, bar(C::kReady + s), i * 128, bh);
       const size_t w = static_cast<size_t>(bh) * p.n_pad + i * 128;
-      ptx::bulk_load(dst + 2 * C::kTile, p.nlse2 + w, C::kVecBytes, bar(C::kReady + s));
-      ptx::bulk_load(dst + 2 * C::kTile + C::kVecBytes, p.ndelta + w, C::kVecBytes, bar(C::kReady + s));
-      last_fill[s] = f;
+      const uint32_t vec = sbase + C::kKvVecOff + s * 2 * C::kVecBytes;
+      ptx::bulk_load(vec, p.nlse2 + w, C::kVecBytes, bar(C::kReady + s));
+      ptx::bulk_load(vec + C::kVecBytes, p.ndelta + w, C::kVecBytes, bar(C::kReady + s));
+      ++nq;
+      if (!ptx::mbar_wait(bar(C::kDoFree + s), (f & 1u) ^ 1u, ctl, 1u)) goto drain;
+      ptx::mbar_arrive_expect_tx(bar(C::kDoFull + s), C::kTile);
+      load_tile<D, E>(&p.tm_do, sbase + C::kKvDoOff + s * C::kTile, bar(C::kDoFull + s), i * 128, bh);
+      ++nd;
     }
   }
 drain:
-  producer_drain<D>(sbase, last_fill, units, ctl, 8u);
+  // Copies still in flight must land before the CTA may exit: the last fill of every slot
+  // issued so far (immediate on the normal path)
+  for (uint32_t t = nd > static_cast<uint32_t>(kBwdStages) ? nd - kBwdStages : 0; t < nd; ++t)
+    if (!ptx::mbar_wait_drain(bar(C::kDoFull + t % kBwdStages), (t / kBwdStages) & 1u, ctl.timeout_ns))
+      atomicOr(ctl.status, 8u);
+  for (uint32_t t = nq > static_cast<uint32_t>(kBwdStages) ? nq - kBwdStages : 0; t < nq; ++t)
+    if (!ptx::mbar_wait_drain(bar(C::kReady + t % kBwdStages), (t / kBwdStages) & 1u, ctl.timeout_ns))
+      atomicOr(ctl.status, 8u);
+  if (units > 0 && !ptx::mbar_wait_drain(bar(C::kStFull), (units - 1u) & 1u, ctl.timeout_ns))
+    atomicOr(ctl.status, 8u);
 }
 
 template <int D, Elem E>
 __device__ __noinline__ void dkdv_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const ptx::WaitCtl& ctl) {
   using C = BwdCfg<D>;
   auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
+  constexpr uint32_t kTileDesc = C::kTile >> 4;
   const uint32_t k_lo = ptx::sdesc_lo(sbase + C::kStatOff, 16);                  // K as K-major A of S^T
   const uint32_t v_lo = ptx::sdesc_lo(sbase + C::kStatOff + C::kTile, 16);       // V as K-major A of dP^T
-  constexpr uint32_t kStageDesc = C::kStageBytes >> 4;
-  const uint32_t q_lo0 = ptx::sdesc_lo(sbase + C::kRingOff, 16);                 // Q as K-major B of S^T
-  const uint32_t do_lo0 = ptx::sdesc_lo(sbase + C::kRingOff + C::kTile, 16);     // dO as K-major B of dP^T
-  const uint32_t qmn_lo0 = ptx::sdesc_lo(sbase + C::kRingOff, v_lbo<D, E>());    // Q as MN-major B of dK
-  const uint32_t domn_lo0 = ptx::sdesc_lo(sbase + C::kRingOff + C::kTile, v_lbo<D, E>());  // dO, of dV
-  const uint32_t tDV = tmem + kTmAcc, tDK = tmem + kTmAcc + D;
-  // S^T_h = K Q_h^T and dP^T_h = V dO_h^T for query half h of the tile in ring stage s
-  auto sdp = [&](uint32_t s, int h) {
-    const uint32_t tS = tmem + kTmHalf * h;
-    issue_s64<D, E>(tS, k_lo, q_lo0 + s * kStageDesc + kHalfDesc * h);
-    issue_s64<D, E>(tS + kTmDP, v_lo, do_lo0 + s * kStageDesc + kHalfDesc * h);
-    ptx::mma_commit(bar(C::kSdpFull + h));
+  const uint32_t q_lo0 = ptx::sdesc_lo(sbase + C::kKvQOff, 16);                  // Q as K-major B of S^T
+  const uint32_t do_lo0 = ptx::sdesc_lo(sbase + C::kKvDoOff, 16);                // dO as K-major B of dP^T
+  const uint32_t qmn_lo0 = ptx::sdesc_lo(sbase + C::kKvQOff, v_lbo<D, E>());     // Q as MN-major B of dK
+  const uint32_t domn_lo0 = ptx::sdesc_lo(sbase + C::kKvDoOff, v_lbo<D, E>());   // dO as MN-major B of dV
+  const uint32_t ds_lo = ptx::sdesc_lo(sbase + C::kKvDsOff, 16);                 // dS^T as K-major A of dK
+  const uint32_t tS = tmem + kTmS, tDP = tmem + kTmDP, tDV = tmem + kTmAcc, tDK = tmem + kTmAcc + D;
+  // S^T = K Q^T and dP^T = V dO^T of streamed tile t (N = 128), each with its commit
+  auto st = [&](uint32_t t) -> bool {
+    const uint32_t s = t % kBwdStages;
+    if (!ptx::mbar_wait(bar(C::kReady + s), (t / kBwdStages) & 1u, ctl, 2u)) return false;
+    ptx::tc_fence_after();
+    issue_s<D, E>(tS, k_lo, q_lo0 + s * kTileDesc);
+    ptx::mma_commit(bar(C::kSdpFull));
+    return true;
+  };
+  auto dp = [&](uint32_t t) -> bool {
+    const uint32_t s = t % kBwdStages;
+    if (!ptx::mbar_wait(bar(C::kDoFull + s), (t / kBwdStages) & 1u, ctl, 2u)) return false;
+    ptx::tc_fence_after();
+    issue_s<D, E>(tDP, v_lo, do_lo0 + s * kTileDesc);
+    ptx::mma_commit(bar(C::kSdpFull + 1));
+    return true;
   };
   uint32_t tile = 0, units = 0;
   int bh, j;
   for (int k = 0; bwd_unit_at(p, k, false, bh, j); ++k) {
     const int i0 = p.causal ? j : 0;
     if (!ptx::mbar_wait(bar(C::kStFull), units & 1u, ctl, 2u)) goto done;
-    {
-      const uint32_t s0 = tile % kBwdStages;
-      if (!ptx::mbar_wait(bar(C::kReady + s0), (tile / kBwdStages) & 1u, ctl, 2u)) goto done;
-      sdp(s0, 0);
-      sdp(s0, 1);
-    }
+    if (!st(tile) || !dp(tile)) goto done;
     for (int i = i0; i < p.n_blk; ++i, ++tile) {
       const uint32_t s = tile % kBwdStages;
       const bool more = i + 1 < p.n_blk;
-      const uint32_t sn = (tile + 1) % kBwdStages;
-      // half a: dV += P^T_a dO_a, dK += dS^T_a Q_a, then the next tile's half a
-      if (!ptx::mbar_wait(bar(C::kDsFull), tile & 1u, ctl, 2u)) goto done;
-      ptx::tc_fence_after();
-      if (i == i0) {
-        issue_pv64<D, E, false>(tDV, tmem, domn_lo0 + s * kStageDesc);
-        issue_pv64<D, E, false>(tDK, tmem + kTmDP, qmn_lo0 + s * kStageDesc);
-      } else {
-        issue_pv64<D, E, true>(tDV, tmem, domn_lo0 + s * kStageDesc);
-        issue_pv64<D, E, true>(tDK, tmem + kTmDP, qmn_lo0 + s * kStageDesc);
-      }
-      if (more) {
-        if (!ptx::mbar_wait(bar(C::kReady + sn), ((tile + 1) / kBwdStages) & 1u, ctl, 2u)) goto done;
-        sdp(sn, 0);
-      }
-      // half b
+      // P^T(i) in TMEM: dV += P^T dO, then S^T(i+1) into the columns dV has just read
       if (!ptx::mbar_wait(bar(C::kDsFull + 1), tile & 1u, ctl, 2u)) goto done;
       ptx::tc_fence_after();
-      issue_pv64<D, E, true>(tDV, tmem + kTmHalf, domn_lo0 + s * kStageDesc + kHalfDesc);
-      issue_pv64<D, E, true>(tDK, tmem + kTmHalf + kTmDP, qmn_lo0 + s * kStageDesc + kHalfDesc);
+      if (i == i0) issue_dv<D, E, false>(tDV, tS, domn_lo0 + s * kTileDesc);
+      else issue_dv<D, E, true>(tDV, tS, domn_lo0 + s * kTileDesc);
+      ptx::mma_commit(bar(C::kDoFree + s));
+      if (more && !st(tile + 1)) goto done;
+      // dS^T(i) in shared memory: dK += dS^T Q, then dP^T(i+1) (dP^T(i) has been read)
+      if (!ptx::mbar_wait(bar(C::kDsFull), tile & 1u, ctl, 2u)) goto done;
+      ptx::tc_fence_after();
+      if (i == i0) issue_dk<D, E, false>(tDK, ds_lo, qmn_lo0 + s * kTileDesc);
+      else issue_dk<D, E, true>(tDK, ds_lo, qmn_lo0 + s * kTileDesc);
       ptx::mma_commit(bar(C::kDone + s));
-      if (more) sdp(sn, 1);
+      if (more && !dp(tile + 1)) goto done;
     }
     ptx::mma_commit(bar(C::kStEmpty));
     ptx::mma_commit(bar(C::kAccFull));
@@ -560,6 +595,22 @@ done:
   if (!ptx::mbar_wait_drain(bar(C::kMmaDone), 0, ctl.timeout_ns)) atomicOr(ctl.status, 8u);
 }
 
+// Row kr of the dS^T tile: 16 packed words (queries q0 .. q0+31, q0 a multiple of 32) into
+// the K-major, 128-byte-swizzled layout the MMA reads (16-byte chunk u of a row lands at
+// chunk u ^ (row % 8)).
+template <int D>
+__device__ __forceinline__ void st_ds_row(uint32_t ds_base, int kr, int q0, const uint32_t (&w)[16]) {
+  const uint32_t row = ds_base + static_cast<uint32_t>(q0 / 64) * BwdCfg<D>::kDsAtom + static_cast<uint32_t>(kr) * 128u;
+  const int u0 = (q0 % 64) / 8;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t a = row + (static_cast<uint32_t>((u0 + k) ^ (kr & 7)) << 4);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w[4 * k]), "r"(w[4 * k + 1]),
+                 "r"(w[4 * k + 2]), "r"(w[4 * k + 3])
+                 : "memory");
+  }
+}
+
 template <int D, Elem E>
 __device__ __forceinline__ void dkdv_compute(const BwdParams& p, uint32_t sbase, uint8_t* smem, uint32_t tmem,
                                              const ptx::WaitCtl& ctl) {
@@ -568,43 +619,69 @@ __device__ __forceinline__ void dkdv_compute(const BwdParams& p, uint32_t sbase,
   auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const int kr = (warp & 3) * 32 + lane;                       // key row in the K/V tile = TMEM lane
-  const int sub = warp >> 2;                                   // queries 32*sub .. +31 of each 64-query half
+  const int sub = warp >> 2;                                   // queries 64*sub .. +63 of each tile
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  const uint32_t tS = tmem + lane_base + kTmS + 64 * sub, tDP = tmem + lane_base + kTmDP + 64 * sub;
   const uint32_t tDV = tmem + lane_base + kTmAcc + (D / 2) * sub, tDK = tDV + D;
+  const uint32_t ds_base = sbase + C::kKvDsOff;
+  const float2 cc = make_float2(p.scale_log2, p.scale_log2);
   uint32_t tile = 0, units = 0;
   int bh, j;
   for (int k = 0; bwd_unit_at(p, k, false, bh, j); ++k) {
     const int i0 = p.causal ? j : 0;
     const int key = j * 128 + kr;
-    const float2 cc = make_float2(p.scale_log2, p.scale_log2);
     for (int i = i0; i < p.n_blk; ++i, ++tile) {
       const uint32_t s = tile % kBwdStages;
-      const float* vec = reinterpret_cast<const float*>(smem + C::kRingOff + s * C::kStageBytes + 2 * C::kTile);
+      // P^T(i) as soon as S^T(i) is in
+      bool got = ptx::mbar_wait(bar(C::kSdpFull), tile & 1u, ctl, 4u);
+      if (!__all_sync(0xFFFFFFFFu, got)) return;
+      // the Q slot's vectors landed with Q itself, before S^T(i) could run (an
+      // already-completed phase: this only orders the reads below after the copy)
+      got = ptx::mbar_wait(bar(C::kReady + s), (tile / kBwdStages) & 1u, ctl, 4u);
+      if (!__all_sync(0xFFFFFFFFu, got)) return;
+      ptx::tc_fence_after();
+      uint32_t sr[2][32];
+      ptx::tmem_ld32(tS, sr[0]);
+      ptx::tmem_ld32(tS + 32, sr[1]);
+      const float* vec = reinterpret_cast<const float*>(smem + C::kKvVecOff + s * 2 * C::kVecBytes);
+      const bool diag = p.causal && i == j;
+      ptx::tmem_wait_ld();
+      float2 pv[2][16];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const bool got = ptx::mbar_wait(bar(C::kSdpFull + h), tile & 1u, ctl, 4u);
-        if (!__all_sync(0xFFFFFFFFu, got)) return;
-        ptx::tc_fence_after();
-        const int q0 = 64 * h + 32 * sub;                      // first query of this thread's 32
+      for (int c = 0; c < 2; ++c) {
+        const int q0 = 64 * sub + 32 * c;                      // first query of this chunk
         const float2* nl = reinterpret_cast<const float2*>(vec + q0);
-        const float2* nd = reinterpret_cast<const float2*>(vec + 128 + q0);
-        const uint32_t tS = tmem + lane_base + kTmHalf * h + 32 * sub, tDP = tS + kTmDP;
-        uint32_t sr[32], dr[32];
-        ptx::tmem_ld32(tS, sr);
-        ptx::tmem_ld32(tDP, dr);
-        ptx::tmem_wait_ld();
-        uint32_t wp[16], wd[16];
+        uint32_t wp[16];
         // causal diagonal tile: query i*128 + q0 + x sees this key iff q0 + x >= kr (padded
         // queries have -LSE*log2(e) = -inf and so P = 0 already)
-        if (p.causal && i == j) dkdv_row32<kBf16, true>(sr, dr, cc, nl, nd, kr - q0, wp, wd);
-        else dkdv_row32<kBf16, false>(sr, dr, cc, nl, nd, 0, wp, wd);
-        ptx::tmem_st16(tS, wp);                                // over this thread's first 16 columns
-        ptx::tmem_st16(tDP, wd);
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar(C::kDsFull + h));
+        if (diag) dkdv_p32<kBf16, true>(sr[c], cc, nl, kr - q0, pv[c], wp);
+        else dkdv_p32<kBf16, false>(sr[c], cc, nl, 0, pv[c], wp);
+        ptx::tmem_st16(tS + 16 * c, wp);                       // over S^T columns already read
       }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(C::kDsFull + 1));
+      // dS^T(i) once dP^T(i) is in (which also means dK(i-1) has read the dS^T tile)
+      got = ptx::mbar_wait(bar(C::kSdpFull + 1), tile & 1u, ctl, 4u);
+      if (!__all_sync(0xFFFFFFFFu, got)) return;
+      ptx::tc_fence_after();
+      uint32_t dr[2][32];
+      ptx::tmem_ld32(tDP, dr[0]);
+      ptx::tmem_ld32(tDP + 32, dr[1]);
+      ptx::tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int q0 = 64 * sub + 32 * c;
+        const float2* nd = reinterpret_cast<const float2*>(vec + 128 + q0);
+        uint32_t wd[16];
+        dkdv_ds32<kBf16>(dr[c], pv[c], nd, wd);
+        st_ds_row<D>(ds_base, kr, q0, wd);
+      }
+      ptx::fence_proxy_async();                                // dS^T: generic writes -> MMA reads
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(C::kDsFull));
     }
     const bool got = ptx::mbar_wait(bar(C::kAccFull), units & 1u, ctl, 4u);
     if (!__all_sync(0xFFFFFFFFu, got)) return;
@@ -623,8 +700,12 @@ template <int D, Elem E, bool DKDV>
 __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_raw;
   const uint32_t sbase = ptx::smem_u32(smem);
+  if ((sbase & 1023u) != 0) {      // the layout has no slack to align it (see BwdCfg)
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusSmemAlign);
+    return;
+  }
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
