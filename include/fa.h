@@ -294,8 +294,7 @@ const char* fa_strerror(int status);
  * word, which kernels set when a bounded pipeline wait gives up.  Returns FA_OK
  * or FA_ERR_DEVICE_TIMEOUT; *bits (if not NULL) receives the raw word
  * (1 load warp, or a quantisation load wait; 2 MMA warp; 4 softmax warps; 8 drain
- * of in-flight copies; 16 a decode load wait; 32 a backward kernel whose dynamic
- * shared memory did not start on a 1 KB boundary, which then did no work).
+ * of in-flight copies; 16 a decode load wait).
  */
 int fa_last_device_status(void* stream, unsigned int* bits);
 

@@ -19,8 +19,8 @@
 //          packed into a TMEM region of its own, then dQ += dS K (TS MMA, K as an
 //          MN-major operand)
 //   dkdv   K/V-stationary: per 128-key tile, stream Q_i, dO_i (+ their LSE, D);
-//          S^T = K Q^T and dP^T = V dO^T (SS), then P^T (into TMEM) and dS^T (into
-//          shared memory) per key row, then dV += P^T dO (TS) and dK += dS^T Q (SS)
+//          S^T = K Q^T and dP^T = V dO^T (SS), then P^T and dS^T per key row (packed
+//          into TMEM), then dV += P^T dO and dK += dS^T Q (TS)
 // S and dP are computed twice (once per kernel) in exchange for no dQ reduction.
 //
 // Each main kernel is a persistent grid with these roles (320 threads):
@@ -39,11 +39,12 @@
 //   ... S^T(i)  dP^T(i)  dV(i)  S^T(i+1)  dK(i)  dP^T(i+1)  dV(i+1) ...
 // The compute threads form P^T(i) as soon as S^T(i) is in, packed over the S^T columns
 // they have read (queries 0-63 at columns 0-31, 64-127 at 64-95), for dV += P^T dO; then,
-// once dP^T(i) is in, dS^T(i) from the P values they kept in registers, into shared memory
-// as a K-major tile for dK += dS^T Q.  So each half of their work overlaps two products
-// of the pipe.  The pipe runs its MMAs in order: S^T(i+1) overwrites P^T(i) only after
-// dV(i) has read it, and dP^T(i+1) completes only after dK(i) has read the dS^T tile.  32
-// MMA instructions a Q tile (d = 128).
+// once dP^T(i) is in, dS^T(i) from the P values they kept in registers, packed the same
+// way over the dP^T columns, for dK += dS^T Q.  So each half of their work overlaps two
+// products of the pipe.  The pipe runs its MMAs in order: S^T(i+1) overwrites P^T(i) only
+// after dV(i) has read it, dP^T(i+1) overwrites dS^T(i) only after dK(i).  Both A operands
+// come from TMEM, which keeps shared memory (the operand feed of the S^T and dP^T MMAs)
+// for the B operands and the loads.  32 MMA instructions a Q tile (d = 128).
 // TMEM (512 columns at d = 128): S^T | dP^T (128 columns each) | dV | dK.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -77,15 +78,12 @@ struct BwdCfg {
   static constexpr int kDqVOff = kDqKOff + kDqKSlots * kTile;
   static constexpr int kDqEnd = kDqVOff + kDqVSlots * kTile;
   // dkdv kernel: the stationary K and V tiles, Q and dO in rings of kBwdStages slots (Q_i is
-  // free after dK += dS^T Q_i, dO_i after dV += P^T dO_i), each Q slot's -LSE*log2(e) and -D
-  // vectors, and the dS^T tile (128 keys x 128 queries, K-major, two 128-byte swizzle atoms)
+  // free after dK += dS^T Q_i, dO_i after dV += P^T dO_i), and each Q slot's -LSE*log2(e)
+  // and -D vectors
   static constexpr int kKvQOff = 2 * kTile;
   static constexpr int kKvDoOff = kKvQOff + kBwdStages * kTile;
   static constexpr int kKvVecOff = kKvDoOff + kBwdStages * kTile;
-  static constexpr int kKvDsOff = kKvVecOff + kBwdStages * 2 * kVecBytes;
-  static constexpr int kDsAtom = 128 * 128;           // 64 queries of all 128 key rows
-  static_assert(kKvDsOff % 1024 == 0, "the dS^T tile is 1 KB aligned");
-  static constexpr int kDkdvEnd = kKvDsOff + 2 * kDsAtom;
+  static constexpr int kDkdvEnd = kKvVecOff + kBwdStages * 2 * kVecBytes;
   static constexpr int kBarOff = kDqEnd > kDkdvEnd ? kDqEnd : kDkdvEnd;
   // barriers
   static constexpr int kStFull = 0, kStEmpty = 1, kReady = 2, kDone = kReady + kBwdStages;
@@ -103,10 +101,7 @@ struct BwdCfg {
   static constexpr int kNumBars = kDoFree + kBwdStages;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
-  // No alignment slack: the kernel checks that its dynamic shared memory starts on a 1 KB
-  // boundary (which the 128-byte swizzle of TMA and the MMA descriptors needs) and does no
-  // work, setting a status bit, if it does not.
-  static constexpr int kAlloc = kBytes;
+  static constexpr int kAlloc = kBytes + 1024;        // slack to align the base to 1 KB
   static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
@@ -278,11 +273,11 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, float mul, void* o
   }
 }
 
-// dV += P^T dO over a tile's 128 queries: A = P^T packed in TMEM by the two compute threads
-// of each key row (queries 0-63 at columns 0-31, 64-127 at columns 64-95), B = dO as an
-// MN-major operand (16 query rows, 2 KB, a step).
+// dV += P^T dO or dK += dS^T Q over a tile's 128 queries: A = P^T or dS^T packed in TMEM by
+// the two compute threads of each key row (queries 0-63 at columns 0-31, 64-127 at columns
+// 64-95), B = dO or Q as an MN-major operand (16 query rows, 2 KB, a step).
 template <int D, Elem E, bool ACC, int KK = 0>
-__device__ __forceinline__ void issue_dv(uint32_t tD, uint32_t tA, uint32_t b_lo) {
+__device__ __forceinline__ void issue_t128(uint32_t tD, uint32_t tA, uint32_t b_lo) {
   using L = FwdCfg<D, E>;
   static_assert(!L::kFp8, "16-bit operands");
   if constexpr (KK < 8) {
@@ -292,24 +287,7 @@ __device__ __forceinline__ void issue_dv(uint32_t tD, uint32_t tA, uint32_t b_lo
     constexpr uint32_t kOt = 8 * KK + (KK >= 4 ? 32 : 0);
     constexpr uint32_t kOb = (KK * 16 * 128) >> 4;
     ptx::mma_f16_ts_o<kAcc, kOt, kOb>(tD, tA, b_lo, desc_hi, idesc);
-    issue_dv<D, E, ACC, KK + 1>(tD, tA, b_lo);
-  }
-}
-
-// dK += dS^T Q: A = the dS^T tile in shared memory (K-major, 32 bytes of queries a step
-// inside a 128-byte swizzle atom), B = Q as an MN-major operand.
-template <int D, Elem E, bool ACC, int KK = 0>
-__device__ __forceinline__ void issue_dk(uint32_t tD, uint32_t a_lo, uint32_t b_lo) {
-  using L = FwdCfg<D, E>;
-  static_assert(!L::kFp8, "16-bit operands");
-  if constexpr (KK < 8) {
-    constexpr uint32_t idesc = ptx::idesc_make(kBlockM, D, L::kAbType, false, true);
-    constexpr uint32_t desc_hi = ptx::sdesc_hi(1024);
-    constexpr int kAcc = (ACC || KK > 0) ? 1 : 0;
-    constexpr uint32_t kOa = ((KK * 32 / 128) * BwdCfg<D>::kDsAtom + (KK * 32) % 128) >> 4;
-    constexpr uint32_t kOb = (KK * 16 * 128) >> 4;
-    ptx::mma_f16_ss_o<kAcc, kOa, kOb>(tD, a_lo, b_lo, desc_hi, idesc);
-    issue_dk<D, E, ACC, KK + 1>(tD, a_lo, b_lo);
+    issue_t128<D, E, ACC, KK + 1>(tD, tA, b_lo);
   }
 }
 
@@ -543,7 +521,6 @@ __device__ __noinline__ void dkdv_mma(const BwdParams& p, uint32_t sbase, uint32
   const uint32_t do_lo0 = ptx::sdesc_lo(sbase + C::kKvDoOff, 16);                // dO as K-major B of dP^T
   const uint32_t qmn_lo0 = ptx::sdesc_lo(sbase + C::kKvQOff, v_lbo<D, E>());     // Q as MN-major B of dK
   const uint32_t domn_lo0 = ptx::sdesc_lo(sbase + C::kKvDoOff, v_lbo<D, E>());   // dO as MN-major B of dV
-  const uint32_t ds_lo = ptx::sdesc_lo(sbase + C::kKvDsOff, 16);                 // dS^T as K-major A of dK
   const uint32_t tS = tmem + kTmS, tDP = tmem + kTmDP, tDV = tmem + kTmAcc, tDK = tmem + kTmAcc + D;
   // S^T = K Q^T and dP^T = V dO^T of streamed tile t (N = 128), each with its commit
   auto st = [&](uint32_t t) -> bool {
@@ -574,15 +551,15 @@ __device__ __noinline__ void dkdv_mma(const BwdParams& p, uint32_t sbase, uint32
       // P^T(i) in TMEM: dV += P^T dO, then S^T(i+1) into the columns dV has just read
       if (!ptx::mbar_wait(bar(C::kDsFull + 1), tile & 1u, ctl, 2u)) goto done;
       ptx::tc_fence_after();
-      if (i == i0) issue_dv<D, E, false>(tDV, tS, domn_lo0 + s * kTileDesc);
-      else issue_dv<D, E, true>(tDV, tS, domn_lo0 + s * kTileDesc);
+      if (i == i0) issue_t128<D, E, false>(tDV, tS, domn_lo0 + s * kTileDesc);
+      else issue_t128<D, E, true>(tDV, tS, domn_lo0 + s * kTileDesc);
       ptx::mma_commit(bar(C::kDoFree + s));
       if (more && !st(tile + 1)) goto done;
-      // dS^T(i) in shared memory: dK += dS^T Q, then dP^T(i+1) (dP^T(i) has been read)
+      // dS^T(i) in TMEM: dK += dS^T Q, then dP^T(i+1) into the columns dK has just read
       if (!ptx::mbar_wait(bar(C::kDsFull), tile & 1u, ctl, 2u)) goto done;
       ptx::tc_fence_after();
-      if (i == i0) issue_dk<D, E, false>(tDK, ds_lo, qmn_lo0 + s * kTileDesc);
-      else issue_dk<D, E, true>(tDK, ds_lo, qmn_lo0 + s * kTileDesc);
+      if (i == i0) issue_t128<D, E, false>(tDK, tDP, qmn_lo0 + s * kTileDesc);
+      else issue_t128<D, E, true>(tDK, tDP, qmn_lo0 + s * kTileDesc);
       ptx::mma_commit(bar(C::kDone + s));
       if (more && !dp(tile + 1)) goto done;
     }
@@ -593,22 +570,6 @@ __device__ __noinline__ void dkdv_mma(const BwdParams& p, uint32_t sbase, uint32
 done:
   ptx::mma_commit(bar(C::kMmaDone));
   if (!ptx::mbar_wait_drain(bar(C::kMmaDone), 0, ctl.timeout_ns)) atomicOr(ctl.status, 8u);
-}
-
-// Row kr of the dS^T tile: 16 packed words (queries q0 .. q0+31, q0 a multiple of 32) into
-// the K-major, 128-byte-swizzled layout the MMA reads (16-byte chunk u of a row lands at
-// chunk u ^ (row % 8)).
-template <int D>
-__device__ __forceinline__ void st_ds_row(uint32_t ds_base, int kr, int q0, const uint32_t (&w)[16]) {
-  const uint32_t row = ds_base + static_cast<uint32_t>(q0 / 64) * BwdCfg<D>::kDsAtom + static_cast<uint32_t>(kr) * 128u;
-  const int u0 = (q0 % 64) / 8;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint32_t a = row + (static_cast<uint32_t>((u0 + k) ^ (kr & 7)) << 4);
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w[4 * k]), "r"(w[4 * k + 1]),
-                 "r"(w[4 * k + 2]), "r"(w[4 * k + 3])
-                 : "memory");
-  }
 }
 
 template <int D, Elem E>
@@ -623,7 +584,6 @@ __device__ __forceinline__ void dkdv_compute(const BwdParams& p, uint32_t sbase,
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
   const uint32_t tS = tmem + lane_base + kTmS + 64 * sub, tDP = tmem + lane_base + kTmDP + 64 * sub;
   const uint32_t tDV = tmem + lane_base + kTmAcc + (D / 2) * sub, tDK = tDV + D;
-  const uint32_t ds_base = sbase + C::kKvDsOff;
   const float2 cc = make_float2(p.scale_log2, p.scale_log2);
   uint32_t tile = 0, units = 0;
   int bh, j;
@@ -662,7 +622,7 @@ __device__ __forceinline__ void dkdv_compute(const BwdParams& p, uint32_t sbase,
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(C::kDsFull + 1));
-      // dS^T(i) once dP^T(i) is in (which also means dK(i-1) has read the dS^T tile)
+      // dS^T(i) once dP^T(i) is in
       got = ptx::mbar_wait(bar(C::kSdpFull + 1), tile & 1u, ctl, 4u);
       if (!__all_sync(0xFFFFFFFFu, got)) return;
       ptx::tc_fence_after();
@@ -676,9 +636,9 @@ __device__ __forceinline__ void dkdv_compute(const BwdParams& p, uint32_t sbase,
         const float2* nd = reinterpret_cast<const float2*>(vec + 128 + q0);
         uint32_t wd[16];
         dkdv_ds32<kBf16>(dr[c], pv[c], nd, wd);
-        st_ds_row<D>(ds_base, kr, q0, wd);
+        ptx::tmem_st16(tDP + 16 * c, wd);                      // over dP^T columns already read
       }
-      ptx::fence_proxy_async();                                // dS^T: generic writes -> MMA reads
+      ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(C::kDsFull));
@@ -700,12 +660,8 @@ template <int D, Elem E, bool DKDV>
 __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = smem_raw;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = ptx::smem_u32(smem);
-  if ((sbase & 1023u) != 0) {      // the layout has no slack to align it (see BwdCfg)
-    if (threadIdx.x == 0) atomicOr(p.status, kStatusSmemAlign);
-    return;
-  }
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);

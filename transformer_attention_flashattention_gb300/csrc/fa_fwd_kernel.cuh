@@ -60,8 +60,6 @@ constexpr unsigned kStatusLoadTimeout = 1u;
 constexpr unsigned kStatusMmaTimeout = 2u;
 constexpr unsigned kStatusSoftmaxTimeout = 4u;
 constexpr unsigned kStatusDrainTimeout = 8u;
-// (16 is the decode kernels' load wait)
-constexpr unsigned kStatusSmemAlign = 32u;     // dynamic shared memory not on a 1 KB boundary
 
 enum class Elem : int { F16 = 0, BF16 = 1, E4M3 = 2 };
 

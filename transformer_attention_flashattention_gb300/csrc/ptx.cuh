@@ -24,12 +24,6 @@ __device__ __forceinline__ uint64_t globaltimer() {
 
 // ------------------------------------------------------------------ mbarrier
 
-// Orders this thread's generic-proxy shared-memory writes before later async-proxy reads
-// of them (tcgen05.mma operands).
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
