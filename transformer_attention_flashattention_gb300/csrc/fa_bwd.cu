@@ -98,7 +98,10 @@ struct BwdCfg {
   // its Q slots' full / free barriers, kSdpFull / kSdpFull + 1 as "S^T in" / "dP^T in"
   // (commits), and kDsFull / kDsFull + 1 as "dS^T written" / "P^T written" (compute arrives).
   static constexpr int kDoFull = kVFree + kDqVSlots, kDoFree = kDoFull + kBwdStages;
-  static constexpr int kNumBars = kDoFree + kBwdStages;
+  // dkdv kernel only: the stationary V tile's full / empty barriers (kStFull / kStEmpty are
+  // its K tile's), so that each is reloaded as soon as the unit's last product using it ran
+  static constexpr int kVsFull = kDoFree + kBwdStages, kVsEmpty = kVsFull + 1;
+  static constexpr int kNumBars = kVsEmpty + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes + 1024;        // slack to align the base to 1 KB
@@ -362,11 +365,17 @@ __device__ __noinline__ void dq_mma(const BwdParams& p, uint32_t sbase, uint32_t
     const int n = p.causal ? i + 1 : p.n_blk;
     if (!ptx::mbar_wait(bar(C::kStFull), units & 1u, ctl, 2u)) goto done;
     if (!sdp(tile)) goto done;
+    // Q and dO are free once the unit's last S and dP have run: the next unit's load
+    // overlaps this unit's last dQ products
+    if (n == 1) ptx::mma_commit(bar(C::kStEmpty));
     for (int j = 0; j < n; ++j, ++tile) {
       // S(j) and dP(j) are in the compute threads' registers: the next tile's go into
       // the same columns while dS(j) is formed
       if (!ptx::mbar_wait(bar(C::kSdpFree), tile & 1u, ctl, 2u)) goto done;
-      if (j + 1 < n && !sdp(tile + 1)) goto done;
+      if (j + 1 < n) {
+        if (!sdp(tile + 1)) goto done;
+        if (j + 2 == n) ptx::mma_commit(bar(C::kStEmpty));
+      }
       // dQ += dS(j) K_j, after which K_j's slot and the dS region are free
       if (!ptx::mbar_wait(bar(C::kDsFull), tile & 1u, ctl, 2u)) goto done;
       ptx::tc_fence_after();
@@ -376,7 +385,6 @@ __device__ __noinline__ void dq_mma(const BwdParams& p, uint32_t sbase, uint32_t
       ptx::mma_commit(bar(C::kDsFree));
       ptx::mma_commit(bar(C::kKFree + ks));
     }
-    ptx::mma_commit(bar(C::kStEmpty));
     ptx::mma_commit(bar(C::kAccFull));
     ++units;
   }
@@ -461,7 +469,7 @@ __device__ __noinline__ void dkdv_producer(const BwdParams& p, uint32_t sbase, c
   using C = BwdCfg<D>;
   using L = FwdCfg<D, E>;
   auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
-  uint32_t nd = 0, nq = 0, units = 0;   // dO and Q fills issued so far, stationary fills
+  uint32_t nd = 0, nq = 0, units = 0, vunits = 0;   // dO, Q, K and V fills issued so far
   int bh, j;
   for (int k = 0; bwd_unit_at(p, k, false, bh, j); ++k) {
     const int i0 = p.causal ? j : 0;
@@ -474,11 +482,15 @@ __device__ __noinline__ void dkdv_producer(const BwdParams& p, uint32_t sbase, c
         ptx::tma_prefetch_3d(&p.tm_v, a * L::kAtomElems, jn * 128, bhn);
       }
     }
+    // K once the previous unit's last S^T has run, V once its last dP^T has
     if (!ptx::mbar_wait(bar(C::kStEmpty), (units & 1u) ^ 1u, ctl, 1u)) goto drain;
-    ptx::mbar_arrive_expect_tx(bar(C::kStFull), 2 * C::kTile);
+    ptx::mbar_arrive_expect_tx(bar(C::kStFull), C::kTile);
     load_tile<D, E>(&p.tm_k, sbase + C::kStatOff, bar(C::kStFull), j * 128, bh);
-    load_tile<D, E>(&p.tm_v, sbase + C::kStatOff + C::kTile, bar(C::kStFull), j * 128, bh);
     ++units;
+    if (!ptx::mbar_wait(bar(C::kVsEmpty), (vunits & 1u) ^ 1u, ctl, 1u)) goto drain;
+    ptx::mbar_arrive_expect_tx(bar(C::kVsFull), C::kTile);
+    load_tile<D, E>(&p.tm_v, sbase + C::kStatOff + C::kTile, bar(C::kVsFull), j * 128, bh);
+    ++vunits;
     for (int i = i0; i < p.n_blk; ++i) {
       // tile number nq == nd: its ring slot and the slot's fill count
       const uint32_t s = nq % kBwdStages, f = nq / kBwdStages;
@@ -507,6 +519,8 @@ drain:
     if (!ptx::mbar_wait_drain(bar(C::kReady + t % kBwdStages), (t / kBwdStages) & 1u, ctl.timeout_ns))
       atomicOr(ctl.status, 8u);
   if (units > 0 && !ptx::mbar_wait_drain(bar(C::kStFull), (units - 1u) & 1u, ctl.timeout_ns))
+    atomicOr(ctl.status, 8u);
+  if (vunits > 0 && !ptx::mbar_wait_drain(bar(C::kVsFull), (vunits - 1u) & 1u, ctl.timeout_ns))
     atomicOr(ctl.status, 8u);
 }
 
@@ -543,8 +557,15 @@ __device__ __noinline__ void dkdv_mma(const BwdParams& p, uint32_t sbase, uint32
   int bh, j;
   for (int k = 0; bwd_unit_at(p, k, false, bh, j); ++k) {
     const int i0 = p.causal ? j : 0;
+    // K is free once the unit's last S^T has run, V once its last dP^T has: the next
+    // unit's loads overlap this unit's last products
+    const bool one = i0 + 1 == p.n_blk;
     if (!ptx::mbar_wait(bar(C::kStFull), units & 1u, ctl, 2u)) goto done;
-    if (!st(tile) || !dp(tile)) goto done;
+    if (!st(tile)) goto done;
+    if (one) ptx::mma_commit(bar(C::kStEmpty));
+    if (!ptx::mbar_wait(bar(C::kVsFull), units & 1u, ctl, 2u)) goto done;
+    if (!dp(tile)) goto done;
+    if (one) ptx::mma_commit(bar(C::kVsEmpty));
     for (int i = i0; i < p.n_blk; ++i, ++tile) {
       const uint32_t s = tile % kBwdStages;
       const bool more = i + 1 < p.n_blk;
@@ -554,16 +575,21 @@ __device__ __noinline__ void dkdv_mma(const BwdParams& p, uint32_t sbase, uint32
       if (i == i0) issue_t128<D, E, false>(tDV, tS, domn_lo0 + s * kTileDesc);
       else issue_t128<D, E, true>(tDV, tS, domn_lo0 + s * kTileDesc);
       ptx::mma_commit(bar(C::kDoFree + s));
-      if (more && !st(tile + 1)) goto done;
+      if (more) {
+        if (!st(tile + 1)) goto done;
+        if (i + 2 == p.n_blk) ptx::mma_commit(bar(C::kStEmpty));
+      }
       // dS^T(i) in TMEM: dK += dS^T Q, then dP^T(i+1) into the columns dK has just read
       if (!ptx::mbar_wait(bar(C::kDsFull), tile & 1u, ctl, 2u)) goto done;
       ptx::tc_fence_after();
       if (i == i0) issue_t128<D, E, false>(tDK, tDP, qmn_lo0 + s * kTileDesc);
       else issue_t128<D, E, true>(tDK, tDP, qmn_lo0 + s * kTileDesc);
       ptx::mma_commit(bar(C::kDone + s));
-      if (more && !dp(tile + 1)) goto done;
+      if (more) {
+        if (!dp(tile + 1)) goto done;
+        if (i + 2 == p.n_blk) ptx::mma_commit(bar(C::kVsEmpty));
+      }
     }
-    ptx::mma_commit(bar(C::kStEmpty));
     ptx::mma_commit(bar(C::kAccFull));
     ++units;
   }
