@@ -14,10 +14,10 @@
 //   prep   -D and -LSE*log2(e) into a workspace padded to 128 rows per head (padding:
 //          0 and -inf, so padded queries get P = 0); negated so that both enter the
 //          packed-pair arithmetic below as addends
-//   dq     Q-stationary: per 128-row Q tile, stream K_j, V_j;
-//          S = Q K^T and dP = dO V^T (two SS MMAs into TMEM), dS in registers,
-//          packed into a TMEM region of its own, then dQ += dS K (TS MMA, K as an
-//          MN-major operand)
+//   dq     Q-stationary: per 128-row Q tile (Q and dO copied into TMEM once per tile),
+//          stream K_j, V_j; S = Q K^T and dP = dO V^T (TS MMAs), P and dS in
+//          registers, dS packed into TMEM over the dP columns, then dQ += dS K (TS
+//          MMA, K as an MN-major operand)
 //   dkdv   K/V-stationary: per 128-key tile, stream Q_i, dO_i (+ their LSE, D);
 //          S^T = K Q^T and dP^T = V dO^T (SS), then P^T and dS^T per key row (packed
 //          into TMEM), then dV += P^T dO and dK += dS^T Q (TS)
@@ -30,11 +30,16 @@
 //              (dq: K in a 3-slot ring and V in a 2-slot ring; dkdv: Q and dO in
 //              2-slot rings)
 //   warp 9     MMA issuer (one thread) and TMEM owner
-// dq kernel: whole 128-key tiles, S and dP with N = 128.  The compute threads signal as
-// soon as S(j) and dP(j) are in their registers, and the MMA thread then issues S(j+1)
-// and dP(j+1) into the same TMEM columns while dS(j) is being computed; dS goes to a
-// region of its own, read by dQ += dS K.  24 MMA instructions a key tile (d = 128).
-// TMEM: S (128 columns) | dP (128) | dS (64, two 16-bit values a column) | dQ (D).
+// dq kernel: whole 128-key tiles, S and dP with N = 128, in the tensor-pipe order
+//   ... S(j)  dP(j)  S(j+1)  dQ(j)  dP(j+1)  S(j+2)  dQ(j+1) ...
+// The unit's Q and dO tiles are copied from shared memory into TMEM once, so all three
+// products take their A operand from TMEM and read only B (K or V) from shared memory.
+// The compute threads form P(j) as soon as S(j) is in, and signal once S(j) is in their
+// registers so that S(j+1) can follow; once dP(j) is in, they form dS(j) and pack it over
+// the dP columns they have read.  dP(j+1) follows dQ(j) in the in-order pipe.  24 MMA
+// instructions a key tile (d = 128).
+// TMEM: Q | dO (64 columns each, two 16-bit values a column) | S | dP, then dS (128 each) |
+// dQ (D).
 // dkdv kernel: whole 128-query tiles, S^T and dP^T with N = 128, in the tensor-pipe order
 //   ... S^T(i)  dP^T(i)  dV(i)  S^T(i+1)  dK(i)  dP^T(i+1)  dV(i+1) ...
 // The compute threads form P^T(i) as soon as S^T(i) is in, packed over the S^T columns
@@ -61,7 +66,7 @@ constexpr int kBwdLoadWarp = 8;
 constexpr int kBwdMmaWarp = 9;
 constexpr int kBwdStages = 2;                                      // dkdv: Q and dO ring slots
 constexpr uint32_t kTmS = 0, kTmDP = 128, kTmAcc = 256;            // dkdv: S^T | dP^T | dV | dK
-constexpr uint32_t kQS = 0, kQDP = 128, kQDS = 256, kQAcc = 320;  // dq: S | dP | dS | dQ
+constexpr uint32_t kQQ = 0, kQDO = 64, kQS = 128, kQDP = 256, kQAcc = 384;   // dq: Q | dO | S | dP | dQ
 constexpr float kLog2e = 1.44269504088896340736f;
 
 template <int D>
@@ -89,10 +94,12 @@ struct BwdCfg {
   static constexpr int kStFull = 0, kStEmpty = 1, kReady = 2, kDone = kReady + kBwdStages;
   static constexpr int kSdpFull = kDone + kBwdStages, kDsFull = kSdpFull + 2, kAccFull = kDsFull + 2;   // per half
   static constexpr int kMmaDone = kAccFull + 1;
-  // dq kernel only: S/dP read into registers (compute arrives), dS region free again (commit),
-  // and the K and V rings' full / free barriers per slot
-  static constexpr int kSdpFree = kMmaDone + 1, kDsFree = kSdpFree + 1;
-  static constexpr int kKFull = kDsFree + 1, kKFree = kKFull + kDqKSlots;
+  // dq kernel only: S read into registers (compute arrives); Q and dO in TMEM (compute
+  // arrives) and free again (commit after the unit's last S and dP); the K and V rings'
+  // full / free barriers per slot.  It takes kSdpFull / kSdpFull + 1 as "S in" / "dP in"
+  // (commits) and kStEmpty as "stationary tiles copied out of shared memory" (compute).
+  static constexpr int kSdpFree = kMmaDone + 1, kQtFull = kSdpFree + 1, kQtFree = kQtFull + 1;
+  static constexpr int kKFull = kQtFree + 1, kKFree = kKFull + kDqKSlots;
   static constexpr int kVFull = kKFree + kDqKSlots, kVFree = kVFull + kDqVSlots;
   // dkdv kernel only: its dO slots' full / free barriers.  It also takes kReady / kDone as
   // its Q slots' full / free barriers, kSdpFull / kSdpFull + 1 as "S^T in" / "dP^T in"
@@ -196,26 +203,6 @@ __device__ __forceinline__ void load_tile(const CUtensorMap* map, uint32_t dst, 
     ptx::tma_load_3d(dst + a * L::kAtomBytes, map, bar, a * L::kAtomElems, row0, bh);
 }
 
-// dS = P (dP - D) of 32 scores of one dq row, packed: P = 2^(s * c + nl) with the row's
-// nl = -LSE*log2(e) and nd = -D; with MASK, keys x >= visible get P = 0.  Pairs of columns
-// go through the packed fp32 forms (one instruction for two lanes of work).
-template <bool BF16, bool MASK>
-__device__ __forceinline__ void dq_row32(const uint32_t (&sr)[32], const uint32_t (&dr)[32], float2 cc, float2 nl,
-                                         float2 nd, int visible, uint32_t (&w)[16]) {
-#pragma unroll
-  for (int x = 0; x < 16; ++x) {
-    const float2 t = ptx::fma2(make_float2(__uint_as_float(sr[2 * x]), __uint_as_float(sr[2 * x + 1])), cc, nl);
-    float2 pv = make_float2(ptx::ex2(t.x), ptx::ex2(t.y));
-    if constexpr (MASK) {
-      if (2 * x >= visible) pv.x = 0.f;
-      if (2 * x + 1 >= visible) pv.y = 0.f;
-    }
-    const float2 ds =
-        ptx::mul2(pv, ptx::add2(make_float2(__uint_as_float(dr[2 * x]), __uint_as_float(dr[2 * x + 1])), nd));
-    w[x] = ptx::pack2<BF16>(ds.x, ds.y);
-  }
-}
-
 // P^T of one key row against 32 queries: P = 2^(s * c + nl) with the queries'
 // -LSE*log2(e) as pairs from shared memory; with MASK, queries x < first get P = 0.  The
 // values stay in pv for dS; w gets them packed.
@@ -294,6 +281,21 @@ __device__ __forceinline__ void issue_t128(uint32_t tD, uint32_t tA, uint32_t b_
   }
 }
 
+// S = Q K^T or dP = dO V^T with A (Q or dO) packed in TMEM (16 elements of d, 8 columns, a
+// step) and B a K-major K or V tile (N = 128 keys).
+template <int D, Elem E, int KK = 0>
+__device__ __forceinline__ void issue_ts_s(uint32_t tD, uint32_t tA, uint32_t b_lo) {
+  using L = FwdCfg<D, E>;
+  static_assert(!L::kFp8, "16-bit operands");
+  if constexpr (KK < D / 16) {
+    constexpr uint32_t idesc = ptx::idesc_make(kBlockM, kBlockN, L::kAbType, false, false);
+    constexpr uint32_t desc_hi = ptx::sdesc_hi(1024);
+    constexpr uint32_t kOb = ((KK * 32 / 128) * L::kAtomBytes + (KK * 32) % 128) >> 4;
+    ptx::mma_f16_ts_o<KK ? 1 : 0, 8 * KK, kOb>(tD, tA, b_lo, desc_hi, idesc);
+    issue_ts_s<D, E, KK + 1>(tD, tA, b_lo);
+  }
+}
+
 // ---------------------------------------------------------------------------- dq kernel
 
 template <int D, Elem E>
@@ -339,23 +341,27 @@ template <int D, Elem E>
 __device__ __noinline__ void dq_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const ptx::WaitCtl& ctl) {
   using C = BwdCfg<D>;
   auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
-  const uint32_t q_lo = ptx::sdesc_lo(sbase + C::kStatOff, 16);
-  const uint32_t do_lo = ptx::sdesc_lo(sbase + C::kStatOff + C::kTile, 16);
   constexpr uint32_t kTileDesc = C::kTile >> 4;
   const uint32_t k_lo0 = ptx::sdesc_lo(sbase + C::kDqKOff, 16);                 // K as K-major B of S
   const uint32_t kmn_lo0 = ptx::sdesc_lo(sbase + C::kDqKOff, v_lbo<D, E>());    // K as MN-major B of dQ
   const uint32_t v_lo0 = ptx::sdesc_lo(sbase + C::kDqVOff, 16);                 // V as K-major B of dP
-  const uint32_t tS = tmem + kQS, tDP = tmem + kQDP, tDS = tmem + kQDS, tAcc = tmem + kQAcc;
-  // S = Q K^T and dP = dO V^T for global tile number t (N = 128); V's slot is free once
-  // dP has run
-  auto sdp = [&](uint32_t t) -> bool {
-    const uint32_t ks = t % C::kDqKSlots, vs = t % C::kDqVSlots;
+  const uint32_t tQ = tmem + kQQ, tDO = tmem + kQDO, tS = tmem + kQS, tDP = tmem + kQDP, tAcc = tmem + kQAcc;
+  // S = Q K^T and dP = dO V^T for global tile number t, each with its commit; V's slot is
+  // free once dP has run
+  auto s_ = [&](uint32_t t) -> bool {
+    const uint32_t ks = t % C::kDqKSlots;
     if (!ptx::mbar_wait(bar(C::kKFull + ks), (t / C::kDqKSlots) & 1u, ctl, 2u)) return false;
+    ptx::tc_fence_after();
+    issue_ts_s<D, E>(tS, tQ, k_lo0 + ks * kTileDesc);
+    ptx::mma_commit(bar(C::kSdpFull));
+    return true;
+  };
+  auto dp_ = [&](uint32_t t) -> bool {
+    const uint32_t vs = t % C::kDqVSlots;
     if (!ptx::mbar_wait(bar(C::kVFull + vs), (t / C::kDqVSlots) & 1u, ctl, 2u)) return false;
     ptx::tc_fence_after();
-    issue_s<D, E>(tS, q_lo, k_lo0 + ks * kTileDesc);
-    issue_s<D, E>(tDP, do_lo, v_lo0 + vs * kTileDesc);
-    ptx::mma_commit(bar(C::kSdpFull));
+    issue_ts_s<D, E>(tDP, tDO, v_lo0 + vs * kTileDesc);
+    ptx::mma_commit(bar(C::kSdpFull + 1));
     ptx::mma_commit(bar(C::kVFree + vs));
     return true;
   };
@@ -363,27 +369,29 @@ __device__ __noinline__ void dq_mma(const BwdParams& p, uint32_t sbase, uint32_t
   int bh, i;
   for (int k = 0; bwd_unit_at(p, k, true, bh, i); ++k) {
     const int n = p.causal ? i + 1 : p.n_blk;
-    if (!ptx::mbar_wait(bar(C::kStFull), units & 1u, ctl, 2u)) goto done;
-    if (!sdp(tile)) goto done;
-    // Q and dO are free once the unit's last S and dP have run: the next unit's load
-    // overlaps this unit's last dQ products
-    if (n == 1) ptx::mma_commit(bar(C::kStEmpty));
+    // the unit's Q and dO are in TMEM
+    if (!ptx::mbar_wait(bar(C::kQtFull), units & 1u, ctl, 2u)) goto done;
+    ptx::tc_fence_after();
+    if (!s_(tile) || !dp_(tile)) goto done;
+    // Q and dO are free once the unit's last S and dP have run
+    if (n == 1) ptx::mma_commit(bar(C::kQtFree));
     for (int j = 0; j < n; ++j, ++tile) {
-      // S(j) and dP(j) are in the compute threads' registers: the next tile's go into
-      // the same columns while dS(j) is formed
+      const bool more = j + 1 < n;
+      // S(j) is in the compute threads' registers: S(j+1) goes into its columns
       if (!ptx::mbar_wait(bar(C::kSdpFree), tile & 1u, ctl, 2u)) goto done;
-      if (j + 1 < n) {
-        if (!sdp(tile + 1)) goto done;
-        if (j + 2 == n) ptx::mma_commit(bar(C::kStEmpty));
-      }
-      // dQ += dS(j) K_j, after which K_j's slot and the dS region are free
+      if (more && !s_(tile + 1)) goto done;
+      // dS(j) packed over the dP(j) columns: dQ += dS K_j, after which K_j's slot is free
       if (!ptx::mbar_wait(bar(C::kDsFull), tile & 1u, ctl, 2u)) goto done;
       ptx::tc_fence_after();
       const uint32_t ks = tile % C::kDqKSlots;
-      if (j == 0) issue_pv<D, E, false>(tAcc, tDS, kmn_lo0 + ks * kTileDesc);
-      else issue_pv<D, E, true>(tAcc, tDS, kmn_lo0 + ks * kTileDesc);
-      ptx::mma_commit(bar(C::kDsFree));
+      if (j == 0) issue_t128<D, E, false>(tAcc, tDP, kmn_lo0 + ks * kTileDesc);
+      else issue_t128<D, E, true>(tAcc, tDP, kmn_lo0 + ks * kTileDesc);
       ptx::mma_commit(bar(C::kKFree + ks));
+      // dP(j+1) into the columns dQ has just read
+      if (more) {
+        if (!dp_(tile + 1)) goto done;
+        if (j + 2 == n) ptx::mma_commit(bar(C::kQtFree));
+      }
     }
     ptx::mma_commit(bar(C::kAccFull));
     ++units;
@@ -393,8 +401,58 @@ done:
   if (!ptx::mbar_wait_drain(bar(C::kMmaDone), 0, ctl.timeout_ns)) atomicOr(ctl.status, 8u);
 }
 
+// Half of row r of a stationary 128-row tile in shared memory (128-byte swizzle atoms of
+// 64 elements; 16-byte chunk c of a row sits at chunk c ^ (r % 8)): elements
+// sub*D/2 .. +D/2-1, as D/4 words of two 16-bit values, into TMEM at taddr.
 template <int D, Elem E>
-__device__ __forceinline__ void dq_compute(const BwdParams& p, uint32_t sbase, uint32_t tmem,
+__device__ __forceinline__ void tile_row_to_tmem(const uint8_t* tile, int r, int sub, uint32_t taddr) {
+  using L = FwdCfg<D, E>;
+  constexpr int kChunks = D / 16;                    // 16-byte chunks in half a row
+  const int e0 = sub * (D / 2);
+  const uint8_t* row = tile + (e0 / 64) * L::kAtomBytes + r * 128;
+  const int c0 = (e0 % 64) / 8;
+  uint32_t w[D / 4];
+#pragma unroll
+  for (int k = 0; k < kChunks; ++k) {
+    const uint4 v = *reinterpret_cast<const uint4*>(row + (((c0 + k) ^ (r & 7)) << 4));
+    w[4 * k] = v.x;
+    w[4 * k + 1] = v.y;
+    w[4 * k + 2] = v.z;
+    w[4 * k + 3] = v.w;
+  }
+  if constexpr (D == 128) ptx::tmem_st32(taddr, w);
+  else ptx::tmem_st16(taddr, w);
+}
+
+// P of 32 scores of one dq row: P = 2^(s * c + nl) with the row's nl = -LSE*log2(e); with
+// MASK, keys x >= visible get P = 0.
+template <bool MASK>
+__device__ __forceinline__ void dq_p32(const uint32_t (&sr)[32], float2 cc, float2 nl, int visible, float2 (&pv)[16]) {
+#pragma unroll
+  for (int x = 0; x < 16; ++x) {
+    const float2 t = ptx::fma2(make_float2(__uint_as_float(sr[2 * x]), __uint_as_float(sr[2 * x + 1])), cc, nl);
+    float2 v = make_float2(ptx::ex2(t.x), ptx::ex2(t.y));
+    if constexpr (MASK) {
+      if (2 * x >= visible) v.x = 0.f;
+      if (2 * x + 1 >= visible) v.y = 0.f;
+    }
+    pv[x] = v;
+  }
+}
+
+// dS = P (dP - D) of 32 keys of one dq row, packed (nd = the row's -D in both halves).
+template <bool BF16>
+__device__ __forceinline__ void dq_ds32(const uint32_t (&dr)[32], const float2 (&pv)[16], float2 nd, uint32_t (&w)[16]) {
+#pragma unroll
+  for (int x = 0; x < 16; ++x) {
+    const float2 ds =
+        ptx::mul2(pv[x], ptx::add2(make_float2(__uint_as_float(dr[2 * x]), __uint_as_float(dr[2 * x + 1])), nd));
+    w[x] = ptx::pack2<BF16>(ds.x, ds.y);
+  }
+}
+
+template <int D, Elem E>
+__device__ __forceinline__ void dq_compute(const BwdParams& p, uint32_t sbase, uint8_t* smem, uint32_t tmem,
                                            const ptx::WaitCtl& ctl) {
   using C = BwdCfg<D>;
   constexpr bool kBf16 = E == Elem::BF16;
@@ -404,53 +462,82 @@ __device__ __forceinline__ void dq_compute(const BwdParams& p, uint32_t sbase, u
   const int sub = warp >> 2;                                   // keys 64*sub .. +63 of each tile
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
   const uint32_t tS = tmem + lane_base + kQS + 64 * sub, tDP = tmem + lane_base + kQDP + 64 * sub;
-  const uint32_t tDS = tmem + lane_base + kQDS + 32 * sub;     // this thread's 64 keys, packed
   const uint32_t tAcc = tmem + lane_base + kQAcc + (D / 2) * sub;
+  const float2 cc = make_float2(p.scale_log2, p.scale_log2);
+  // Unit u's Q and dO rows into TMEM (A operands of S and dP), once the tiles have landed
+  // in shared memory and unit u-1's last S and dP have run; then shared memory is free
+  // for the next unit's tiles.
+  auto copy_in = [&](uint32_t u) -> bool {
+    bool ok = ptx::mbar_wait(bar(C::kStFull), u & 1u, ctl, 4u);
+    if (ok && u > 0) ok = ptx::mbar_wait(bar(C::kQtFree), (u - 1) & 1u, ctl, 4u);
+    if (!__all_sync(0xFFFFFFFFu, ok)) return false;
+    ptx::tc_fence_after();
+    tile_row_to_tmem<D, E>(smem + C::kStatOff, r, sub, tmem + lane_base + kQQ + (D / 4) * sub);
+    tile_row_to_tmem<D, E>(smem + C::kStatOff + C::kTile, r, sub, tmem + lane_base + kQDO + (D / 4) * sub);
+    ptx::tmem_wait_st();
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      ptx::mbar_arrive(bar(C::kQtFull));
+      ptx::mbar_arrive(bar(C::kStEmpty));
+    }
+    return true;
+  };
   uint32_t tile = 0, units = 0;
   int bh, i;
+  if (bwd_unit_at(p, 0, true, bh, i) && !copy_in(0)) return;
   for (int k = 0; bwd_unit_at(p, k, true, bh, i); ++k) {
     const int n = p.causal ? i + 1 : p.n_blk;
     const int row = i * 128 + r;
     const size_t wrow = static_cast<size_t>(bh) * p.n_pad + row;
     const float nl = p.nlse2[wrow], nd = p.ndelta[wrow];
-    const float2 cc = make_float2(p.scale_log2, p.scale_log2), nl2 = make_float2(nl, nl), nd2 = make_float2(nd, nd);
+    const float2 nl2 = make_float2(nl, nl), nd2 = make_float2(nd, nd);
     const int limit = min(p.N, p.causal ? row + 1 : p.N);      // keys >= limit get P = 0
     for (int j = 0; j < n; ++j, ++tile) {
-      const bool got = ptx::mbar_wait(bar(C::kSdpFull), tile & 1u, ctl, 4u);
+      // P(j) as soon as S(j) is in
+      bool got = ptx::mbar_wait(bar(C::kSdpFull), tile & 1u, ctl, 4u);
       if (!__all_sync(0xFFFFFFFFu, got)) return;
       ptx::tc_fence_after();
-      uint32_t sr[2][32], dr[2][32];
+      uint32_t sr[2][32];
       ptx::tmem_ld32(tS, sr[0]);
       ptx::tmem_ld32(tS + 32, sr[1]);
-      ptx::tmem_ld32(tDP, dr[0]);
-      ptx::tmem_ld32(tDP + 32, dr[1]);
       ptx::tmem_wait_ld();
-      // S and dP are read: the MMA thread may overwrite them with the next tile's
+      // S is read: the MMA thread may overwrite it with the next tile's
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(C::kSdpFree));
       const int visible = limit - (j * 128 + 64 * sub);
-      uint32_t w[2][16];
+      float2 pv[2][16];
       if (visible >= 64) {
-        dq_row32<kBf16, false>(sr[0], dr[0], cc, nl2, nd2, 0, w[0]);
-        dq_row32<kBf16, false>(sr[1], dr[1], cc, nl2, nd2, 0, w[1]);
+        dq_p32<false>(sr[0], cc, nl2, 0, pv[0]);
+        dq_p32<false>(sr[1], cc, nl2, 0, pv[1]);
       } else {
-        dq_row32<kBf16, true>(sr[0], dr[0], cc, nl2, nd2, visible, w[0]);
-        dq_row32<kBf16, true>(sr[1], dr[1], cc, nl2, nd2, visible - 32, w[1]);
+        dq_p32<true>(sr[0], cc, nl2, visible, pv[0]);
+        dq_p32<true>(sr[1], cc, nl2, visible - 32, pv[1]);
       }
-      // the previous tile's dQ MMAs have read the dS region
-      if (j > 0 || units > 0) {
-        const bool fr = ptx::mbar_wait(bar(C::kDsFree), (tile - 1) & 1u, ctl, 4u);
-        if (!__all_sync(0xFFFFFFFFu, fr)) return;
-        ptx::tc_fence_after();
+      // dS(j) once dP(j) is in, packed over the dP columns this thread has read
+      got = ptx::mbar_wait(bar(C::kSdpFull + 1), tile & 1u, ctl, 4u);
+      if (!__all_sync(0xFFFFFFFFu, got)) return;
+      ptx::tc_fence_after();
+      uint32_t dr[2][32];
+      ptx::tmem_ld32(tDP, dr[0]);
+      ptx::tmem_ld32(tDP + 32, dr[1]);
+      ptx::tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t w[16];
+        dq_ds32<kBf16>(dr[c], pv[c], nd2, w);
+        ptx::tmem_st16(tDP + 16 * c, w);
       }
-      ptx::tmem_st16(tDS, w[0]);
-      ptx::tmem_st16(tDS + 16, w[1]);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(C::kDsFull));
     }
+    // the next unit's Q and dO go into TMEM before this unit's dQ is read out, so that
+    // its first S and dP run meanwhile
+    int bhn, inext;
+    if (bwd_unit_at(p, k + 1, true, bhn, inext) && !copy_in(units + 1)) return;
     const bool got = ptx::mbar_wait(bar(C::kAccFull), units & 1u, ctl, 4u);
     if (!__all_sync(0xFFFFFFFFu, got)) return;
     ++units;
@@ -696,7 +783,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumBars; ++i)
-      ptx::mbar_init(bar(i), (i == C::kDsFull || i == C::kDsFull + 1 || i == C::kSdpFree) ? kBwdComputeWarps : 1);
+      ptx::mbar_init(bar(i), (i == C::kDsFull || i == C::kDsFull + 1 || i == C::kSdpFree || i == C::kQtFull ||
+                              (!DKDV && i == C::kStEmpty))
+                                 ? kBwdComputeWarps : 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -728,7 +817,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
     }
   } else {
     if constexpr (DKDV) dkdv_compute<D, E>(p, sbase, smem, tmem, ctl);
-    else dq_compute<D, E>(p, sbase, tmem, ctl);
+    else dq_compute<D, E>(p, sbase, smem, tmem, ctl);
   }
 
   ptx::tc_fence_before();
