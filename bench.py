@@ -415,6 +415,31 @@ def _variants(fa, dev, timer, n, peaks, e2e_steps):
         out[name] = _perf(ms, w.flops(causal), "bf16", peaks, kern)
     cache.clear()
     out.update(_fp8_figures(fa, WORKLOADS["fp8"], dev, timer, n, peaks, WORKLOADS["fp8"].seed, e2e_steps))
+    out.update(_bwd_figures(fa, dev, timer, n, peaks))
+    return out
+
+
+def _bwd_figures(fa, dev, timer, n, peaks):
+    """The backward pass (dQ, dK, dV: prep + two kernels a call) on its workload, both masks;
+    the forward's O and LSE are computed once, outside the timing."""
+    import ctypes
+    from fa_inputs import make_dout
+    w = _workload("bwd")
+    q, k, v = (t.to(dev) for t in make_qkv(w.shape, w.dtype, w.seed))
+    do = make_dout(w.shape, w.dtype, w.seed).to(dev)
+    need = ctypes.c_ulonglong(0)
+    fa.load_library().fa_bwd_workspace_size(w.B, w.H, w.N, w.d, ctypes.byref(need))
+    ws = torch.empty(max(need.value, 256), device=dev, dtype=torch.uint8)
+    grads = tuple(torch.empty_like(q) for _ in range(3))
+    out = {}
+    for causal in (False, True):
+        o, lse = fa.attention(q, k, v, causal=causal)
+        ms = timer.launches(lambda: fa.attention_backward(q, k, v, o, lse, do, causal=causal, dq=grads[0],
+                                                          dk=grads[1], dv=grads[2], workspace=ws), n,
+                            flush=_needs_flush(7 * q.numel() * q.element_size()))
+        name = f"bwd_{w.B}x{w.H}x{w.N}x{w.d}_{'causal' if causal else 'non_causal'}"
+        out[name] = _perf(ms, w.flops(causal) * BWD_FLOP_RATIO, "bf16", peaks,
+                          "fa_bwd_prep_kernel + fa_bwd_kernel (dQ) + fa_bwd_kernel (dK, dV)")
     return out
 
 

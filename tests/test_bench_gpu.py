@@ -42,7 +42,8 @@ def test_our_arm_prints_the_contract_line(gpu_lib):
 
 def test_default_line_carries_the_variants(gpu_lib):
     """The default workload (long context) with its in-process variants: the throughput
-    bar's points, the bf16 and d=64 points and the E4M3 figures, each with its own numbers."""
+    bar's points, the bf16 and d=64 points, the E4M3 figures and the backward pass, each with
+    its own numbers."""
     buf = io.StringIO()
     with contextlib.redirect_stdout(buf):
         rc = bench.main(["--steps", "3", "--warmup", "3", "--skip-cpu-baseline"])
@@ -53,7 +54,8 @@ def test_default_line_carries_the_variants(gpu_lib):
     for name in ("2x16x8192x128_non_causal", "1x16x16384x128_non_causal", "16x16x2048x128_non_causal",
                  "16x16x2048x128_causal", "2x16x8192x64_non_causal", "fp8_4x16x4096x128_forward",
                  "2x16x8192x128_non_causal_2cta", "16x16x2048x128_causal_2cta",
-                 "fp8_4x16x4096x128_prologue_and_forward"):
+                 "fp8_4x16x4096x128_prologue_and_forward", "bwd_16x16x2048x128_non_causal",
+                 "bwd_16x16x2048x128_causal"):
         assert v[name]["tflops"] > 0 and 0 < v[name]["roofline_frac"], name
     assert v["fp8_4x16x4096x128_prologue"]["gbs"] > 0
     assert v["fp8_4x16x4096x128_end_to_end"]["tflops"] > 0
