@@ -275,7 +275,7 @@ __host__ __device__ constexpr uint32_t v_lbo() {
 // The MMAs of one PV or S block, unrolled at compile time so that every operand
 // offset is an immediate (see the _o wrappers).
 template <int D, Elem E, bool ACC, int KK = 0>
-__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tS, uint32_t v_lo) {
+__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tS, uint32_t v_lo, uint32_t lead = 1) {
   using L = FwdCfg<D, E>;
   if constexpr (KK < L::kPvSteps) {
     constexpr uint32_t idesc_pv = ptx::idesc_make(kBlockM, D, L::kAbType, false, !L::kFp8);
@@ -284,27 +284,28 @@ __device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tS, uint32_t v_lo
     // P: 8 TMEM columns per step (16 packed 16-bit or 32 packed E4M3 keys).  B: 16-bit
     // V is [N, d], 16 key rows (2 KB) per step; E4M3 V^T rows hold 32 keys per step.
     constexpr uint32_t kOb = L::kFp8 ? (KK * 32) >> 4 : (KK * 16 * 128) >> 4;
-    if constexpr (L::kFp8) ptx::mma_f8_ts_o<kAcc, KK * 8, kOb>(tO, tS, v_lo, desc_hi, idesc_pv);
-    else ptx::mma_f16_ts_o<kAcc, KK * 8, kOb>(tO, tS, v_lo, desc_hi, idesc_pv);
-    issue_pv<D, E, ACC, KK + 1>(tO, tS, v_lo);
+    if constexpr (L::kFp8) ptx::mma_f8_ts_oe<kAcc, KK * 8, kOb>(lead, tO, tS, v_lo, desc_hi, idesc_pv);
+    else ptx::mma_f16_ts_oe<kAcc, KK * 8, kOb>(lead, tO, tS, v_lo, desc_hi, idesc_pv);
+    issue_pv<D, E, ACC, KK + 1>(tO, tS, v_lo, lead);
   }
 }
 
 template <int D, Elem E, int KK = 0>
-__device__ __forceinline__ void issue_s(uint32_t tS, uint32_t q_lo, uint32_t k_lo) {
+__device__ __forceinline__ void issue_s(uint32_t tS, uint32_t q_lo, uint32_t k_lo, uint32_t lead = 1) {
   using L = FwdCfg<D, E>;
   if constexpr (KK < D / L::kMmaK) {
     constexpr uint32_t idesc_qk = ptx::idesc_make(kBlockM, kBlockN, L::kAbType, false, false);
     constexpr uint32_t desc_hi = ptx::sdesc_hi(1024);
     // K-major operands: 32 bytes of d per step inside a 128-byte swizzle atom
     constexpr uint32_t kOff = ((KK * 32 / 128) * L::kAtomBytes + (KK * 32) % 128) >> 4;
-    if constexpr (L::kFp8) ptx::mma_f8_ss_o<KK ? 1 : 0, kOff, kOff>(tS, q_lo, k_lo, desc_hi, idesc_qk);
-    else ptx::mma_f16_ss_o<KK ? 1 : 0, kOff, kOff>(tS, q_lo, k_lo, desc_hi, idesc_qk);
-    issue_s<D, E, KK + 1>(tS, q_lo, k_lo);
+    if constexpr (L::kFp8) ptx::mma_f8_ss_oe<KK ? 1 : 0, kOff, kOff>(lead, tS, q_lo, k_lo, desc_hi, idesc_qk);
+    else ptx::mma_f16_ss_oe<KK ? 1 : 0, kOff, kOff>(lead, tS, q_lo, k_lo, desc_hi, idesc_qk);
+    issue_s<D, E, KK + 1>(tS, q_lo, k_lo, lead);
   }
 }
 
-// One thread issues every MMA, in the order
+// One lane of the MMA warp issues every MMA (the warp runs the loop converged, see
+// ptx::mma_f16_ss_oe), in the order
 //   O_0 += P_0 V_{j-1};  S_0 = Q_0 K_j^T;  O_1 += P_1 V_{j-1};  S_1 = Q_1 K_j^T
 // so the tensor pipe runs one tile's pair while the other tile's softmax works.
 // tcgen05.mma issue blocks on a very short queue: an MMA takes about as long to
@@ -333,6 +334,7 @@ __device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_
   uint32_t step = 0;                     // MMA steps issued so far (the producer counts alike)
   uint32_t q_uses[kQTiles] = {0, 0};
   uint32_t p_uses[kQTiles] = {0, 0};
+  const uint32_t lead = ptx::elect_one();   // the whole warp runs this loop, one lane issues
 
   int bh, qb;
   bool have = unit_at(p, 0, bh, qb);
@@ -361,15 +363,15 @@ __device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_
           if (!ptx::mbar_wait(ready0 + 8u * si, sph, ctl, kStatusMmaTimeout)) goto done;
           if (!ptx::mbar_wait(bar(L::kPFull), pp0, ctl, kStatusMmaTimeout)) goto done;
           ptx::tc_fence_after();
-          issue_pv<D, E, true>(tO0, tS0, v_lo);
-          issue_s<D, E>(tS0, q_lo0, k_lo);
-          ptx::mma_commit(bar(L::kSFull));
+          issue_pv<D, E, true>(tO0, tS0, v_lo, lead);
+          issue_s<D, E>(tS0, q_lo0, k_lo, lead);
+          ptx::mma_commit_e(lead, bar(L::kSFull));
           if (!ptx::mbar_wait(bar(L::kPFull + 1), pp1, ctl, kStatusMmaTimeout)) goto done;
           ptx::tc_fence_after();
-          issue_pv<D, E, true>(tO1, tS1, v_lo);
-          issue_s<D, E>(tS1, q_lo1, k_lo);
-          ptx::mma_commit(bar(L::kSFull + 1));
-          ptx::mma_commit(done0 + 8u * si);
+          issue_pv<D, E, true>(tO1, tS1, v_lo, lead);
+          issue_s<D, E>(tS1, q_lo1, k_lo, lead);
+          ptx::mma_commit_e(lead, bar(L::kSFull + 1));
+          ptx::mma_commit_e(lead, done0 + 8u * si);
           pp0 ^= 1u;
           pp1 ^= 1u;
           ks = vs + 1 == L::kStages ? 0u : vs + 1;
@@ -393,9 +395,9 @@ __device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_
           ++p_uses[t];
           ptx::tc_fence_after();
           const uint32_t v_lo = v_lo0 + vslot * kSlotDesc;
-          if (j - 1 > 0) issue_pv<D, E, true>(t ? tO1 : tO0, tS, v_lo);
-          else issue_pv<D, E, false>(t ? tO1 : tO0, tS, v_lo);
-          if (j - 1 == nt[t] - 1) ptx::mma_commit(bar(L::kOFull + t));
+          if (j - 1 > 0) issue_pv<D, E, true>(t ? tO1 : tO0, tS, v_lo, lead);
+          else issue_pv<D, E, false>(t ? tO1 : tO0, tS, v_lo, lead);
+          if (j - 1 == nt[t] - 1) ptx::mma_commit_e(lead, bar(L::kOFull + t));
         }
         if (j < nt[t]) {
           // S_t = Q_t K_j^T
@@ -403,9 +405,9 @@ __device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_
             if (!ptx::mbar_wait(bar(L::kQFull + t), q_uses[t] & 1u, ctl, kStatusMmaTimeout)) goto done;
             ++q_uses[t];
           }
-          issue_s<D, E>(tS, t == 0 ? q_lo0 : q_lo1, k_lo0 + kslot * kSlotDesc);
-          ptx::mma_commit(bar(L::kSFull + t));
-          if (j == nt[t] - 1) ptx::mma_commit(bar(L::kQEmpty + t));
+          issue_s<D, E>(tS, t == 0 ? q_lo0 : q_lo1, k_lo0 + kslot * kSlotDesc, lead);
+          ptx::mma_commit_e(lead, bar(L::kSFull + t));
+          if (j == nt[t] - 1) ptx::mma_commit_e(lead, bar(L::kQEmpty + t));
         }
         if (has_next && ntn[t] > 0 && j == (nt[t] > 0 ? nt[t] : n)) {
           // the next unit's S_t = Q_t K_0^T, right after this tile's last P.V (its O is
@@ -418,13 +420,13 @@ __device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_
           }
           if (!ptx::mbar_wait(bar(L::kQFull + t), q_uses[t] & 1u, ctl, kStatusMmaTimeout)) goto done;
           ++q_uses[t];
-          issue_s<D, E>(tS, t == 0 ? q_lo0 : q_lo1, k_lo0 + kslot_next * kSlotDesc);
-          ptx::mma_commit(bar(L::kSFull + t));
-          if (ntn[t] == 1) ptx::mma_commit(bar(L::kQEmpty + t));
+          issue_s<D, E>(tS, t == 0 ? q_lo0 : q_lo1, k_lo0 + kslot_next * kSlotDesc, lead);
+          ptx::mma_commit_e(lead, bar(L::kSFull + t));
+          if (ntn[t] == 1) ptx::mma_commit_e(lead, bar(L::kQEmpty + t));
         }
       }
-      ptx::mma_commit(done0 + 8u * (step % L::kSteps));
-      if (j == n && has_next) ptx::mma_commit(done0 + 8u * (next0 % L::kSteps));
+      ptx::mma_commit_e(lead, done0 + 8u * (step % L::kSteps));
+      if (j == n && has_next) ptx::mma_commit_e(lead, done0 + 8u * (next0 % L::kSteps));
     }
     load_idx += 2u * n;
     // the next unit's step 0 has been issued: it starts at step 1
@@ -436,7 +438,7 @@ __device__ __noinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_
   }
 done:
   // Every MMA issued so far must finish before TMEM is released.
-  ptx::mma_commit(bar(L::kMmaDone));
+  ptx::mma_commit_e(lead, bar(L::kMmaDone));
   if (!ptx::mbar_wait_drain(bar(L::kMmaDone), 0, ctl.timeout_ns)) atomicOr(ctl.status, kStatusDrainTimeout);
 }
 
@@ -722,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     if (warp == kLoadWarp) {
       if (lane == 0) fwd_producer<D, E>(p, sbase, ctl);
     } else if (warp == kMmaWarp) {
-      if (lane == 0) fwd_mma<D, E>(p, sbase, tmem, ctl);
+      fwd_mma<D, E>(p, sbase, tmem, ctl);
     }
   } else {
     ptx::setmaxnreg_inc<kSoftmaxRegs>();

@@ -288,6 +288,73 @@ __device__ __forceinline__ void mma_f8_ts_o(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// The same four MMA forms and the commit, executed by a whole warp with the instruction
+// predicated on `lead` (non-zero in exactly one lane, see elect_one).  A warp that runs
+// the issuing loop converged, with one lane issuing, keeps the tensor pipe fed through
+// the barrier polls, fences and commits between MMA groups; the same loop run by one lane
+// alone idles the pipe for about 75 clocks per such group (measured on GB300).
+template <int ACC, uint32_t OA, uint32_t OB>
+__device__ __forceinline__ void mma_f16_ss_oe(uint32_t lead, uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                              uint32_t hi, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 la, lb;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\tsetp.ne.b32 e, %8, 0;\n\t"
+      "add.u32 la, %1, %6;\n\tadd.u32 lb, %2, %7;\n\t"
+      "mov.b64 da, {la, %3};\n\tmov.b64 db, {lb, %3};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "n"(ACC), "n"(OA), "n"(OB), "r"(lead)
+      : "memory");
+}
+template <int ACC, uint32_t OT, uint32_t OB>
+__device__ __forceinline__ void mma_f16_ts_oe(uint32_t lead, uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                              uint32_t hi, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 ta, lb;\n\t.reg .b64 db;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\tsetp.ne.b32 e, %8, 0;\n\t"
+      "add.u32 ta, %1, %6;\n\tadd.u32 lb, %2, %7;\n\t"
+      "mov.b64 db, {lb, %3};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "n"(ACC), "n"(OT), "n"(OB), "r"(lead)
+      : "memory");
+}
+template <int ACC, uint32_t OA, uint32_t OB>
+__device__ __forceinline__ void mma_f8_ss_oe(uint32_t lead, uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                             uint32_t hi, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 la, lb;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\tsetp.ne.b32 e, %8, 0;\n\t"
+      "add.u32 la, %1, %6;\n\tadd.u32 lb, %2, %7;\n\t"
+      "mov.b64 da, {la, %3};\n\tmov.b64 db, {lb, %3};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "n"(ACC), "n"(OA), "n"(OB), "r"(lead)
+      : "memory");
+}
+template <int ACC, uint32_t OT, uint32_t OB>
+__device__ __forceinline__ void mma_f8_ts_oe(uint32_t lead, uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                             uint32_t hi, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 ta, lb;\n\t.reg .b64 db;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\tsetp.ne.b32 e, %8, 0;\n\t"
+      "add.u32 ta, %1, %6;\n\tadd.u32 lb, %2, %7;\n\t"
+      "mov.b64 db, {lb, %3};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [ta], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "n"(ACC), "n"(OT), "n"(OB), "r"(lead)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_e(uint32_t lead, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\tsetp.ne.b32 e, %1, 0;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
+      "r"(lead)
+      : "memory");
+}
+// 1 in one lane of the (converged) warp, 0 in the others.
+__device__ __forceinline__ uint32_t elect_one() {
+  uint32_t pred = 0;
+  asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(pred));
+  return pred;
+}
+
 // Arrives once on `bar` when every tcgen05 operation issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
