@@ -29,7 +29,8 @@
 //   warp 8     TMA producer: the unit's two stationary tiles, then the streamed tiles
 //              (dq: K in a 3-slot ring and V in a 2-slot ring; dkdv: Q and dO in
 //              2-slot rings)
-//   warp 9     MMA issuer (one thread) and TMEM owner
+//   warp 9     MMA issuer (the warp runs the loop converged, one elected lane issues)
+//              and TMEM owner
 // dq kernel: whole 128-key tiles, S and dP with N = 128, in the tensor-pipe order
 //   ... S(j)  dP(j)  S(j+1)  dQ(j)  dP(j+1)  S(j+2)  dQ(j+1) ...
 // The unit's Q and dO tiles are copied from shared memory into TMEM once, so all three
@@ -267,7 +268,7 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, float mul, void* o
 // the two compute threads of each key row (queries 0-63 at columns 0-31, 64-127 at columns
 // 64-95), B = dO or Q as an MN-major operand (16 query rows, 2 KB, a step).
 template <int D, Elem E, bool ACC, int KK = 0>
-__device__ __forceinline__ void issue_t128(uint32_t tD, uint32_t tA, uint32_t b_lo) {
+__device__ __forceinline__ void issue_t128(uint32_t tD, uint32_t tA, uint32_t b_lo, uint32_t lead) {
   using L = FwdCfg<D, E>;
   static_assert(!L::kFp8, "16-bit operands");
   if constexpr (KK < 8) {
@@ -276,23 +277,23 @@ __device__ __forceinline__ void issue_t128(uint32_t tD, uint32_t tA, uint32_t b_
     constexpr int kAcc = (ACC || KK > 0) ? 1 : 0;
     constexpr uint32_t kOt = 8 * KK + (KK >= 4 ? 32 : 0);
     constexpr uint32_t kOb = (KK * 16 * 128) >> 4;
-    ptx::mma_f16_ts_o<kAcc, kOt, kOb>(tD, tA, b_lo, desc_hi, idesc);
-    issue_t128<D, E, ACC, KK + 1>(tD, tA, b_lo);
+    ptx::mma_f16_ts_oe<kAcc, kOt, kOb>(lead, tD, tA, b_lo, desc_hi, idesc);
+    issue_t128<D, E, ACC, KK + 1>(tD, tA, b_lo, lead);
   }
 }
 
 // S = Q K^T or dP = dO V^T with A (Q or dO) packed in TMEM (16 elements of d, 8 columns, a
 // step) and B a K-major K or V tile (N = 128 keys).
 template <int D, Elem E, int KK = 0>
-__device__ __forceinline__ void issue_ts_s(uint32_t tD, uint32_t tA, uint32_t b_lo) {
+__device__ __forceinline__ void issue_ts_s(uint32_t tD, uint32_t tA, uint32_t b_lo, uint32_t lead) {
   using L = FwdCfg<D, E>;
   static_assert(!L::kFp8, "16-bit operands");
   if constexpr (KK < D / 16) {
     constexpr uint32_t idesc = ptx::idesc_make(kBlockM, kBlockN, L::kAbType, false, false);
     constexpr uint32_t desc_hi = ptx::sdesc_hi(1024);
     constexpr uint32_t kOb = ((KK * 32 / 128) * L::kAtomBytes + (KK * 32) % 128) >> 4;
-    ptx::mma_f16_ts_o<KK ? 1 : 0, 8 * KK, kOb>(tD, tA, b_lo, desc_hi, idesc);
-    issue_ts_s<D, E, KK + 1>(tD, tA, b_lo);
+    ptx::mma_f16_ts_oe<KK ? 1 : 0, 8 * KK, kOb>(lead, tD, tA, b_lo, desc_hi, idesc);
+    issue_ts_s<D, E, KK + 1>(tD, tA, b_lo, lead);
   }
 }
 
@@ -341,6 +342,7 @@ template <int D, Elem E>
 __device__ __noinline__ void dq_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const ptx::WaitCtl& ctl) {
   using C = BwdCfg<D>;
   auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
+  const uint32_t lead = ptx::elect_one();   // the whole warp runs this loop, one lane issues
   constexpr uint32_t kTileDesc = C::kTile >> 4;
   const uint32_t k_lo0 = ptx::sdesc_lo(sbase + C::kDqKOff, 16);                 // K as K-major B of S
   const uint32_t kmn_lo0 = ptx::sdesc_lo(sbase + C::kDqKOff, v_lbo<D, E>());    // K as MN-major B of dQ
@@ -352,17 +354,17 @@ __device__ __noinline__ void dq_mma(const BwdParams& p, uint32_t sbase, uint32_t
     const uint32_t ks = t % C::kDqKSlots;
     if (!ptx::mbar_wait(bar(C::kKFull + ks), (t / C::kDqKSlots) & 1u, ctl, 2u)) return false;
     ptx::tc_fence_after();
-    issue_ts_s<D, E>(tS, tQ, k_lo0 + ks * kTileDesc);
-    ptx::mma_commit(bar(C::kSdpFull));
+    issue_ts_s<D, E>(tS, tQ, k_lo0 + ks * kTileDesc, lead);
+    ptx::mma_commit_e(lead, bar(C::kSdpFull));
     return true;
   };
   auto dp_ = [&](uint32_t t) -> bool {
     const uint32_t vs = t % C::kDqVSlots;
     if (!ptx::mbar_wait(bar(C::kVFull + vs), (t / C::kDqVSlots) & 1u, ctl, 2u)) return false;
     ptx::tc_fence_after();
-    issue_ts_s<D, E>(tDP, tDO, v_lo0 + vs * kTileDesc);
-    ptx::mma_commit(bar(C::kSdpFull + 1));
-    ptx::mma_commit(bar(C::kVFree + vs));
+    issue_ts_s<D, E>(tDP, tDO, v_lo0 + vs * kTileDesc, lead);
+    ptx::mma_commit_e(lead, bar(C::kSdpFull + 1));
+    ptx::mma_commit_e(lead, bar(C::kVFree + vs));
     return true;
   };
   uint32_t tile = 0, units = 0;
@@ -374,7 +376,7 @@ __device__ __noinline__ void dq_mma(const BwdParams& p, uint32_t sbase, uint32_t
     ptx::tc_fence_after();
     if (!s_(tile) || !dp_(tile)) goto done;
     // Q and dO are free once the unit's last S and dP have run
-    if (n == 1) ptx::mma_commit(bar(C::kQtFree));
+    if (n == 1) ptx::mma_commit_e(lead, bar(C::kQtFree));
     for (int j = 0; j < n; ++j, ++tile) {
       const bool more = j + 1 < n;
       // S(j) is in the compute threads' registers: S(j+1) goes into its columns
@@ -384,20 +386,20 @@ __device__ __noinline__ void dq_mma(const BwdParams& p, uint32_t sbase, uint32_t
       if (!ptx::mbar_wait(bar(C::kDsFull), tile & 1u, ctl, 2u)) goto done;
       ptx::tc_fence_after();
       const uint32_t ks = tile % C::kDqKSlots;
-      if (j == 0) issue_t128<D, E, false>(tAcc, tDP, kmn_lo0 + ks * kTileDesc);
-      else issue_t128<D, E, true>(tAcc, tDP, kmn_lo0 + ks * kTileDesc);
-      ptx::mma_commit(bar(C::kKFree + ks));
+      if (j == 0) issue_t128<D, E, false>(tAcc, tDP, kmn_lo0 + ks * kTileDesc, lead);
+      else issue_t128<D, E, true>(tAcc, tDP, kmn_lo0 + ks * kTileDesc, lead);
+      ptx::mma_commit_e(lead, bar(C::kKFree + ks));
       // dP(j+1) into the columns dQ has just read
       if (more) {
         if (!dp_(tile + 1)) goto done;
-        if (j + 2 == n) ptx::mma_commit(bar(C::kQtFree));
+        if (j + 2 == n) ptx::mma_commit_e(lead, bar(C::kQtFree));
       }
     }
-    ptx::mma_commit(bar(C::kAccFull));
+    ptx::mma_commit_e(lead, bar(C::kAccFull));
     ++units;
   }
 done:
-  ptx::mma_commit(bar(C::kMmaDone));
+  ptx::mma_commit_e(lead, bar(C::kMmaDone));
   if (!ptx::mbar_wait_drain(bar(C::kMmaDone), 0, ctl.timeout_ns)) atomicOr(ctl.status, 8u);
 }
 
@@ -615,6 +617,7 @@ template <int D, Elem E>
 __device__ __noinline__ void dkdv_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const ptx::WaitCtl& ctl) {
   using C = BwdCfg<D>;
   auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
+  const uint32_t lead = ptx::elect_one();   // the whole warp runs this loop, one lane issues
   constexpr uint32_t kTileDesc = C::kTile >> 4;
   const uint32_t k_lo = ptx::sdesc_lo(sbase + C::kStatOff, 16);                  // K as K-major A of S^T
   const uint32_t v_lo = ptx::sdesc_lo(sbase + C::kStatOff + C::kTile, 16);       // V as K-major A of dP^T
@@ -628,16 +631,16 @@ __device__ __noinline__ void dkdv_mma(const BwdParams& p, uint32_t sbase, uint32
     const uint32_t s = t % kBwdStages;
     if (!ptx::mbar_wait(bar(C::kReady + s), (t / kBwdStages) & 1u, ctl, 2u)) return false;
     ptx::tc_fence_after();
-    issue_s<D, E>(tS, k_lo, q_lo0 + s * kTileDesc);
-    ptx::mma_commit(bar(C::kSdpFull));
+    issue_s<D, E>(tS, k_lo, q_lo0 + s * kTileDesc, lead);
+    ptx::mma_commit_e(lead, bar(C::kSdpFull));
     return true;
   };
   auto dp = [&](uint32_t t) -> bool {
     const uint32_t s = t % kBwdStages;
     if (!ptx::mbar_wait(bar(C::kDoFull + s), (t / kBwdStages) & 1u, ctl, 2u)) return false;
     ptx::tc_fence_after();
-    issue_s<D, E>(tDP, v_lo, do_lo0 + s * kTileDesc);
-    ptx::mma_commit(bar(C::kSdpFull + 1));
+    issue_s<D, E>(tDP, v_lo, do_lo0 + s * kTileDesc, lead);
+    ptx::mma_commit_e(lead, bar(C::kSdpFull + 1));
     return true;
   };
   uint32_t tile = 0, units = 0;
@@ -649,39 +652,39 @@ __device__ __noinline__ void dkdv_mma(const BwdParams& p, uint32_t sbase, uint32
     const bool one = i0 + 1 == p.n_blk;
     if (!ptx::mbar_wait(bar(C::kStFull), units & 1u, ctl, 2u)) goto done;
     if (!st(tile)) goto done;
-    if (one) ptx::mma_commit(bar(C::kStEmpty));
+    if (one) ptx::mma_commit_e(lead, bar(C::kStEmpty));
     if (!ptx::mbar_wait(bar(C::kVsFull), units & 1u, ctl, 2u)) goto done;
     if (!dp(tile)) goto done;
-    if (one) ptx::mma_commit(bar(C::kVsEmpty));
+    if (one) ptx::mma_commit_e(lead, bar(C::kVsEmpty));
     for (int i = i0; i < p.n_blk; ++i, ++tile) {
       const uint32_t s = tile % kBwdStages;
       const bool more = i + 1 < p.n_blk;
       // P^T(i) in TMEM: dV += P^T dO, then S^T(i+1) into the columns dV has just read
       if (!ptx::mbar_wait(bar(C::kDsFull + 1), tile & 1u, ctl, 2u)) goto done;
       ptx::tc_fence_after();
-      if (i == i0) issue_t128<D, E, false>(tDV, tS, domn_lo0 + s * kTileDesc);
-      else issue_t128<D, E, true>(tDV, tS, domn_lo0 + s * kTileDesc);
-      ptx::mma_commit(bar(C::kDoFree + s));
+      if (i == i0) issue_t128<D, E, false>(tDV, tS, domn_lo0 + s * kTileDesc, lead);
+      else issue_t128<D, E, true>(tDV, tS, domn_lo0 + s * kTileDesc, lead);
+      ptx::mma_commit_e(lead, bar(C::kDoFree + s));
       if (more) {
         if (!st(tile + 1)) goto done;
-        if (i + 2 == p.n_blk) ptx::mma_commit(bar(C::kStEmpty));
+        if (i + 2 == p.n_blk) ptx::mma_commit_e(lead, bar(C::kStEmpty));
       }
       // dS^T(i) in TMEM: dK += dS^T Q, then dP^T(i+1) into the columns dK has just read
       if (!ptx::mbar_wait(bar(C::kDsFull), tile & 1u, ctl, 2u)) goto done;
       ptx::tc_fence_after();
-      if (i == i0) issue_t128<D, E, false>(tDK, tDP, qmn_lo0 + s * kTileDesc);
-      else issue_t128<D, E, true>(tDK, tDP, qmn_lo0 + s * kTileDesc);
-      ptx::mma_commit(bar(C::kDone + s));
+      if (i == i0) issue_t128<D, E, false>(tDK, tDP, qmn_lo0 + s * kTileDesc, lead);
+      else issue_t128<D, E, true>(tDK, tDP, qmn_lo0 + s * kTileDesc, lead);
+      ptx::mma_commit_e(lead, bar(C::kDone + s));
       if (more) {
         if (!dp(tile + 1)) goto done;
-        if (i + 2 == p.n_blk) ptx::mma_commit(bar(C::kVsEmpty));
+        if (i + 2 == p.n_blk) ptx::mma_commit_e(lead, bar(C::kVsEmpty));
       }
     }
-    ptx::mma_commit(bar(C::kAccFull));
+    ptx::mma_commit_e(lead, bar(C::kAccFull));
     ++units;
   }
 done:
-  ptx::mma_commit(bar(C::kMmaDone));
+  ptx::mma_commit_e(lead, bar(C::kMmaDone));
   if (!ptx::mbar_wait_drain(bar(C::kMmaDone), 0, ctl.timeout_ns)) atomicOr(ctl.status, 8u);
 }
 
@@ -811,10 +814,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
       else dq_producer<D, E>(p, sbase, ctl);
     }
   } else if (warp == kBwdMmaWarp) {
-    if (lane == 0) {
-      if constexpr (DKDV) dkdv_mma<D, E>(p, sbase, tmem, ctl);
-      else dq_mma<D, E>(p, sbase, tmem, ctl);
-    }
+    if constexpr (DKDV) dkdv_mma<D, E>(p, sbase, tmem, ctl);
+    else dq_mma<D, E>(p, sbase, tmem, ctl);
   } else {
     if constexpr (DKDV) dkdv_compute<D, E>(p, sbase, smem, tmem, ctl);
     else dq_compute<D, E>(p, sbase, smem, tmem, ctl);
