@@ -169,6 +169,8 @@ __device__ __noinline__ void fwd_producer(const FwdParams& p, uint32_t sbase,
 #pragma unroll
   for (int s = 0; s < L::kStages; ++s) slot_step[s] = 0;
   uint32_t armed = 0;                    // bit g % kSteps: step g's loads were issued
+  // the whole warp runs this loop converged (its waits included); one lane issues
+  const bool lead = ptx::elect_one() != 0;
 
   int bh, qb;
   for (int k = 0; unit_at(p, k, bh, qb); ++k) {
@@ -181,7 +183,7 @@ __device__ __noinline__ void fwd_producer(const FwdParams& p, uint32_t sbase,
       if (unit_at(p, k + 1, bhn, qbn)) {
 #pragma unroll
         for (int t = 0; t < kQTiles; ++t)
-          if (tile_nkv(p, qbn, t) > 0)
+          if (lead && tile_nkv(p, qbn, t) > 0)
 #pragma unroll
             for (int a = 0; a < L::kAtoms; ++a)
               ptx::tma_prefetch_3d(&p.tm_q, a * L::kAtomElems, qbn * kUnitRows + t * kBlockM, bhn);
@@ -204,12 +206,12 @@ __device__ __noinline__ void fwd_producer(const FwdParams& p, uint32_t sbase,
                                          ((prev - 1) / L::kSteps) & 1u, ctl, kStatusLoadTimeout)) {
           if (i > 0 && !skip) {
             // a copy of this step is in flight: arrive so its phase completes when it lands
-            ptx::mbar_arrive(rb);
+            if (lead) ptx::mbar_arrive(rb);
             armed |= bit;
           }
           goto drain;
         }
-        if (!skip) {
+        if (!skip && lead) {
           if (i + 1 < cnt) ptx::mbar_expect_tx(rb, L::kTileBytes);
           else ptx::mbar_arrive_expect_tx(rb, L::kTileBytes);
           const bool is_k = i == 0 && j < n;
@@ -238,11 +240,13 @@ __device__ __noinline__ void fwd_producer(const FwdParams& p, uint32_t sbase,
           if ((t == 0 ? n0 : n1) == 0) continue;
           if (!ptx::mbar_wait(bar(L::kQEmpty + t), (q_fills[t] & 1u) ^ 1u, ctl, kStatusLoadTimeout))
             goto drain;
-          ptx::mbar_arrive_expect_tx(bar(L::kQFull + t), L::kTileBytes);
+          if (lead) {
+            ptx::mbar_arrive_expect_tx(bar(L::kQFull + t), L::kTileBytes);
 #pragma unroll
-          for (int a = 0; a < L::kAtoms; ++a)
-            ptx::tma_load_3d(sbase + L::kQOff + t * L::kTileBytes + a * L::kAtomBytes, &p.tm_q,
-                             bar(L::kQFull + t), a * L::kAtomElems, qb * kUnitRows + t * kBlockM, bh);
+            for (int a = 0; a < L::kAtoms; ++a)
+              ptx::tma_load_3d(sbase + L::kQOff + t * L::kTileBytes + a * L::kAtomBytes, &p.tm_q,
+                               bar(L::kQFull + t), a * L::kAtomElems, qb * kUnitRows + t * kBlockM, bh);
+          }
           ++q_fills[t];
         }
       }
@@ -722,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   if (warp >= 8) {
     ptx::setmaxnreg_dec<kControlRegs>();
     if (warp == kLoadWarp) {
-      if (lane == 0) fwd_producer<D, E>(p, sbase, ctl);
+      fwd_producer<D, E>(p, sbase, ctl);
     } else if (warp == kMmaWarp) {
       fwd_mma<D, E>(p, sbase, tmem, ctl);
     }
