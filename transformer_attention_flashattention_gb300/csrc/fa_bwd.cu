@@ -26,7 +26,8 @@
 // Each main kernel is a persistent grid with these roles (320 threads):
 //   warps 0-7  compute: warp w takes TMEM lanes 32*(w%4).. (Q rows, or key rows) and
 //              column half w/4, so every row is shared by two threads
-//   warp 8     TMA producer: the unit's two stationary tiles, then the streamed tiles
+//   warp 8     TMA producer (the warp runs the loop, one elected lane issues): the
+//              unit's two stationary tiles, then the streamed tiles
 //              (dq: K in a 3-slot ring and V in a 2-slot ring; dkdv: Q and dO in
 //              2-slot rings)
 //   warp 9     MMA issuer (the warp runs the loop converged, one elected lane issues)
@@ -304,24 +305,32 @@ __device__ __noinline__ void dq_producer(const BwdParams& p, uint32_t sbase, con
   using C = BwdCfg<D>;
   auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
   uint32_t nk = 0, nv = 0, units = 0;     // K and V loads issued so far, stationary fills
+  // the whole warp runs this loop converged (its waits included); one lane issues
+  const bool lead = ptx::elect_one() != 0;
   int bh, i;
   for (int k = 0; bwd_unit_at(p, k, true, bh, i); ++k) {
     const int n = p.causal ? i + 1 : p.n_blk;
     if (!ptx::mbar_wait(bar(C::kStEmpty), (units & 1u) ^ 1u, ctl, 1u)) goto drain;
-    ptx::mbar_arrive_expect_tx(bar(C::kStFull), 2 * C::kTile);
-    load_tile<D, E>(&p.tm_q, sbase + C::kStatOff, bar(C::kStFull), i * 128, bh);
-    load_tile<D, E>(&p.tm_do, sbase + C::kStatOff + C::kTile, bar(C::kStFull), i * 128, bh);
+    if (lead) {
+      ptx::mbar_arrive_expect_tx(bar(C::kStFull), 2 * C::kTile);
+      load_tile<D, E>(&p.tm_q, sbase + C::kStatOff, bar(C::kStFull), i * 128, bh);
+      load_tile<D, E>(&p.tm_do, sbase + C::kStatOff + C::kTile, bar(C::kStFull), i * 128, bh);
+    }
     ++units;
     for (int j = 0; j < n; ++j) {
       const uint32_t ks = nk % C::kDqKSlots, kf = nk / C::kDqKSlots;
       if (!ptx::mbar_wait(bar(C::kKFree + ks), (kf & 1u) ^ 1u, ctl, 1u)) goto drain;
-      ptx::mbar_arrive_expect_tx(bar(C::kKFull + ks), C::kTile);
-      load_tile<D, E>(&p.tm_k, sbase + C::kDqKOff + ks * C::kTile, bar(C::kKFull + ks), j * 128, bh);
+      if (lead) {
+        ptx::mbar_arrive_expect_tx(bar(C::kKFull + ks), C::kTile);
+        load_tile<D, E>(&p.tm_k, sbase + C::kDqKOff + ks * C::kTile, bar(C::kKFull + ks), j * 128, bh);
+      }
       ++nk;
       const uint32_t vs = nv % C::kDqVSlots, vf = nv / C::kDqVSlots;
       if (!ptx::mbar_wait(bar(C::kVFree + vs), (vf & 1u) ^ 1u, ctl, 1u)) goto drain;
-      ptx::mbar_arrive_expect_tx(bar(C::kVFull + vs), C::kTile);
-      load_tile<D, E>(&p.tm_v, sbase + C::kDqVOff + vs * C::kTile, bar(C::kVFull + vs), j * 128, bh);
+      if (lead) {
+        ptx::mbar_arrive_expect_tx(bar(C::kVFull + vs), C::kTile);
+        load_tile<D, E>(&p.tm_v, sbase + C::kDqVOff + vs * C::kTile, bar(C::kVFull + vs), j * 128, bh);
+      }
       ++nv;
     }
   }
@@ -559,12 +568,14 @@ __device__ __noinline__ void dkdv_producer(const BwdParams& p, uint32_t sbase, c
   using L = FwdCfg<D, E>;
   auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
   uint32_t nd = 0, nq = 0, units = 0, vunits = 0;   // dO, Q, K and V fills issued so far
+  // the whole warp runs this loop converged (its waits included); one lane issues
+  const bool lead = ptx::elect_one() != 0;
   int bh, j;
   for (int k = 0; bwd_unit_at(p, k, false, bh, j); ++k) {
     const int i0 = p.causal ? j : 0;
     // the next unit's stationary tiles into L2 while this unit runs
     int bhn, jn;
-    if (bwd_unit_at(p, k + 1, false, bhn, jn)) {
+    if (lead && bwd_unit_at(p, k + 1, false, bhn, jn)) {
 #pragma unroll
       for (int a = 0; a < L::kAtoms; ++a) {
         ptx::tma_prefetch_3d(&p.tm_k, a * L::kAtomElems, jn * 128, bhn);
@@ -573,28 +584,36 @@ __device__ __noinline__ void dkdv_producer(const BwdParams& p, uint32_t sbase, c
     }
     // K once the previous unit's last S^T has run, V once its last dP^T has
     if (!ptx::mbar_wait(bar(C::kStEmpty), (units & 1u) ^ 1u, ctl, 1u)) goto drain;
-    ptx::mbar_arrive_expect_tx(bar(C::kStFull), C::kTile);
-    load_tile<D, E>(&p.tm_k, sbase + C::kStatOff, bar(C::kStFull), j * 128, bh);
+    if (lead) {
+      ptx::mbar_arrive_expect_tx(bar(C::kStFull), C::kTile);
+      load_tile<D, E>(&p.tm_k, sbase + C::kStatOff, bar(C::kStFull), j * 128, bh);
+    }
     ++units;
     if (!ptx::mbar_wait(bar(C::kVsEmpty), (vunits & 1u) ^ 1u, ctl, 1u)) goto drain;
-    ptx::mbar_arrive_expect_tx(bar(C::kVsFull), C::kTile);
-    load_tile<D, E>(&p.tm_v, sbase + C::kStatOff + C::kTile, bar(C::kVsFull), j * 128, bh);
+    if (lead) {
+      ptx::mbar_arrive_expect_tx(bar(C::kVsFull), C::kTile);
+      load_tile<D, E>(&p.tm_v, sbase + C::kStatOff + C::kTile, bar(C::kVsFull), j * 128, bh);
+    }
     ++vunits;
     for (int i = i0; i < p.n_blk; ++i) {
       // tile number nq == nd: its ring slot and the slot's fill count
       const uint32_t s = nq % kBwdStages, f = nq / kBwdStages;
       // Q first: S^T is the first product of a tile
       if (!ptx::mbar_wait(bar(C::kDone + s), (f & 1u) ^ 1u, ctl, 1u)) goto drain;
-      ptx::mbar_arrive_expect_tx(bar(C::kReady + s), C::kTile + 2 * C::kVecBytes);
-      load_tile<D, E>(&p.tm_q, sbase + C::kKvQOff + s * C::kTile, bar(C::kReady + s), i * 128, bh);
-      const size_t w = static_cast<size_t>(bh) * p.n_pad + i * 128;
-      const uint32_t vec = sbase + C::kKvVecOff + s * 2 * C::kVecBytes;
-      ptx::bulk_load(vec, p.nlse2 + w, C::kVecBytes, bar(C::kReady + s));
-      ptx::bulk_load(vec + C::kVecBytes, p.ndelta + w, C::kVecBytes, bar(C::kReady + s));
+      if (lead) {
+        ptx::mbar_arrive_expect_tx(bar(C::kReady + s), C::kTile + 2 * C::kVecBytes);
+        load_tile<D, E>(&p.tm_q, sbase + C::kKvQOff + s * C::kTile, bar(C::kReady + s), i * 128, bh);
+        const size_t w = static_cast<size_t>(bh) * p.n_pad + i * 128;
+        const uint32_t vec = sbase + C::kKvVecOff + s * 2 * C::kVecBytes;
+        ptx::bulk_load(vec, p.nlse2 + w, C::kVecBytes, bar(C::kReady + s));
+        ptx::bulk_load(vec + C::kVecBytes, p.ndelta + w, C::kVecBytes, bar(C::kReady + s));
+      }
       ++nq;
       if (!ptx::mbar_wait(bar(C::kDoFree + s), (f & 1u) ^ 1u, ctl, 1u)) goto drain;
-      ptx::mbar_arrive_expect_tx(bar(C::kDoFull + s), C::kTile);
-      load_tile<D, E>(&p.tm_do, sbase + C::kKvDoOff + s * C::kTile, bar(C::kDoFull + s), i * 128, bh);
+      if (lead) {
+        ptx::mbar_arrive_expect_tx(bar(C::kDoFull + s), C::kTile);
+        load_tile<D, E>(&p.tm_do, sbase + C::kKvDoOff + s * C::kTile, bar(C::kDoFull + s), i * 128, bh);
+      }
       ++nd;
     }
   }
@@ -809,10 +828,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
   const ptx::WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
 
   if (warp == kBwdLoadWarp) {
-    if (lane == 0) {
-      if constexpr (DKDV) dkdv_producer<D, E>(p, sbase, ctl);
-      else dq_producer<D, E>(p, sbase, ctl);
-    }
+    if constexpr (DKDV) dkdv_producer<D, E>(p, sbase, ctl);
+    else dq_producer<D, E>(p, sbase, ctl);
   } else if (warp == kBwdMmaWarp) {
     if constexpr (DKDV) dkdv_mma<D, E>(p, sbase, tmem, ctl);
     else dq_mma<D, E>(p, sbase, tmem, ctl);
