@@ -401,8 +401,10 @@ def _variants(fa, dev, timer, n, peaks, e2e_steps):
              ("16x16x2048x128_non_causal_2cta", WORKLOADS["bf16"], False, True),
              ("16x16x2048x128_causal_2cta", WORKLOADS["bf16"], True, True),
              ("2x16x8192x64_non_causal", Workload("v8192d64", 2, 16, 8192, 64, torch.bfloat16, 2), False, False),
-             # the bf16 kernel at the E4M3 workload's shape, for the E4M3 / bf16 comparison
-             ("4x16x4096x128_non_causal", Workload("v4096", 4, 16, 4096, 128, torch.bfloat16, 3), False, False)]
+             # the bf16 kernel on the E4M3 workload's inputs (shape, seed, outliers), for the
+             # E4M3 / bf16 comparison
+             ("4x16x4096x128_non_causal_fp8_inputs",
+              Workload("v4096o", 4, 16, 4096, 128, torch.bfloat16, 3, (False,), True), False, False)]
     cache = {}
     for name, w, causal, pair in specs:
         if w.name not in cache:

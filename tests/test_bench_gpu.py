@@ -55,7 +55,7 @@ def test_default_line_carries_the_variants(gpu_lib):
                  "16x16x2048x128_causal", "2x16x8192x64_non_causal", "fp8_4x16x4096x128_forward",
                  "2x16x8192x128_non_causal_2cta", "16x16x2048x128_causal_2cta",
                  "fp8_4x16x4096x128_prologue_and_forward", "bwd_16x16x2048x128_non_causal",
-                 "4x16x4096x128_non_causal",
+                 "4x16x4096x128_non_causal_fp8_inputs",
                  "bwd_16x16x2048x128_causal"):
         assert v[name]["tflops"] > 0 and 0 < v[name]["roofline_frac"], name
     assert v["fp8_4x16x4096x128_prologue"]["gbs"] > 0
