@@ -650,12 +650,12 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, int t, uint32_t 
         pk[i] = ptx::pack2<L::kBf16Out>(v.x, v.y);
       }
     }
-    // In long 16-bit units, the warps that share an SMSP with the MMA-issuing warp hold their O
+    // In long units, the warps that share an SMSP with the MMA-issuing warp hold their O
     // stores until the next unit's S_t(0) is in (the wait step 0 of that unit does anyway):
     // their row-scattered stores queue ahead of that warp's tcgen05 instructions, and by
     // then the MMA thread has issued this unit boundary's MMAs.  In short units the held
     // stores would delay the next unit more than they save.
-    if (!L::kFp8 && ntile > kHoldStoresMinTiles && ((threadIdx.x / 32) & 3) == (kMmaWarp & 3)) {
+    if (ntile > kHoldStoresMinTiles && ((threadIdx.x / 32) & 3) == (kMmaWarp & 3)) {
       int bhn, qbn;
       if (unit_at(p, k + 1, bhn, qbn) && tile_nkv(p, qbn, t) > 0) {
         const bool held = ptx::mbar_wait(bar(L::kSFull + t), s_uses & 1u, ctl, kStatusSoftmaxTimeout);
