@@ -87,6 +87,9 @@ CASES = [
     (1, 2, 1000, 128, torch.float16),
     (1, 1, 129, 128, torch.bfloat16),
     (2, 1, 640, 128, torch.bfloat16),
+    # more units than SMs: CTAs run several units in turn (causal: units of one tile among
+    # them), so each epilogue's staging slots are refilled while later units run
+    (4, 48, 384, 128, torch.bfloat16),
 ]
 
 
@@ -155,8 +158,8 @@ def test_rejections(gpu_lib):
 
 
 def test_outputs_16_byte_aligned_match_aligned_outputs(gpu_lib):
-    # dQ, dK, dV at a 16-byte (not 32-byte) offset take the 16-byte store path; the
-    # values must be the same bits as with 32-byte aligned outputs
+    # dQ, dK, dV at a 16-byte (not 32-byte) offset: the values must be the same bits as with
+    # 32-byte aligned outputs (d = 128 writes them by TMA, d = 64 by 16-byte stores here)
     fa = gpu_lib
     shape = (1, 2, 300, 128)
     q, k, v = (t.cuda() for t in make_qkv(shape, torch.bfloat16, 13))

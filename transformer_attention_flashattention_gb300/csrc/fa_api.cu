@@ -496,6 +496,9 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   if (!encode_3d(&p.tm_q, dt, 2, q, d, N, BH, 64, 128) || !encode_3d(&p.tm_k, dt, 2, k, d, N, BH, 64, 128) ||
       !encode_3d(&p.tm_v, dt, 2, v, d, N, BH, 64, 128) || !encode_3d(&p.tm_do, dt, 2, dout, d, N, BH, 64, 128))
     return FA_ERR_CUDA;
+  if (d == 128 && (!encode_3d(&p.tm_dq, dt, 2, dq, d, N, BH, 64, 32) || !encode_3d(&p.tm_dk, dt, 2, dk, d, N, BH, 64, 32) ||
+                   !encode_3d(&p.tm_dv, dt, 2, dv, d, N, BH, 64, 32)))
+    return FA_ERR_CUDA;
   p.o = o;
   p.dout = dout;
   p.lse = lse;

@@ -110,7 +110,14 @@ struct BwdCfg {
   // dkdv kernel only: the stationary V tile's full / empty barriers (kStFull / kStEmpty are
   // its K tile's), so that each is reloaded as soon as the unit's last product using it ran
   static constexpr int kVsFull = kDoFree + kBwdStages, kVsEmpty = kVsFull + 1;
-  static constexpr int kNumBars = kVsEmpty + 1;
+  // d = 128, both kernels: unit u's epilogue has staged its accumulators in the ring slots of
+  // its last tile and its TMA stores have read them (compute arrives on kEpiFree + u % 3);
+  // the producer refills those slots only then.  Three barriers in turn, so that no barrier
+  // completes twice before the producer has waited for it (a unit can finish while the
+  // producer waits for an earlier unit's epilogue: at most two, with the dq kernel's three
+  // K slots and units of one tile)
+  static constexpr int kEpiFree = kVsEmpty + 1;
+  static constexpr int kNumBars = kEpiFree + 3;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes + 1024;        // slack to align the base to 1 KB
@@ -265,6 +272,31 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, float mul, void* o
   }
 }
 
+// The epilogue slice of one compute warp at d = 128: its 32 accumulator rows (TMEM lanes)
+// x 64 columns from taddr, times `mul`, packed to 16 bits into 4 KB of a free ring slot
+// laid out like a loaded tile (128-byte rows, 16-byte chunk c of row r at c ^ (r % 8)),
+// which is the 128-byte swizzle of the store's tensor map.  Each lane writes its own row.
+template <bool BF16>
+__device__ __forceinline__ void stage_slice(uint32_t taddr, float mul, uint8_t* slice, int lane) {
+  uint32_t r[2][32];
+  ptx::tmem_ld32(taddr, r[0]);
+  ptx::tmem_ld32(taddr + 32, r[1]);
+  ptx::tmem_wait_ld();
+  uint8_t* row = slice + lane * 128;
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {               // chunk 4c + kk: columns 32c + 8kk .. +7
+      const uint32_t* x = r[c] + 8 * kk;
+      const uint4 v = make_uint4(ptx::pack2<BF16>(__uint_as_float(x[0]) * mul, __uint_as_float(x[1]) * mul),
+                                 ptx::pack2<BF16>(__uint_as_float(x[2]) * mul, __uint_as_float(x[3]) * mul),
+                                 ptx::pack2<BF16>(__uint_as_float(x[4]) * mul, __uint_as_float(x[5]) * mul),
+                                 ptx::pack2<BF16>(__uint_as_float(x[6]) * mul, __uint_as_float(x[7]) * mul));
+      *reinterpret_cast<uint4*>(row + (((4 * c + kk) ^ (lane & 7)) << 4)) = v;
+    }
+  ptx::fence_proxy_async();
+}
+
 // dV += P^T dO or dK += dS^T Q over a tile's 128 queries: A = P^T or dS^T packed in TMEM by
 // the two compute threads of each key row (queries 0-63 at columns 0-31, 64-127 at columns
 // 64-95), B = dO or Q as an MN-major operand (16 query rows, 2 KB, a step).
@@ -305,6 +337,9 @@ __device__ __noinline__ void dq_producer(const BwdParams& p, uint32_t sbase, con
   using C = BwdCfg<D>;
   auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
   uint32_t nk = 0, nv = 0, units = 0;     // K and V loads issued so far, stationary fills
+  // d = 128: bit b of `last` says K fill nk-1-b was its unit's last tile, whose slot then
+  // holds that unit's epilogue staging; `epi` counts the epilogues waited for
+  uint32_t last = 0, epi = 0;
   // the whole warp runs this loop converged (its waits included); one lane issues
   const bool lead = ptx::elect_one() != 0;
   int bh, i;
@@ -319,6 +354,12 @@ __device__ __noinline__ void dq_producer(const BwdParams& p, uint32_t sbase, con
     ++units;
     for (int j = 0; j < n; ++j) {
       const uint32_t ks = nk % C::kDqKSlots, kf = nk / C::kDqKSlots;
+      static_assert(C::kDqKSlots == 3, "the history below spans three K fills");
+      if (D == 128 && (last & 4u)) {
+        if (!ptx::mbar_wait(bar(C::kEpiFree + epi % 3u), (epi / 3u) & 1u, ctl, 1u)) goto drain;
+        ++epi;
+      }
+      last = ((last << 1) | (j + 1 == n ? 1u : 0u)) & 7u;
       if (!ptx::mbar_wait(bar(C::kKFree + ks), (kf & 1u) ^ 1u, ctl, 1u)) goto drain;
       if (lead) {
         ptx::mbar_arrive_expect_tx(bar(C::kKFull + ks), C::kTile);
@@ -466,6 +507,7 @@ template <int D, Elem E>
 __device__ __forceinline__ void dq_compute(const BwdParams& p, uint32_t sbase, uint8_t* smem, uint32_t tmem,
                                            const ptx::WaitCtl& ctl) {
   using C = BwdCfg<D>;
+  using L = FwdCfg<D, E>;
   constexpr bool kBf16 = E == Elem::BF16;
   auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
@@ -495,13 +537,18 @@ __device__ __forceinline__ void dq_compute(const BwdParams& p, uint32_t sbase, u
     return true;
   };
   uint32_t tile = 0, units = 0;
+  uint32_t pend = 0;   // d = 128: 1 + the unit whose epilogue store may still read its staging
   int bh, i;
-  if (bwd_unit_at(p, 0, true, bh, i) && !copy_in(0)) return;
+  float nl = 0.f, nd = 0.f;   // this row's -LSE*log2(e) and -D, loaded a unit ahead
+  if (bwd_unit_at(p, 0, true, bh, i)) {
+    if (!copy_in(0)) return;
+    const size_t w0 = static_cast<size_t>(bh) * p.n_pad + i * 128 + r;
+    nl = p.nlse2[w0];
+    nd = p.ndelta[w0];
+  }
   for (int k = 0; bwd_unit_at(p, k, true, bh, i); ++k) {
     const int n = p.causal ? i + 1 : p.n_blk;
     const int row = i * 128 + r;
-    const size_t wrow = static_cast<size_t>(bh) * p.n_pad + row;
-    const float nl = p.nlse2[wrow], nd = p.ndelta[wrow];
     const float2 nl2 = make_float2(nl, nl), nd2 = make_float2(nd, nd);
     const int limit = min(p.N, p.causal ? row + 1 : p.N);      // keys >= limit get P = 0
     for (int j = 0; j < n; ++j, ++tile) {
@@ -544,19 +591,50 @@ __device__ __forceinline__ void dq_compute(const BwdParams& p, uint32_t sbase, u
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(C::kDsFull));
+      // the previous unit's epilogue store has long read its staging by now: hand the slot
+      // back to the producer (it refills it for this unit's third tile at the earliest)
+      if (D == 128 && pend != 0) {
+        if (lane == 0) {
+          ptx::bulk_wait_read<0>();
+          ptx::mbar_arrive(bar(C::kEpiFree + (pend - 1) % 3u));
+        }
+        pend = 0;
+      }
     }
     // the next unit's Q and dO go into TMEM before this unit's dQ is read out, so that
-    // its first S and dP run meanwhile
+    // its first S and dP run meanwhile; its rows' -LSE*log2(e) and -D are loaded meanwhile
     int bhn, inext;
-    if (bwd_unit_at(p, k + 1, true, bhn, inext) && !copy_in(units + 1)) return;
+    if (bwd_unit_at(p, k + 1, true, bhn, inext)) {
+      if (!copy_in(units + 1)) return;
+      const size_t wn = static_cast<size_t>(bhn) * p.n_pad + inext * 128 + r;
+      nl = p.nlse2[wn];
+      nd = p.ndelta[wn];
+    }
     const bool got = ptx::mbar_wait(bar(C::kAccFull), units & 1u, ctl, 4u);
     if (!__all_sync(0xFFFFFFFFu, got)) return;
-    ++units;
     ptx::tc_fence_after();
-    store_acc_row<D / 2, kBf16>(tAcc, p.scale, p.dq,
-                                (static_cast<size_t>(bh) * p.N + (row < p.N ? row : 0)) * D + (D / 2) * sub,
-                                row < p.N);
-    ptx::tc_fence_before();
+    if constexpr (D == 128) {
+      // dQ staged in the K slot of the unit's last tile (its products have run; the producer
+      // refills it once the store below has read it), then one TMA store, and no wait here
+      const uint32_t at = C::kDqKOff + ((tile - 1) % C::kDqKSlots) * C::kTile + sub * L::kAtomBytes +
+                          (warp & 3) * 32 * 128;
+      stage_slice<kBf16>(tAcc, p.scale, smem + at, lane);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        const int row0 = i * 128 + (warp & 3) * 32;
+        if (row0 < p.N) ptx::tma_store_3d(&p.tm_dq, sbase + at, 64 * sub, row0, bh);
+        ptx::bulk_commit();
+      }
+      pend = units + 1;
+      __syncwarp();
+    } else {
+      store_acc_row<D / 2, kBf16>(tAcc, p.scale, p.dq,
+                                  (static_cast<size_t>(bh) * p.N + (row < p.N ? row : 0)) * D + (D / 2) * sub,
+                                  row < p.N);
+      ptx::tc_fence_before();
+    }
+    ++units;
   }
 }
 
@@ -568,6 +646,9 @@ __device__ __noinline__ void dkdv_producer(const BwdParams& p, uint32_t sbase, c
   using L = FwdCfg<D, E>;
   auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
   uint32_t nd = 0, nq = 0, units = 0, vunits = 0;   // dO, Q, K and V fills issued so far
+  // d = 128: bit b of `last` says fill nq-1-b was its unit's last tile, whose slots then hold
+  // that unit's epilogue staging; `epi` counts the epilogues waited for
+  uint32_t last = 0, epi = 0;
   // the whole warp runs this loop converged (its waits included); one lane issues
   const bool lead = ptx::elect_one() != 0;
   int bh, j;
@@ -598,6 +679,11 @@ __device__ __noinline__ void dkdv_producer(const BwdParams& p, uint32_t sbase, c
     for (int i = i0; i < p.n_blk; ++i) {
       // tile number nq == nd: its ring slot and the slot's fill count
       const uint32_t s = nq % kBwdStages, f = nq / kBwdStages;
+      if (D == 128 && (last & 2u)) {
+        if (!ptx::mbar_wait(bar(C::kEpiFree + epi % 3u), (epi / 3u) & 1u, ctl, 1u)) goto drain;
+        ++epi;
+      }
+      last = ((last << 1) | (i + 1 == p.n_blk ? 1u : 0u)) & 3u;
       // Q first: S^T is the first product of a tile
       if (!ptx::mbar_wait(bar(C::kDone + s), (f & 1u) ^ 1u, ctl, 1u)) goto drain;
       if (lead) {
@@ -711,6 +797,7 @@ template <int D, Elem E>
 __device__ __forceinline__ void dkdv_compute(const BwdParams& p, uint32_t sbase, uint8_t* smem, uint32_t tmem,
                                              const ptx::WaitCtl& ctl) {
   using C = BwdCfg<D>;
+  using L = FwdCfg<D, E>;
   constexpr bool kBf16 = E == Elem::BF16;
   auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
@@ -721,6 +808,7 @@ __device__ __forceinline__ void dkdv_compute(const BwdParams& p, uint32_t sbase,
   const uint32_t tDV = tmem + lane_base + kTmAcc + (D / 2) * sub, tDK = tDV + D;
   const float2 cc = make_float2(p.scale_log2, p.scale_log2);
   uint32_t tile = 0, units = 0;
+  uint32_t pend = 0;   // d = 128: 1 + the unit whose epilogue stores may still read its staging
   int bh, j;
   for (int k = 0; bwd_unit_at(p, k, false, bh, j); ++k) {
     const int i0 = p.causal ? j : 0;
@@ -757,6 +845,15 @@ __device__ __forceinline__ void dkdv_compute(const BwdParams& p, uint32_t sbase,
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(C::kDsFull + 1));
+      // the previous unit's epilogue stores have long read their staging by now: hand the
+      // slots back to the producer (it refills them for this unit's second tile at the earliest)
+      if (D == 128 && pend != 0) {
+        if (lane == 0) {
+          ptx::bulk_wait_read<0>();
+          ptx::mbar_arrive(bar(C::kEpiFree + (pend - 1) % 3u));
+        }
+        pend = 0;
+      }
       // dS^T(i) once dP^T(i) is in
       got = ptx::mbar_wait(bar(C::kSdpFull + 1), tile & 1u, ctl, 4u);
       if (!__all_sync(0xFFFFFFFFu, got)) return;
@@ -780,12 +877,35 @@ __device__ __forceinline__ void dkdv_compute(const BwdParams& p, uint32_t sbase,
     }
     const bool got = ptx::mbar_wait(bar(C::kAccFull), units & 1u, ctl, 4u);
     if (!__all_sync(0xFFFFFFFFu, got)) return;
-    ++units;
     ptx::tc_fence_after();
-    const size_t off = (static_cast<size_t>(bh) * p.N + (key < p.N ? key : 0)) * D + (D / 2) * sub;
-    store_acc_row<D / 2, kBf16>(tDV, 1.f, p.dv, off, key < p.N);
-    store_acc_row<D / 2, kBf16>(tDK, p.scale, p.dk, off, key < p.N);
-    ptx::tc_fence_before();
+    if constexpr (D == 128) {
+      // dV staged in the dO slot and dK in the Q slot of the unit's last tile (its products
+      // have run; the producer refills the slots once the stores below have read them),
+      // then one TMA store per accumulator: no scattered row stores, and no wait here
+      const uint32_t sl = (tile - 1) % kBwdStages;
+      const uint32_t slice = sub * L::kAtomBytes + (warp & 3) * 32 * 128;
+      const uint32_t dv_at = C::kKvDoOff + sl * C::kTile + slice, dk_at = C::kKvQOff + sl * C::kTile + slice;
+      stage_slice<kBf16>(tDV, 1.f, smem + dv_at, lane);
+      stage_slice<kBf16>(tDK, p.scale, smem + dk_at, lane);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        const int row0 = j * 128 + (warp & 3) * 32;
+        if (row0 < p.N) {
+          ptx::tma_store_3d(&p.tm_dv, sbase + dv_at, 64 * sub, row0, bh);
+          ptx::tma_store_3d(&p.tm_dk, sbase + dk_at, 64 * sub, row0, bh);
+        }
+        ptx::bulk_commit();
+      }
+      pend = units + 1;
+      __syncwarp();
+    } else {
+      const size_t off = (static_cast<size_t>(bh) * p.N + (key < p.N ? key : 0)) * D + (D / 2) * sub;
+      store_acc_row<D / 2, kBf16>(tDV, 1.f, p.dv, off, key < p.N);
+      store_acc_row<D / 2, kBf16>(tDK, p.scale, p.dk, off, key < p.N);
+      ptx::tc_fence_before();
+    }
+    ++units;
   }
 }
 
@@ -806,7 +926,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumBars; ++i)
       ptx::mbar_init(bar(i), (i == C::kDsFull || i == C::kDsFull + 1 || i == C::kSdpFree || i == C::kQtFull ||
-                              (!DKDV && i == C::kStEmpty))
+                              (!DKDV && i == C::kStEmpty) || (i >= C::kEpiFree && i < C::kEpiFree + 3))
                                  ? kBwdComputeWarps : 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
@@ -836,6 +956,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
   } else {
     if constexpr (DKDV) dkdv_compute<D, E>(p, sbase, smem, tmem, ctl);
     else dq_compute<D, E>(p, sbase, smem, tmem, ctl);
+    // the epilogues' TMA stores (issued by lane 0) complete before the CTA leaves
+    if (D == 128 && lane == 0) ptx::bulk_wait<0>();
   }
 
   ptx::tc_fence_before();

@@ -82,6 +82,11 @@ struct BwdParams {
   CUtensorMap tm_k;
   CUtensorMap tm_v;
   CUtensorMap tm_do;
+  // d = 128: the epilogues' TMA stores of dQ, dK and dV, box {128 bytes of d, 32 rows, 1}
+  // (one compute warp's slice), 128-byte swizzle
+  CUtensorMap tm_dq;
+  CUtensorMap tm_dk;
+  CUtensorMap tm_dv;
   const void* o;      // [B*H, N, d] (prep kernel)
   const void* dout;   // [B*H, N, d] (prep kernel)
   const float* lse;   // [B*H, N] natural-log LSE of the forward pass
