@@ -297,6 +297,34 @@ __device__ __forceinline__ void stage_slice(uint32_t taddr, float mul, uint8_t* 
   ptx::fence_proxy_async();
 }
 
+// Two such slices (dV and dK: the first unscaled, the second times `mul2`) with their
+// four TMEM loads in flight at once.
+template <bool BF16>
+__device__ __forceinline__ void stage_slices(uint32_t ta1, uint32_t ta2, float mul2, uint8_t* s1, uint8_t* s2,
+                                             int lane) {
+  uint32_t r[4][32];
+  ptx::tmem_ld32(ta1, r[0]);
+  ptx::tmem_ld32(ta1 + 32, r[1]);
+  ptx::tmem_ld32(ta2, r[2]);
+  ptx::tmem_ld32(ta2 + 32, r[3]);
+  ptx::tmem_wait_ld();
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint8_t* row = (c < 2 ? s1 : s2) + lane * 128;
+    const float mul = c < 2 ? 1.f : mul2;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {               // chunk 4(c % 2) + kk: columns 32(c % 2) + 8kk .. +7
+      const uint32_t* x = r[c] + 8 * kk;
+      const uint4 v = make_uint4(ptx::pack2<BF16>(__uint_as_float(x[0]) * mul, __uint_as_float(x[1]) * mul),
+                                 ptx::pack2<BF16>(__uint_as_float(x[2]) * mul, __uint_as_float(x[3]) * mul),
+                                 ptx::pack2<BF16>(__uint_as_float(x[4]) * mul, __uint_as_float(x[5]) * mul),
+                                 ptx::pack2<BF16>(__uint_as_float(x[6]) * mul, __uint_as_float(x[7]) * mul));
+      *reinterpret_cast<uint4*>(row + (((4 * (c & 1) + kk) ^ (lane & 7)) << 4)) = v;
+    }
+  }
+  ptx::fence_proxy_async();
+}
+
 // dV += P^T dO or dK += dS^T Q over a tile's 128 queries: A = P^T or dS^T packed in TMEM by
 // the two compute threads of each key row (queries 0-63 at columns 0-31, 64-127 at columns
 // 64-95), B = dO or Q as an MN-major operand (16 query rows, 2 KB, a step).
@@ -418,8 +446,9 @@ __device__ __noinline__ void dq_mma(const BwdParams& p, uint32_t sbase, uint32_t
     return true;
   };
   uint32_t tile = 0, units = 0;
-  int bh, i;
-  for (int k = 0; bwd_unit_at(p, k, true, bh, i); ++k) {
+  int bh = 0, i = 0;
+  bool have = bwd_unit_at(p, 0, true, bh, i);
+  for (int k = 0; have; ++k) {
     const int n = p.causal ? i + 1 : p.n_blk;
     // the unit's Q and dO are in TMEM
     if (!ptx::mbar_wait(bar(C::kQtFull), units & 1u, ctl, 2u)) goto done;
@@ -427,6 +456,9 @@ __device__ __noinline__ void dq_mma(const BwdParams& p, uint32_t sbase, uint32_t
     if (!s_(tile) || !dp_(tile)) goto done;
     // Q and dO are free once the unit's last S and dP have run
     if (n == 1) ptx::mma_commit_e(lead, bar(C::kQtFree));
+    // the next unit, worked out while these products run
+    int bhn = 0, inext = 0;
+    const bool more_units = bwd_unit_at(p, k + 1, true, bhn, inext);
     for (int j = 0; j < n; ++j, ++tile) {
       const bool more = j + 1 < n;
       // S(j) is in the compute threads' registers: S(j+1) goes into its columns
@@ -447,6 +479,9 @@ __device__ __noinline__ void dq_mma(const BwdParams& p, uint32_t sbase, uint32_t
     }
     ptx::mma_commit_e(lead, bar(C::kAccFull));
     ++units;
+    bh = bhn;
+    i = inext;
+    have = more_units;
   }
 done:
   ptx::mma_commit_e(lead, bar(C::kMmaDone));
@@ -538,15 +573,16 @@ __device__ __forceinline__ void dq_compute(const BwdParams& p, uint32_t sbase, u
   };
   uint32_t tile = 0, units = 0;
   uint32_t pend = 0;   // d = 128: 1 + the unit whose epilogue store may still read its staging
-  int bh, i;
+  int bh = 0, i = 0;
   float nl = 0.f, nd = 0.f;   // this row's -LSE*log2(e) and -D, loaded a unit ahead
-  if (bwd_unit_at(p, 0, true, bh, i)) {
+  bool have = bwd_unit_at(p, 0, true, bh, i);
+  if (have) {
     if (!copy_in(0)) return;
     const size_t w0 = static_cast<size_t>(bh) * p.n_pad + i * 128 + r;
     nl = p.nlse2[w0];
     nd = p.ndelta[w0];
   }
-  for (int k = 0; bwd_unit_at(p, k, true, bh, i); ++k) {
+  for (int k = 0; have; ++k) {
     const int n = p.causal ? i + 1 : p.n_blk;
     const int row = i * 128 + r;
     const float2 nl2 = make_float2(nl, nl), nd2 = make_float2(nd, nd);
@@ -603,8 +639,9 @@ __device__ __forceinline__ void dq_compute(const BwdParams& p, uint32_t sbase, u
     }
     // the next unit's Q and dO go into TMEM before this unit's dQ is read out, so that
     // its first S and dP run meanwhile; its rows' -LSE*log2(e) and -D are loaded meanwhile
-    int bhn, inext;
-    if (bwd_unit_at(p, k + 1, true, bhn, inext)) {
+    int bhn = 0, inext = 0;
+    const bool more = bwd_unit_at(p, k + 1, true, bhn, inext);
+    if (more) {
       if (!copy_in(units + 1)) return;
       const size_t wn = static_cast<size_t>(bhn) * p.n_pad + inext * 128 + r;
       nl = p.nlse2[wn];
@@ -635,6 +672,9 @@ __device__ __forceinline__ void dq_compute(const BwdParams& p, uint32_t sbase, u
       ptx::tc_fence_before();
     }
     ++units;
+    bh = bhn;
+    i = inext;
+    have = more;
   }
 }
 
@@ -749,8 +789,9 @@ __device__ __noinline__ void dkdv_mma(const BwdParams& p, uint32_t sbase, uint32
     return true;
   };
   uint32_t tile = 0, units = 0;
-  int bh, j;
-  for (int k = 0; bwd_unit_at(p, k, false, bh, j); ++k) {
+  int bh = 0, j = 0;
+  bool have = bwd_unit_at(p, 0, false, bh, j);
+  for (int k = 0; have; ++k) {
     const int i0 = p.causal ? j : 0;
     // K is free once the unit's last S^T has run, V once its last dP^T has: the next
     // unit's loads overlap this unit's last products
@@ -761,6 +802,9 @@ __device__ __noinline__ void dkdv_mma(const BwdParams& p, uint32_t sbase, uint32
     if (!ptx::mbar_wait(bar(C::kVsFull), units & 1u, ctl, 2u)) goto done;
     if (!dp(tile)) goto done;
     if (one) ptx::mma_commit_e(lead, bar(C::kVsEmpty));
+    // the next unit, worked out while these products run
+    int bhn = 0, jn = 0;
+    const bool more_units = bwd_unit_at(p, k + 1, false, bhn, jn);
     for (int i = i0; i < p.n_blk; ++i, ++tile) {
       const uint32_t s = tile % kBwdStages;
       const bool more = i + 1 < p.n_blk;
@@ -787,6 +831,9 @@ __device__ __noinline__ void dkdv_mma(const BwdParams& p, uint32_t sbase, uint32
     }
     ptx::mma_commit_e(lead, bar(C::kAccFull));
     ++units;
+    bh = bhn;
+    j = jn;
+    have = more_units;
   }
 done:
   ptx::mma_commit_e(lead, bar(C::kMmaDone));
@@ -809,8 +856,9 @@ __device__ __forceinline__ void dkdv_compute(const BwdParams& p, uint32_t sbase,
   const float2 cc = make_float2(p.scale_log2, p.scale_log2);
   uint32_t tile = 0, units = 0;
   uint32_t pend = 0;   // d = 128: 1 + the unit whose epilogue stores may still read its staging
-  int bh, j;
-  for (int k = 0; bwd_unit_at(p, k, false, bh, j); ++k) {
+  int bh = 0, j = 0;
+  bool have = bwd_unit_at(p, 0, false, bh, j);
+  for (int k = 0; have; ++k) {
     const int i0 = p.causal ? j : 0;
     const int key = j * 128 + kr;
     for (int i = i0; i < p.n_blk; ++i, ++tile) {
@@ -875,6 +923,9 @@ __device__ __forceinline__ void dkdv_compute(const BwdParams& p, uint32_t sbase,
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(C::kDsFull));
     }
+    // the next unit, worked out while the last dK product runs (not after the epilogue)
+    int bhn = 0, jn = 0;
+    const bool more = bwd_unit_at(p, k + 1, false, bhn, jn);
     const bool got = ptx::mbar_wait(bar(C::kAccFull), units & 1u, ctl, 4u);
     if (!__all_sync(0xFFFFFFFFu, got)) return;
     ptx::tc_fence_after();
@@ -885,8 +936,7 @@ __device__ __forceinline__ void dkdv_compute(const BwdParams& p, uint32_t sbase,
       const uint32_t sl = (tile - 1) % kBwdStages;
       const uint32_t slice = sub * L::kAtomBytes + (warp & 3) * 32 * 128;
       const uint32_t dv_at = C::kKvDoOff + sl * C::kTile + slice, dk_at = C::kKvQOff + sl * C::kTile + slice;
-      stage_slice<kBf16>(tDV, 1.f, smem + dv_at, lane);
-      stage_slice<kBf16>(tDK, p.scale, smem + dk_at, lane);
+      stage_slices<kBf16>(tDV, tDK, p.scale, smem + dv_at, smem + dk_at, lane);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -906,6 +956,9 @@ __device__ __forceinline__ void dkdv_compute(const BwdParams& p, uint32_t sbase,
       ptx::tc_fence_before();
     }
     ++units;
+    bh = bhn;
+    j = jn;
+    have = more;
   }
 }
 
