@@ -216,11 +216,13 @@ __device__ __forceinline__ void load_tile(const CUtensorMap* map, uint32_t dst, 
 // -LSE*log2(e) as pairs from shared memory; with MASK, queries x < first get P = 0.  The
 // values stay in pv for dS; w gets them packed.
 template <bool BF16, bool MASK>
-__device__ __forceinline__ void dkdv_p32(const uint32_t (&sr)[32], float2 cc, const float2* nl, int first,
+__device__ __forceinline__ void dkdv_p32(const uint32_t (&sr)[32], float2 cc, const float4* nl, int first,
                                          float2 (&pv)[16], uint32_t (&w)[16]) {
 #pragma unroll
   for (int x = 0; x < 16; ++x) {
-    const float2 t = ptx::fma2(make_float2(__uint_as_float(sr[2 * x]), __uint_as_float(sr[2 * x + 1])), cc, nl[x]);
+    const float4 n4 = nl[x / 2];                   // 16-byte broadcast loads: two pairs each
+    const float2 n = (x & 1) ? make_float2(n4.z, n4.w) : make_float2(n4.x, n4.y);
+    const float2 t = ptx::fma2(make_float2(__uint_as_float(sr[2 * x]), __uint_as_float(sr[2 * x + 1])), cc, n);
     float2 v = make_float2(ptx::ex2(t.x), ptx::ex2(t.y));
     if constexpr (MASK) {
       if (2 * x < first) v.x = 0.f;
@@ -233,12 +235,14 @@ __device__ __forceinline__ void dkdv_p32(const uint32_t (&sr)[32], float2 cc, co
 
 // dS^T = P (dP - D) of one key row against 32 queries, packed (nd: the queries' -D pairs).
 template <bool BF16>
-__device__ __forceinline__ void dkdv_ds32(const uint32_t (&dr)[32], const float2 (&pv)[16], const float2* nd,
+__device__ __forceinline__ void dkdv_ds32(const uint32_t (&dr)[32], const float2 (&pv)[16], const float4* nd,
                                           uint32_t (&w)[16]) {
 #pragma unroll
   for (int x = 0; x < 16; ++x) {
+    const float4 n4 = nd[x / 2];
+    const float2 n = (x & 1) ? make_float2(n4.z, n4.w) : make_float2(n4.x, n4.y);
     const float2 ds =
-        ptx::mul2(pv[x], ptx::add2(make_float2(__uint_as_float(dr[2 * x]), __uint_as_float(dr[2 * x + 1])), nd[x]));
+        ptx::mul2(pv[x], ptx::add2(make_float2(__uint_as_float(dr[2 * x]), __uint_as_float(dr[2 * x + 1])), n));
     w[x] = ptx::pack2<BF16>(ds.x, ds.y);
   }
 }
@@ -881,7 +885,7 @@ __device__ __forceinline__ void dkdv_compute(const BwdParams& p, uint32_t sbase,
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const int q0 = 64 * sub + 32 * c;                      // first query of this chunk
-        const float2* nl = reinterpret_cast<const float2*>(vec + q0);
+        const float4* nl = reinterpret_cast<const float4*>(vec + q0);   // 128-byte aligned
         uint32_t wp[16];
         // causal diagonal tile: query i*128 + q0 + x sees this key iff q0 + x >= kr (padded
         // queries have -LSE*log2(e) = -inf and so P = 0 already)
@@ -913,7 +917,7 @@ __device__ __forceinline__ void dkdv_compute(const BwdParams& p, uint32_t sbase,
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const int q0 = 64 * sub + 32 * c;
-        const float2* nd = reinterpret_cast<const float2*>(vec + 128 + q0);
+        const float4* nd = reinterpret_cast<const float4*>(vec + 128 + q0);
         uint32_t wd[16];
         dkdv_ds32<kBf16>(dr[c], pv[c], nd, wd);
         ptx::tmem_st16(tDP + 16 * c, wd);                      // over dP^T columns already read
