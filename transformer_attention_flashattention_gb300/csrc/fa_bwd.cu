@@ -34,7 +34,8 @@
 //              and TMEM owner
 // dq kernel: whole 128-key tiles, S and dP with N = 128, in the tensor-pipe order
 //   ... S(j)  dP(j)  S(j+1)  dQ(j)  dP(j+1)  S(j+2)  dQ(j+1) ...
-// The unit's Q and dO tiles are copied from shared memory into TMEM once, so all three
+// The unit's Q and dO tiles are copied from shared memory into TMEM once (tcgen05.cp, issued
+// by the MMA thread in order before the unit's products), so all three
 // products take their A operand from TMEM and read only B (K or V) from shared memory.
 // The compute threads form P(j) as soon as S(j) is in, and signal once S(j) is in their
 // registers so that S(j+1) can follow; once dP(j) is in, they form dS(j) and pack it over
@@ -96,11 +97,11 @@ struct BwdCfg {
   static constexpr int kStFull = 0, kStEmpty = 1, kReady = 2, kDone = kReady + kBwdStages;
   static constexpr int kSdpFull = kDone + kBwdStages, kDsFull = kSdpFull + 2, kAccFull = kDsFull + 2;   // per half
   static constexpr int kMmaDone = kAccFull + 1;
-  // dq kernel only: S read into registers (compute arrives); Q and dO in TMEM (compute
-  // arrives) and free again (commit after the unit's last S and dP); the K and V rings'
-  // full / free barriers per slot.  It takes kSdpFull / kSdpFull + 1 as "S in" / "dP in"
-  // (commits) and kStEmpty as "stationary tiles copied out of shared memory" (compute).
-  static constexpr int kSdpFree = kMmaDone + 1, kQtFull = kSdpFree + 1, kQtFree = kQtFull + 1;
+  // dq kernel only: S read into registers (compute arrives); Q and dO's TMEM columns free
+  // again (commit after the unit's last S and dP); the K and V rings' full / free
+  // barriers per slot.  It takes kSdpFull / kSdpFull + 1 as "S in" / "dP in" (commits) and
+  // kStEmpty as "stationary tiles copied into TMEM" (commit after the copies).
+  static constexpr int kSdpFree = kMmaDone + 1, kQtFree = kSdpFree + 1;
   static constexpr int kKFull = kQtFree + 1, kKFree = kKFull + kDqKSlots;
   static constexpr int kVFull = kKFree + kDqKSlots, kVFree = kVFull + kDqVSlots;
   // dkdv kernel only: its dO slots' full / free barriers.  It also takes kReady / kDone as
@@ -362,6 +363,20 @@ __device__ __forceinline__ void issue_ts_s(uint32_t tD, uint32_t tA, uint32_t b_
   }
 }
 
+// A 128-row tile of shared memory (D elements a row, 128-byte swizzle atoms) into TMEM as an
+// A operand (two 16-bit values a column, D / 2 columns at tD), by tcgen05.cp: one 32-byte
+// K step (8 columns) a copy, in order before the MMAs issued after it.
+template <int D, Elem E, int KK = 0>
+__device__ __forceinline__ void copy_tile_tmem(uint32_t tD, uint32_t lo, uint32_t lead) {
+  using L = FwdCfg<D, E>;
+  if constexpr (KK < D / 16) {
+    constexpr uint32_t desc_hi = ptx::sdesc_hi(1024);
+    constexpr uint32_t kOb = ((KK * 32 / 128) * L::kAtomBytes + (KK * 32) % 128) >> 4;
+    ptx::cp_128x256b_oe<kOb>(lead, tD + 8 * KK, lo, desc_hi);
+    copy_tile_tmem<D, E, KK + 1>(tD, lo, lead);
+  }
+}
+
 // ---------------------------------------------------------------------------- dq kernel
 
 template <int D, Elem E>
@@ -430,6 +445,8 @@ __device__ __noinline__ void dq_mma(const BwdParams& p, uint32_t sbase, uint32_t
   const uint32_t kmn_lo0 = ptx::sdesc_lo(sbase + C::kDqKOff, v_lbo<D, E>());    // K as MN-major B of dQ
   const uint32_t v_lo0 = ptx::sdesc_lo(sbase + C::kDqVOff, 16);                 // V as K-major B of dP
   const uint32_t tQ = tmem + kQQ, tDO = tmem + kQDO, tS = tmem + kQS, tDP = tmem + kQDP, tAcc = tmem + kQAcc;
+  const uint32_t q_lo = ptx::sdesc_lo(sbase + C::kStatOff, 16);                 // stationary Q
+  const uint32_t do_lo = ptx::sdesc_lo(sbase + C::kStatOff + C::kTile, 16);     // stationary dO
   // S = Q K^T and dP = dO V^T for global tile number t, each with its commit; V's slot is
   // free once dP has run
   auto s_ = [&](uint32_t t) -> bool {
@@ -449,14 +466,25 @@ __device__ __noinline__ void dq_mma(const BwdParams& p, uint32_t sbase, uint32_t
     ptx::mma_commit_e(lead, bar(C::kVFree + vs));
     return true;
   };
+  // unit u's Q and dO into TMEM once they have landed in shared memory and unit u-1's
+  // last S and dP (which read those columns) have completed; the copies run in order
+  // before the products issued after them, and their commit frees the shared memory for
+  // unit u+1's tiles
+  auto copy_in = [&](uint32_t u) -> bool {
+    if (!ptx::mbar_wait(bar(C::kStFull), u & 1u, ctl, 2u)) return false;
+    if (u > 0 && !ptx::mbar_wait(bar(C::kQtFree), (u - 1u) & 1u, ctl, 2u)) return false;
+    ptx::tc_fence_after();
+    copy_tile_tmem<D, E>(tQ, q_lo, lead);
+    copy_tile_tmem<D, E>(tDO, do_lo, lead);
+    ptx::mma_commit_e(lead, bar(C::kStEmpty));
+    return true;
+  };
   uint32_t tile = 0, units = 0;
   int bh = 0, i = 0;
   bool have = bwd_unit_at(p, 0, true, bh, i);
+  if (have && !copy_in(0)) goto done;
   for (int k = 0; have; ++k) {
     const int n = p.causal ? i + 1 : p.n_blk;
-    // the unit's Q and dO are in TMEM
-    if (!ptx::mbar_wait(bar(C::kQtFull), units & 1u, ctl, 2u)) goto done;
-    ptx::tc_fence_after();
     if (!s_(tile) || !dp_(tile)) goto done;
     // Q and dO are free once the unit's last S and dP have run
     if (n == 1) ptx::mma_commit_e(lead, bar(C::kQtFree));
@@ -468,6 +496,9 @@ __device__ __noinline__ void dq_mma(const BwdParams& p, uint32_t sbase, uint32_t
       // S(j) is in the compute threads' registers: S(j+1) goes into its columns
       if (!ptx::mbar_wait(bar(C::kSdpFree), tile & 1u, ctl, 2u)) goto done;
       if (more && !s_(tile + 1)) goto done;
+      // the next unit's Q and dO go in as soon as this unit's last S and dP have completed,
+      // ahead of its last dQ: the copies then overlap the compute threads' last dS
+      if (!more && more_units && !copy_in(units + 1)) goto done;
       // dS(j) packed over the dP(j) columns: dQ += dS K_j, after which K_j's slot is free
       if (!ptx::mbar_wait(bar(C::kDsFull), tile & 1u, ctl, 2u)) goto done;
       ptx::tc_fence_after();
@@ -490,29 +521,6 @@ __device__ __noinline__ void dq_mma(const BwdParams& p, uint32_t sbase, uint32_t
 done:
   ptx::mma_commit_e(lead, bar(C::kMmaDone));
   if (!ptx::mbar_wait_drain(bar(C::kMmaDone), 0, ctl.timeout_ns)) atomicOr(ctl.status, 8u);
-}
-
-// Half of row r of a stationary 128-row tile in shared memory (128-byte swizzle atoms of
-// 64 elements; 16-byte chunk c of a row sits at chunk c ^ (r % 8)): elements
-// sub*D/2 .. +D/2-1, as D/4 words of two 16-bit values, into TMEM at taddr.
-template <int D, Elem E>
-__device__ __forceinline__ void tile_row_to_tmem(const uint8_t* tile, int r, int sub, uint32_t taddr) {
-  using L = FwdCfg<D, E>;
-  constexpr int kChunks = D / 16;                    // 16-byte chunks in half a row
-  const int e0 = sub * (D / 2);
-  const uint8_t* row = tile + (e0 / 64) * L::kAtomBytes + r * 128;
-  const int c0 = (e0 % 64) / 8;
-  uint32_t w[D / 4];
-#pragma unroll
-  for (int k = 0; k < kChunks; ++k) {
-    const uint4 v = *reinterpret_cast<const uint4*>(row + (((c0 + k) ^ (r & 7)) << 4));
-    w[4 * k] = v.x;
-    w[4 * k + 1] = v.y;
-    w[4 * k + 2] = v.z;
-    w[4 * k + 3] = v.w;
-  }
-  if constexpr (D == 128) ptx::tmem_st32(taddr, w);
-  else ptx::tmem_st16(taddr, w);
 }
 
 // P of 32 scores of one dq row: P = 2^(s * c + nl) with the row's nl = -LSE*log2(e); with
@@ -556,32 +564,12 @@ __device__ __forceinline__ void dq_compute(const BwdParams& p, uint32_t sbase, u
   const uint32_t tS = tmem + lane_base + kQS + 64 * sub, tDP = tmem + lane_base + kQDP + 64 * sub;
   const uint32_t tAcc = tmem + lane_base + kQAcc + (D / 2) * sub;
   const float2 cc = make_float2(p.scale_log2, p.scale_log2);
-  // Unit u's Q and dO rows into TMEM (A operands of S and dP), once the tiles have landed
-  // in shared memory and unit u-1's last S and dP have run; then shared memory is free
-  // for the next unit's tiles.
-  auto copy_in = [&](uint32_t u) -> bool {
-    bool ok = ptx::mbar_wait(bar(C::kStFull), u & 1u, ctl, 4u);
-    if (ok && u > 0) ok = ptx::mbar_wait(bar(C::kQtFree), (u - 1) & 1u, ctl, 4u);
-    if (!__all_sync(0xFFFFFFFFu, ok)) return false;
-    ptx::tc_fence_after();
-    tile_row_to_tmem<D, E>(smem + C::kStatOff, r, sub, tmem + lane_base + kQQ + (D / 4) * sub);
-    tile_row_to_tmem<D, E>(smem + C::kStatOff + C::kTile, r, sub, tmem + lane_base + kQDO + (D / 4) * sub);
-    ptx::tmem_wait_st();
-    ptx::tc_fence_before();
-    __syncwarp();
-    if (lane == 0) {
-      ptx::mbar_arrive(bar(C::kQtFull));
-      ptx::mbar_arrive(bar(C::kStEmpty));
-    }
-    return true;
-  };
   uint32_t tile = 0, units = 0;
   uint32_t pend = 0;   // d = 128: 1 + the unit whose epilogue store may still read its staging
   int bh = 0, i = 0;
   float nl = 0.f, nd = 0.f;   // this row's -LSE*log2(e) and -D, loaded a unit ahead
   bool have = bwd_unit_at(p, 0, true, bh, i);
   if (have) {
-    if (!copy_in(0)) return;
     const size_t w0 = static_cast<size_t>(bh) * p.n_pad + i * 128 + r;
     nl = p.nlse2[w0];
     nd = p.ndelta[w0];
@@ -641,12 +629,10 @@ __device__ __forceinline__ void dq_compute(const BwdParams& p, uint32_t sbase, u
         pend = 0;
       }
     }
-    // the next unit's Q and dO go into TMEM before this unit's dQ is read out, so that
-    // its first S and dP run meanwhile; its rows' -LSE*log2(e) and -D are loaded meanwhile
+    // the next unit's rows' -LSE*log2(e) and -D, loaded while the last dQ product runs
     int bhn = 0, inext = 0;
     const bool more = bwd_unit_at(p, k + 1, true, bhn, inext);
     if (more) {
-      if (!copy_in(units + 1)) return;
       const size_t wn = static_cast<size_t>(bhn) * p.n_pad + inext * 128 + r;
       nl = p.nlse2[wn];
       nd = p.ndelta[wn];
@@ -982,8 +968,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumBars; ++i)
-      ptx::mbar_init(bar(i), (i == C::kDsFull || i == C::kDsFull + 1 || i == C::kSdpFree || i == C::kQtFull ||
-                              (!DKDV && i == C::kStEmpty) || (i >= C::kEpiFree && i < C::kEpiFree + 3))
+      ptx::mbar_init(bar(i), (i == C::kDsFull || i == C::kDsFull + 1 || i == C::kSdpFree ||
+                              (i >= C::kEpiFree && i < C::kEpiFree + 3))
                                  ? kBwdComputeWarps : 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();

@@ -341,6 +341,24 @@ __device__ __forceinline__ void mma_f16_ts_oe(uint32_t lead, uint32_t d_tmem, ui
       "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "n"(ACC), "n"(OT), "n"(OB), "r"(lead)
       : "memory");
 }
+// tcgen05.cp of a 128-row x 256-bit block from shared memory into 8 TMEM columns at taddr
+// (row r to lane r, its 32 bytes to the columns in order: the layout of an A operand in
+// TMEM), the block described by a matrix descriptor (b_lo + OB, hi) as for an MMA operand.
+// Executes after the MMAs and copies this thread issued before it, and before the MMAs it
+// issues after (a later MMA may read the columns at once); an MMA issued before it that
+// reads the columns must have completed.  Only the lanes with lead != 0 issue.
+template <uint32_t OB>
+__device__ __forceinline__ void cp_128x256b_oe(uint32_t lead, uint32_t taddr, uint32_t b_lo, uint32_t hi) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 lb;\n\t.reg .b64 db;\n\t"
+      "setp.ne.b32 e, %3, 0;\n\t"
+      "add.u32 lb, %1, %4;\n\t"
+      "mov.b64 db, {lb, %2};\n\t"
+      "@e tcgen05.cp.cta_group::1.128x256b [%0], db;\n\t}" ::"r"(taddr),
+      "r"(b_lo), "r"(hi), "r"(lead), "n"(OB)
+      : "memory");
+}
+
 template <int ACC, uint32_t OA, uint32_t OB>
 __device__ __forceinline__ void mma_f8_ss_oe(uint32_t lead, uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
                                              uint32_t hi, uint32_t idesc) {
