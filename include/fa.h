@@ -99,9 +99,11 @@ int fa_fwd_2cta(const void* q, const void* k, const void* v, void* o, float* lse
  *                256-byte aligned, owned by the caller; calls sharing one workspace must
  *                be on one stream (the copies wait for earlier work on `stream`)
  * Asynchronous: the results are on the host once `stream` reaches this point
- * (synchronise it).  Two copy streams and a few events per device are created on the
- * first call there; concurrent calls from several host threads are serialised while
- * they enqueue.  Errors as fa_fwd, plus FA_ERR_WORKSPACE.
+ * (synchronise it).  Two copy streams, two compute streams (consecutive chunks run on
+ * them in turn, so that one chunk's grid fills the SMs the previous one's last CTAs
+ * leave idle) and a few events per device are created on the first call there;
+ * concurrent calls from several host threads are serialised while they enqueue.
+ * Errors as fa_fwd, plus FA_ERR_WORKSPACE.
  */
 int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
                 float scale, int causal, int dtype, int chunks, void* workspace,

@@ -2,10 +2,13 @@
 // host<->device copies overlapped with the computation.
 //
 // The heads are cut into chunks.  Chunk c's Q, K, V go to the device on one copy
-// stream, its fa_fwd runs on the caller's stream once they have landed, and its O
-// and LSE come back on a second copy stream once it is done.  The link carries chunk
-// c+1 in while chunk c computes and chunk c-1 goes out, so a call costs about one
-// pass of the inputs over the link instead of inputs + compute + outputs in a row.
+// stream, its fa_fwd runs on one of two compute streams (in turn) once they have
+// landed, and its O and LSE come back on a second copy stream once it is done.  The
+// link carries chunk c+1 in while chunk c computes and chunk c-1 goes out, so a call
+// costs about one pass of the inputs over the link instead of inputs + compute +
+// outputs in a row.  The two compute streams let chunk c+1's persistent grid take the
+// SMs that chunk c's last CTAs leave idle (a chunk of a few heads is only a few units
+// per SM, so each launch alone would end on a ragged last wave).
 // The device copies live in a caller-provided workspace; the copy streams and
 // events are created once per device and reused.  The FP8 variant runs the E4M3
 // prologue (one launch for Q, K and V) and the E4M3 forward on each chunk.
@@ -26,6 +29,7 @@ struct CopyEngine {
   bool ready = false;
   cudaStream_t h2d = nullptr;
   cudaStream_t d2h = nullptr;
+  cudaStream_t comp[2] = {nullptr, nullptr};
   cudaEvent_t start = nullptr;
   cudaEvent_t out_done = nullptr;
   cudaEvent_t in[kMaxChunks] = {};
@@ -44,6 +48,8 @@ int engine(CopyEngine** out) {
     const unsigned ef = cudaEventDisableTiming;
     if (cudaStreamCreateWithFlags(&e.h2d, cudaStreamNonBlocking) != cudaSuccess ||
         cudaStreamCreateWithFlags(&e.d2h, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&e.comp[0], cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&e.comp[1], cudaStreamNonBlocking) != cudaSuccess ||
         cudaEventCreateWithFlags(&e.start, ef) != cudaSuccess ||
         cudaEventCreateWithFlags(&e.out_done, ef) != cudaSuccess)
       return FA_ERR_CUDA;
@@ -59,8 +65,8 @@ int engine(CopyEngine** out) {
 
 unsigned long long round256(unsigned long long x) { return (x + 255) / 256 * 256; }
 
-// The chunked schedule shared by both entry points.  `compute(h0, hn)` enqueues the
-// work on heads h0 .. h0+hn-1 on the caller's stream, after their inputs landed; the
+// The chunked schedule shared by both entry points.  `compute(h0, hn, cs)` enqueues the
+// work on heads h0 .. h0+hn-1 on stream cs, after their inputs landed; the
 // three inputs are `in_bytes` per head from the host to `dev_in[i]`, and `out_bytes` per
 // head of O (plus N floats of LSE when `lse`) come back from `dev_o` / `dev_lse`.
 template <class Compute>
@@ -77,7 +83,9 @@ int run_chunked(const void* const host_in[3], uint8_t* const dev_in[3], unsigned
   int st = engine(&e);
   if (st != FA_OK) return st;
   // the workspace may still be in use by earlier work on the caller's stream
-  if (cudaEventRecord(e->start, s) != cudaSuccess || cudaStreamWaitEvent(e->h2d, e->start, 0) != cudaSuccess)
+  if (cudaEventRecord(e->start, s) != cudaSuccess || cudaStreamWaitEvent(e->h2d, e->start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(e->comp[0], e->start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(e->comp[1], e->start, 0) != cudaSuccess)
     return FA_ERR_CUDA;
   for (int c = 0; c < nc; ++c) {
     const long long h0 = c * per_chunk;
@@ -87,11 +95,12 @@ int run_chunked(const void* const host_in[3], uint8_t* const dev_in[3], unsigned
       if (cudaMemcpyAsync(dev_in[i] + h0 * in_bytes, static_cast<const uint8_t*>(host_in[i]) + h0 * in_bytes,
                           hn * in_bytes, cudaMemcpyHostToDevice, e->h2d) != cudaSuccess)
         return FA_ERR_CUDA;
-    if (cudaEventRecord(e->in[c], e->h2d) != cudaSuccess || cudaStreamWaitEvent(s, e->in[c], 0) != cudaSuccess)
+    cudaStream_t cs = e->comp[c & 1];
+    if (cudaEventRecord(e->in[c], e->h2d) != cudaSuccess || cudaStreamWaitEvent(cs, e->in[c], 0) != cudaSuccess)
       return FA_ERR_CUDA;
-    st = compute(h0, hn);
+    st = compute(h0, hn, cs);
     if (st != FA_OK) return st;
-    if (cudaEventRecord(e->computed[c], s) != cudaSuccess ||
+    if (cudaEventRecord(e->computed[c], cs) != cudaSuccess ||
         cudaStreamWaitEvent(e->d2h, e->computed[c], 0) != cudaSuccess ||
         cudaMemcpyAsync(static_cast<uint8_t*>(host_o) + h0 * out_bytes, dev_o + h0 * out_bytes, hn * out_bytes,
                         cudaMemcpyDeviceToHost, e->d2h) != cudaSuccess)
@@ -100,7 +109,8 @@ int run_chunked(const void* const host_in[3], uint8_t* const dev_in[3], unsigned
                                     cudaMemcpyDeviceToHost, e->d2h) != cudaSuccess)
       return FA_ERR_CUDA;
   }
-  // the caller's stream resumes once the last result is on the host
+  // the caller's stream resumes once the last result is on the host (the copy stream
+  // ran every chunk's copy after that chunk's computation)
   if (cudaEventRecord(e->out_done, e->d2h) != cudaSuccess || cudaStreamWaitEvent(s, e->out_done, 0) != cudaSuccess)
     return FA_ERR_CUDA;
   return FA_OK;
@@ -140,11 +150,11 @@ extern "C" int fa_fwd_host(const void* q, const void* k, const void* v, void* o,
   const void* const host_in[3] = {q, k, v};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return run_chunked(host_in, dev_in, head_bytes, o, dO, head_bytes, lse, dl, BH, N, chunks, s,
-                     [&](long long h0, long long hn) {
+                     [&](long long h0, long long hn, cudaStream_t cs) {
                        const unsigned long long off = static_cast<unsigned long long>(h0) * head_bytes;
                        return fa_fwd(dev_in[0] + off, dev_in[1] + off, dev_in[2] + off, dO + off,
                                      lse ? dl + h0 * N : nullptr, 1, static_cast<int>(hn), N, d, scale, causal,
-                                     dtype, s);
+                                     dtype, cs);
                      });
 }
 
@@ -191,16 +201,16 @@ extern "C" int fa_fwd_fp8_host(const void* q, const void* k, const void* v, void
   const void* const host_in[3] = {q, k, v};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return run_chunked(host_in, dev_in, 2 * head_elems, o, dO, 2 * head_elems, lse, dl, BH, N, chunks, s,
-                     [&](long long h0, long long hn) {
+                     [&](long long h0, long long hn, cudaStream_t cs) {
                        const unsigned long long o16 = h0 * 2 * head_elems, o8 = h0 * head_elems;
                        const long long os = h0 * nsb;
                        const int n = static_cast<int>(hn);
                        // Q, K rotated; V transposed, not rotated: one launch
                        const int r = fa_quantize_fp8_qkv(dev_in[0] + o16, dev_in[1] + o16, dev_in[2] + o16,
                                                          x8[0] + o8, x8[1] + o8, x8[2] + o8, sc[0] + os,
-                                                         sc[1] + os, sc[2] + os, 1, n, N, d, hadamard, s);
+                                                         sc[1] + os, sc[2] + os, 1, n, N, d, hadamard, cs);
                        if (r != FA_OK) return r;
                        return fa_fwd_fp8(x8[0] + o8, x8[1] + o8, x8[2] + o8, dO + o16, lse ? dl + h0 * N : nullptr,
-                                         1, n, N, d, scale, causal, sc[0] + os, sc[1] + os, sc[2] + os, hadamard, s);
+                                         1, n, N, d, scale, causal, sc[0] + os, sc[1] + os, sc[2] + os, hadamard, cs);
                      });
 }
