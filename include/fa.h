@@ -94,7 +94,9 @@ int fa_fwd_2cta(const void* q, const void* k, const void* v, void* o, float* lse
  *   q, k, v, o : [B, H, N, d] of `dtype` in host memory (pinned memory lets the copies
  *                run asynchronously; pageable memory works, without overlap)
  *   lse        : [B, H, N] float32 in host memory, or NULL
- *   chunks     : number of head chunks (0 picks 8; at most 32 and B*H)
+ *   chunks     : number of equal head chunks (at most 32 and B*H); 0 picks chunks of
+ *                1, 2, 4, ... heads up to B*H/8 and back down to 1 at the end, so that
+ *                little crosses the link while nothing computes
  *   workspace  : DEVICE scratch of at least fa_fwd_host_workspace_size() bytes,
  *                256-byte aligned, owned by the caller; calls sharing one workspace must
  *                be on one stream (the copies wait for earlier work on `stream`)
@@ -185,7 +187,9 @@ int fa_fwd_fp8(const void* q8, const void* k8, const void* v8t, void* o, float* 
  *   q, k, v, o : [B, H, N, d] bfloat16 in host memory (pinned lets the copies overlap)
  *   lse        : [B, H, N] float32 in host memory, or NULL
  *   hadamard   : 0 or 1
- *   chunks     : number of head chunks (0 picks 8; at most 32 and B*H)
+ *   chunks     : number of equal head chunks (at most 32 and B*H); 0 picks chunks of
+ *                1, 2, 4, ... heads up to B*H/8 and back down to 1 at the end, so that
+ *                little crosses the link while nothing computes
  *   workspace  : DEVICE scratch of at least fa_fwd_fp8_host_workspace_size() bytes,
  *                256-byte aligned, owned by the caller; calls sharing one workspace must
  *                be on one stream

@@ -256,6 +256,16 @@ def test_host_pipeline_matches_device_call_bitwise(gpu_lib, chunks, pinned):
     assert torch.equal(o, od.cpu()) and torch.equal(lse, ld.cpu())
 
 
+def test_host_pipeline_ramped_chunks_match_device_call_bitwise(gpu_lib):
+    # 40 heads: the default chunks grow 1, 2, 4 heads, run 5 at a time and shrink again,
+    # on two compute streams in turn
+    q, k, v = (t.pin_memory() for t in make_qkv((4, 10, 130, 128), torch.bfloat16, 16))
+    o, lse = gpu_lib.attention_host(q, k, v, causal=True)
+    od, ld = gpu_lib.attention(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o, od.cpu()) and torch.equal(lse, ld.cpu())
+
+
 def test_device_rejections(gpu_lib):
     q = torch.zeros((1, 1, 64, 96), device="cuda", dtype=torch.bfloat16)
     with pytest.raises(gpu_lib.FAError) as e:

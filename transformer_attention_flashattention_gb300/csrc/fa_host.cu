@@ -65,6 +65,40 @@ int engine(CopyEngine** out) {
 
 unsigned long long round256(unsigned long long x) { return (x + 255) / 256 * 256; }
 
+// Head counts of the chunks; returns how many.  `chunks` > 0: that many equal chunks (the
+// last one shorter).  0: chunks that grow 1, 2, 4, ... heads up to a cap of BH / 8 and
+// shrink the same way at the end, so that only a small first chunk's inputs and a small
+// last chunk's outputs cross the link while nothing computes; equal chunks of BH / 8
+// where BH is too small (or too large) for that.
+int chunk_sizes(long long BH, int chunks, long long (&size)[kMaxChunks]) {
+  if (chunks == 0) {
+    const long long cap = (BH + kAutoChunks - 1) / kAutoChunks;
+    long long ramp[kMaxChunks];
+    int nr = 0;
+    long long ramp_sum = 0;
+    for (long long h = 1; h < cap && nr < 8; h *= 2) {
+      ramp[nr++] = h;
+      ramp_sum += h;
+    }
+    const long long middle = BH - 2 * ramp_sum;
+    const long long nm = middle > 0 ? (middle + cap - 1) / cap : 0;
+    if (nr > 0 && middle > 0 && 2 * nr + nm <= kMaxChunks) {
+      int n = 0;
+      for (int i = 0; i < nr; ++i) size[n++] = ramp[i];
+      for (long long left = middle; left > 0; left -= cap) size[n++] = left < cap ? left : cap;
+      for (int i = nr - 1; i >= 0; --i) size[n++] = ramp[i];
+      return n;
+    }
+  }
+  int nc = chunks == 0 ? kAutoChunks : chunks;
+  if (nc > kMaxChunks) nc = kMaxChunks;
+  if (nc > BH) nc = static_cast<int>(BH);
+  const long long per_chunk = (BH + nc - 1) / nc;
+  int n = 0;
+  for (long long h0 = 0; h0 < BH; h0 += per_chunk) size[n++] = BH - h0 < per_chunk ? BH - h0 : per_chunk;
+  return n;
+}
+
 // The chunked schedule shared by both entry points.  `compute(h0, hn, cs)` enqueues the
 // work on heads h0 .. h0+hn-1 on stream cs, after their inputs landed; the
 // three inputs are `in_bytes` per head from the host to `dev_in[i]`, and `out_bytes` per
@@ -73,10 +107,8 @@ template <class Compute>
 int run_chunked(const void* const host_in[3], uint8_t* const dev_in[3], unsigned long long in_bytes,
                 void* host_o, const uint8_t* dev_o, unsigned long long out_bytes, float* host_lse,
                 const float* dev_lse, long long BH, int N, int chunks, cudaStream_t s, Compute compute) {
-  int nc = chunks == 0 ? kAutoChunks : chunks;
-  if (nc > kMaxChunks) nc = kMaxChunks;
-  if (nc > BH) nc = static_cast<int>(BH);
-  const long long per_chunk = (BH + nc - 1) / nc;
+  long long size[kMaxChunks];
+  const int nc = chunk_sizes(BH, chunks, size);
   // one call's enqueue at a time per process: the events are shared
   std::lock_guard<std::mutex> lock(g_host_mu);
   CopyEngine* e = nullptr;
@@ -87,10 +119,9 @@ int run_chunked(const void* const host_in[3], uint8_t* const dev_in[3], unsigned
       cudaStreamWaitEvent(e->comp[0], e->start, 0) != cudaSuccess ||
       cudaStreamWaitEvent(e->comp[1], e->start, 0) != cudaSuccess)
     return FA_ERR_CUDA;
-  for (int c = 0; c < nc; ++c) {
-    const long long h0 = c * per_chunk;
-    const long long hn = BH - h0 < per_chunk ? BH - h0 : per_chunk;
-    if (hn <= 0) break;
+  long long h0 = 0;
+  for (int c = 0; c < nc; h0 += size[c], ++c) {
+    const long long hn = size[c];
     for (int i = 0; i < 3; ++i)
       if (cudaMemcpyAsync(dev_in[i] + h0 * in_bytes, static_cast<const uint8_t*>(host_in[i]) + h0 * in_bytes,
                           hn * in_bytes, cudaMemcpyHostToDevice, e->h2d) != cudaSuccess)
