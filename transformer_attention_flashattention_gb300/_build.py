@@ -25,7 +25,7 @@ ROOT = os.path.dirname(PKG_DIR)
 CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libfa.so")
-SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd2.cu", "fa_fwd_fp8.cu", "fa_quant.cu", "fa_decode.cu",
+SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd1.cu", "fa_fwd2.cu", "fa_fwd_fp8.cu", "fa_quant.cu", "fa_decode.cu",
            "fa_decode_noalloc.cu", "fa_bwd.cu",
            "fa_host.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

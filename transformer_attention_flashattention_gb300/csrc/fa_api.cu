@@ -158,7 +158,9 @@ int fwd_call(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.scale_log2 = scale * 1.44269504088896340736f;
   p.N = N;
   p.BH = static_cast<int>(BH);
-  const int unit_rows = pair ? 2 * kUnitRows : kUnitRows;
+  // head dim 64 (16-bit) runs one 128-row Q tile per CTA, two CTAs per SM
+  const bool one_tile = !pair && d == 64;
+  const int unit_rows = pair ? 2 * kUnitRows : (one_tile ? kUnitRows / 2 : kUnitRows);
   p.n_qblk = (N + unit_rows - 1) / unit_rows;
   const long long units = static_cast<long long>(p.n_qblk) * p.BH;
   if (units >= (1ll << 31)) return FA_ERR_SHAPE;
@@ -178,6 +180,10 @@ int fwd_call(const void* q, const void* k, const void* v, void* o, float* lse, i
     const long long pairs = di->sm_count / 2;
     const int grid = 2 * static_cast<int>(units < pairs ? units : pairs);
     e = launch_fwd2(dtype == FA_BF16, p, grid, static_cast<cudaStream_t>(stream));
+  } else if (one_tile) {
+    const long long slots = 2ll * di->sm_count;
+    const int grid = static_cast<int>(units < slots ? units : slots);
+    e = launch_fwd1(dtype == FA_BF16, p, grid, static_cast<cudaStream_t>(stream));
   } else {
     const int grid = static_cast<int>(units < di->sm_count ? units : di->sm_count);
     e = launch_fwd(d, dtype == FA_BF16, p, grid, static_cast<cudaStream_t>(stream));

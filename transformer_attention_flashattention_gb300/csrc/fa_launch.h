@@ -14,6 +14,8 @@ struct BwdParams;
 // Launch one forward kernel instantiation on `stream`; returns the launch status.
 cudaError_t launch_fwd(int d, bool bf16, const FwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_fwd_fp8(const FwdParams& p, int grid, cudaStream_t stream);
+// One-tile-per-CTA forward (16-bit, head dim 64, two CTAs a SM): 128-row units.
+cudaError_t launch_fwd1(bool bf16, const FwdParams& p, int grid, cudaStream_t stream);
 // CTA-pair forward (16-bit, head dim 128); `grid` is even (two CTAs a cluster).
 cudaError_t launch_fwd2(bool bf16, const FwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_quant_fp8(const QuantParams& p, cudaStream_t stream);
