@@ -130,9 +130,8 @@ struct BwdCfg {
 //  - Non-causal: head-major, dealt round-robin, so concurrent CTAs share a few heads
 //    and the streamed tiles hit L2.
 //  - Causal: a unit's cost grows with its Q tile (dq: tile i sees i + 1 key tiles) or
-//    shrinks with its K/V tile (dkdv: tile j is seen by n - j Q tiles), so tiles b and
-//    n-1-b of one head form a pair of equal cost.  A CTA takes whole pairs, longer half
-//    first, in head-major order; the middle tile of an odd count comes after the pairs.
+//    shrinks with its K/V tile (dkdv: tile j is seen by n - j Q tiles); causal_unit pairs
+//    tiles b and n-1-b of one head and levels the grid's last wave.
 __device__ __forceinline__ bool bwd_unit_at(const BwdParams& p, int k, bool cost_grows, int& bh, int& blk) {
   const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
   if (!p.causal) {
@@ -142,24 +141,7 @@ __device__ __forceinline__ bool bwd_unit_at(const BwdParams& p, int k, bool cost
     blk = u % p.n_blk;
     return true;
   }
-  const int P = p.n_blk / 2;
-  const int pairs = p.BH * P;
-  const int mine = c < pairs ? (pairs - c + G - 1) / G : 0;
-  if (k < 2 * mine) {
-    const int s = c + (k >> 1) * G;
-    bh = s / P;
-    const int i = s % P;
-    const int lo = i, hi = p.n_blk - 1 - i;
-    const int longer = cost_grows ? hi : lo, shorter = cost_grows ? lo : hi;
-    blk = (k & 1) ? shorter : longer;
-    return true;
-  }
-  if ((p.n_blk & 1) == 0) return false;
-  const int r = c + (mine + (k - 2 * mine)) * G - pairs;
-  if (r >= p.BH) return false;
-  bh = r;
-  blk = P;
-  return true;
+  return causal_unit(G, c, p.BH, p.n_blk, k, cost_grows, bh, blk);
 }
 
 // ---------------------------------------------------------------------------- prep

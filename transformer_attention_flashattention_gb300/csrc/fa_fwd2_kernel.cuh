@@ -70,22 +70,7 @@ __device__ __forceinline__ bool unit_at2(const FwdParams& p, int k, int& bh, int
     qb = u % p.n_qblk;
     return true;
   }
-  const int P = p.n_qblk / 2;
-  const int pairs = p.BH * P;
-  const int mine = c < pairs ? (pairs - c + G - 1) / G : 0;
-  if (k < 2 * mine) {
-    const int s = c + (k >> 1) * G;
-    bh = s / P;
-    const int i = s % P;
-    qb = (k & 1) ? i : p.n_qblk - 1 - i;
-    return true;
-  }
-  if ((p.n_qblk & 1) == 0) return false;
-  const int r = c + (mine + (k - 2 * mine)) * G - pairs;
-  if (r >= p.BH) return false;
-  bh = r;
-  qb = P;
-  return true;
+  return causal_unit(G, c, p.BH, p.n_qblk, k, true, bh, qb);
 }
 
 // Key tiles the pair's 256-row tile t of q-block qb needs (0 if it lies past N).  Both

@@ -101,15 +101,81 @@ struct FwdCfg {
   static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
-// The k-th (b*h, q-block) unit of this CTA of the persistent grid; false once the
-// CTA has none left.  Every role of the CTA walks the same sequence.
-//  - Non-causal: units in head-major order, dealt round-robin, so the CTAs running at
-//    the same time share a few heads and their K/V re-reads hit L2.
-//  - Causal: the cost of q-block qb grows with qb, so qb and n_qblk-1-qb of one head
-//    form a pair of equal total cost.  A CTA takes whole pairs round-robin in
-//    head-major order (the longer half first), which balances the grid and keeps
-//    concurrent CTAs on few heads; the middle q-block of each head (odd n_qblk)
-//    comes after the pairs, dealt on with the same stride.
+// The k-th causal unit (b*h, block) of CTA c of a persistent grid of G CTAs, for n blocks
+// per head whose cost grows with the block index (cost_grows: the forward's q-blocks and the
+// dQ kernel's Q tiles) or shrinks with it (the dK/dV kernel's K/V tiles); false once the CTA
+// has none left.  Blocks b and n-1-b of one head form a pair of equal total cost.
+//  - Whole rounds of G pairs: a CTA takes whole pairs round-robin in head-major order (the
+//    longer half first), which balances those rounds and keeps concurrent CTAs on few
+//    heads, so their K/V or Q re-reads hit L2.
+//  - The rest (the partial last round, and with n >= 16 blocks a head the last whole round
+//    as well; the middle block of each head when n is odd): their units sorted by cost,
+//    longest first, and dealt in snake order (G CTAs left to right, then right to left), so
+//    the grid's last wave ends nearly level instead of leaving part of it idle.  The long
+//    halves of the remaining pairs come first (by pair position within the head, then
+//    head), then the middle blocks, then the short halves in reverse.  Units dealt this way
+//    lose the head order; below 16 blocks a head a unit is too short for that to pay with a
+//    whole round.
+__device__ __forceinline__ bool causal_unit(int G, int c, int BH, int n, int k, bool cost_grows, int& bh,
+                                            int& blk) {
+  const int P = n / 2;                                // pairs per head
+  const int pairs = BH * P;
+  const int R = max(0, pairs / G - (n >= 16 ? 1 : 0));   // rounds dealt as whole pairs
+  if (k < 2 * R) {
+    const int s = c + (k >> 1) * G;
+    bh = s / P;
+    const int i = s % P;
+    const int lo = i, hi = n - 1 - i;
+    const int longer = cost_grows ? hi : lo, shorter = cost_grows ? lo : hi;
+    blk = (k & 1) ? shorter : longer;
+    return true;
+  }
+  const int t = k - 2 * R;
+  const int idx = t * G + ((t & 1) ? G - 1 - c : c);
+  const int S0 = R * G;                               // first remaining pair
+  const int Ltot = pairs - S0;                        // remaining pairs
+  const int M = (n & 1) ? BH : 0;                     // middle blocks
+  // the x-th remaining pair ordered by position i within its head, then by head
+  auto entry = [&](int x, int& h, int& i) {
+    const int h0 = S0 / P, i0 = S0 % P;
+    const int A = BH - 1 - h0;                        // whole heads after the first remaining one
+    int r;
+    if (x < i0 * A) {
+      i = x / A;
+      r = x % A;
+    } else {
+      i = (x + i0) / (A + 1);
+      r = (x + i0) % (A + 1);
+    }
+    h = (i >= i0 ? h0 : h0 + 1) + r;
+  };
+  if (idx < Ltot) {
+    int h, i;
+    entry(idx, h, i);
+    bh = h;
+    blk = cost_grows ? n - 1 - i : i;                 // the longer half
+    return true;
+  }
+  if (idx < Ltot + M) {
+    bh = idx - Ltot;
+    blk = P;
+    return true;
+  }
+  if (idx < 2 * Ltot + M) {
+    int h, i;
+    entry(Ltot - 1 - (idx - Ltot - M), h, i);
+    bh = h;
+    blk = cost_grows ? i : n - 1 - i;                 // the shorter half
+    return true;
+  }
+  return false;
+}
+
+// The k-th (b*h, q-block) unit of this CTA of the persistent grid; false once the CTA
+// has none left.  Every role of the CTA walks the same sequence.  Non-causal: units in
+// head-major order, dealt round-robin, so the CTAs running at the same time share a few
+// heads and their K/V re-reads hit L2.  Causal: causal_unit (the cost of q-block qb grows
+// with qb).
 __device__ __forceinline__ bool unit_at(const FwdParams& p, int k, int& bh, int& qb) {
   const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
   if (!p.causal) {
@@ -119,22 +185,7 @@ __device__ __forceinline__ bool unit_at(const FwdParams& p, int k, int& bh, int&
     qb = u % p.n_qblk;
     return true;
   }
-  const int P = p.n_qblk / 2;                         // pairs per head
-  const int pairs = p.BH * P;
-  const int mine = c < pairs ? (pairs - c + G - 1) / G : 0;
-  if (k < 2 * mine) {
-    const int s = c + (k >> 1) * G;
-    bh = s / P;
-    const int i = s % P;
-    qb = (k & 1) ? i : p.n_qblk - 1 - i;
-    return true;
-  }
-  if ((p.n_qblk & 1) == 0) return false;
-  const int r = c + (mine + (k - 2 * mine)) * G - pairs;   // >= 0 by the choice of mine
-  if (r >= p.BH) return false;
-  bh = r;
-  qb = P;
-  return true;
+  return causal_unit(G, c, p.BH, p.n_qblk, k, true, bh, qb);
 }
 
 // Number of K/V tiles Q tile t of q-block qb attends to (0 if the tile is past N).
