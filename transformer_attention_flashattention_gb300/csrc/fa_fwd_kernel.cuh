@@ -116,7 +116,7 @@ struct FwdCfg {
 //    head), then the middle blocks, then the short halves in reverse.  Units dealt this way
 //    lose the head order; below 16 blocks a head a unit is too short for that to pay with a
 //    whole round.
-__device__ __forceinline__ bool causal_unit(int G, int c, int BH, int n, int k, bool cost_grows, int& bh,
+static __device__ __noinline__ bool causal_unit(int G, int c, int BH, int n, int k, bool cost_grows, int& bh,
                                             int& blk) {
   const int P = n / 2;                                // pairs per head
   const int pairs = BH * P;
