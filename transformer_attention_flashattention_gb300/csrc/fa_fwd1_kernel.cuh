@@ -320,20 +320,22 @@ __device__ __forceinline__ void fwd1_softmax(const FwdParams& p, uint32_t sbase,
         ptx::tc_fence_after();
       }
       if (rescale_o) {
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          uint32_t orr[32];
-          ptx::tmem_ld32(tO + 32 * c, orr);
-          ptx::tmem_wait_ld();
+        // both 32-column chunks of O in one TMEM round trip
+        uint32_t orr[2][32];
+        ptx::tmem_ld32(tO, orr[0]);
+        ptx::tmem_ld32(tO + 32, orr[1]);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            const float2 v = ptx::mul2(make_float2(__uint_as_float(orr[i]), __uint_as_float(orr[i + 1])),
+            const float2 v = ptx::mul2(make_float2(__uint_as_float(orr[h][i]), __uint_as_float(orr[h][i + 1])),
                                        make_float2(alpha, alpha));
-            orr[i] = __float_as_uint(v.x);
-            orr[i + 1] = __float_as_uint(v.y);
+            orr[h][i] = __float_as_uint(v.x);
+            orr[h][i + 1] = __float_as_uint(v.y);
           }
-          ptx::tmem_st32(tO + 32 * c, orr);
-        }
+        ptx::tmem_st32(tO, orr[0]);
+        ptx::tmem_st32(tO + 32, orr[1]);
       }
       ptx::tmem_st32(tP, sr[0]);
       ptx::tmem_st32(tP + 32, sr[1]);

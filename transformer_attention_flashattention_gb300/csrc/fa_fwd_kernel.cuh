@@ -652,19 +652,24 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, int t, uint32_t 
 
       if (rescale_o) {
         // The previous O_t += P V has completed: the S_t commit that woke us tracks it.
+        // Two 32-column chunks per TMEM round trip.
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t orr[32];
-          ptx::tmem_ld32(tO + 32 * c, orr);
+        for (int c = 0; c < D / 32; c += 2) {
+          uint32_t orr[2][32];
+          ptx::tmem_ld32(tO + 32 * c, orr[0]);
+          ptx::tmem_ld32(tO + 32 * c + 32, orr[1]);
           ptx::tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const float2 v = ptx::mul2(make_float2(__uint_as_float(orr[i]), __uint_as_float(orr[i + 1])),
-                                       make_float2(alpha, alpha));
-            orr[i] = __float_as_uint(v.x);
-            orr[i + 1] = __float_as_uint(v.y);
-          }
-          ptx::tmem_st32(tO + 32 * c, orr);
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const float2 v = ptx::mul2(make_float2(__uint_as_float(orr[h][i]), __uint_as_float(orr[h][i + 1])),
+                                         make_float2(alpha, alpha));
+              orr[h][i] = __float_as_uint(v.x);
+              orr[h][i + 1] = __float_as_uint(v.y);
+            }
+          ptx::tmem_st32(tO + 32 * c, orr[0]);
+          ptx::tmem_st32(tO + 32 * c + 32, orr[1]);
         }
       }
 #undef S_
