@@ -13,7 +13,10 @@ bracketed by CUDA events, L2 flushed before each launch whose inputs fit in it):
     16x16x2048x128, beside the single-CTA kernel;
   * the E4M3 forward on [4, 16, 4096, 128] (Hadamard on): the forward alone, the
     quantisation prologue (three launches, in GB/s against HBM), both together,
-    and end to end from host bf16 Q/K/V to host bf16 O through ``fa_fwd_fp8_host``.
+    and end to end from host bf16 Q/K/V to host bf16 O through ``fa_fwd_fp8_host``;
+  * the backward pass on [16, 16, 2048, 128], both masks;
+  * standard attention with the N x N scores in HBM (``fa_fwd_naive``) on
+    16x16x2048x128 (both masks) and 2x16x8192x128 (non-causal), against the tiled kernel.
 
 Single workloads (``--workload``; the line then carries that workload alone):
   bf16            [16, 16, 2048, 128], both masks
@@ -420,6 +423,60 @@ def _variants(fa, dev, timer, n, peaks, e2e_steps):
     cache.clear()
     out.update(_fp8_figures(fa, WORKLOADS["fp8"], dev, timer, n, peaks, WORKLOADS["fp8"].seed, e2e_steps))
     out.update(_bwd_figures(fa, dev, timer, n, peaks))
+    out.update(_naive_figures(fa, dev, timer, max(5, n // 4), peaks, out))
+    return out
+
+
+def naive_bytes(B, H, N, d, causal, elem=2):
+    """Algorithmic HBM bytes of one materialising attention call (fa_fwd_naive): the GEMM
+    reads Q and K and writes the fp32 scores; the row softmax reads the visible scores and
+    writes P (16-bit, every column) and the LSE; the second GEMM reads P and V and writes O.
+    Rows of S are padded to whole float4 vectors (N rounded up to 4)."""
+    ld = (N + 3) // 4 * 4
+    visible = N * (N + 1) // 2 if causal else N * N
+    per_head = (2 * N * d * elem + 4 * N * ld            # S = scale Q K^T
+                + 4 * visible + 2 * N * N + 4 * N        # softmax: S in, P and LSE out
+                + 2 * N * N + 2 * N * d * elem)          # O = P V
+    return B * H * per_head
+
+
+def _naive_figures(fa, dev, timer, n, peaks, fused):
+    """The materialising attention (fa_fwd_naive: cuBLAS S, the row softmax, cuBLAS O) on the
+    same inputs as two of the tiled kernel's variants: time per call, TFLOP/s of the same
+    algorithmic flops, its HBM bytes against the measured copy bandwidth, and how many times
+    longer it takes than the tiled kernel timed above."""
+    import ctypes
+    from fa_inputs import Workload
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    out = {}
+    specs = [("16x16x2048x128", WORKLOADS["bf16"], (False, True)),
+             ("2x16x8192x128", Workload("v8192", 2, 16, 8192, 128, torch.bfloat16, 2), (False,))]
+    for tag, w, masks in specs:
+        q, k, v = (t.to(dev) for t in make_inputs(w))
+        need = ctypes.c_ulonglong(0)
+        fa.load_library().fa_fwd_naive_workspace_size(w.B, w.H, w.N, w.d, ctypes.byref(need))
+        ws = torch.empty(need.value, device=dev, dtype=torch.uint8)
+        o, lse = torch.empty_like(q), torch.empty(w.shape[:3], device=dev)
+        for causal in masks:
+            name = f"{tag}_{'causal' if causal else 'non_causal'}"
+            ms = timer.launches(lambda: fa.attention_naive(q, k, v, causal=causal, out=o, lse=lse, workspace=ws),
+                                n, flush=False)
+            fig = _perf(ms, w.flops(causal), "bf16", peaks,
+                        "cuBLAS GEMM (S, fp32) + fa_naive_softmax_kernel + cuBLAS GEMM (O)")
+            nb = naive_bytes(w.B, w.H, w.N, w.d, causal)
+            mean = sum(ms) / len(ms)
+            fig.update({"bound": "hbm", "bytes": nb, "gbs": nb / (fig["median_ms"] * 1e-3) / 1e9,
+                        "hbm_frac": nb / (mean * 1e-3) / 1e9 / hbm,
+                        "nxn_hbm_passes": 4, "workspace_bytes": need.value})
+            traffic = _committed_traffic(f"naive_{name}", False)
+            if traffic is not None:
+                fig["traffic"] = traffic
+                fig["traffic_source"] = "profiles/dram_traffic.json (ncu, not this run)"
+            f = fused.get(name)
+            if f is not None:
+                fig["naive_over_tiled_time"] = fig["median_ms"] / f["median_ms"]
+            out["naive_" + name] = fig
+        del ws, q, k, v, o, lse
     return out
 
 

@@ -255,6 +255,35 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
 /* Scratch bytes fa_bwd needs for these sizes (8 * B * H * N rounded up to 128 per head). */
 int fa_bwd_workspace_size(int B, int H, int N, int d, unsigned long long* bytes);
 
+/*
+ * Standard attention with the N x N score matrix materialised in HBM: the comparison the
+ * concept card "FlashAttention 2 + 3 — speicherbewusste Attention-Kernels" draws
+ * ("Worum es geht": scores written to HBM and read back for the softmax and the
+ * weighted sum; "Begriffe auf dieser Seite", HBM: 5-10 HBM passes against about one;
+ * "Warum es zählt": 3-10x the GPU hours at long context).  Same operation, arguments and
+ * outputs as fa_fwd, computed in three passes:
+ *   1. S = scale * Q K^T in fp32 into the workspace (a cuBLAS strided-batched GEMM);
+ *   2. a row softmax kernel: reads each row's visible scores once, writes P = softmax(S)
+ *      in `dtype` over the start of the same row (zeros at masked columns), and the LSE;
+ *   3. O = P V (a second cuBLAS GEMM), fp32 accumulation, rounded to `dtype`.
+ *   workspace : device scratch of at least fa_fwd_naive_workspace_size() bytes (4 bytes
+ *               per score: B * H * N * ceil(N/4)*4 * 4), 256-byte aligned, owned by the
+ *               caller; calls sharing one workspace must not overlap on the GPU
+ * Supported: fa_fwd's shapes with N <= 32768 and B*H*N < 2^31 (else FA_ERR_UNSUPPORTED or
+ * FA_ERR_SHAPE).  cuBLAS (libcublas.so.13) is resolved at the first call, from the copy
+ * the process already has loaded or from the loader's search path, and one cuBLAS handle
+ * is created per device (cuBLAS keeps its own workspace there); calls from several host
+ * threads are serialised while they enqueue.
+ * Errors as fa_fwd, plus FA_ERR_WORKSPACE, and FA_ERR_CUDA when cuBLAS cannot be loaded or
+ * its handle created.
+ */
+int fa_fwd_naive(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                 float scale, int causal, int dtype, void* workspace, unsigned long long workspace_bytes,
+                 void* stream);
+
+/* Scratch bytes fa_fwd_naive needs: the fp32 score matrix of every head. */
+int fa_fwd_naive_workspace_size(int B, int H, int N, int d, unsigned long long* bytes);
+
 /* Size of the static scratch area behind fa_decode_noalloc, per device (8 MiB). */
 #define FA_DECODE_NOALLOC_SCRATCH_BYTES (8ull << 20)
 

@@ -36,7 +36,8 @@ def test_header_declares_the_boundary():
                                   "fa_decode", "fa_decode_workspace_size", "fa_decode_noalloc",
                                   "fa_bwd", "fa_bwd_workspace_size", "fa_quantize_fp8_ex",
                                   "fa_fwd_host", "fa_fwd_host_workspace_size", "fa_fwd_fp8_host",
-                                  "fa_fwd_fp8_host_workspace_size", "fa_build_id", "fa_fwd_2cta", "fa_quantize_fp8_qkv"])
+                                  "fa_fwd_fp8_host_workspace_size", "fa_build_id", "fa_fwd_2cta", "fa_quantize_fp8_qkv",
+                                  "fa_fwd_naive", "fa_fwd_naive_workspace_size"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -213,3 +214,27 @@ def test_quantize_qkv_rejects_bad_arguments_on_the_host(lib):
     assert call(N=100) == fa.FA_ERR_SHAPE               # V is written transposed: N % 16 == 0
     assert call(q=A + 8) == fa.FA_ERR_ALIGN
     assert call(vs=A + 2) == fa.FA_ERR_ALIGN
+
+
+def test_fwd_naive_rejects_bad_arguments_on_the_host(lib):
+    n = ctypes.c_ulonglong(0)
+    # fp32 scores, rows rounded up to whole float4 vectors
+    assert lib.fa_fwd_naive_workspace_size(2, 3, 130, 64, ctypes.byref(n)) == fa.FA_OK
+    assert n.value == 2 * 3 * 130 * 132 * 4
+    assert lib.fa_fwd_naive_workspace_size(1, 1, 32768, 128, ctypes.byref(n)) == fa.FA_OK
+    assert lib.fa_fwd_naive_workspace_size(1, 1, 32769, 128, ctypes.byref(n)) == fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_fwd_naive_workspace_size(1, 1, 128, 96, ctypes.byref(n)) == fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_fwd_naive_workspace_size(1 << 16, 1 << 10, 64, 64, ctypes.byref(n)) == fa.FA_ERR_SHAPE
+    assert lib.fa_fwd_naive_workspace_size(1, 1, 128, 64, None) == fa.FA_ERR_NULL
+    ws = 0x100000
+    call = lambda q=A, wsp=ws, wsb=1 << 30, dtype=1, causal=0, scale=0.125, d=64, N=130: lib.fa_fwd_naive(
+        q or None, A, A, A, None, 2, 3, N, d, scale, causal, dtype, wsp or None, wsb, None)
+    assert call(q=0) == fa.FA_ERR_NULL
+    assert call(wsp=0) == fa.FA_ERR_NULL
+    assert call(wsb=1024) == fa.FA_ERR_WORKSPACE
+    assert call(wsp=ws + 64) == fa.FA_ERR_ALIGN
+    assert call(dtype=4) == fa.FA_ERR_UNSUPPORTED
+    assert call(causal=2) == fa.FA_ERR_UNSUPPORTED
+    assert call(scale=-1.0) == fa.FA_ERR_UNSUPPORTED
+    assert call(d=80) == fa.FA_ERR_UNSUPPORTED
+    assert call(N=40000) == fa.FA_ERR_UNSUPPORTED

@@ -30,6 +30,7 @@ __all__ = [
     "decode",
     "decode_noalloc",
     "attention_backward",
+    "attention_naive",
     "DECODE_NOALLOC_SCRATCH_BYTES",
     "last_device_status",
     "inject_stall",
@@ -78,6 +79,8 @@ _SIGNATURES = {
     "fa_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _vp]),
     "fa_bwd": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _i, _vp, ctypes.c_ulonglong, _vp]),
     "fa_bwd_workspace_size": (_i, [_i, _i, _i, _i, ctypes.POINTER(ctypes.c_ulonglong)]),
+    "fa_fwd_naive": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _vp, ctypes.c_ulonglong, _vp]),
+    "fa_fwd_naive_workspace_size": (_i, [_i, _i, _i, _i, ctypes.POINTER(ctypes.c_ulonglong)]),
     "fa_fwd_host": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _i, _vp, ctypes.c_ulonglong, _vp]),
     "fa_fwd_host_workspace_size": (_i, [_i, _i, _i, _i, ctypes.POINTER(ctypes.c_ulonglong)]),
     "fa_fwd_fp8_host": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _i, _vp, ctypes.c_ulonglong,
@@ -498,6 +501,39 @@ def attention_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: tor
                         workspace.numel() * workspace.element_size(), _stream_handle(stream, q.device))
     _check(st, "fa_bwd")
     return dq, dk, dv
+
+
+def attention_naive(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+                    scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                    lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                    stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """``attention`` computed the standard way, with the N x N score matrix in HBM
+    (``fa_fwd_naive``: a cuBLAS GEMM for S, the library's row softmax, a cuBLAS GEMM
+    for O).  The comparison the tiled kernels are measured against; N <= 32768.  The
+    fp32 score workspace (4 * B * H * N * N bytes, about) is allocated with torch unless
+    one is given.
+    """
+    lib = load_library()
+    _check_qkv(q, k, v)
+    if q.dtype not in _DTYPES:
+        raise ValueError(f"dtype must be float16 or bfloat16, got {q.dtype}")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = ctypes.c_ulonglong(0)
+    _check(lib.fa_fwd_naive_workspace_size(B, H, N, d, ctypes.byref(need)), "fa_fwd_naive_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(max(need.value, 256), device=q.device, dtype=torch.uint8)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    with torch.cuda.device(q.device):
+        st = lib.fa_fwd_naive(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, float(scale),
+                              int(bool(causal)), _DTYPES[q.dtype], _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream_handle(stream, q.device))
+    _check(st, "fa_fwd_naive")
+    return out, lse
 
 
 def last_device_status(stream: Optional[torch.cuda.Stream] = None) -> Tuple[int, int]:

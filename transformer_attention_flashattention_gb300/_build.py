@@ -27,7 +27,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libfa.so")
 SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd1.cu", "fa_fwd2.cu", "fa_fwd_fp8.cu", "fa_quant.cu", "fa_decode.cu",
            "fa_decode_noalloc.cu", "fa_bwd.cu",
-           "fa_host.cu"]
+           "fa_host.cu", "fa_naive.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
           "-I" + os.path.join(ROOT, "include")]
@@ -100,7 +100,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=(), quiet: boo
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(lambda s: _compile(s, extra), SOURCES))
     tmp = LIB_PATH + ".tmp"
-    cmd = [nvcc(), *ARCH_FLAGS, "-shared", "-o", tmp, *objs]
+    cmd = [nvcc(), *ARCH_FLAGS, "-shared", "-o", tmp, *objs, "-ldl"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")

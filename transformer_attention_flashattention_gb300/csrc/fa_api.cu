@@ -533,6 +533,44 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
+namespace {
+constexpr int kNaiveMaxN = 32768;   // the row softmax keeps a row in 256 threads' registers
+
+// fp32 score row stride of the materialising path: N rounded up to whole float4 vectors.
+long long naive_ld(int N) { return (static_cast<long long>(N) + 3) / 4 * 4; }
+}  // namespace
+
+extern "C" int fa_fwd_naive_workspace_size(int B, int H, int N, int d, unsigned long long* bytes) {
+  if (!bytes) return FA_ERR_NULL;
+  const int st = check_shape(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (N > kNaiveMaxN) return FA_ERR_UNSUPPORTED;
+  const long double rows = static_cast<long double>(B) * H * N;
+  if (rows >= static_cast<long double>(1ll << 31)) return FA_ERR_SHAPE;
+  *bytes = static_cast<unsigned long long>(B) * H * N * static_cast<unsigned long long>(naive_ld(N)) * 4ull;
+  return FA_OK;
+}
+
+extern "C" int fa_fwd_naive(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                            int d, float scale, int causal, int dtype, void* workspace,
+                            unsigned long long workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !workspace) return FA_ERR_NULL;
+  if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+  if (causal != 0 && causal != 1) return FA_ERR_UNSUPPORTED;
+  unsigned long long need = 0;
+  int st = fa_fwd_naive_workspace_size(B, H, N, d, &need);
+  if (st != FA_OK) return st;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || (lse && !aligned(lse, 4)) ||
+      !aligned(workspace, 256))
+    return FA_ERR_ALIGN;
+  if (workspace_bytes < need) return FA_ERR_WORKSPACE;
+  const DeviceInfo* di = current_device(&st);
+  if (!di) return st;
+  return run_naive(q, k, v, o, lse, static_cast<float*>(workspace), naive_ld(N), B * H, N, d, scale, causal,
+                   dtype == FA_BF16, static_cast<cudaStream_t>(stream));
+}
+
 extern "C" int fa_last_device_status(void* stream, unsigned int* bits) {
   int st = FA_OK;
   const DeviceInfo* di = current_device(&st);

@@ -23,6 +23,12 @@ cudaError_t launch_decode(int d, bool bf16, const DecodeParams& p, cudaStream_t 
 // Prep (D, LSE*log2e), then the dQ kernel, then the dK/dV kernel, all on `stream`.
 cudaError_t launch_bwd(int d, bool bf16, const BwdParams& p, int grid, cudaStream_t stream);
 
+// Materialising attention (fa_fwd_naive): library GEMM S = scale Q K^T into `s` (fp32 rows
+// `ld` floats apart), the row softmax in place (P in the input dtype, LSE), library GEMM
+// O = P V, all on `stream`.  Returns an fa_status.
+int run_naive(const void* q, const void* k, const void* v, void* o, float* lse, float* s, long long ld, int BH,
+              int N, int d, float scale, int causal, bool bf16, cudaStream_t stream);
+
 // fa_decode's shape and size checks (FA_OK, FA_ERR_SHAPE or FA_ERR_UNSUPPORTED).
 int check_decode(int B, int H, int Nq, int Nk, int d);
 
