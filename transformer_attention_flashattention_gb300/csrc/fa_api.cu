@@ -354,8 +354,9 @@ unsigned long long decode_workspace(int BH, int Nq, int d, int splits) {
   return (o + 255) / 256 * 256 + l;
 }
 
-// Key chunks per head.  One split CTA fills an SM at d = 128 and half of one at d = 64
-// (shared memory), so B*H*splits CTAs run in waves of `slots`.  With splits = 0 the
+// Key chunks per head.  Two split CTAs share an SM at d = 64 and, with at most 4 query
+// rows, at d = 128 (registers and a 96 KB ring each); one fills an SM at d = 128 with more
+// rows.  So B*H*splits CTAs run in waves of `slots`.  With splits = 0 the
 // count minimises  waves * (64-key tiles per chunk + 4 tiles of per-CTA overhead),
 // taking the fewest splits within 2 % of the best, with chunks of at least 256 keys
 // and at most 4 MiB of split scratch (so that every automatic choice also fits the
@@ -373,7 +374,7 @@ void decode_split(int BH, int Nq, int Nk, int d, int requested, int sm_count, in
     *splits = shape(requested, chunk);
     return;
   }
-  const long long slots = static_cast<long long>(sm_count) * (d == 64 ? 2 : 1);
+  const long long slots = static_cast<long long>(sm_count) * (d == 64 || Nq <= 4 ? 2 : 1);
   int s_max = Nk / 256;
   if (s_max > 128) s_max = 128;
   if (s_max < 1) s_max = 1;

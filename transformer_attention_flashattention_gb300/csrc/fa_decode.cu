@@ -32,25 +32,35 @@ namespace fa {
 namespace {
 
 constexpr int kDecTile = 64;                 // keys per stage
-constexpr int kDecStages = 6;
 constexpr int kDecCompute = 256;             // compute threads (8 warps)
 constexpr int kDecThreads = kDecCompute;
-constexpr int kDecMaxQ = 16;
+constexpr int kDecMaxQ = 16;                 // query rows a call may have
+constexpr int kDecFewQ = 4;                  // bound of the few-row instantiation
 constexpr float kDecLn2 = 0.693147180559945309f;
 constexpr unsigned kDecStatusTimeout = 16u;
 
-template <int D>
+// NQ bounds the query rows (registers hold NQ rows of O and statistics per thread).  Two
+// CTAs share an SM whenever their registers allow it (head dim 64, or at most kDecFewQ rows):
+// the ring is then 96 KB a CTA, and one CTA's start and finish overlap the other's stream.
+// Otherwise (head dim 128 with up to 16 rows, 204 registers) one CTA has a 192 KB ring.
+template <int D, int NQ>
 struct DecCfg {
+  static constexpr int kCtasPerSm = (D == 64 || NQ <= kDecFewQ) ? 2 : 1;
   static constexpr int kBoxes = D / 64;                    // 128-byte swizzle atoms per row
   static constexpr int kBoxBytes = kDecTile * 128;         // one atom column of a tile
   static constexpr int kTileBytes = kBoxes * kBoxBytes;    // K (or V) tile
   static constexpr int kStageBytes = 2 * kTileBytes;       // K and V of one tile
+  static constexpr int kStages = (96 * 1024 * (3 - kCtasPerSm)) / kStageBytes;   // 96 or 192 KB
   static constexpr int kKOff = 0;
-  static constexpr int kQOff = kDecStages * kStageBytes;   // q * scale * log2(e), fp32 [kDecMaxQ][D]
-  static constexpr int kSOff = kQOff + kDecMaxQ * D * 4;   // scores / weights [kDecMaxQ][kDecTile]
-  static constexpr int kStatOff = kSOff + kDecMaxQ * kDecTile * 4;  // m, l, alpha per row
-  static constexpr int kBarOff = (kStatOff + 3 * kDecMaxQ * 4 + 7) / 8 * 8;
-  static constexpr int kBytes = kBarOff + 2 * kDecStages * 8 + 16;
+  static constexpr int kQOff = kStages * kStageBytes;      // q * scale * log2(e), fp32 [NQ][D]
+  static constexpr int kSOff = kQOff + NQ * D * 4;         // scores / weights [NQ][kDecTile]
+  static constexpr int kStatOff = kSOff + NQ * kDecTile * 4;   // m, l, alpha per row
+  static constexpr int kBarOff = (kStatOff + 3 * NQ * 4 + 7) / 8 * 8;
+  static constexpr int kBytes = kBarOff + 2 * kStages * 8 + 16;
+  // the final merge of the 8 warps reuses the ring: [8 warps][NQ][D] fp32, and the
+  // per-warp m and l in the score area
+  static_assert((kDecCompute / 32) * NQ * D * 4 <= kStages * kStageBytes, "merge buffer exceeds the ring");
+  static_assert(2 * (kDecCompute / 32) * NQ <= NQ * kDecTile, "merge statistics exceed the score area");
 };
 
 __device__ __forceinline__ void compute_sync() {
@@ -60,7 +70,7 @@ __device__ __forceinline__ void compute_sync() {
 // Byte offset of 16-byte chunk c (0 .. D/8-1) of tile row r under the 128-byte swizzle.
 template <int D>
 __device__ __forceinline__ uint32_t swz(int r, int c) {
-  return (c / 8) * DecCfg<D>::kBoxBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+  return (c / 8) * (kDecTile * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
 template <bool BF16>
@@ -72,9 +82,11 @@ __device__ __forceinline__ float2 unpack2(uint32_t w) {
   }
 }
 
-template <int D, bool BF16>
-__global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const __grid_constant__ DecodeParams p) {
-  using C = DecCfg<D>;
+template <int D, bool BF16, int NQ>
+__global__ void __launch_bounds__(kDecThreads, DecCfg<D, NQ>::kCtasPerSm)
+    fa_decode_split_kernel(const __grid_constant__ DecodeParams p) {
+  using C = DecCfg<D, NQ>;
+  constexpr int kDecStages = C::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = ptx::smem_u32(smem);
@@ -84,8 +96,8 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const __gr
   float* qs = reinterpret_cast<float*>(smem + C::kQOff);
   float* sc = reinterpret_cast<float*>(smem + C::kSOff);
   float* m_run = reinterpret_cast<float*>(smem + C::kStatOff);
-  float* l_run = m_run + kDecMaxQ;
-  float* alpha = l_run + kDecMaxQ;
+  float* l_run = m_run + NQ;
+  float* alpha = l_run + NQ;
 
   const int bh = blockIdx.x / p.splits;
   const int split = blockIdx.x % p.splits;
@@ -112,7 +124,7 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const __gr
     else x = __half2float(__ushort_as_half(raw));
     qs[i] = x * p.scale_log2;
   }
-  if (tid < kDecMaxQ) {
+  if (tid < NQ) {
     m_run[tid] = -INFINITY;
     l_run[tid] = 0.f;
     alpha[tid] = 1.f;
@@ -152,10 +164,10 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const __gr
   constexpr int E = D / 32;
   constexpr int kKeysPerWarp = kDecTile / (kDecCompute / 32);   // 8
   const int last_key_shift = p.Nk - p.Nq;                       // causal: row i sees keys <= shift + i
-  float acc[kDecMaxQ][E];
-  float m_w[kDecMaxQ], l_w[kDecMaxQ];
+  float acc[NQ][E];
+  float m_w[NQ], l_w[NQ];
 #pragma unroll
-  for (int qi = 0; qi < kDecMaxQ; ++qi) {
+  for (int qi = 0; qi < NQ; ++qi) {
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[qi][e] = 0.f;
     m_w[qi] = -INFINITY;
@@ -189,7 +201,7 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const __gr
     }
 
 #pragma unroll
-    for (int qi = 0; qi < kDecMaxQ; ++qi) {
+    for (int qi = 0; qi < NQ; ++qi) {
       if (qi >= p.Nq) break;
       // partial dot products over this lane's slice, then a reduce-scatter across lanes
       float qv[E];
@@ -293,16 +305,16 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const __gr
 
   // merge the 8 warps: M = max m_w, L = sum l_w 2^(m_w - M), O = sum acc_w 2^(m_w - M) / L
   float* red_o = reinterpret_cast<float*>(smem + C::kKOff);     // the ring is idle now
-  float* red_m = sc;                                            // [8 warps][kDecMaxQ]
-  float* red_l = sc + (kDecCompute / 32) * kDecMaxQ;
+  float* red_m = sc;                                            // [8 warps][NQ]
+  float* red_l = sc + (kDecCompute / 32) * NQ;
 #pragma unroll
-  for (int qi = 0; qi < kDecMaxQ; ++qi) {
+  for (int qi = 0; qi < NQ; ++qi) {
     if (qi >= p.Nq) break;
 #pragma unroll
-    for (int e = 0; e < E; ++e) red_o[(warp * kDecMaxQ + qi) * D + E * lane + e] = acc[qi][e];
+    for (int e = 0; e < E; ++e) red_o[(warp * NQ + qi) * D + E * lane + e] = acc[qi][e];
     if (lane == 0) {
-      red_m[warp * kDecMaxQ + qi] = m_w[qi];
-      red_l[warp * kDecMaxQ + qi] = l_w[qi];
+      red_m[warp * NQ + qi] = m_w[qi];
+      red_l[warp * NQ + qi] = l_w[qi];
     }
   }
   compute_sync();
@@ -310,15 +322,15 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const __gr
   for (int idx = tid; idx < p.Nq * (D / 2); idx += kDecCompute) {
     const int qi = idx / (D / 2), cpair = idx % (D / 2);
     float M = -INFINITY;
-    for (int w = 0; w < kDecCompute / 32; ++w) M = fmaxf(M, red_m[w * kDecMaxQ + qi]);
+    for (int w = 0; w < kDecCompute / 32; ++w) M = fmaxf(M, red_m[w * NQ + qi]);
     float L = 0.f, ox = 0.f, oy = 0.f;
     if (M != -INFINITY) {
       for (int w = 0; w < kDecCompute / 32; ++w) {
-        const float mw = red_m[w * kDecMaxQ + qi];
+        const float mw = red_m[w * NQ + qi];
         const float f = mw == -INFINITY ? 0.f : ptx::ex2(mw - M);
-        L = fmaf(red_l[w * kDecMaxQ + qi], f, L);
-        ox = fmaf(red_o[(w * kDecMaxQ + qi) * D + 2 * cpair], f, ox);
-        oy = fmaf(red_o[(w * kDecMaxQ + qi) * D + 2 * cpair + 1], f, oy);
+        L = fmaf(red_l[w * NQ + qi], f, L);
+        ox = fmaf(red_o[(w * NQ + qi) * D + 2 * cpair], f, ox);
+        oy = fmaf(red_o[(w * NQ + qi) * D + 2 * cpair + 1], f, oy);
       }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
@@ -393,14 +405,24 @@ __global__ void __launch_bounds__(256) fa_decode_merge_kernel(const __grid_const
   if (lane == 0 && p.lse) p.lse[static_cast<size_t>(bh) * p.Nq + qi] = total > 0.f ? mx + __logf(total) : -INFINITY;
 }
 
-template <int D, bool BF16>
-cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
-  auto split = fa_decode_split_kernel<D, BF16>;
-  constexpr int kSmem = DecCfg<D>::kBytes + 1024;          // room to align the base to 1 KB
+template <int D, bool BF16, int NQ>
+cudaError_t launch_split(const DecodeParams& p, cudaStream_t stream) {
+  auto split = fa_decode_split_kernel<D, BF16, NQ>;
+  constexpr int kSmem = DecCfg<D, NQ>::kBytes + 1024;      // room to align the base to 1 KB
   cudaError_t e = cudaFuncSetAttribute(split, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
+  if (DecCfg<D, NQ>::kCtasPerSm > 1) {
+    e = cudaFuncSetAttribute(split, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+  }
   split<<<p.BH * p.splits, kDecThreads, kSmem, stream>>>(p);
-  e = cudaGetLastError();
+  return cudaGetLastError();
+}
+
+template <int D, bool BF16>
+cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
+  cudaError_t e = p.Nq <= kDecFewQ ? launch_split<D, BF16, kDecFewQ>(p, stream)
+                                   : launch_split<D, BF16, kDecMaxQ>(p, stream);
   if (e != cudaSuccess || p.splits == 1) return e;
   fa_decode_merge_kernel<D, BF16><<<(p.BH * p.Nq + 7) / 8, 256, 0, stream>>>(p);
   return cudaGetLastError();
