@@ -34,3 +34,17 @@ def test_warmup_rule():
 
 def test_aggregate_counts_every_rank():
     assert bench.aggregate_tflops(1e12, 2, 4, 1000.0) == pytest.approx(8.0)
+
+
+def test_naive_bytes_counts_each_pass_once():
+    """Standard attention on one head of N = 4, d = 2 (16-bit inputs): the S GEMM reads Q and K
+    (2 * 4 * 2 * 2 bytes) and writes 16 fp32 scores; the softmax reads the visible scores
+    (16, or 10 when causal) and writes 16 16-bit weights and 4 LSE floats; the P V GEMM reads
+    the 16 weights and V and writes O (4 * 2 * 2 bytes each)."""
+    qk, s_out, p_out, lse, p_in, vo = 32, 64, 32, 16, 32, 32
+    assert bench.naive_bytes(1, 1, 4, 2, False) == qk + s_out + 64 + p_out + lse + p_in + vo
+    assert bench.naive_bytes(1, 1, 4, 2, True) == qk + s_out + 40 + p_out + lse + p_in + vo
+    # rows padded to whole float4 vectors: N = 5 writes 5 x 8 fp32 scores
+    n5 = bench.naive_bytes(1, 1, 5, 2, False)
+    assert n5 == 2 * 5 * 2 * 2 + 4 * 5 * 8 + 4 * 25 + 2 * 25 + 4 * 5 + 2 * 25 + 2 * 5 * 2 * 2
+    assert bench.naive_bytes(3, 2, 5, 2, False) == 6 * n5

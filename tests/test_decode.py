@@ -53,6 +53,9 @@ CASES = [
     (1, 4, 5, 4096, 128, torch.float16),
     (4, 8, 1, 8192, 128, torch.bfloat16),
     (1, 2, 16, 16, 128, torch.bfloat16),
+    # the bound of the two-CTAs-per-SM instantiation (4 rows) at both head dims
+    (1, 3, 4, 1000, 64, torch.bfloat16),
+    (2, 2, 2, 3000, 128, torch.float16),
 ]
 
 
