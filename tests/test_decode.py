@@ -111,3 +111,33 @@ def test_equal_scores_closed_form(gpu_lib, causal, num_splits):
     bound = _half_ulp(ref_o, 7) + 1e-5 * np.abs(vd).max()
     assert (np.abs(on - ref_o) <= bound).all(), f"max|dO| {np.abs(on - ref_o).max():.3e}"
     assert np.abs(ln - ref_lse).max() <= 1e-5
+
+
+def test_decode_benchmark_workload(gpu_lib):
+    """The benchmark's decode workload at full size, in the launch configuration it times (the
+    automatic split count, two CTAs per SM): one query row of 8 x 32 heads against 32768 cached
+    keys.  Sampled heads against the oracle; every head against a property that holds at any
+    size: O is a convex combination of the V rows, so each coordinate lies between that
+    column's smallest and largest value (up to the output's rounding)."""
+    fa = gpu_lib
+    B, H, Nk, d = 8, 32, 32768, 128
+    q, _, _ = make_qkv((B, H, 1, d), torch.bfloat16, 5)
+    _, k, v = make_qkv((B, H, Nk, d), torch.bfloat16, 6)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o, lse = fa.decode(qd, kd, vd)
+    torch.cuda.synchronize()
+    st, bits = fa.last_device_status()
+    assert st == fa.FA_OK, f"status {bits:#x}"
+    of = o.float()
+    lo = vd.float().amin(dim=2, keepdim=True)
+    hi = vd.float().amax(dim=2, keepdim=True)
+    slack = 2.0 ** -8 * torch.maximum(lo.abs(), hi.abs())
+    assert bool(torch.isfinite(of).all()) and bool(torch.isfinite(lse).all())
+    assert bool(((of >= lo - slack) & (of <= hi + slack)).all())
+    on, ln = of.cpu().numpy(), lse.cpu().numpy()
+    for b, h in [(0, 0), (3, 17), (7, 31)]:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ro, rl = oracle.attention_decode(q[sl], k[sl], v[sl], 1 / math.sqrt(d), False)
+        excess = float((np.abs(on[sl] - ro) - 1e-2 - _half_ulp(ro, 7)).max())
+        el = float(np.abs(ln[sl] - rl).max())
+        assert excess <= 0 and el <= 1e-3, f"head ({b},{h}): excess={excess:.3e} max|dLSE|={el:.3e}"
