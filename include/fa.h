@@ -266,14 +266,16 @@ int fa_bwd_workspace_size(int B, int H, int N, int d, unsigned long long* bytes)
  *   2. a row softmax kernel: reads each row's visible scores once, writes P = softmax(S)
  *      in `dtype` over the start of the same row (zeros at masked columns), and the LSE;
  *   3. O = P V (a second cuBLAS GEMM), fp32 accumulation, rounded to `dtype`.
- *   workspace : device scratch of at least fa_fwd_naive_workspace_size() bytes (4 bytes
- *               per score: B * H * N * ceil(N/4)*4 * 4), 256-byte aligned, owned by the
- *               caller; calls sharing one workspace must not overlap on the GPU
+ *   workspace : device scratch of at least fa_fwd_naive_workspace_size() bytes, 256-byte
+ *               aligned, owned by the caller: the fp32 scores (B * H * N * ceil(N/4)*4 * 4
+ *               bytes, rounded up to 256) and then 32 MiB of scratch for the two GEMMs;
+ *               calls sharing one workspace must not overlap on the GPU
  * Supported: fa_fwd's shapes with N <= 32768 and B*H*N < 2^31 (else FA_ERR_UNSUPPORTED or
  * FA_ERR_SHAPE).  cuBLAS (libcublas.so.13) is resolved at the first call, from the copy
  * the process already has loaded or from the loader's search path, and one cuBLAS handle
- * is created per device (cuBLAS keeps its own workspace there); calls from several host
- * threads are serialised while they enqueue.
+ * is created per device; each call points that handle at its own stream and at the GEMM
+ * scratch in its own workspace, so calls with separate workspaces may overlap on separate
+ * streams.  Calls from several host threads are serialised while they enqueue.
  * Errors as fa_fwd, plus FA_ERR_WORKSPACE, and FA_ERR_CUDA when cuBLAS cannot be loaded or
  * its handle created.
  */
@@ -281,7 +283,7 @@ int fa_fwd_naive(const void* q, const void* k, const void* v, void* o, float* ls
                  float scale, int causal, int dtype, void* workspace, unsigned long long workspace_bytes,
                  void* stream);
 
-/* Scratch bytes fa_fwd_naive needs: the fp32 score matrix of every head. */
+/* Scratch bytes fa_fwd_naive needs: the fp32 score matrix of every head, then 32 MiB for the GEMMs. */
 int fa_fwd_naive_workspace_size(int B, int H, int N, int d, unsigned long long* bytes);
 
 /* Size of the static scratch area behind fa_decode_noalloc, per device (8 MiB). */

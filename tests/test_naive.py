@@ -100,3 +100,29 @@ def test_naive_8192_workload(gpu_lib):
     rows = sample_rows(w.N)
     ro, rl = oracle.attention(q, k, v, 1 / math.sqrt(w.d), False, rows=rows)
     _assert_close(o[:, :, rows], lse[:, :, rows], ro, rl, "naive 2x16x8192 sampled rows", plain=True)
+
+
+def test_naive_calls_on_two_streams(gpu_lib):
+    """Calls share one cuBLAS handle per device but each brings its own workspace (scores and
+    GEMM scratch): two calls enqueued on two streams at once give, bit for bit, what each
+    gives alone."""
+    fa = gpu_lib
+    shape = (2, 4, 1536, 128)
+    a = [t.cuda() for t in make_qkv(shape, torch.bfloat16, 91)]
+    b = [t.cuda() for t in make_qkv(shape, torch.bfloat16, 92)]
+    ra = fa.attention_naive(*a, causal=True)
+    rb = fa.attention_naive(*b, causal=False)
+    torch.cuda.synchronize()
+    need = ctypes.c_ulonglong(0)
+    assert fa.load_library().fa_fwd_naive_workspace_size(*shape, ctypes.byref(need)) == fa.FA_OK
+    ws = [torch.empty(need.value, device="cuda", dtype=torch.uint8) for _ in range(2)]
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for _ in range(3):
+        oa, ob = torch.empty_like(a[0]), torch.empty_like(b[0])
+        la = torch.empty(shape[:3], device="cuda")
+        lb = torch.empty(shape[:3], device="cuda")
+        fa.attention_naive(*a, causal=True, out=oa, lse=la, workspace=ws[0], stream=s1)
+        fa.attention_naive(*b, causal=False, out=ob, lse=lb, workspace=ws[1], stream=s2)
+        torch.cuda.synchronize()
+        assert torch.equal(oa, ra[0]) and torch.equal(la, ra[1])
+        assert torch.equal(ob, rb[0]) and torch.equal(lb, rb[1])

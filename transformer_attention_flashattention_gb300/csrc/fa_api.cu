@@ -536,9 +536,15 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
 
 namespace {
 constexpr int kNaiveMaxN = 32768;   // the row softmax keeps a row in 256 threads' registers
+constexpr unsigned long long kNaiveBlasWs = 32ull << 20;   // the cuBLAS GEMMs' scratch
 
 // fp32 score row stride of the materialising path: N rounded up to whole float4 vectors.
 long long naive_ld(int N) { return (static_cast<long long>(N) + 3) / 4 * 4; }
+// bytes of the fp32 score matrices, rounded up to 256 (the GEMM scratch follows them)
+unsigned long long naive_scores(int B, int H, int N) {
+  return (static_cast<unsigned long long>(B) * H * N * static_cast<unsigned long long>(naive_ld(N)) * 4ull + 255) /
+         256 * 256;
+}
 }  // namespace
 
 extern "C" int fa_fwd_naive_workspace_size(int B, int H, int N, int d, unsigned long long* bytes) {
@@ -548,7 +554,7 @@ extern "C" int fa_fwd_naive_workspace_size(int B, int H, int N, int d, unsigned 
   if (N > kNaiveMaxN) return FA_ERR_UNSUPPORTED;
   const long double rows = static_cast<long double>(B) * H * N;
   if (rows >= static_cast<long double>(1ll << 31)) return FA_ERR_SHAPE;
-  *bytes = static_cast<unsigned long long>(B) * H * N * static_cast<unsigned long long>(naive_ld(N)) * 4ull;
+  *bytes = naive_scores(B, H, N) + kNaiveBlasWs;
   return FA_OK;
 }
 
@@ -568,8 +574,9 @@ extern "C" int fa_fwd_naive(const void* q, const void* k, const void* v, void* o
   if (workspace_bytes < need) return FA_ERR_WORKSPACE;
   const DeviceInfo* di = current_device(&st);
   if (!di) return st;
-  return run_naive(q, k, v, o, lse, static_cast<float*>(workspace), naive_ld(N), B * H, N, d, scale, causal,
-                   dtype == FA_BF16, static_cast<cudaStream_t>(stream));
+  uint8_t* const base = static_cast<uint8_t*>(workspace);
+  return run_naive(q, k, v, o, lse, reinterpret_cast<float*>(base), naive_ld(N), base + naive_scores(B, H, N),
+                   kNaiveBlasWs, B * H, N, d, scale, causal, dtype == FA_BF16, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int fa_last_device_status(void* stream, unsigned int* bits) {

@@ -25,9 +25,10 @@ cudaError_t launch_bwd(int d, bool bf16, const BwdParams& p, int grid, cudaStrea
 
 // Materialising attention (fa_fwd_naive): library GEMM S = scale Q K^T into `s` (fp32 rows
 // `ld` floats apart), the row softmax in place (P in the input dtype, LSE), library GEMM
-// O = P V, all on `stream`.  Returns an fa_status.
-int run_naive(const void* q, const void* k, const void* v, void* o, float* lse, float* s, long long ld, int BH,
-              int N, int d, float scale, int causal, bool bf16, cudaStream_t stream);
+// O = P V, all on `stream`; `blas_ws` is the GEMMs' scratch.  Returns an fa_status.
+int run_naive(const void* q, const void* k, const void* v, void* o, float* lse, float* s, long long ld,
+              void* blas_ws, unsigned long long blas_ws_bytes, int BH, int N, int d, float scale, int causal,
+              bool bf16, cudaStream_t stream);
 
 // fa_decode's shape and size checks (FA_OK, FA_ERR_SHAPE or FA_ERR_UNSUPPORTED).
 int check_decode(int B, int H, int Nq, int Nk, int d);

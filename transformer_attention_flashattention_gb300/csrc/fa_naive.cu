@@ -147,6 +147,7 @@ struct Blas {
   bool tried = false;
   decltype(&cublasCreate_v2) create = nullptr;
   decltype(&cublasSetStream_v2) set_stream = nullptr;
+  decltype(&cublasSetWorkspace_v2) set_workspace = nullptr;
   GemmFn gemm = nullptr;
   cublasHandle_t handle[64] = {};
 };
@@ -162,8 +163,9 @@ bool load_blas() {
   if (lib == nullptr) return false;
   g_blas.create = reinterpret_cast<decltype(&cublasCreate_v2)>(dlsym(lib, "cublasCreate_v2"));
   g_blas.set_stream = reinterpret_cast<decltype(&cublasSetStream_v2)>(dlsym(lib, "cublasSetStream_v2"));
+  g_blas.set_workspace = reinterpret_cast<decltype(&cublasSetWorkspace_v2)>(dlsym(lib, "cublasSetWorkspace_v2"));
   g_blas.gemm = reinterpret_cast<GemmFn>(dlsym(lib, "cublasGemmStridedBatchedEx"));
-  if (!g_blas.create || !g_blas.set_stream || !g_blas.gemm) {
+  if (!g_blas.create || !g_blas.set_stream || !g_blas.set_workspace || !g_blas.gemm) {
     g_blas.gemm = nullptr;
     return false;
   }
@@ -172,8 +174,9 @@ bool load_blas() {
 
 }  // namespace
 
-int run_naive(const void* q, const void* k, const void* v, void* o, float* lse, float* s, long long ld, int BH,
-              int N, int d, float scale, int causal, bool bf16, cudaStream_t stream) {
+int run_naive(const void* q, const void* k, const void* v, void* o, float* lse, float* s, long long ld,
+              void* blas_ws, unsigned long long blas_ws_bytes, int BH, int N, int d, float scale, int causal,
+              bool bf16, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_blas_mu);
@@ -183,7 +186,11 @@ int run_naive(const void* q, const void* k, const void* v, void* o, float* lse, 
     h = nullptr;
     return FA_ERR_CUDA;
   }
-  if (g_blas.set_stream(h, stream) != CUBLAS_STATUS_SUCCESS) return FA_ERR_CUDA;
+  // the GEMMs' scratch is this call's own (part of the caller's workspace), so calls that
+  // share the handle but run at once on other streams, with other workspaces, do not share it
+  if (g_blas.set_stream(h, stream) != CUBLAS_STATUS_SUCCESS ||
+      g_blas.set_workspace(h, blas_ws, static_cast<size_t>(blas_ws_bytes)) != CUBLAS_STATUS_SUCCESS)
+    return FA_ERR_CUDA;
   const cudaDataType dt = bf16 ? CUDA_R_16BF : CUDA_R_16F;
   const float zero = 0.f, one = 1.f;
   const long long nd = static_cast<long long>(N) * d, nld = static_cast<long long>(N) * ld;
