@@ -16,7 +16,8 @@ bracketed by CUDA events, L2 flushed before each launch whose inputs fit in it):
     and end to end from host bf16 Q/K/V to host bf16 O through ``fa_fwd_fp8_host``;
   * the backward pass on [16, 16, 2048, 128], both masks;
   * standard attention with the N x N scores in HBM (``fa_fwd_naive``) on
-    16x16x2048x128 (both masks) and 2x16x8192x128 (non-causal), against the tiled kernel.
+    16x16x2048x128 (both masks), 2x16x8192x128 and 1x16x16384x128 (non-causal), against
+    the tiled kernel.
 
 Single workloads (``--workload``; the line then carries that workload alone):
   bf16            [16, 16, 2048, 128], both masks
@@ -450,7 +451,8 @@ def _naive_figures(fa, dev, timer, n, peaks, fused):
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     out = {}
     specs = [("16x16x2048x128", WORKLOADS["bf16"], (False, True)),
-             ("2x16x8192x128", Workload("v8192", 2, 16, 8192, 128, torch.bfloat16, 2), (False,))]
+             ("2x16x8192x128", Workload("v8192", 2, 16, 8192, 128, torch.bfloat16, 2), (False,)),
+             ("1x16x16384x128", Workload("v16384", 1, 16, 16384, 128, torch.bfloat16, 2), (False,))]
     for tag, w, masks in specs:
         q, k, v = (t.to(dev) for t in make_inputs(w))
         need = ctypes.c_ulonglong(0)

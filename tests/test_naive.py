@@ -90,16 +90,17 @@ def test_naive_agrees_with_the_tiled_kernel(gpu_lib):
         assert (l1 - l2).abs().max().item() <= 2e-3
 
 
-def test_naive_8192_workload(gpu_lib):
-    """2x16x8192x128 non-causal, the benchmark's second standard-attention case, on sampled
-    rows of every head."""
+@pytest.mark.parametrize("B,N", [(2, 8192), (1, 16384)])
+def test_naive_long_workloads(gpu_lib, B, N):
+    """2x16x8192x128 and 1x16x16384x128 non-causal, the benchmark's longer standard-attention
+    cases, on sampled rows of every head."""
     from fa_inputs import Workload
-    w = Workload("v8192", 2, 16, 8192, 128, torch.bfloat16, 2)
+    w = Workload(f"v{N}", B, 16, N, 128, torch.bfloat16, 2)
     q, k, v = make_inputs(w)
     o, lse = _run_naive(gpu_lib, q, k, v, False)
     rows = sample_rows(w.N)
     ro, rl = oracle.attention(q, k, v, 1 / math.sqrt(w.d), False, rows=rows)
-    _assert_close(o[:, :, rows], lse[:, :, rows], ro, rl, "naive 2x16x8192 sampled rows", plain=True)
+    _assert_close(o[:, :, rows], lse[:, :, rows], ro, rl, f"naive {B}x16x{N} sampled rows", plain=True)
 
 
 def test_naive_calls_on_two_streams(gpu_lib):
